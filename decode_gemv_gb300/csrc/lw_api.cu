@@ -1,0 +1,142 @@
+// Device-facing C-ABI calls of liblw: argument checks, then the launchers.
+#include <cstdint>
+#include <mutex>
+#include <unordered_map>
+
+#include "lw_internal.h"
+#include "lw_launch.h"
+
+namespace lw {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[128] = {0};
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 128) return 1;
+  std::lock_guard<std::mutex> g(mu);
+  if (!cache[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    cache[d] = n > 0 ? n : 1;
+  }
+  return cache[d];
+}
+
+int resident_blocks(const void* kernel, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> cache;
+  int d = 0;
+  cudaGetDevice(&d);
+  const uint64_t key = (reinterpret_cast<uint64_t>(kernel) * 1315423911ull) ^ (smem << 8) ^ (uint64_t)d;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    cache[key] = 0;
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lw_status check_dev_bundle(const lw_dev_bundle* b, bool want_twin, bool product) {
+  if (!b) return fail(LW_ERR_INVALID_ARG, "NULL bundle");
+  if (b->fmt != LW_FMT_Q4_PAIR && b->fmt != LW_FMT_Q6 && b->fmt != LW_FMT_BF16_EXP)
+    return fail(LW_ERR_UNSUPPORTED, "unknown format %d", b->fmt);
+  if (b->rows <= 0 || b->cols <= 0 || b->rows % 64 || b->cols % 256)
+    return fail(LW_ERR_SHAPE, "shape %lldx%lld is not a positive multiple of 64x256",
+                (long long)b->rows, (long long)b->cols);
+  if (b->rows > (1ll << 30) || b->cols > (1ll << 30) || tiles_of(b->rows, b->cols) > (1ll << 30))
+    return fail(LW_ERR_SHAPE, "matrix too large");
+  if (want_twin && !b->twin) return fail(LW_ERR_INVALID_ARG, "expected a twin bundle");
+  if (!want_twin && product && b->twin) return fail(LW_ERR_INVALID_ARG, "expected a coded bundle, got a twin");
+  if (!b->words || !b->tile_off || !b->lane_bits || !b->table)
+    return fail(LW_ERR_INVALID_ARG, "missing words/tile_off/lane_bits/table");
+  if (!aligned16(b->words)) return fail(LW_ERR_INVALID_ARG, "words must be 16-byte aligned");
+  if (b->max_tile_rows < 0 || b->max_tile_rows > 1024)
+    return fail(LW_ERR_INVALID_ARG, "max_tile_rows %d out of range", b->max_tile_rows);
+  if (!b->twin && (b->lmin < 1 || b->lmax > LW_MAX_CODE_LEN || b->lmin > b->lmax))
+    return fail(LW_ERR_INVALID_ARG, "lmin/lmax %d/%d out of range", b->lmin, b->lmax);
+  if (b->fmt != LW_FMT_BF16_EXP) {
+    if (product && (!b->qparams || !aligned16(b->qparams)))
+      return fail(LW_ERR_INVALID_ARG, "qparams missing or not 16-byte aligned");
+  } else if (!b->signman || !b->vflags || !b->vrow_off || !aligned16(b->signman) ||
+             (!b->vexp && b->twin == 0 && false)) {
+    return fail(LW_ERR_INVALID_ARG, "BF16 side sections missing or misaligned");
+  }
+  return LW_OK;
+}
+
+}  // namespace lw
+
+using namespace lw;
+
+extern "C" size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch) {
+  if (!b || batch < 1 || b->rows <= 0 || b->cols <= 0) return 0;
+  const int64_t chunk = batch > 8 ? 8 : batch;
+  return (size_t)(b->cols / 256) * (size_t)chunk * (size_t)b->rows * sizeof(float);
+}
+
+static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, float* Y, void* ws,
+                         size_t ws_bytes, int32_t* d_status, void* stream, bool twin) {
+  clear_error();
+  lw_status s = check_dev_bundle(b, twin, true);
+  if (s != LW_OK) return s;
+  if (!X || !Y || !ws) return fail(LW_ERR_INVALID_ARG, "NULL x/y/workspace");
+  if (batch < 1 || batch > 64) return fail(LW_ERR_INVALID_ARG, "batch %d outside 1..64", batch);
+  if (!aligned16(X) || (reinterpret_cast<uintptr_t>(Y) & 7u) || !aligned16(ws))
+    return fail(LW_ERR_INVALID_ARG, "x/workspace must be 16-byte aligned, y 8-byte aligned");
+  if (ws_bytes < lw_workspace_bytes(b, batch))
+    return fail(LW_ERR_INVALID_ARG, "workspace of %zu bytes < %zu", ws_bytes, lw_workspace_bytes(b, batch));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (b->fmt == LW_FMT_BF16_EXP)
+    return launch_bf16_product(b, static_cast<const uint16_t*>(X), batch, Y,
+                               static_cast<float*>(ws), d_status, st);
+  // activation rows in chunks of up to 8 (each chunk decodes the matrix once)
+  for (int b0 = 0; b0 < batch; b0 += 8) {
+    const int nb = batch - b0 < 8 ? batch - b0 : 8;
+    s = launch_q_product(b, static_cast<const float*>(X) + (size_t)b0 * b->cols, nb,
+                         Y + (size_t)b0 * b->rows, static_cast<float*>(ws), d_status, st);
+    if (s != LW_OK) return s;
+  }
+  return LW_OK;
+}
+
+extern "C" lw_status lw_decode_gemv(const lw_dev_bundle* b, const void* x, float* y, void* ws,
+                                    size_t ws_bytes, int32_t* d_status, void* stream) {
+  return product(b, x, 1, y, ws, ws_bytes, d_status, stream, false);
+}
+
+extern "C" lw_status lw_decode_gemm(const lw_dev_bundle* b, const void* X, int32_t batch, float* Y,
+                                    void* ws, size_t ws_bytes, int32_t* d_status, void* stream) {
+  return product(b, X, batch, Y, ws, ws_bytes, d_status, stream, false);
+}
+
+extern "C" lw_status lw_twin_gemv(const lw_dev_bundle* b, const void* x, float* y, void* ws,
+                                  size_t ws_bytes, int32_t* d_status, void* stream) {
+  return product(b, x, 1, y, ws, ws_bytes, d_status, stream, true);
+}
+
+extern "C" lw_status lw_twin_gemm(const lw_dev_bundle* b, const void* X, int32_t batch, float* Y,
+                                  void* ws, size_t ws_bytes, int32_t* d_status, void* stream) {
+  return product(b, X, batch, Y, ws, ws_bytes, d_status, stream, true);
+}
+
+extern "C" lw_status lw_decode(const lw_dev_bundle* b, void* out, int32_t* d_status, void* stream) {
+  clear_error();
+  lw_status s = check_dev_bundle(b, b ? b->twin != 0 : false, false);
+  if (s != LW_OK) return s;
+  if (!out || !aligned16(out)) return fail(LW_ERR_INVALID_ARG, "out must be non-NULL and 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (b->fmt == LW_FMT_BF16_EXP) return launch_bf16_decode(b, out, d_status, st);
+  return launch_q_decode(b, out, d_status, st);
+}

@@ -1,0 +1,111 @@
+// Device helpers shared by liblw's kernels: bulk asynchronous copies into
+// shared memory completed on an mbarrier, with bounded waits, and the status
+// word.  sm_103a only.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "lw.h"
+
+namespace lw {
+namespace dev {
+
+// A wait on one of our own copies gives up after this many SM cycles (about
+// 1 s at 2 GHz), reports LW_DEV_TIMEOUT and returns; a healthy copy of a few
+// kilobytes completes in microseconds.
+constexpr long long kWaitCycles = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make mbarrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later asynchronous-proxy writes to the same buffer (buffer reuse).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Bulk copy global -> this CTA's shared memory (no multicast).  dst, src and
+// bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`; false if it did not complete in time.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Table checks run by one thread per CTA before any decoding: the length
+// span fits the launch's comparator count, limits are ordered, and every
+// window maps to an index inside the symbol table.  Returns true if good.
+__device__ inline bool table_ok(const lw_table* tb, int want_fmt, int want_alpha, int ncmp) {
+  const int lmin = tb->lmin, lmax = tb->lmax;
+  if (tb->fmt != want_fmt || tb->alpha != want_alpha) return false;
+  if (lmin < 1 || lmax > LW_MAX_CODE_LEN || lmin > lmax || lmax - lmin > ncmp) return false;
+  const int n_entries = tb->n_sym + (tb->phantom ? 1 : 0);
+  if (n_entries < 1 || n_entries > want_alpha + 1 || n_entries > 256) return false;
+  const int nl = lmax - lmin;
+  for (int j = nl; j < 12; ++j)
+    if (tb->lim_m1[j] != 0xFFFFFFFFu) return false;
+  uint32_t prev_hi = 0;
+  for (int j = 0; j <= nl; ++j) {
+    const int L = lmin + j;
+    const uint32_t hi = tb->lim_m1[j];          // largest window of length <= L
+    if (j > 0 && hi < prev_hi) return false;
+    const uint32_t cmax = hi >> (32 - L);
+    const uint32_t cmin = j == 0 ? 0u : (prev_hi + 1u) >> (32 - L);
+    const long long lo_idx = (long long)tb->off[j] + cmin;
+    const long long hi_idx = (long long)tb->off[j] + cmax;
+    if (j > 0 && prev_hi == 0xFFFFFFFFu) return false;
+    if (lo_idx < 0 || hi_idx >= n_entries) return false;
+    prev_hi = hi;
+  }
+  return true;
+}
+
+}  // namespace dev
+}  // namespace lw

@@ -1,0 +1,49 @@
+// Host-side launch helpers shared by liblw's .cu files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "lw_internal.h"
+
+namespace lw {
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Resident blocks per SM for `kernel` with `threads` threads and `smem` bytes of
+// dynamic shared memory; raises the kernel's dynamic shared-memory limit first.
+// Cached per (kernel, smem).  0 if it cannot run.
+int resident_blocks(const void* kernel, int threads, size_t smem);
+
+inline lw_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(LW_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return LW_OK;
+}
+
+// Launch a persistent grid: as many blocks as are resident on the device, but
+// no more than there are tiles to share among `warps`-warp blocks.
+template <class Launch>
+lw_status launch_persistent(const void* kernel, int warps, size_t smem, int n_tiles,
+                            cudaStream_t st, Launch&& launch) {
+  (void)st;
+  const int per_sm = resident_blocks(kernel, warps * 32, smem);
+  if (per_sm < 1)
+    return fail(LW_ERR_UNSUPPORTED, "kernel does not fit on an SM (%zu bytes of shared memory)",
+                smem);
+  long long blocks = (long long)per_sm * device_sm_count();
+  const long long need = (n_tiles + warps - 1) / warps;
+  if (need < blocks) blocks = need;
+  if (blocks < 1) blocks = 1;
+  launch((int)blocks);
+  return check_launch("product kernel");
+}
+
+lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, float* ws,
+                           int32_t* status, cudaStream_t st);
+lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);
+lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
+                              float* ws, int32_t* status, cudaStream_t st);
+lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);
+
+}  // namespace lw

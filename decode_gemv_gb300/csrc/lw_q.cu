@@ -1,0 +1,119 @@
+// Launchers for the 4-/6-bit kernels (instantiations of lw_qkern.cuh).
+#include <mutex>
+#include <unordered_map>
+
+#include "lw_internal.h"
+#include "lw_launch.h"
+#include "lw_qkern.cuh"
+
+namespace lw {
+
+namespace {
+
+constexpr int kWarps = 4;
+
+int ncmp_bucket(int span) { return span <= 4 ? 4 : (span <= 7 ? 7 : (span <= 8 ? 8 : 10)); }
+
+using QKernel = void (*)(const dev::QArgs);
+
+template <int FMT, bool TWIN, int BP>
+QKernel pick_product(int ncmp) {
+  if (TWIN) return dev::q_product_kernel<FMT, true, BP, 0, kWarps>;
+  switch (ncmp) {
+    case 4: return dev::q_product_kernel<FMT, false, BP, 4, kWarps>;
+    case 7: return dev::q_product_kernel<FMT, false, BP, 7, kWarps>;
+    case 8: return dev::q_product_kernel<FMT, false, BP, 8, kWarps>;
+    default: return dev::q_product_kernel<FMT, false, BP, 10, kWarps>;
+  }
+}
+
+template <int FMT, bool TWIN>
+QKernel pick_product_b(int bp, int ncmp) {
+  switch (bp) {
+    case 1: return pick_product<FMT, TWIN, 1>(ncmp);
+    case 2: return pick_product<FMT, TWIN, 2>(ncmp);
+    case 4: return pick_product<FMT, TWIN, 4>(ncmp);
+    default: return pick_product<FMT, TWIN, 8>(ncmp);
+  }
+}
+
+template <int FMT, bool TWIN>
+QKernel pick_decode(int ncmp) {
+  if (TWIN) return dev::q_decode_kernel<FMT, true, 0, kWarps>;
+  switch (ncmp) {
+    case 4: return dev::q_decode_kernel<FMT, false, 4, kWarps>;
+    case 7: return dev::q_decode_kernel<FMT, false, 7, kWarps>;
+    case 8: return dev::q_decode_kernel<FMT, false, 8, kWarps>;
+    default: return dev::q_decode_kernel<FMT, false, 10, kWarps>;
+  }
+}
+
+}  // namespace
+
+lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, float* ws,
+                           int32_t* status, cudaStream_t st) {
+  const int fmt = b->fmt;
+  const bool twin = b->twin != 0;
+  const int ncmp = twin ? 0 : ncmp_bucket(b->lmax - b->lmin);
+  const int bp = batch <= 1 ? 1 : (batch <= 2 ? 2 : (batch <= 4 ? 4 : 8));
+  QKernel k;
+  if (fmt == LW_FMT_Q4_PAIR)
+    k = twin ? pick_product_b<dev::kQ4, true>(bp, ncmp) : pick_product_b<dev::kQ4, false>(bp, ncmp);
+  else
+    k = twin ? pick_product_b<dev::kQ6, true>(bp, ncmp) : pick_product_b<dev::kQ6, false>(bp, ncmp);
+  dev::QArgs a{};
+  a.words = b->words;
+  a.tile_off = b->tile_off;
+  a.lane_bits = b->lane_bits;
+  a.table = b->table;
+  a.qparams = static_cast<const uint8_t*>(b->qparams);
+  a.x = x;
+  a.ws = ws;
+  a.status = status;
+  a.TK = (int)(b->cols / 256);
+  a.N = (int)b->rows;
+  a.K = (int)b->cols;
+  a.n_tiles = (int)tiles_of(b->rows, b->cols);
+  a.batch = batch;
+  a.stage_rows = b->max_tile_rows + 2;
+  const int qpb = qparam_tile_bytes(fmt);
+  a.stage_bytes = (a.stage_rows * 128 + qpb + bp * 1024 + 127) / 128 * 128;
+  const size_t smem = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
+  lw_status s = launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
+    k<<<blocks, kWarps * 32, smem, st>>>(a);
+  });
+  if (s != LW_OK) return s;
+  const int bn = batch * a.N;
+  dev::reduce_tiles_kernel<<<(bn + 255) / 256, 256, 0, st>>>(ws, y, a.TK, bn);
+  return check_launch("reduce_tiles_kernel");
+}
+
+lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st) {
+  const int fmt = b->fmt;
+  const bool twin = b->twin != 0;
+  const int ncmp = twin ? 0 : ncmp_bucket(b->lmax - b->lmin);
+  QKernel k;
+  if (fmt == LW_FMT_Q4_PAIR)
+    k = twin ? pick_decode<dev::kQ4, true>(ncmp) : pick_decode<dev::kQ4, false>(ncmp);
+  else
+    k = twin ? pick_decode<dev::kQ6, true>(ncmp) : pick_decode<dev::kQ6, false>(ncmp);
+  dev::QArgs a{};
+  a.words = b->words;
+  a.tile_off = b->tile_off;
+  a.lane_bits = b->lane_bits;
+  a.table = b->table;
+  a.out = static_cast<uint8_t*>(out);
+  a.status = status;
+  a.TK = (int)(b->cols / 256);
+  a.N = (int)b->rows;
+  a.K = (int)b->cols;
+  a.n_tiles = (int)tiles_of(b->rows, b->cols);
+  a.stage_rows = b->max_tile_rows + 2;
+  a.stage_bytes = (a.stage_rows * 128 + 127) / 128 * 128;
+  const size_t smem = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
+  return launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
+    k<<<blocks, kWarps * 32, smem, st>>>(a);
+  });
+}
+
+}  // namespace lw

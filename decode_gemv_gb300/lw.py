@@ -1,0 +1,298 @@
+"""Thin Python binding of liblw (the C ABI in include/lw.h).
+
+Argument marshalling only: every step of the path runs in liblw's host code or
+CUDA kernels.  PyTorch is used for device memory and streams.  If the compiled
+library is missing this module raises at load time -- there is no fallback.
+Functions carry the C names; see include/lw.h for the contract of each.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "liblw.so")
+
+LW_FMT_Q4_PAIR, LW_FMT_Q6, LW_FMT_BF16_EXP = 1, 2, 3
+SECTION_NAMES = ["words", "tile_off", "lane_bits", "table", "qparams", "signman",
+                 "vflags", "vrow_off", "vexp"]
+STATUS_NAMES = {0: "LW_OK", 1: "LW_ERR_INVALID_ARG", 2: "LW_ERR_SHAPE", 3: "LW_ERR_UNSUPPORTED",
+                4: "LW_ERR_ALLOC", 5: "LW_ERR_CORRUPT", 6: "LW_ERR_CUDA"}
+DEV_STATUS = {0: "ok", 1: "lane length", 2: "bad code", 3: "tile size", 4: "timeout",
+              5: "bad table"}
+TABLE_BYTES = 1024
+EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_table_from_lengths",
+            "lw_validate_sections", "lw_workspace_bytes", "lw_decode", "lw_decode_gemv",
+            "lw_decode_gemm", "lw_twin_gemv", "lw_twin_gemm", "lw_status_string",
+            "lw_last_error", "lw_version"]
+
+
+class LwError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}: {_last_error()}")
+
+
+class LwDesc(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("twin", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class LwSections(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p * 9), ("bytes", ctypes.c_uint64 * 9),
+                ("coded_bytes", ctypes.c_uint64), ("n_tiles", ctypes.c_uint64),
+                ("n_verbatim", ctypes.c_int64), ("max_tile_rows", ctypes.c_int32),
+                ("max_len", ctypes.c_int32), ("min_len", ctypes.c_int32),
+                ("palette_size", ctypes.c_int32), ("bits_per_weight", ctypes.c_double)]
+
+
+class LwDevBundle(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("twin", ctypes.c_int32),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("max_tile_rows", ctypes.c_int32), ("lmin", ctypes.c_int32),
+                ("lmax", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("words", ctypes.c_void_p), ("tile_off", ctypes.c_void_p),
+                ("lane_bits", ctypes.c_void_p), ("table", ctypes.c_void_p),
+                ("qparams", ctypes.c_void_p), ("signman", ctypes.c_void_p),
+                ("vflags", ctypes.c_void_p), ("vrow_off", ctypes.c_void_p),
+                ("vexp", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load():
+    """Load liblw.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"liblw is not built ({LIB_PATH} missing): run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "lw_encode_bundle": ([P, P, P, P, P], i32),
+        "lw_bundle_sections": ([P, P], i32),
+        "lw_bundle_free": ([P], None),
+        "lw_table_from_lengths": ([i32, P, i32, P, i32, P], i32),
+        "lw_validate_sections": ([P, P], i32),
+        "lw_workspace_bytes": ([P, i32], sz),
+        "lw_decode": ([P, P, P, P], i32),
+        "lw_decode_gemv": ([P, P, P, P, sz, P, P], i32),
+        "lw_decode_gemm": ([P, P, i32, P, P, sz, P, P], i32),
+        "lw_twin_gemv": ([P, P, P, P, sz, P, P], i32),
+        "lw_twin_gemm": ([P, P, i32, P, P, sz, P, P], i32),
+        "lw_status_string": ([i32], ctypes.c_char_p),
+        "lw_last_error": ([], ctypes.c_char_p),
+        "lw_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _last_error() -> str:
+    try:
+        return load().lw_last_error().decode()
+    except Exception:  # noqa: BLE001
+        return ""
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise LwError(st, what)
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------------------
+# host bundles
+# ----------------------------------------------------------------------------
+
+@dataclass
+class BundleStats:
+    coded_bytes: int
+    n_tiles: int
+    n_verbatim: int
+    max_tile_rows: int
+    max_len: int
+    min_len: int
+    palette_size: int
+    bits_per_weight: float
+
+
+class HostBundle:
+    """Owns an lw_bundle*; `sections` are numpy copies of its sections."""
+
+    def __init__(self, handle, desc: LwDesc):
+        self._h = handle
+        self.desc = desc
+        s = LwSections()
+        _check(load().lw_bundle_sections(self._h, ctypes.byref(s)), "lw_bundle_sections")
+        self.stats = BundleStats(int(s.coded_bytes), int(s.n_tiles), int(s.n_verbatim),
+                                 int(s.max_tile_rows), int(s.max_len), int(s.min_len),
+                                 int(s.palette_size), float(s.bits_per_weight))
+        self.sections = {}
+        for i, name in enumerate(SECTION_NAMES):
+            n = int(s.bytes[i])
+            if n:
+                buf = (ctypes.c_uint8 * n).from_address(s.ptr[i])
+                self.sections[name] = np.frombuffer(buf, dtype=np.uint8).copy()
+        self._raw = s
+
+    @property
+    def fmt(self):
+        return self.desc.fmt
+
+    @property
+    def twin(self):
+        return bool(self.desc.twin)
+
+    def view(self, name, dtype):
+        return self.sections[name].view(dtype)
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.lw_bundle_free(self._h)
+            self._h = None
+
+
+def lw_encode_bundle(fmt: int, payload: np.ndarray, scales=None, mins=None,
+                     twin: bool = False) -> HostBundle:
+    """payload: uint8 codes [N][K] or uint16 bf16 bits [N][K]."""
+    payload = np.ascontiguousarray(payload)
+    n, k = payload.shape
+    desc = LwDesc(fmt, int(twin), n, k)
+    sc = None if scales is None else np.ascontiguousarray(scales, dtype=np.uint16)
+    mn = None if mins is None else np.ascontiguousarray(mins, dtype=np.uint16)
+    h = ctypes.c_void_p()
+    _check(load().lw_encode_bundle(ctypes.byref(desc), _np_ptr(payload), _np_ptr(sc),
+                                   _np_ptr(mn), ctypes.byref(h)), "lw_encode_bundle")
+    return HostBundle(h, desc)
+
+
+def lw_table_from_lengths(fmt: int, code_len, palette=None) -> np.ndarray:
+    cl = np.ascontiguousarray(code_len, dtype=np.uint8)
+    pal = None if palette is None else np.ascontiguousarray(palette, dtype=np.uint8)
+    out = np.zeros(TABLE_BYTES, dtype=np.uint8)
+    _check(load().lw_table_from_lengths(fmt, _np_ptr(cl), len(cl), _np_ptr(pal),
+                                        0 if pal is None else len(pal), _np_ptr(out)),
+           "lw_table_from_lengths")
+    return out
+
+
+def table_fields(table: np.ndarray) -> dict:
+    """Decode the documented lw_table layout (for tests and reports)."""
+    t = np.asarray(table, dtype=np.uint8)
+    i32 = t[:32].view(np.int32)
+    return dict(fmt=int(i32[0]), alpha=int(i32[1]), n_sym=int(i32[2]), lmin=int(i32[3]),
+                lmax=int(i32[4]), n_palette=int(i32[5]), phantom=int(i32[6]),
+                lim_m1=t[32:80].view(np.uint32).copy(), off=t[80:128].view(np.int32).copy(),
+                sym=t[128:640].view(np.uint16).copy(), code_len=t[640:896].copy(),
+                palette=t[896:912].copy())
+
+
+def lw_validate_sections(fmt: int, rows: int, cols: int, sections: dict, max_tile_rows: int,
+                         twin: bool = False) -> None:
+    desc = LwDesc(fmt, int(twin), rows, cols)
+    s = LwSections()
+    keep = []
+    for i, name in enumerate(SECTION_NAMES):
+        a = sections.get(name)
+        if a is not None and a.size:
+            a = np.ascontiguousarray(a).view(np.uint8)
+            keep.append(a)
+            s.ptr[i] = a.ctypes.data
+            s.bytes[i] = a.nbytes
+    s.max_tile_rows = max_tile_rows
+    _check(load().lw_validate_sections(ctypes.byref(desc), ctypes.byref(s)),
+           "lw_validate_sections")
+
+
+# ----------------------------------------------------------------------------
+# device bundles (caller-owned device memory: torch tensors)
+# ----------------------------------------------------------------------------
+
+class DeviceBundle:
+    """Byte-for-byte device copies of a bundle's sections plus the
+    lw_dev_bundle view that the C calls take."""
+
+    def __init__(self, fmt, twin, rows, cols, sections: dict, max_tile_rows, lmin, lmax,
+                 device="cuda", coded_bytes=None):
+        import torch
+        self.fmt, self.twin, self.rows, self.cols = fmt, bool(twin), rows, cols
+        self.tensors = {}
+        for name in SECTION_NAMES:
+            a = sections.get(name)
+            if a is not None and a.size:
+                host = torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).copy())
+                self.tensors[name] = host.to(device)
+        self.coded_bytes = int(coded_bytes if coded_bytes is not None else
+                               sum(t.numel() for t in self.tensors.values()))
+        v = LwDevBundle()
+        v.fmt, v.twin, v.rows, v.cols = fmt, int(twin), rows, cols
+        v.max_tile_rows, v.lmin, v.lmax = max_tile_rows, lmin, lmax
+        for name in SECTION_NAMES:
+            t = self.tensors.get(name)
+            setattr(v, name, t.data_ptr() if t is not None else None)
+        self.view = v
+
+    @classmethod
+    def upload(cls, hb: HostBundle, device="cuda"):
+        return cls(hb.desc.fmt, hb.desc.twin, hb.desc.rows, hb.desc.cols, hb.sections,
+                   hb.stats.max_tile_rows, hb.stats.min_len, hb.stats.max_len, device,
+                   hb.stats.coded_bytes)
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.view)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _tp(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def lw_workspace_bytes(db: DeviceBundle, batch: int = 1) -> int:
+    return int(load().lw_workspace_bytes(db.ref, batch))
+
+
+def lw_decode(db: DeviceBundle, out, d_status, stream=None) -> None:
+    _check(load().lw_decode(db.ref, _tp(out), _tp(d_status), _stream_ptr(stream)), "lw_decode")
+
+
+def lw_decode_gemv(db: DeviceBundle, x, y, ws, d_status, stream=None) -> None:
+    _check(load().lw_decode_gemv(db.ref, _tp(x), _tp(y), _tp(ws), ws.numel() * ws.element_size(),
+                                 _tp(d_status), _stream_ptr(stream)), "lw_decode_gemv")
+
+
+def lw_decode_gemm(db: DeviceBundle, X, batch, Y, ws, d_status, stream=None) -> None:
+    _check(load().lw_decode_gemm(db.ref, _tp(X), batch, _tp(Y), _tp(ws),
+                                 ws.numel() * ws.element_size(), _tp(d_status),
+                                 _stream_ptr(stream)), "lw_decode_gemm")
+
+
+def lw_twin_gemv(db: DeviceBundle, x, y, ws, d_status, stream=None) -> None:
+    _check(load().lw_twin_gemv(db.ref, _tp(x), _tp(y), _tp(ws), ws.numel() * ws.element_size(),
+                               _tp(d_status), _stream_ptr(stream)), "lw_twin_gemv")
+
+
+def lw_twin_gemm(db: DeviceBundle, X, batch, Y, ws, d_status, stream=None) -> None:
+    _check(load().lw_twin_gemm(db.ref, _tp(X), batch, _tp(Y), _tp(ws),
+                               ws.numel() * ws.element_size(), _tp(d_status),
+                               _stream_ptr(stream)), "lw_twin_gemm")

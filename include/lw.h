@@ -1,0 +1,310 @@
+/*
+ * lw.h -- C ABI of liblw: LLM weights kept losslessly entropy-coded in HBM and
+ * decoded on demand inside the batch-1 / small-batch matrix products of token
+ * generation, so that HBM moves only coded bytes.
+ *
+ * Sources (page title, then section / figure / equation):
+ *  [LW]  "LazyWeights: Decode-on-Demand Edge LLMs" -- TL;DR and Fig. 1 (codes
+ *        decoded on demand so DRAM moves only coded bytes); "2 . Code them"
+ *        and Fig. 3(a) (one 11-bit length-limited Huffman table per matrix,
+ *        4-bit codes coded in pairs, a 64x256 tile = 32 lanes of two rows,
+ *        lanes' 32-bit words interleaved, per-tile lane offsets, scales and
+ *        minimums kept as stored); "3 . Decode on demand" and Fig. 3(b)
+ *        (11-bit peek compared with per-length limits, plus the length's
+ *        offset into a symbol table; no 2048-entry table); the runtime
+ *        paragraph after Fig. 3 (software decode fused with GEMV, and the
+ *        decode-free fixed-width "twin").
+ *  [UW]  "Unweight: Compressing LLM Weights for Faster Inference" --
+ *        "Understanding BF16 weight structure" (sign 1 / exponent 8 /
+ *        mantissa 7), "The exponent's exploitable redundancy" (Huffman on the
+ *        exponent byte over a top-16 palette, sign+mantissa raw, a row of 64
+ *        with an out-of-palette exponent stored verbatim), "Four approaches
+ *        to using compressed weights" and "How reconstructive matmul works"
+ *        (full decode vs. reconstruction in shared memory feeding tensor
+ *        cores).
+ *  [SDB] "Software-Defined Bandwidth Expansion" -- eq. (1) (dense-equivalent
+ *        effective bandwidth), section IV.A (b + 16/G storage cost).
+ *
+ * Shapes.  W is N x K (rows = outputs, as nn.Linear.weight); y = W x.  Every
+ * call requires N % 64 == 0 and K % 256 == 0 (else LW_ERR_SHAPE).  Tile t =
+ * (r/64) * (K/256) + (k/256) covers 64 rows x 256 columns.  Lane l of a tile
+ * carries rows 2l and 2l+1 (row 2l first), columns ascending.
+ *
+ * Ownership.  Host bundles (lw_bundle) belong to the library: free them with
+ * lw_bundle_free.  Device memory and streams belong to the caller: the
+ * library never allocates or frees device memory and never synchronises a
+ * stream.  Device calls are asynchronous on `stream` (a cudaStream_t passed
+ * as void*; NULL = the legacy default stream) and deterministic: a fixed
+ * reduction order, no floating-point atomics.
+ *
+ * Errors.  Argument, shape and format checks run on the host before any
+ * launch and return a status; a failed launch returns LW_ERR_CUDA.  A kernel
+ * that finds a corrupt stream never traps and never reads outside its tile:
+ * it writes a nonzero LW_DEV_* code into *d_status (first writer wins) and
+ * finishes.  The caller zeroes *d_status before the call and reads it after
+ * synchronising.  lw_last_error() returns a thread-local text for the last
+ * failing host call.
+ */
+#ifndef LW_H_
+#define LW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LW_OK = 0,
+  LW_ERR_INVALID_ARG = 1,
+  LW_ERR_SHAPE = 2,
+  LW_ERR_UNSUPPORTED = 3,
+  LW_ERR_ALLOC = 4,       /* host allocation failed */
+  LW_ERR_CORRUPT = 5,     /* malformed bundle or table detected on the host */
+  LW_ERR_CUDA = 6         /* launch or CUDA runtime error */
+} lw_status;
+
+/* device-side error codes written to *d_status */
+enum {
+  LW_DEV_OK = 0,
+  LW_DEV_LANE_LENGTH = 1,   /* a lane ended at a bit count other than lane_bits */
+  LW_DEV_BAD_CODE = 2,      /* a peek matched no codeword (incomplete table) */
+  LW_DEV_TILE_SIZE = 3,     /* a tile is longer than max_tile_rows */
+  LW_DEV_TIMEOUT = 4,       /* a bounded wait on an asynchronous copy ran out */
+  LW_DEV_BAD_TABLE = 5      /* the device table fails its in-kernel checks, or
+                               its length span exceeds what the launch expects */
+};
+
+typedef enum {
+  LW_FMT_Q4_PAIR = 1,  /* 4-bit codes, coded in pairs (8-bit symbols) [LW] */
+  LW_FMT_Q6 = 2,       /* 6-bit codes, one symbol each (Q6_K-like)      [LW] */
+  LW_FMT_BF16_EXP = 3  /* BF16: exponent byte coded over a top-16 palette [UW] */
+} lw_format;
+
+#define LW_MAX_CODE_LEN 11
+
+/* What to build.  twin = 1 builds the decode-free fixed-width "twin" of the
+   same tiles, lanes and interleave [LW]: 4-bit codes at 4 bits, 6-bit codes at
+   6 bits, BF16 exponents as a 4-bit palette index ([UW] "direct palette"). */
+typedef struct {
+  int32_t fmt;    /* lw_format */
+  int32_t twin;   /* 0: Huffman-coded, 1: fixed-width twin */
+  int64_t rows;   /* N, multiple of 64 */
+  int64_t cols;   /* K, multiple of 256 */
+} lw_desc;
+
+/*
+ * Decoder table, one per matrix (device-ready, 1024 bytes, byte-copyable).
+ * Canonical code: lengths come from code_len; codes are assigned shortest
+ * first, ties by ascending symbol value (the RFC 1951 section 3.2.2 rule).
+ * The comparator rule [LW "3 . Decode on demand"]: for a 32-bit window whose
+ * first stream bit is the MSB, L = lmin + #{ j < lmax - lmin :
+ * window > lim_m1[j] }, where lim_m1[j] = (limit(lmin+j) << 21) - 1 and
+ * limit(L) = (first_code(L) + count(L)) << (11 - L); then the symbol is
+ * sym[(window >> (32 - L)) + off[L - lmin]].
+ */
+typedef struct {
+  int32_t fmt;
+  int32_t alpha;          /* 256 (Q4 pairs), 64 (Q6), 16 (BF16 palette idx) */
+  int32_t n_sym;          /* symbols that have a code */
+  int32_t lmin, lmax;     /* shortest and longest code length */
+  int32_t n_palette;      /* BF16 only: entries of palette[] in use */
+  int32_t phantom;        /* 1 if the table was completed with a phantom code
+                             (a lone symbol of length 1) */
+  int32_t reserved0;
+  uint32_t lim_m1[12];    /* see above; unused entries 0xFFFFFFFF */
+  int32_t off[12];        /* base(L) - first_code(L), index L - lmin */
+  uint16_t sym[256];      /* symbols in canonical order (+ phantom) */
+  uint8_t code_len[256];  /* code length per symbol, 0 = no code */
+  uint8_t palette[16];    /* BF16: exponent byte of each palette index,
+                             ascending */
+  uint8_t reserved1[112];
+} lw_table;
+
+/* Opaque host bundle. */
+typedef struct lw_bundle lw_bundle;
+
+/* Sections of a bundle, in the order of lw_sections.ptr[] */
+enum {
+  LW_SEC_WORDS = 0,   /* uint32: coded (or fixed-width) lane words.  Word j of
+                         lane l of tile t is words[(tile_off[t] + j)*32 + l]:
+                         one aligned 128-byte row holds the next word of every
+                         lane [LW Fig. 3(a)].  Codes MSB-first: stream bit p
+                         is bit 31 - p%32 of word p/32.  Lanes are zero-padded
+                         to the tile's longest lane (W_t words). */
+  LW_SEC_TILE_OFF,    /* uint32 [n_tiles + 1]: start of each tile's words in
+                         128-byte rows (prefix sum of W_t) -- the per-tile
+                         offsets that let any tile start on its own. */
+  LW_SEC_LANE_BITS,   /* uint16 [n_tiles][32]: bits in each lane (checked at
+                         the end of every lane). */
+  LW_SEC_TABLE,       /* lw_table (1024 bytes). */
+  LW_SEC_QPARAMS,     /* Q4: per tile, per row of the tile (64), the fp16
+                         scale then the fp16 min of the row's 256-weight
+                         super-block: [n_tiles][64][2] uint16.
+                         Q6: per tile, per 16-byte chunk q (0..3), per lane
+                         l: 8 fp16 scales; lane l's 32 scales (row 2l groups
+                         0..15, then row 2l+1) are chunks 0..3:
+                         [n_tiles][4][32][8] uint16.  BF16: empty. */
+  LW_SEC_SIGNMAN,     /* BF16: sign+mantissa bytes, sm = sign<<7 | mantissa,
+                         every weight.  Tile-major, 16-byte chunks
+                         interleaved over lanes: byte q (0..511) of lane l of
+                         tile t is at t*16384 + ((q/16)*32 + l)*16 + q%16;
+                         a lane's bytes follow its lane order. */
+  LW_SEC_VFLAGS,      /* BF16: uint32 [N][GW], GW = ceil(K/64/32): bit g%32
+                         of word g/32 of row r is set iff the 64-column group
+                         g of row r is stored verbatim. */
+  LW_SEC_VROW_OFF,    /* BF16: uint32 [N + 1]: verbatim groups before row r. */
+  LW_SEC_VEXP,        /* BF16: uint8 [n_verbatim][64]: raw exponent bytes of
+                         each verbatim group, ordered by row, then group. */
+  LW_NUM_SECTIONS
+};
+
+typedef struct {
+  const void* ptr[LW_NUM_SECTIONS];   /* host pointers, owned by the bundle */
+  uint64_t bytes[LW_NUM_SECTIONS];    /* 0 = section absent */
+  uint64_t coded_bytes;     /* all sections a product reads (its HBM bytes,
+                               activations and outputs excluded) */
+  uint64_t n_tiles;
+  int64_t n_verbatim;       /* BF16 verbatim groups */
+  int32_t max_tile_rows;    /* max W_t over the tiles */
+  int32_t max_len;          /* longest code length (lmax) */
+  int32_t min_len;          /* shortest code length (lmin) */
+  int32_t palette_size;     /* BF16 */
+  double bits_per_weight;   /* 8 * coded_bytes / (N*K) */
+} lw_sections;
+
+/*
+ * Device view of an uploaded bundle: raw device pointers into caller-owned
+ * buffers holding byte-for-byte copies of the host sections (NULL where a
+ * section is absent).  Filled by the caller; the library only reads it on the
+ * host at call time.
+ */
+typedef struct {
+  int32_t fmt;
+  int32_t twin;
+  int64_t rows;
+  int64_t cols;
+  int32_t max_tile_rows;    /* from lw_sections; bounds shared-memory staging */
+  int32_t lmin, lmax;       /* from lw_sections: code-length span of the table
+                               (selects the kernel variant; checked on device) */
+  int32_t reserved;
+  const uint32_t* words;
+  const uint32_t* tile_off;
+  const uint16_t* lane_bits;
+  const lw_table* table;
+  const void* qparams;
+  const uint8_t* signman;
+  const uint32_t* vflags;
+  const uint32_t* vrow_off;
+  const uint8_t* vexp;
+} lw_dev_bundle;
+
+/*
+ * Build a bundle on the host [LW "2 . Code them"; UW "The exponent's
+ * exploitable redundancy"].
+ *  payload: Q4 / Q6: uint8 codes [N][K] (values < 16 / < 64);
+ *           BF16: uint16 bf16 bit patterns [N][K].
+ *  scales:  Q4: fp16 bits [N][K/256]; Q6: fp16 bits [N][K/16]; BF16: NULL.
+ *  mins:    Q4: fp16 bits [N][K/256]; otherwise NULL.
+ * One length-limited (<= 11 bits) optimal Huffman table per matrix over the
+ * symbols actually coded.  On success *out owns copies of everything.
+ * Errors: LW_ERR_INVALID_ARG (NULL pointers, code values out of range),
+ * LW_ERR_SHAPE, LW_ERR_UNSUPPORTED (fmt), LW_ERR_ALLOC.
+ */
+lw_status lw_encode_bundle(const lw_desc* desc, const void* payload,
+                           const uint16_t* scales, const uint16_t* mins,
+                           lw_bundle** out);
+
+/* Section pointers and sizes of a bundle (valid until lw_bundle_free). */
+lw_status lw_bundle_sections(const lw_bundle* b, lw_sections* out);
+
+void lw_bundle_free(lw_bundle* b);
+
+/*
+ * Fill an lw_table from per-symbol code lengths (for bundles built or stored
+ * elsewhere).  code_len[alpha]: lengths 0..11.  palette: BF16 exponent bytes
+ * (n_palette <= 16, ascending), NULL otherwise.  The code must be complete
+ * (Kraft sum exactly 1) unless a single symbol has a code, which gets a
+ * phantom partner.  Errors: LW_ERR_CORRUPT (length > 11, over- or
+ * under-full code), LW_ERR_INVALID_ARG.
+ */
+lw_status lw_table_from_lengths(int32_t fmt, const uint8_t* code_len,
+                                int32_t alpha, const uint8_t* palette,
+                                int32_t n_palette, lw_table* out);
+
+/*
+ * Check the host sections of a coded bundle for consistency (tile offsets
+ * non-decreasing and within the word count, lane bit counts within W_t*32,
+ * table well formed, BF16 verbatim offsets consistent).  Returns LW_OK or
+ * LW_ERR_CORRUPT with the reason in lw_last_error().
+ */
+lw_status lw_validate_sections(const lw_desc* desc, const lw_sections* s);
+
+/* Device workspace the product calls need for `batch` activation rows: the
+   per-tile partial sums, fp32 [K/256][batch][N].  0 for lw_decode. */
+size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch);
+
+/*
+ * Decode only: restore the fixed-width weights into `out` (device)
+ * [LW "3 . Decode on demand"; UW "Four approaches": full decode].
+ *  Q4: packed bytes [N][K/2], low nibble = even column (the pair symbol);
+ *  Q6: uint8 [N][K];  BF16: uint16 bf16 bits [N][K].
+ * Works on coded bundles and on twins.
+ */
+lw_status lw_decode(const lw_dev_bundle* b, void* out, int32_t* d_status,
+                    void* stream);
+
+/*
+ * Fused decode + matrix-vector product, batch 1: y[r] = sum_k W[r][k] x[k]
+ * [LW runtime paragraph: software decode fused with GEMV; UW "How
+ * reconstructive matmul works"].  x: fp32 [K] (Q4, Q6) or bf16 [K] (BF16);
+ * y: fp32 [N].  ws: device workspace of at least lw_workspace_bytes(b, 1).
+ * Dequantisation: Q4 w = scale*c + min per 256-weight super-block; Q6 w =
+ * scale*(c - 32) per 16 weights; BF16 the value itself.
+ * Reduction order (fixed): within a lane and row, two fp32 accumulators
+ * (even, odd column) over the tile's columns ascending; Q4 folds the
+ * super-block scale and min once per tile row; Q6 folds each 16-weight group
+ * into the row sum as it ends; the per-tile partial sums of a row are added
+ * in ascending tile order.
+ */
+lw_status lw_decode_gemv(const lw_dev_bundle* b, const void* x, float* y,
+                         void* ws, size_t ws_bytes, int32_t* d_status,
+                         void* stream);
+
+/*
+ * Fused decode + small-batch product: Y[b][r] = sum_k W[r][k] X[b][k],
+ * X [batch][K] row-major (fp32, or bf16 for BF16), Y fp32 [batch][N].
+ * Same order as lw_decode_gemv per activation row.  batch 1..64; the BF16
+ * format uses tensor cores (tcgen05, BF16 x BF16 -> FP32) for batch >= 16.
+ */
+lw_status lw_decode_gemm(const lw_dev_bundle* b, const void* X, int32_t batch,
+                         float* Y, void* ws, size_t ws_bytes,
+                         int32_t* d_status, void* stream);
+
+/*
+ * The decode-free fixed-width twin [LW: its measured time stands in for the
+ * decode unit's]: same product, same order, read from a twin bundle
+ * (desc.twin = 1).  Same arguments as lw_decode_gemv.
+ */
+lw_status lw_twin_gemv(const lw_dev_bundle* twin, const void* x, float* y,
+                       void* ws, size_t ws_bytes, int32_t* d_status,
+                       void* stream);
+
+/* Twin product for a batch of activation rows (same contract as
+   lw_decode_gemm). */
+lw_status lw_twin_gemm(const lw_dev_bundle* twin, const void* X, int32_t batch,
+                       float* Y, void* ws, size_t ws_bytes, int32_t* d_status,
+                       void* stream);
+
+const char* lw_status_string(lw_status s);
+const char* lw_last_error(void);
+
+/* Library version, for the bundle file header and for checks. */
+int32_t lw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LW_H_ */
