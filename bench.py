@@ -1,0 +1,430 @@
+"""Benchmark: fused decode + GEMV over entropy-coded weights on one GB300.
+
+Step = one pass of the hot path over one batch: fused decode + GEMV (batch 1)
+of every matrix of one Mistral-7B-shaped layer of 4-bit codes (q, k, v, o,
+gate, up, down; one Huffman table per matrix), through the C ABI.  Metric:
+coded bytes read per step / step time (GB/s), reported against the measured
+HBM copy bandwidth; also the dense-equivalent effective bandwidth (2 bytes
+per weight / time, "Software-Defined Bandwidth Expansion" eq. (1)), and the
+same step on the fixed-width twin and on an uncompressed BF16 GEMV (cuBLAS).
+
+The layer's coded bytes (~80 MB) fit in L2, so every step reads a different
+device copy of the layer, rotating over enough copies to exceed 4x L2.
+
+`--impl reference` times the CPU oracle instead (decode + dequant + fp64 GEMV
+on a bounded sample of the same workload, single-threaded on the host).
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused decode+GEMV coded GB/s vs HBM peak; dense-equiv eff. bandwidth, batch 1"
+WORKLOAD = "mistral7b_layer_q4_batch1"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--only", default="", help="comma list of matrix names (profiling)")
+    p.add_argument("--copies", type=int, default=0, help="layer copies to rotate (0 = auto)")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip twin / bf16 / cpu baseline / e2e legs (profiling)")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:  # noqa: BLE001
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _one(self):
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                  "--format=csv,noheader,nounits"], capture_output=True,
+                                 text=True, timeout=5).stdout.strip()
+            if out:
+                self.rows.append([c.strip() for c in out.split(",")])
+        except Exception:  # noqa: BLE001
+            pass
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._one()
+            self._stop.wait(0.05)
+
+    def start(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+        if not self.rows:
+            self._one()
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (cpu_baseline and --impl reference)
+# ----------------------------------------------------------------------------
+
+def layer_matrices():
+    from decode_gemv_gb300 import inputs
+    out = []
+    for i, s in enumerate(inputs.workload_specs(inputs.MISTRAL_LAYER)):
+        out.append((s, inputs.make_matrix(inputs.MISTRAL_LAYER, s, 0, i)))
+    return out
+
+
+def oracle_sample_setup(mats, target_weights: int):
+    """Sample = the first row strips of every matrix of the layer, about
+    `target_weights` weights in all, coded by the oracle's own encoder."""
+    import oracle
+    per = max(1, target_weights // len(mats))
+    jobs = []
+    for s, m in mats:
+        rows = max(64, min(s.rows, (per // s.cols) // 64 * 64))
+        sub = dict(codes=m["codes"][:rows], scales=m["scales"][:rows], mins=m["mins"][:rows],
+                   x=m["x"])
+        ob = oracle.encode(oracle.Q4, sub["codes"])
+        coded = (ob["words"].nbytes + ob["tile_off"].nbytes + ob["lane_bits"].nbytes + 1024
+                 + sub["scales"].nbytes + sub["mins"].nbytes + sub["x"].nbytes)
+        jobs.append((rows, s.cols, ob, sub, coded))
+    return jobs
+
+
+def oracle_sample_step(jobs):
+    """One oracle pass: decode every lane, dequantise, fp64 GEMV."""
+    import oracle
+    out = []
+    for rows, cols, ob, sub, _ in jobs:
+        packed = oracle.decode(oracle.Q4, rows, cols, ob["code_len"], ob["words"], ob["tile_off"])
+        w = oracle.dequant_q4(oracle.unpack_q4(packed), sub["scales"], sub["mins"])
+        out.append(oracle.gemm(w, sub["x"]))
+    return out
+
+
+def oracle_rate(mats):
+    """Weights per second of one oracle pass on a small sample (calibration)."""
+    jobs = oracle_sample_setup(mats, 1_000_000)
+    w = sum(j[0] * j[1] for j in jobs)
+    t0 = time.perf_counter()
+    oracle_sample_step(jobs)
+    return w / (time.perf_counter() - t0)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    mats = layer_matrices()
+    # size each step so that warm-up + timed steps take about 90 s of CPU time
+    rate = oracle_rate(mats)
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    target = int(min(30_000_000, max(64 * 4096 * 7, rate * per_step)))
+    jobs = oracle_sample_setup(mats, target)
+    coded = sum(j[4] for j in jobs)
+    weights = sum(j[0] * j[1] for j in jobs)
+    for _ in range(max(0, args.warmup)):
+        oracle_sample_step(jobs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(jobs)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    gbs = coded / dt / 1e9
+    sample = (f"first row strips of all 7 matrices of the layer: {weights} weights, "
+              f"{coded} coded bytes per step; decode + dequant + fp64 GEMV")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_weights": weights},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def build_layer(names):
+    from decode_gemv_gb300 import lw
+    mats = []
+    for s, m in layer_matrices():
+        if names and s.name not in names:
+            continue
+        hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"])
+        tw = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"], twin=True)
+        mats.append(dict(spec=s, m=m, hb=hb, tw=tw))
+    return mats
+
+
+def dequant_bf16(m):
+    import torch
+    s = np.repeat(m["scales"].view(np.float16).astype(np.float32), 256, axis=1)
+    mi = np.repeat(m["mins"].view(np.float16).astype(np.float32), 256, axis=1)
+    w = torch.from_numpy(s * m["codes"].astype(np.float32) + mi)
+    return w.to(torch.bfloat16)
+
+
+def time_steps(torch, stream, step_fn, steps, warmup, copies):
+    for i in range(warmup):
+        step_fn(i % copies)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step_fn(i % copies)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / steps
+
+
+def run_ours(args):
+    import torch
+    from decode_gemv_gb300 import lw
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lw.load()
+    names = [n for n in args.only.split(",") if n]
+    mats = build_layer(names)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    layer_coded = sum(x["hb"].stats.coded_bytes for x in mats)
+    copies = args.copies or max(2, math.ceil(4 * l2 / layer_coded))
+    # device copies of the layer (distinct addresses), activations, outputs
+    dbs = [[lw.DeviceBundle.upload(x["hb"], dev) for x in mats] for _ in range(copies)]
+    xs = [torch.from_numpy(x["m"]["x"][0]).to(dev) for x in mats]
+    ys = [torch.empty(x["spec"].rows, dtype=torch.float32, device=dev) for x in mats]
+    wsb = max(lw.lw_workspace_bytes(d, 1) for d in dbs[0])
+    ws = torch.empty(wsb // 4 + 64, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    x_bytes = sum(t.numel() * 4 for t in xs)
+    coded_step = layer_coded + x_bytes          # every byte the step must read
+    weights = sum(x["spec"].rows * x["spec"].cols for x in mats)
+
+    def step(c):
+        for d, x, y in zip(dbs[c], xs, ys):
+            lw.lw_decode_gemv(d, x, y, ws, st, stream)
+
+    # per-call durations inside the timed region (events on the launching stream)
+    n_mat = len(mats)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_mat + 1)] for _ in range(8)]
+    if world > 1:
+        torch.distributed.barrier()
+    for i in range(args.warmup):
+        step(i % copies)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    probe = []
+    for i in range(args.steps):
+        c = i % copies
+        if i % max(1, args.steps // 8) == 0 and len(probe) < 8:
+            e = evs[len(probe)]
+            for j, (d, x, y) in enumerate(zip(dbs[c], xs, ys)):
+                e[j].record(stream)
+                lw.lw_decode_gemv(d, x, y, ws, st, stream)
+            e[n_mat].record(stream)
+            probe.append(e)
+        else:
+            step(c)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    t_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(t.item())
+    status = int(st.item())
+    # per-matrix call durations from the probe steps
+    per_mat = np.zeros(n_mat)
+    for e in probe:
+        for j in range(n_mat):
+            per_mat[j] += e[j].elapsed_time(e[j + 1])
+    per_mat /= max(1, len(probe))
+
+    value = coded_step * world / (t_max * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    launches_per_step = 2 * n_mat        # fused kernel + ordered reduction per matrix
+    # dominant kernel: the fused decode+GEMV call, algorithmic bytes per launch
+    mean_call_ms = float(per_mat.mean())
+    mean_call_bytes = coded_step / n_mat
+    achieved = mean_call_bytes / (mean_call_ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "matrices": [x["spec"].name for x in mats],
+                       "weights": weights, "coded_bytes_per_step": coded_step,
+                       "bits_per_weight": 8 * layer_coded / weights, "batch": 1,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": f"rotate {copies} device copies of the layer "
+                             f"({copies * layer_coded / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)"},
+            "b_eff_gbs": 2.0 * weights * world / (t_max * 1e-3) / 1e9,
+            "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_kind": peak_kind,
+                         "kernel": "fused decode+GEMV call (q_product_kernel + ordered reduction)",
+                         "per_matrix_ms": {x["spec"].name: float(v) for x, v in zip(mats, per_mat)}},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks, "device_status": status}
+    if rank == 0 and not args.no_extras:
+        extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, coded_step,
+               weights, t_max)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, coded_step,
+           weights, t_ours):
+    """Comparators and the end-to-end leg (outside the timed region above)."""
+    steps = max(10, min(args.steps, 400))
+    # fixed-width twin, same rotation
+    twins = [[lw.DeviceBundle.upload(x["tw"], dev) for x in mats]
+             for _ in range(max(2, math.ceil(copies * 0.75)))]
+    nt = len(twins)
+
+    def tstep(c):
+        for d, x, y in zip(twins[c], xs, ys):
+            lw.lw_twin_gemv(d, x, y, ws, st, stream)
+    t_twin = time_steps(torch, stream, tstep, steps, 5, nt)
+    del twins
+    # uncompressed BF16 GEMV (cuBLAS) on the dequantised weights
+    wb = [dequant_bf16(x["m"]).to(dev) for x in mats]
+    xb = [x.to(torch.bfloat16) for x in xs]
+
+    def bstep(c):
+        for w, x in zip(wb, xb):
+            torch.mv(w, x)
+    t_bf16 = time_steps(torch, stream, bstep, steps, 5, 1)
+    del wb
+    line["twin"] = {"ms_per_step": t_twin, "speedup_of_coded": t_twin / t_ours}
+    line["bf16_dense"] = {"ms_per_step": t_bf16, "speedup_of_coded": t_bf16 / t_ours,
+                          "kind": "torch.mv on bf16 weights (cuBLAS)"}
+    # end to end through the public API: pinned host activations in, results out
+    hx = [x.cpu().pin_memory() for x in xs]
+    hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in ys]
+    dbs = [lw.DeviceBundle.upload(x["hb"], dev) for x in mats]
+    for i in range(3):
+        for d, h, x, y, o in zip(dbs, hx, xs, ys, hy):
+            x.copy_(h, non_blocking=True)
+            lw.lw_decode_gemv(d, x, y, ws, st, stream)
+            o.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+    e_steps = max(10, min(args.steps, 200))
+    t0 = time.perf_counter()
+    for i in range(e_steps):
+        for d, h, x, y, o in zip(dbs, hx, xs, ys, hy):
+            x.copy_(h, non_blocking=True)
+            lw.lw_decode_gemv(d, x, y, ws, st, stream)
+            o.copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+        _ = float(hy[0][0])
+    dt = (time.perf_counter() - t0) / e_steps
+    line["e2e"] = {"value": coded_step / dt / 1e9, "unit": "GB/s",
+                   "h2d_bytes_per_step": int(sum(h.numel() * 4 for h in hx)),
+                   "d2h_bytes_per_step": int(sum(o.numel() * 4 for o in hy)),
+                   "ms_per_step": dt * 1e3,
+                   "note": "one layer copy (L2-warm weights), wall clock incl. H2D/D2H and sync"}
+    # the oracle on the host, bounded sample (about 10-20 s of CPU work)
+    pairs = [(x["spec"], x["m"]) for x in mats]
+    rate = oracle_rate(pairs)
+    jobs = oracle_sample_setup(pairs, int(min(30_000_000, rate * 5.0)))
+    coded = sum(j[4] for j in jobs)
+    wts = sum(j[0] * j[1] for j in jobs)
+    reps = 2
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_sample_step(jobs)
+    dt = (time.perf_counter() - t0) / reps
+    line["cpu_baseline"] = {"value": coded / dt / 1e9, "unit": "GB/s", "cores": 1,
+                            "kind": "oracle",
+                            "sample": f"first row strips of every matrix of the layer: {wts} "
+                                      f"weights, {coded} coded bytes; decode + dequant + fp64 "
+                                      f"GEMV, {reps} timed passes"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -24,25 +24,32 @@ int device_sm_count() {
 
 int resident_blocks(const void* kernel, int threads, size_t smem) {
   static std::mutex mu;
-  static std::unordered_map<uint64_t, int> cache;
+  static std::unordered_map<uint64_t, int> occ;           // (kernel, smem, device) -> blocks
+  static std::unordered_map<uint64_t, size_t> smem_set;   // (kernel, device) -> limit set
   int d = 0;
   cudaGetDevice(&d);
-  const uint64_t key = (reinterpret_cast<uint64_t>(kernel) * 1315423911ull) ^ (smem << 8) ^ (uint64_t)d;
+  const uint64_t kd = (reinterpret_cast<uint64_t>(kernel) << 7) ^ (uint64_t)d;
+  const uint64_t key = kd * 1315423911ull ^ (uint64_t)smem;
   std::lock_guard<std::mutex> g(mu);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-    cudaGetLastError();
-    cache[key] = 0;
-    return 0;
+  // the dynamic shared-memory limit of a kernel only ever grows, so a cached
+  // occupancy answer stays valid for every size at or below it
+  size_t& cur = smem_set[kd];
+  if (smem > 48 * 1024 && smem > cur) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cur = smem;
   }
+  auto it = occ.find(key);
+  if (it != occ.end()) return it->second;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
-  cache[key] = n;
+  occ[key] = n;
   return n;
 }
 

@@ -145,12 +145,20 @@ def test_corrupted_words_are_reported_not_trapped():
     hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"])
     words = hb.view("words", np.uint32).copy()
     toff = hb.view("tile_off", np.uint32)
-    # flip the first bit of lane 3 of tile 1; the oracle confirms the lane no
-    # longer ends at its recorded length
-    words[(toff[1] + 0) * 32 + 3] ^= 0x80000000
+    # flip one bit of lane 3 of tile 1, choosing the first bit whose flip the
+    # oracle sees as a lane that no longer ends at its recorded length
     tf = lw.table_fields(hb.sections["table"])
-    _, used = oracle.decode_lanes(tf["code_len"], words, toff, np.full((len(toff) - 1, 32), 256, np.int32), 256)
-    assert used[1, 3] != hb.view("lane_bits", np.uint16).reshape(-1, 32)[1, 3]
+    nsym = np.full((len(toff) - 1, 32), 256, np.int32)
+    want = hb.view("lane_bits", np.uint16).reshape(-1, 32)[1, 3]
+    for bit in range(31, -1, -1):
+        trial = words.copy()
+        trial[toff[1] * 32 + 3] ^= np.uint32(1 << bit)
+        _, used = oracle.decode_lanes(tf["code_len"], trial, toff, nsym, 256)
+        if used[1, 3] != want:
+            words = trial
+            break
+    else:
+        pytest.fail("no detectable single-bit flip in the first word")
     secs = dict(hb.sections, words=words.view(np.uint8))
     db = lw.DeviceBundle(lw.LW_FMT_Q4_PAIR, False, n, k, secs, hb.stats.max_tile_rows,
                          hb.stats.min_len, hb.stats.max_len, DEV)
