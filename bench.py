@@ -256,16 +256,38 @@ def run_ours(args):
     xs = [torch.from_numpy(x["m"]["x"][0]).to(dev) for x in mats]
     ys = [torch.empty(x["spec"].rows, dtype=torch.float32, device=dev) for x in mats]
     wsb = max(lw.lw_workspace_bytes(d, 1) for d in dbs[0])
-    ws = torch.empty(wsb // 4 + 64, dtype=torch.float32, device=dev)
+    ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     x_bytes = sum(t.numel() * 4 for t in xs)
     coded_step = layer_coded + x_bytes          # every byte the step must read
     weights = sum(x["spec"].rows * x["spec"].cols for x in mats)
 
+    def call(c, j):
+        lw.lw_decode_gemv(dbs[c][j], xs[j], ys[j], ws, st)
+
+    # one CUDA graph per (layer copy, matrix): the host only replays graphs,
+    # so the timed region measures the device (the pages' runtime also
+    # captures each pass in CUDA graphs)
+    for c in range(copies):
+        for j in range(len(mats)):
+            call(c, j)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(copies):
+        row = []
+        for j in range(len(mats)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call(c, j)
+            row.append(g)
+        graphs.append(row)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
     def step(c):
-        for d, x, y in zip(dbs[c], xs, ys):
-            lw.lw_decode_gemv(d, x, y, ws, st, stream)
+        for g in graphs[c]:
+            g.replay()
 
     # per-call durations inside the timed region (events on the launching stream)
     n_mat = len(mats)
@@ -288,9 +310,9 @@ def run_ours(args):
         c = i % copies
         if i % max(1, args.steps // 8) == 0 and len(probe) < 8:
             e = evs[len(probe)]
-            for j, (d, x, y) in enumerate(zip(dbs[c], xs, ys)):
+            for j, g in enumerate(graphs[c]):
                 e[j].record(stream)
-                lw.lw_decode_gemv(d, x, y, ws, st, stream)
+                g.replay()
             e[n_mat].record(stream)
             probe.append(e)
         else:
@@ -316,7 +338,7 @@ def run_ours(args):
 
     value = coded_step * world / (t_max * 1e-3) / 1e9
     peak, peak_kind = peaks()
-    launches_per_step = 2 * n_mat        # fused kernel + ordered reduction per matrix
+    launches_per_step = n_mat            # one fused kernel per matrix
     # dominant kernel: the fused decode+GEMV call, algorithmic bytes per launch
     mean_call_ms = float(per_mat.mean())
     mean_call_bytes = coded_step / n_mat
@@ -336,7 +358,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None,
                          "peak_kind": peak_kind,
-                         "kernel": "fused decode+GEMV call (q_product_kernel + ordered reduction)",
+                         "kernel": "q_product_kernel (fused decode + GEMV + ordered split-K reduction), one launch per matrix",
                          "per_matrix_ms": {x["spec"].name: float(v) for x, v in zip(mats, per_mat)}},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "device_status": status}

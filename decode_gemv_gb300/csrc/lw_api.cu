@@ -89,8 +89,9 @@ using namespace lw;
 
 extern "C" size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch) {
   if (!b || batch < 1 || b->rows <= 0 || b->cols <= 0) return 0;
-  const int64_t chunk = batch > 8 ? 8 : batch;
-  return (size_t)(b->cols / 256) * (size_t)chunk * (size_t)b->rows * sizeof(float);
+  // partials for up to 8 activation rows (the counters sit after the 8-row
+  // partials so that every batch size finds them at the same place)
+  return workspace_partials_bytes(b, 8) + (size_t)(b->rows / 64) * sizeof(uint32_t);
 }
 
 static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, float* Y, void* ws,

@@ -75,6 +75,48 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Explicit shared-memory loads through 32-bit shared addresses (ld.shared).
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int lds_s32(uint32_t a) { return (int)lds_u32(a); }
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
 __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
@@ -87,7 +129,7 @@ __device__ inline bool table_ok(const lw_table* tb, int want_fmt, int want_alpha
   if (tb->fmt != want_fmt || tb->alpha != want_alpha) return false;
   if (lmin < 1 || lmax > LW_MAX_CODE_LEN || lmin > lmax || lmax - lmin > ncmp) return false;
   const int n_entries = tb->n_sym + (tb->phantom ? 1 : 0);
-  if (n_entries < 1 || n_entries > want_alpha + 1 || n_entries > 256) return false;
+  if (n_entries < 1 || n_entries > want_alpha) return false;
   const int nl = lmax - lmin;
   for (int j = nl; j < 12; ++j)
     if (tb->lim_m1[j] != 0xFFFFFFFFu) return false;

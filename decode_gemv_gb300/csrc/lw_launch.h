@@ -39,6 +39,16 @@ lw_status launch_persistent(const void* kernel, int warps, size_t smem, int n_ti
   return check_launch("product kernel");
 }
 
+// Partial sums fp32 [K/256][min(batch, 8)][N], then one uint32 counter per
+// 64-row strip (16-byte aligned).
+inline size_t workspace_partials_bytes(const lw_dev_bundle* b, int batch) {
+  const size_t chunk = batch > 8 ? 8 : (size_t)batch;
+  return ((size_t)(b->cols / 256) * chunk * (size_t)b->rows * sizeof(float) + 15) / 16 * 16;
+}
+inline uint32_t* workspace_counters(const lw_dev_bundle* b, void* ws) {
+  return reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + workspace_partials_bytes(b, 8));
+}
+
 lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, float* ws,
                            int32_t* status, cudaStream_t st);
 lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);

@@ -69,23 +69,21 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   a.qparams = static_cast<const uint8_t*>(b->qparams);
   a.x = x;
   a.ws = ws;
+  a.counters = workspace_counters(b, ws);
+  a.y = y;
   a.status = status;
   a.TK = (int)(b->cols / 256);
   a.N = (int)b->rows;
   a.K = (int)b->cols;
   a.n_tiles = (int)tiles_of(b->rows, b->cols);
   a.batch = batch;
-  a.stage_rows = b->max_tile_rows + 2;
+  a.stage_rows = b->max_tile_rows + dev::kLookahead;
   const int qpb = qparam_tile_bytes(fmt);
   a.stage_bytes = (a.stage_rows * 128 + qpb + bp * 1024 + 127) / 128 * 128;
   const size_t smem = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
-  lw_status s = launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
+  return launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
     k<<<blocks, kWarps * 32, smem, st>>>(a);
   });
-  if (s != LW_OK) return s;
-  const int bn = batch * a.N;
-  dev::reduce_tiles_kernel<<<(bn + 255) / 256, 256, 0, st>>>(ws, y, a.TK, bn);
-  return check_launch("reduce_tiles_kernel");
 }
 
 lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st) {
@@ -108,7 +106,7 @@ lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cu
   a.N = (int)b->rows;
   a.K = (int)b->cols;
   a.n_tiles = (int)tiles_of(b->rows, b->cols);
-  a.stage_rows = b->max_tile_rows + 2;
+  a.stage_rows = b->max_tile_rows + dev::kLookahead;
   a.stage_bytes = (a.stage_rows * 128 + 127) / 128 * 128;
   const size_t smem = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
   return launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {

@@ -16,8 +16,13 @@
 //    256-column slice of every activation row;
 //  * the interleave puts word j of lane l at shared word 32j + l, so every
 //    lane's refill hits bank l: conflict-free however far lanes drift apart;
-//  * comparator limits live in registers, the per-length offsets and the
-//    symbol table (pre-converted to fp32) in shared memory;
+//  * a lane keeps three stream words in registers; one 32-bit window serves
+//    two symbols (a code is at most 11 bits, so after the first code at
+//    least 21 valid bits remain), and the words advance at most once per
+//    symbol pair;
+//  * comparator limits live in registers; per-length offsets (pre-scaled to
+//    shared addresses) and the symbol table (pre-converted to fp32) in shared
+//    memory, read with explicit ld.shared;
 //  * dot products use packed fp32 FMA (FFMA2): even and odd columns in the
 //    two halves;
 //  * codes enter the FMA as the exact fp32 values 16 + c (4-bit) and 64 + c
@@ -25,9 +30,11 @@
 //    op; the bias is removed once per row (4-bit: - 16 * sum x) or per group
 //    (6-bit: - 96 * sum x, folding the code offset 32 in), so the twin and
 //    the coded kernel execute the same floating-point operations and give
-//    bitwise-equal results.
-//  * per-tile partial sums go to a workspace; a second kernel adds them in
-//    ascending tile order (deterministic split-K).
+//    bitwise-equal results;
+//  * split-K: each tile writes its partial sums to the workspace; the last
+//    tile of a row strip to finish (an atomicInc counter that wraps back to
+//    zero) adds the strip's partials in ascending tile order -- one launch,
+//    deterministic.
 #pragma once
 
 #include "lw_dev.cuh"
@@ -42,11 +49,13 @@ struct QArgs {
   const lw_table* table;
   const uint8_t* qparams;
   const float* x;        // [batch][K] (products)
-  float* ws;             // [TK][batch][N] (products)
+  float* ws;             // partials [TK][batch][N] (products)
+  uint32_t* counters;    // [N/64] strip counters (products), zero between calls
+  float* y;              // [batch][N] (products)
   uint8_t* out;          // decode-only output
   int32_t* status;
   int n_tiles, TK, N, K, batch;
-  int stage_rows;        // rows of 128 B per stage buffer = max_tile_rows + 2
+  int stage_rows;        // rows of 128 B per stage buffer = max_tile_rows + 3
   int stage_bytes;       // bytes per stage buffer (multiple of 128)
 };
 
@@ -54,31 +63,32 @@ constexpr int kQ4 = LW_FMT_Q4_PAIR, kQ6 = LW_FMT_Q6;
 
 template <int FMT> struct QFmt;
 template <> struct QFmt<LW_FMT_Q4_PAIR> {
-  static constexpr int alpha = 256, nsym = 256, qp_bytes = 256, twin_rows = 64;
+  static constexpr int alpha = 256, qp_bytes = 256;
 };
 template <> struct QFmt<LW_FMT_Q6> {
-  static constexpr int alpha = 64, nsym = 512, qp_bytes = 2048, twin_rows = 96;
+  static constexpr int alpha = 64, qp_bytes = 2048;
 };
 
 // shared-memory map (bytes)
-constexpr int kOffOff = 0;       // int[16]: per-length symbol offsets
+constexpr int kOffOff = 0;       // uint32[16]: per-length symbol-table base addresses
 constexpr int kFlagOff = 64;     // int: table rejected
 constexpr int kTabOff = 128;     // symbol values: float2[256] (4-bit) / float[64]
 constexpr int kBarOff = 2176;    // uint64 mbarriers, 2 per warp (<= 8 warps)
 constexpr int kStageOff = 2304;  // per warp: two stage buffers
+constexpr int kLookahead = 3;    // stream words a lane holds in registers
 
 __host__ __device__ constexpr int q_x_offset(int stage_rows, int qp_bytes) {
   return stage_rows * 128 + qp_bytes;
 }
 
-// Issue the copies of tile t into one stage (called by the whole warp; lane 0
-// issues).  Returns false if the tile is longer than the stage allows (the
-// copies of everything else are still issued, so the barrier completes).
+// Issue the copies of tile t into one stage (whole warp; lane 0 issues).
+// Returns false if the tile is longer than the stage allows (the other copies
+// are still issued, so the barrier completes).
 template <int FMT, bool PRODUCT>
 __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint8_t* stage, uint64_t* bar,
                                         int lane) {
   const uint32_t r0 = __ldg(a.tile_off + t), r1 = __ldg(a.tile_off + t + 1);
-  const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(a.stage_rows - 2);
+  const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(a.stage_rows - kLookahead);
   if (lane == 0) {
     const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
     constexpr uint32_t qpb = PRODUCT ? QFmt<FMT>::qp_bytes : 0u;
@@ -96,51 +106,66 @@ __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint8_t* stage, u
   return fits;
 }
 
-// Lane bit reader over a staged tile: cur:nxt hold the 64 stream bits
-// starting at word (consumed/32); pos = consumed % 32.
+// Lane bit reader over a staged tile.  Registers cur:nxt:nx2 hold stream
+// words j, j+1, j+2 where j = consumed / 32; pos = consumed % 32.
 struct LaneBits {
-  uint32_t cur, nxt;
-  const uint32_t* wp;      // next word to load (this lane's column)
-  const uint32_t* wlast;   // last row this lane may read
+  uint32_t cur, nxt, nx2;
+  uint32_t wp;      // shared address of word j + 3 of this lane
+  uint32_t wlast;   // last row this lane may read (clamp for corrupt streams)
   int pos, nref;
-  __device__ __forceinline__ void init(const uint32_t* wb, int lane, int stage_rows) {
-    cur = wb[lane];
-    nxt = wb[32 + lane];
-    wp = wb + 64 + lane;
-    wlast = wb + (stage_rows - 1) * 32 + lane;
+  __device__ __forceinline__ void init(uint32_t wb, int lane, int stage_rows) {
+    const uint32_t base = wb + 4u * (uint32_t)lane;
+    cur = lds_u32(base);
+    nxt = lds_u32(base + 128u);
+    nx2 = lds_u32(base + 256u);
+    wp = base + 384u;
+    wlast = base + (uint32_t)(stage_rows - 1) * 128u;
     pos = 0;
     nref = 0;
   }
   __device__ __forceinline__ uint32_t window() const { return __funnelshift_l(nxt, cur, pos); }
-  __device__ __forceinline__ void advance(int L) {
-    pos += L;
+  // consume n (< 32) bits
+  __device__ __forceinline__ void advance(int n) {
+    pos += n;
     if (pos >= 32) {
       pos -= 32;
       cur = nxt;
-      nxt = *wp;
-      wp = wp < wlast ? wp + 32 : wp;
+      nxt = nx2;
+      nx2 = lds_u32(wp);
+      wp = min(wp + 128u, wlast);
       ++nref;
     }
   }
   __device__ __forceinline__ uint32_t consumed() const { return (uint32_t)nref * 32u + (uint32_t)pos; }
 };
 
-// Comparator decode of one symbol: returns the symbol-table index.
+// Comparator for one window: number of limits below the window's code.
 template <int NCMP>
-__device__ __forceinline__ int q_decode_index(LaneBits& lb, const uint32_t (&lim)[NCMP > 0 ? NCMP : 1],
-                                              int lmin, const int* s_off) {
-  const uint32_t w = lb.window();
+__device__ __forceinline__ int q_count(uint32_t w, const uint32_t (&lim)[NCMP > 0 ? NCMP : 1]) {
   int cnt = 0;
 #pragma unroll
   for (int q = 0; q < NCMP; ++q) cnt += (w > lim[q]) ? 1 : 0;
-  const int L = lmin + cnt;
-  const int idx = (int)(w >> (32 - L)) + s_off[cnt];
-  lb.advance(L);
-  return idx;
+  return cnt;
 }
 
-// fp32 value 16 + c of the 4-bit code whose bits start at `shift_to_19`
-// (positive: right shift, negative: left shift) -- exact, one shift + one op.
+// Decode two symbols from one window.  Returns the shared addresses of their
+// symbol-table entries (entry size ESZ bytes).  sh0 = 32 - lmin.
+template <int NCMP, int ESZ>
+__device__ __forceinline__ void q_decode2(LaneBits& lb, const uint32_t (&lim)[NCMP > 0 ? NCMP : 1],
+                                          int sh0, int lmin, uint32_t s_off, uint32_t& e0,
+                                          uint32_t& e1) {
+  const uint32_t w = lb.window();
+  const int c0 = q_count<NCMP>(w, lim);
+  const int L0 = lmin + c0;
+  const uint32_t w1 = w << L0;
+  const int c1 = q_count<NCMP>(w1, lim);
+  e0 = lds_u32(s_off + 4u * (uint32_t)c0) + (w >> (sh0 - c0)) * ESZ;
+  e1 = lds_u32(s_off + 4u * (uint32_t)c1) + (w1 >> (sh0 - c1)) * ESZ;
+  lb.advance(L0 + lmin + c1);
+}
+
+// fp32 value 16 + c of a 4-bit code: shift the code to bits 19..22 (SH > 0:
+// right shift, SH < 0: left shift) -- exact, one shift + one logic op.
 template <int SH>
 __device__ __forceinline__ float q4_twin_val(uint32_t w) {
   const uint32_t t = SH >= 0 ? (w >> SH) : (w << (-SH));
@@ -159,27 +184,69 @@ __device__ __forceinline__ float q6_twin_val(uint32_t w0, uint32_t w1, uint32_t 
   return __uint_as_float(0x42800000u | (t & 0x007E0000u));
 }
 
-// Sum of the tile's 256 activations of row b (fixed order: 8 sequential per
-// lane, then a butterfly; every lane takes lane 0's value).
-__device__ __forceinline__ float tile_sum256(const float* sx, int lane) {
-  const float4 u = reinterpret_cast<const float4*>(sx)[2 * lane];
-  const float4 v = reinterpret_cast<const float4*>(sx)[2 * lane + 1];
+// Sum of the tile's 256 activations of one row (fixed order: 8 sequential
+// per lane, then a butterfly; every lane takes lane 0's value).
+__device__ __forceinline__ float tile_sum256(uint32_t sx, int lane) {
+  const float4 u = lds_f4(sx + 32u * (uint32_t)lane);
+  const float4 v = lds_f4(sx + 32u * (uint32_t)lane + 16u);
   float s = ((((((u.x + u.y) + u.z) + u.w) + v.x) + v.y) + v.z) + v.w;
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, m);
   return __shfl_sync(0xFFFFFFFFu, s, 0);
 }
 
-// Sum of 16 activations starting at sx[16*g] for g = lane (< 16), sequential.
-__device__ __forceinline__ float group_sum16(const float* sx, int lane) {
-  const float4* p = reinterpret_cast<const float4*>(sx + 16 * (lane & 15));
+// Sum of the 16 activations of group (lane & 15), sequential.
+__device__ __forceinline__ float group_sum16(uint32_t sx, int lane) {
+  const uint32_t p = sx + 64u * (uint32_t)(lane & 15);
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 u = p[i];
+    const float4 u = lds_f4(p + 16u * i);
     s = (((s + u.x) + u.y) + u.z) + u.w;
   }
   return s;
+}
+
+// Partial sums of rows (row0, row0+1) for tile (strip, kt) -> workspace; the
+// last tile of the strip to arrive adds all partials of the strip in
+// ascending tile order and writes y.
+template <int BP>
+__device__ __forceinline__ void q_commit(const QArgs& a, int strip, int kt, int lane,
+                                         const float (&p0)[BP], const float (&p1)[BP]) {
+  const int row0 = strip * 64 + 2 * lane;
+#pragma unroll
+  for (int b = 0; b < BP; ++b)
+    if (b < a.batch)
+      *reinterpret_cast<float2*>(a.ws + ((size_t)kt * a.batch + b) * a.N + row0) =
+          make_float2(p0[b], p1[b]);
+  __threadfence();
+  __syncwarp();
+  uint32_t old = 0;
+  if (lane == 0) old = atomicInc(a.counters + strip, (unsigned)(a.TK - 1));
+  old = __shfl_sync(0xFFFFFFFFu, old, 0);
+  if (old != (uint32_t)(a.TK - 1)) return;
+  __threadfence();
+  for (int b = 0; b < a.batch; ++b) {
+    const float* base = a.ws + (size_t)b * a.N + row0;
+    const size_t step = (size_t)a.batch * a.N;
+    float2 s = __ldcg(reinterpret_cast<const float2*>(base));
+    int k = 1;
+    for (; k + 4 <= a.TK; k += 4) {
+      const float2 v0 = __ldcg(reinterpret_cast<const float2*>(base + (size_t)k * step));
+      const float2 v1 = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(k + 1) * step));
+      const float2 v2 = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(k + 2) * step));
+      const float2 v3 = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(k + 3) * step));
+      s.x += v0.x; s.y += v0.y;
+      s.x += v1.x; s.y += v1.y;
+      s.x += v2.x; s.y += v2.y;
+      s.x += v3.x; s.y += v3.y;
+    }
+    for (; k < a.TK; ++k) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(base + (size_t)k * step));
+      s.x += v.x; s.y += v.y;
+    }
+    *reinterpret_cast<float2*>(a.y + (size_t)b * a.N + row0) = s;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -189,38 +256,44 @@ template <int FMT, bool TWIN, int BP, int NCMP, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) q_product_kernel(const QArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   using F = QFmt<FMT>;
-  int* s_off = reinterpret_cast<int*>(smem + kOffOff);
-  int* s_flag = reinterpret_cast<int*>(smem + kFlagOff);
-  float* s_tab = reinterpret_cast<float*>(smem + kTabOff);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t s_off = sbase + kOffOff;
+  const uint32_t s_tab = sbase + kTabOff;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int xoff = q_x_offset(a.stage_rows, F::qp_bytes);
+  constexpr int ESZ = FMT == kQ4 ? 8 : 4;
 
   if (!TWIN) {
-    if (threadIdx.x == 0) *s_flag = table_ok(a.table, FMT, F::alpha, NCMP) ? 0 : 1;
-    if (threadIdx.x < 16) s_off[threadIdx.x] = threadIdx.x < 12 ? a.table->off[threadIdx.x] : 0;
+    if (threadIdx.x == 0)
+      *reinterpret_cast<int*>(smem + kFlagOff) = table_ok(a.table, FMT, F::alpha, NCMP) ? 0 : 1;
+    if (threadIdx.x < 16)
+      reinterpret_cast<uint32_t*>(smem + kOffOff)[threadIdx.x] =
+          s_tab + (uint32_t)(ESZ * (threadIdx.x < 12 ? a.table->off[threadIdx.x] : 0));
     for (int i = threadIdx.x; i < F::alpha; i += blockDim.x) {
       const uint32_t sy = a.table->sym[i];
       if (FMT == kQ4)
-        reinterpret_cast<float2*>(s_tab)[i] = make_float2(16.f + (float)(sy & 15u), 16.f + (float)((sy >> 4) & 15u));
+        reinterpret_cast<float2*>(smem + kTabOff)[i] =
+            make_float2(16.f + (float)(sy & 15u), 16.f + (float)((sy >> 4) & 15u));
       else
-        s_tab[i] = 64.f + (float)(sy & 63u);
+        reinterpret_cast<float*>(smem + kTabOff)[i] = 64.f + (float)(sy & 63u);
     }
   }
-  uint8_t* stage[2] = {smem + kStageOff + (2 * warp) * a.stage_bytes,
-                       smem + kStageOff + (2 * warp + 1) * a.stage_bytes};
+  uint8_t* stage0 = smem + kStageOff + (2 * warp) * a.stage_bytes;
+  uint8_t* stage1 = stage0 + a.stage_bytes;
   uint64_t* bar = s_bar + 2 * warp;
   // activation rows beyond `batch` stay zero in both stages
-  for (int s = 0; s < 2; ++s)
-    for (int i = a.batch * 256 + lane; i < BP * 256; i += 32)
-      reinterpret_cast<float*>(stage[s] + xoff)[i] = 0.f;
+  for (int i = a.batch * 256 + lane; i < BP * 256; i += 32) {
+    reinterpret_cast<float*>(stage0 + xoff)[i] = 0.f;
+    reinterpret_cast<float*>(stage1 + xoff)[i] = 0.f;
+  }
   if (lane == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     fence_barrier_init();
   }
   __syncthreads();
-  if (!TWIN && *s_flag) {
+  if (!TWIN && *reinterpret_cast<volatile int*>(smem + kFlagOff)) {
     if (threadIdx.x == 0) report(a.status, LW_DEV_BAD_TABLE);
     return;
   }
@@ -231,83 +304,85 @@ __global__ void __launch_bounds__(WARPS * 32) q_product_kernel(const QArgs a) {
     for (int q = 0; q < NCMP; ++q) lim[q] = a.table->lim_m1[q];
     lmin = a.table->lmin;
   }
+  const int sh0 = 32 - lmin;
 
   const int nw = gridDim.x * WARPS;
   int t = blockIdx.x * WARPS + warp;
-  // stage / barrier of the current tile ("c") and of the prefetched one ("n")
-  uint8_t* st_c = stage[0];
-  uint8_t* st_n = stage[1];
-  uint64_t* bar_c = &bar[0];
-  uint64_t* bar_n = &bar[1];
-  uint32_t par_c = 0u, par_n = 0u;
-  bool fit_c = true, fit_n = true;
-  if (t < a.n_tiles) fit_c = q_issue<FMT, true>(a, t, st_c, bar_c, lane);
+  uint32_t par0 = 0u, par1 = 0u;
+  bool fit0 = true, fit1 = true;
+  if (t < a.n_tiles) fit0 = q_issue<FMT, true>(a, t, stage0, &bar[0], lane);
 
-  for (; t < a.n_tiles; t += nw) {
+  for (int it = 0; t < a.n_tiles; ++it, t += nw) {
+    const bool odd = it & 1;
     if (t + nw < a.n_tiles) {
       __syncwarp();
       fence_proxy_async();
-      fit_n = q_issue<FMT, true>(a, t + nw, st_n, bar_n, lane);
+      if (odd) fit0 = q_issue<FMT, true>(a, t + nw, stage0, &bar[0], lane);
+      else fit1 = q_issue<FMT, true>(a, t + nw, stage1, &bar[1], lane);
     }
-    if (!mbar_wait(bar_c, par_c)) {
+    uint8_t* st = odd ? stage1 : stage0;
+    const bool ok = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
+    if (!ok) {
       if (lane == 0) report(a.status, LW_DEV_TIMEOUT);
-      if (t + nw < a.n_tiles) mbar_wait(bar_n, par_n);   // let any copy in flight land
+      if (t + nw < a.n_tiles) {   // let the copy in flight land before leaving
+        if (odd) mbar_wait(&bar[0], par0);
+        else mbar_wait(&bar[1], par1);
+      }
       return;
     }
-    par_c ^= 1u;
-    const uint8_t* cur_stage = st_c;
-    const bool fit = fit_c;
-    {  // rotate: the prefetched tile becomes current for the next iteration
-      uint8_t* ts = st_c; st_c = st_n; st_n = ts;
-      uint64_t* tb = bar_c; bar_c = bar_n; bar_n = tb;
-      const uint32_t tp = par_c; par_c = par_n; par_n = tp;
-      fit_c = fit_n;
-    }
+    if (odd) par1 ^= 1u; else par0 ^= 1u;
+    const bool fit = odd ? fit1 : fit0;
+    const int strip = t / a.TK, kt = t % a.TK;
+    float part0[BP], part1[BP];   // rows 2l and 2l+1
+#pragma unroll
+    for (int b = 0; b < BP; ++b) part0[b] = part1[b] = 0.f;
     if (!fit) {
       if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
+      q_commit<BP>(a, strip, kt, lane, part0, part1);
       continue;
     }
-    const uint32_t* wb = reinterpret_cast<const uint32_t*>(cur_stage);
-    const uint8_t* qp = cur_stage + a.stage_rows * 128;
-    const float* sx = reinterpret_cast<const float*>(cur_stage + xoff);
-    const int strip = t / a.TK, kt = t % a.TK;
-    const int row0 = strip * 64 + 2 * lane;
+    const uint32_t wb = smem_addr(st);
+    const uint32_t qp = wb + (uint32_t)a.stage_rows * 128u;
+    const uint32_t sx = wb + (uint32_t)xoff;
 
     LaneBits lb;
     if (!TWIN) lb.init(wb, lane, a.stage_rows);
-    float part0[BP], part1[BP];   // rows 2l and 2l+1
 
     if (FMT == kQ4) {
       float S[BP];
 #pragma unroll
-      for (int b = 0; b < BP; ++b) S[b] = tile_sum256(sx + 256 * b, lane);
-      const uint2 q2 = reinterpret_cast<const uint2*>(qp)[lane];   // rows 2l, 2l+1: (scale | min<<16)
+      for (int b = 0; b < BP; ++b) S[b] = tile_sum256(sx + 1024u * b, lane);
+      const uint2 q2 = lds_u2(qp + 8u * (uint32_t)lane);   // rows 2l, 2l+1: (scale | min<<16)
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         float2 acc[BP];
 #pragma unroll
         for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
         if (!TWIN) {
-#pragma unroll 4
-          for (int j = 0; j < 128; ++j) {
-            const int idx = q_decode_index<NCMP>(lb, lim, lmin, s_off);
-            const float2 v = reinterpret_cast<const float2*>(s_tab)[idx];
+#pragma unroll 2
+          for (int jj = 0; jj < 64; ++jj) {      // symbol pairs: columns 4jj .. 4jj+3
+            uint32_t e0, e1;
+            q_decode2<NCMP, 8>(lb, lim, sh0, lmin, s_off, e0, e1);
+            const float2 v0 = lds_f2(e0), v1 = lds_f2(e1);
 #pragma unroll
-            for (int b = 0; b < BP; ++b)
-              acc[b] = __ffma2_rn(v, reinterpret_cast<const float2*>(sx + 256 * b)[j], acc[b]);
+            for (int b = 0; b < BP; ++b) {
+              const float4 xv = lds_f4(sx + 1024u * b + 16u * jj);
+              acc[b] = __ffma2_rn(v0, make_float2(xv.x, xv.y), acc[b]);
+              acc[b] = __ffma2_rn(v1, make_float2(xv.z, xv.w), acc[b]);
+            }
           }
         } else {
 #pragma unroll 2
           for (int jj = 0; jj < 32; ++jj) {
-            const uint32_t w = wb[(32 * h + jj) * 32 + lane];
+            const uint32_t w = lds_u32(wb + (uint32_t)((32 * h + jj) * 128 + 4 * lane));
             const float2 v0 = make_float2(q4_twin_val<9>(w), q4_twin_val<5>(w));
             const float2 v1 = make_float2(q4_twin_val<1>(w), q4_twin_val<-3>(w));
             const float2 v2 = make_float2(q4_twin_val<-7>(w), q4_twin_val<-11>(w));
             const float2 v3 = make_float2(q4_twin_val<-15>(w), q4_twin_val<-19>(w));
 #pragma unroll
             for (int b = 0; b < BP; ++b) {
-              const float4 xa = reinterpret_cast<const float4*>(sx + 256 * b)[2 * jj];
-              const float4 xb = reinterpret_cast<const float4*>(sx + 256 * b)[2 * jj + 1];
+              const float4 xa = lds_f4(sx + 1024u * b + 32u * jj);
+              const float4 xb = lds_f4(sx + 1024u * b + 32u * jj + 16u);
               acc[b] = __ffma2_rn(v0, make_float2(xa.x, xa.y), acc[b]);
               acc[b] = __ffma2_rn(v1, make_float2(xa.z, xa.w), acc[b]);
               acc[b] = __ffma2_rn(v2, make_float2(xb.x, xb.y), acc[b]);
@@ -328,8 +403,7 @@ __global__ void __launch_bounds__(WARPS * 32) q_product_kernel(const QArgs a) {
     } else {  // 6-bit
       float X[BP];
 #pragma unroll
-      for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 256 * b, lane);
-      const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(qp);
+      for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         float rowp[BP];
@@ -343,17 +417,17 @@ __global__ void __launch_bounds__(WARPS * 32) q_product_kernel(const QArgs a) {
           if (!TWIN) {
 #pragma unroll 2
             for (int m = 0; m < 8; ++m) {
-              const int i0 = q_decode_index<NCMP>(lb, lim, lmin, s_off);
-              const int i1 = q_decode_index<NCMP>(lb, lim, lmin, s_off);
-              const float2 v = make_float2(s_tab[i0], s_tab[i1]);
+              uint32_t e0, e1;
+              q_decode2<NCMP, 4>(lb, lim, sh0, lmin, s_off, e0, e1);
+              const float2 v = make_float2(lds_f32(e0), lds_f32(e1));
 #pragma unroll
               for (int b = 0; b < BP; ++b)
-                acc[b] = __ffma2_rn(v, reinterpret_cast<const float2*>(sx + 256 * b + 16 * g)[m], acc[b]);
+                acc[b] = __ffma2_rn(v, lds_f2(sx + 1024u * b + 64u * g + 8u * m), acc[b]);
             }
           } else {
-            const int r = 48 * h + 3 * g;
-            const uint32_t w0 = wb[r * 32 + lane], w1 = wb[(r + 1) * 32 + lane],
-                           w2 = wb[(r + 2) * 32 + lane];
+            const uint32_t r = (uint32_t)(48 * h + 3 * g);
+            const uint32_t a0 = wb + r * 128u + 4u * lane;
+            const uint32_t w0 = lds_u32(a0), w1 = lds_u32(a0 + 128u), w2 = lds_u32(a0 + 256u);
             float v[16];
             v[0] = q6_twin_val<0>(w0, w1, w2);    v[1] = q6_twin_val<6>(w0, w1, w2);
             v[2] = q6_twin_val<12>(w0, w1, w2);   v[3] = q6_twin_val<18>(w0, w1, w2);
@@ -368,10 +442,11 @@ __global__ void __launch_bounds__(WARPS * 32) q_product_kernel(const QArgs a) {
 #pragma unroll
               for (int b = 0; b < BP; ++b)
                 acc[b] = __ffma2_rn(make_float2(v[2 * m], v[2 * m + 1]),
-                                    reinterpret_cast<const float2*>(sx + 256 * b + 16 * g)[m], acc[b]);
+                                    lds_f2(sx + 1024u * b + 64u * g + 8u * m), acc[b]);
           }
           // scale of group g of row h: chunk (2h + g/8), position g%8
-          const float sc = __half2float(__ushort_as_half(sc16[(((2 * h + (g >> 3)) * 32) + lane) * 8 + (g & 7)]));
+          const uint32_t sa = qp + (uint32_t)((((2 * h + (g >> 3)) * 32) + lane) * 16 + 2 * (g & 7));
+          const float sc = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], g);
@@ -386,11 +461,7 @@ __global__ void __launch_bounds__(WARPS * 32) q_product_kernel(const QArgs a) {
     }
     if (!TWIN && lb.consumed() != (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane))
       report(a.status, LW_DEV_LANE_LENGTH);
-#pragma unroll
-    for (int b = 0; b < BP; ++b)
-      if (b < a.batch)
-        *reinterpret_cast<float2*>(a.ws + ((size_t)kt * a.batch + b) * a.N + row0) =
-            make_float2(part0[b], part1[b]);
+    q_commit<BP>(a, strip, kt, lane, part0, part1);
   }
 }
 
@@ -402,20 +473,24 @@ template <int FMT, bool TWIN, int NCMP, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   using F = QFmt<FMT>;
-  int* s_off = reinterpret_cast<int*>(smem + kOffOff);
-  int* s_flag = reinterpret_cast<int*>(smem + kFlagOff);
-  uint16_t* s_sym = reinterpret_cast<uint16_t*>(smem + kTabOff);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t s_off = sbase + kOffOff;
+  const uint32_t s_sym = sbase + kTabOff;   // uint32 per canonical index
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_sym = 0;
   if (!TWIN) {
-    if (threadIdx.x == 0) *s_flag = table_ok(a.table, FMT, F::alpha, NCMP) ? 0 : 1;
-    if (threadIdx.x < 16) s_off[threadIdx.x] = threadIdx.x < 12 ? a.table->off[threadIdx.x] : 0;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_sym[i] = a.table->sym[i];
+    if (threadIdx.x == 0)
+      *reinterpret_cast<int*>(smem + kFlagOff) = table_ok(a.table, FMT, F::alpha, NCMP) ? 0 : 1;
+    if (threadIdx.x < 16)
+      reinterpret_cast<uint32_t*>(smem + kOffOff)[threadIdx.x] =
+          s_sym + (uint32_t)(4 * (threadIdx.x < 12 ? a.table->off[threadIdx.x] : 0));
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+      reinterpret_cast<uint32_t*>(smem + kTabOff)[i] = a.table->sym[i];
     n_sym = a.table->n_sym;
   }
-  uint8_t* stage[2] = {smem + kStageOff + (2 * warp) * a.stage_bytes,
-                       smem + kStageOff + (2 * warp + 1) * a.stage_bytes};
+  uint8_t* stage0 = smem + kStageOff + (2 * warp) * a.stage_bytes;
+  uint8_t* stage1 = stage0 + a.stage_bytes;
   uint64_t* bar = s_bar + 2 * warp;
   if (lane == 0) {
     mbar_init(&bar[0], 1);
@@ -423,7 +498,7 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
     fence_barrier_init();
   }
   __syncthreads();
-  if (!TWIN && *s_flag) {
+  if (!TWIN && *reinterpret_cast<volatile int*>(smem + kFlagOff)) {
     if (threadIdx.x == 0) report(a.status, LW_DEV_BAD_TABLE);
     return;
   }
@@ -434,40 +509,37 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
     for (int q = 0; q < NCMP; ++q) lim[q] = a.table->lim_m1[q];
     lmin = a.table->lmin;
   }
+  const int sh0 = 32 - lmin;
+  const uint32_t first_bad = s_sym + 4u * (uint32_t)n_sym;   // entries at or past it are phantom
   const int nw = gridDim.x * WARPS;
   int t = blockIdx.x * WARPS + warp;
-  uint8_t* st_c = stage[0];
-  uint8_t* st_n = stage[1];
-  uint64_t* bar_c = &bar[0];
-  uint64_t* bar_n = &bar[1];
-  uint32_t par_c = 0u, par_n = 0u;
-  bool fit_c = true, fit_n = true;
-  if (t < a.n_tiles) fit_c = q_issue<FMT, false>(a, t, st_c, bar_c, lane);
-  for (; t < a.n_tiles; t += nw) {
+  uint32_t par0 = 0u, par1 = 0u;
+  bool fit0 = true, fit1 = true;
+  if (t < a.n_tiles) fit0 = q_issue<FMT, false>(a, t, stage0, &bar[0], lane);
+  for (int it = 0; t < a.n_tiles; ++it, t += nw) {
+    const bool odd = it & 1;
     if (t + nw < a.n_tiles) {
       __syncwarp();
       fence_proxy_async();
-      fit_n = q_issue<FMT, false>(a, t + nw, st_n, bar_n, lane);
+      if (odd) fit0 = q_issue<FMT, false>(a, t + nw, stage0, &bar[0], lane);
+      else fit1 = q_issue<FMT, false>(a, t + nw, stage1, &bar[1], lane);
     }
-    if (!mbar_wait(bar_c, par_c)) {
+    uint8_t* st = odd ? stage1 : stage0;
+    const bool ok = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
+    if (!ok) {
       if (lane == 0) report(a.status, LW_DEV_TIMEOUT);
-      if (t + nw < a.n_tiles) mbar_wait(bar_n, par_n);
+      if (t + nw < a.n_tiles) {
+        if (odd) mbar_wait(&bar[0], par0);
+        else mbar_wait(&bar[1], par1);
+      }
       return;
     }
-    par_c ^= 1u;
-    const uint8_t* cur_stage = st_c;
-    const bool fit = fit_c;
-    {
-      uint8_t* ts = st_c; st_c = st_n; st_n = ts;
-      uint64_t* tb = bar_c; bar_c = bar_n; bar_n = tb;
-      const uint32_t tp = par_c; par_c = par_n; par_n = tp;
-      fit_c = fit_n;
-    }
-    if (!fit) {
+    if (odd) par1 ^= 1u; else par0 ^= 1u;
+    if (!(odd ? fit1 : fit0)) {
       if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
       continue;
     }
-    const uint32_t* wb = reinterpret_cast<const uint32_t*>(cur_stage);
+    const uint32_t wb = smem_addr(st);
     const int strip = t / a.TK, kt = t % a.TK;
     LaneBits lb;
     if (!TWIN) lb.init(wb, lane, a.stage_rows);
@@ -480,13 +552,15 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
           uint32_t packed = 0;
           if (!TWIN) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int idx = q_decode_index<NCMP>(lb, lim, lmin, s_off);
-              bad |= idx >= n_sym;
-              packed |= (uint32_t)(s_sym[idx] & 0xFFu) << (8 * i);
+            for (int i = 0; i < 4; i += 2) {
+              uint32_t e0, e1;
+              q_decode2<NCMP, 4>(lb, lim, sh0, lmin, s_off, e0, e1);
+              bad |= (e0 >= first_bad) | (e1 >= first_bad);
+              packed |= (lds_u32(e0) & 0xFFu) << (8 * i);
+              packed |= (lds_u32(e1) & 0xFFu) << (8 * i + 8);
             }
           } else {
-            const uint32_t w = wb[(32 * h + q) * 32 + lane];   // codes 8q..8q+7, MSB first
+            const uint32_t w = lds_u32(wb + (uint32_t)((32 * h + q) * 128 + 4 * lane));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const uint32_t ce = (w >> (28 - 8 * i)) & 15u, co = (w >> (24 - 8 * i)) & 15u;
@@ -501,16 +575,18 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
           uint32_t packed = 0;
           if (!TWIN) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int idx = q_decode_index<NCMP>(lb, lim, lmin, s_off);
-              bad |= idx >= n_sym;
-              packed |= (uint32_t)(s_sym[idx] & 0x3Fu) << (8 * i);
+            for (int i = 0; i < 4; i += 2) {
+              uint32_t e0, e1;
+              q_decode2<NCMP, 4>(lb, lim, sh0, lmin, s_off, e0, e1);
+              bad |= (e0 >= first_bad) | (e1 >= first_bad);
+              packed |= (lds_u32(e0) & 0x3Fu) << (8 * i);
+              packed |= (lds_u32(e1) & 0x3Fu) << (8 * i + 8);
             }
           } else {
             // codes 256h + 4q .. +3 at stream bits 6*(256h + 4q): 24 bits
             const uint32_t bit = 6u * (256u * h + 4u * q);
-            const uint32_t w0 = wb[(bit / 32) * 32 + lane];
-            const uint32_t w1 = (bit / 32 + 1 < 96u) ? wb[(bit / 32 + 1) * 32 + lane] : 0u;
+            const uint32_t w0 = lds_u32(wb + (bit / 32) * 128u + 4u * lane);
+            const uint32_t w1 = (bit / 32 + 1 < 96u) ? lds_u32(wb + (bit / 32 + 1) * 128u + 4u * lane) : 0u;
             const uint32_t win = __funnelshift_l(w1, w0, bit % 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) packed |= ((win >> (26 - 6 * i)) & 63u) << (8 * i);
@@ -525,16 +601,6 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
         report(a.status, LW_DEV_LANE_LENGTH);
     }
   }
-}
-
-// y[b][r] = sum over tiles kt of ws[kt][b][r], kt ascending.
-__global__ void reduce_tiles_kernel(const float* __restrict__ ws, float* __restrict__ y, int TK,
-                                    int BN) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= BN) return;
-  float s = ws[i];
-  for (int kt = 1; kt < TK; ++kt) s += ws[(size_t)kt * BN + i];
-  y[i] = s;
 }
 
 }  // namespace dev

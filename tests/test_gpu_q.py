@@ -37,7 +37,7 @@ def run_product(db, x, twin=False, stream=None):
     B = x.shape[0]
     X = torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
     Y = torch.full((B, db.rows), float("nan"), dtype=torch.float32, device=DEV)
-    ws = torch.empty(max(1, lw.lw_workspace_bytes(db, B) // 4), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(max(1, lw.lw_workspace_bytes(db, B) // 4), dtype=torch.float32, device=DEV)
     st = status()
     if twin:
         (lw.lw_twin_gemv if B == 1 else lambda *a, **k: lw.lw_twin_gemm(a[0], a[1], B, *a[2:], **k))(
