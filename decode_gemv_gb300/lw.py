@@ -27,7 +27,7 @@ TABLE_BYTES = 1024
 EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_table_from_lengths",
             "lw_validate_sections", "lw_workspace_bytes", "lw_decode", "lw_decode_gemv",
             "lw_decode_gemm", "lw_twin_gemv", "lw_twin_gemm", "lw_status_string",
-            "lw_last_error", "lw_version"]
+            "lw_last_error", "lw_version", "lw_decode_gemv_noalloc", "lw_noalloc_scratch_bytes"]
 
 
 class LwError(RuntimeError):
@@ -89,6 +89,8 @@ def load():
         "lw_status_string": ([i32], ctypes.c_char_p),
         "lw_last_error": ([], ctypes.c_char_p),
         "lw_version": ([], i32),
+        "lw_decode_gemv_noalloc": ([P, P, P, P, P], i32),
+        "lw_noalloc_scratch_bytes": ([], sz),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -296,3 +298,14 @@ def lw_twin_gemm(db: DeviceBundle, X, batch, Y, ws, d_status, stream=None) -> No
     _check(load().lw_twin_gemm(db.ref, _tp(X), batch, _tp(Y), _tp(ws),
                                ws.numel() * ws.element_size(), _tp(d_status),
                                _stream_ptr(stream)), "lw_twin_gemm")
+
+
+def lw_decode_gemv_noalloc(db: DeviceBundle, x, y, d_status, stream=None) -> None:
+    """lw_decode_gemv with the library's fixed device scratch instead of a
+    caller workspace (allocates nothing)."""
+    _check(load().lw_decode_gemv_noalloc(db.ref, _tp(x), _tp(y), _tp(d_status),
+                                         _stream_ptr(stream)), "lw_decode_gemv_noalloc")
+
+
+def lw_noalloc_scratch_bytes() -> int:
+    return int(load().lw_noalloc_scratch_bytes())

@@ -297,6 +297,26 @@ lw_status lw_twin_gemm(const lw_dev_bundle* twin, const void* X, int32_t batch,
                        float* Y, void* ws, size_t ws_bytes, int32_t* d_status,
                        void* stream);
 
+/*
+ * lw_decode_gemv without a caller workspace, for callers that cannot allocate
+ * device memory: code running under CUDA-graph capture, engines whose pool
+ * allocator owns all device memory, latency-critical paths that cannot afford
+ * cudaMalloc's implicit synchronisation, foreign-language callers without a
+ * device allocator.  The pages have no counterpart; this is an interface
+ * convenience.  Same product, order and arguments as lw_decode_gemv minus
+ * `ws`/`ws_bytes`.  Scratch comes from a fixed array in device memory of
+ * lw_noalloc_scratch_bytes() bytes (16 MiB), held on every GPU that loads
+ * the library until the process exits; a matrix whose
+ * lw_workspace_bytes(b, 1) exceeds it is rejected with LW_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (do it
+ * before any stream capture).  Every call clears the array's counters on
+ * `stream` first.  All calls share the array: calls that overlap on the GPU
+ * race and must be serialised by the caller.  Allocates nothing.
+ */
+lw_status lw_decode_gemv_noalloc(const lw_dev_bundle* b, const void* x, float* y,
+                                 int32_t* d_status, void* stream);
+size_t lw_noalloc_scratch_bytes(void);
+
 const char* lw_status_string(lw_status s);
 const char* lw_last_error(void);
 
