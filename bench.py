@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--only", default="", help="comma list of matrix names (profiling)")
     p.add_argument("--copies", type=int, default=0, help="layer copies to rotate (0 = auto)")
+    p.add_argument("--twin", action="store_true",
+                   help="time the fixed-width twin in the main loop instead (profiling)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip twin / bf16 / cpu baseline / e2e legs (profiling)")
     return p.parse_args()
@@ -249,10 +251,11 @@ def run_ours(args):
     names = [n for n in args.only.split(",") if n]
     mats = build_layer(names)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    layer_coded = sum(x["hb"].stats.coded_bytes for x in mats)
+    layer_coded = sum(x["tw" if args.twin else "hb"].stats.coded_bytes for x in mats)
     copies = args.copies or max(2, math.ceil(4 * l2 / layer_coded))
     # device copies of the layer (distinct addresses), activations, outputs
-    dbs = [[lw.DeviceBundle.upload(x["hb"], dev) for x in mats] for _ in range(copies)]
+    key = "tw" if args.twin else "hb"
+    dbs = [[lw.DeviceBundle.upload(x[key], dev) for x in mats] for _ in range(copies)]
     xs = [torch.from_numpy(x["m"]["x"][0]).to(dev) for x in mats]
     ys = [torch.empty(x["spec"].rows, dtype=torch.float32, device=dev) for x in mats]
     wsb = max(lw.lw_workspace_bytes(d, 1) for d in dbs[0])
@@ -264,7 +267,10 @@ def run_ours(args):
     weights = sum(x["spec"].rows * x["spec"].cols for x in mats)
 
     def call(c, j):
-        lw.lw_decode_gemv(dbs[c][j], xs[j], ys[j], ws, st)
+        if args.twin:
+            lw.lw_twin_gemv(dbs[c][j], xs[j], ys[j], ws, st)
+        else:
+            lw.lw_decode_gemv(dbs[c][j], xs[j], ys[j], ws, st)
 
     # one CUDA graph per (layer copy, matrix): the host only replays graphs,
     # so the timed region measures the device (the pages' runtime also
@@ -376,28 +382,61 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
            weights, t_ours):
     """Comparators and the end-to-end leg (outside the timed region above)."""
     steps = max(10, min(args.steps, 400))
-    # fixed-width twin, same rotation
-    twins = [[lw.DeviceBundle.upload(x["tw"], dev) for x in mats]
-             for _ in range(max(2, math.ceil(copies * 0.75)))]
-    nt = len(twins)
+
+    def graphs_of(calls):
+        for f in calls:
+            f()
+        torch.cuda.synchronize()
+        out = []
+        for f in calls:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                f()
+            out.append(g)
+        torch.cuda.synchronize()
+        return out
+
+    # fixed-width twin, same rotation, one graph per matrix call
+    ntw = max(2, math.ceil(copies * 0.75))
+    twins = [[lw.DeviceBundle.upload(x["tw"], dev) for x in mats] for _ in range(ntw)]
+    tg = [graphs_of([(lambda d=d, x=x, y=y: lw.lw_twin_gemv(d, x, y, ws, st))
+                     for d, x, y in zip(twins[c], xs, ys)]) for c in range(ntw)]
 
     def tstep(c):
-        for d, x, y in zip(twins[c], xs, ys):
-            lw.lw_twin_gemv(d, x, y, ws, st, stream)
-    t_twin = time_steps(torch, stream, tstep, steps, 5, nt)
-    del twins
-    # uncompressed BF16 GEMV (cuBLAS) on the dequantised weights
+        for g in tg[c]:
+            g.replay()
+    t_twin = time_steps(torch, stream, tstep, steps, 5, ntw)
+    # per-matrix twin call durations (events between graph replays)
+    n_mat = len(mats)
+    tw_ms = np.zeros(n_mat)
+    reps = 8
+    for r in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_mat + 1)]
+        for j, g in enumerate(tg[r % ntw]):
+            ev[j].record(stream)
+            g.replay()
+        ev[n_mat].record(stream)
+        torch.cuda.synchronize()
+        tw_ms += [ev[j].elapsed_time(ev[j + 1]) for j in range(n_mat)]
+    tw_ms /= reps
+    del tg, twins
+    # uncompressed BF16 GEMV (cuBLAS) on the dequantised weights, graphed
     wb = [dequant_bf16(x["m"]).to(dev) for x in mats]
     xb = [x.to(torch.bfloat16) for x in xs]
+    yb = [torch.empty(w.shape[0], dtype=torch.bfloat16, device=dev) for w in wb]
+    bg = graphs_of([(lambda w=w, x=x, y=y: torch.mv(w, x, out=y)) for w, x, y in zip(wb, xb, yb)])
 
     def bstep(c):
-        for w, x in zip(wb, xb):
-            torch.mv(w, x)
+        for g in bg:
+            g.replay()
     t_bf16 = time_steps(torch, stream, bstep, steps, 5, 1)
-    del wb
-    line["twin"] = {"ms_per_step": t_twin, "speedup_of_coded": t_twin / t_ours}
+    del bg, wb
+    twin_bytes = sum(x["tw"].stats.coded_bytes for x in mats) + sum(x.numel() * 4 for x in xs)
+    line["twin"] = {"ms_per_step": t_twin, "speedup_of_coded": t_twin / t_ours,
+                    "gbs": twin_bytes / (t_twin * 1e-3) / 1e9,
+                    "per_matrix_ms": {x["spec"].name: float(v) for x, v in zip(mats, tw_ms)}}
     line["bf16_dense"] = {"ms_per_step": t_bf16, "speedup_of_coded": t_bf16 / t_ours,
-                          "kind": "torch.mv on bf16 weights (cuBLAS)"}
+                          "kind": "torch.mv on bf16 weights (cuBLAS), CUDA graphs"}
     # end to end through the public API: pinned host activations in, results out
     hx = [x.cpu().pin_memory() for x in xs]
     hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in ys]

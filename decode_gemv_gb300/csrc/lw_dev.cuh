@@ -133,6 +133,10 @@ __device__ inline bool table_ok(const lw_table* tb, int want_fmt, int want_alpha
   const int nl = lmax - lmin;
   for (int j = nl; j < 12; ++j)
     if (tb->lim_m1[j] != 0xFFFFFFFFu) return false;
+  // every limit below the longest length is even in 11-bit peek space (the
+  // kernels compare 10-bit peeks against limit / 2)
+  for (int j = 0; j < nl; ++j)
+    if (((tb->lim_m1[j] + 1u) >> 21) & 1u) return false;
   uint32_t prev_hi = 0;
   for (int j = 0; j <= nl; ++j) {
     const int L = lmin + j;

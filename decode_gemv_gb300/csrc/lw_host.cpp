@@ -183,7 +183,7 @@ extern "C" lw_status lw_table_from_lengths(int32_t fmt, const uint8_t* code_len,
 struct lw_bundle {
   lw_desc desc{};
   std::vector<uint32_t> words, tile_off;
-  std::vector<uint16_t> lane_bits, qparams;
+  std::vector<uint16_t> lane_bits, lane_mid, qparams;
   lw_table table{};
   std::vector<uint8_t> signman, vexp;
   std::vector<uint32_t> vflags, vrow_off;
@@ -218,10 +218,13 @@ struct LaneSource {
   const uint8_t* codes = nullptr;        // Q4 / Q6
   const uint8_t* palidx = nullptr;       // BF16: palette index per weight
   const uint8_t* verb = nullptr;         // BF16: [N][K/64] 0/1
-  int operator()(int64_t t, int l, uint16_t* out) const {
+  // Symbols of lane l of tile t in lane order; *first = how many belong to
+  // the lane's first row.
+  int operator()(int64_t t, int l, uint16_t* out, int* first = nullptr) const {
     const int64_t s = t / TK, kt = t % TK;
     int n = 0;
     for (int half = 0; half < 2; ++half) {
+      if (half == 1 && first) *first = n;
       const int64_t r = 64 * s + 2 * l + half;
       if (fmt == LW_FMT_Q4_PAIR) {
         const uint8_t* row = codes + r * K + 256 * kt;
@@ -307,17 +310,24 @@ lw_status pack_huffman(lw_bundle* B, const LaneSource& src, int alpha) {
 
   // pass 1: lane bit counts and W_t
   B->lane_bits.assign(n_tiles * 32, 0);
+  B->lane_mid.assign(n_tiles * 32, 0);
   std::vector<uint32_t> wt(n_tiles, 0);
   std::atomic<bool> overflow{false};
   parallel_for(n_tiles, [&](int64_t t) {
     std::vector<uint16_t> buf(maxsym);
     uint32_t w = 0;
     for (int l = 0; l < 32; ++l) {
-      const int n = src(t, l, buf.data());
-      uint64_t bits = 0;
-      for (int k = 0; k < n; ++k) bits += len[buf[k]];
+      int first = 0;
+      const int n = src(t, l, buf.data(), &first);
+      uint64_t bits = 0, mid = 0;
+      for (int k = 0; k < n; ++k) {
+        if (k == first) mid = bits;
+        bits += len[buf[k]];
+      }
+      if (first >= n) mid = bits;
       if (bits > 0xFFFF) overflow = true;
       B->lane_bits[t * 32 + l] = (uint16_t)bits;
+      B->lane_mid[t * 32 + l] = (uint16_t)mid;
       w = std::max<uint32_t>(w, (uint32_t)((bits + 31) / 32));
     }
     wt[t] = w;
@@ -542,6 +552,7 @@ extern "C" lw_status lw_bundle_sections(const lw_bundle* B, lw_sections* s) {
   put(LW_SEC_VFLAGS, B->vflags.data(), B->vflags.size() * 4);
   put(LW_SEC_VROW_OFF, B->vrow_off.data(), B->vrow_off.size() * 4);
   put(LW_SEC_VEXP, B->vexp.data(), B->vexp.size());
+  put(LW_SEC_LANE_MID, B->lane_mid.data(), B->lane_mid.size() * 2);
   uint64_t tot = 0;
   for (int i = 0; i < LW_NUM_SECTIONS; ++i) tot += s->bytes[i];
   s->coded_bytes = tot;
@@ -575,6 +586,13 @@ extern "C" lw_status lw_validate_sections(const lw_desc* d, const lw_sections* s
     if ((int64_t)wt > s->max_tile_rows) return fail(LW_ERR_CORRUPT, "tile %lld longer than max_tile_rows", (long long)t);
     for (int l = 0; l < 32; ++l)
       if (lb[t * 32 + l] > wt * 32) return fail(LW_ERR_CORRUPT, "lane bits exceed W_t at tile %lld", (long long)t);
+  }
+  if (!d->twin) {
+    if (s->bytes[LW_SEC_LANE_MID] != (uint64_t)n_tiles * 64)
+      return fail(LW_ERR_CORRUPT, "lane_mid size does not match the shape");
+    const uint16_t* mid = (const uint16_t*)s->ptr[LW_SEC_LANE_MID];
+    for (int64_t i = 0; i < n_tiles * 32; ++i)
+      if (mid[i] > lb[i]) return fail(LW_ERR_CORRUPT, "lane_mid beyond lane_bits at lane %lld", (long long)i);
   }
   if ((uint64_t)off[n_tiles] * 128 != s->bytes[LW_SEC_WORDS])
     return fail(LW_ERR_CORRUPT, "word count does not match tile_off");
@@ -624,4 +642,4 @@ extern "C" const char* lw_status_string(lw_status s) {
 
 extern "C" const char* lw_last_error(void) { return g_err.c_str(); }
 
-extern "C" int32_t lw_version(void) { return 1; }
+extern "C" int32_t lw_version(void) { return 2; }

@@ -31,9 +31,12 @@ lw_status launch_persistent(const void* kernel, int warps, size_t smem, int n_ti
   if (per_sm < 1)
     return fail(LW_ERR_UNSUPPORTED, "kernel does not fit on an SM (%zu bytes of shared memory)",
                 smem);
-  long long blocks = (long long)per_sm * device_sm_count();
-  const long long need = (n_tiles + warps - 1) / warps;
-  if (need < blocks) blocks = need;
+  // every warp gets the same number of tiles: the fewest warps that still
+  // take ceil(n_tiles / resident warps) tiles each
+  const long long resident_warps = (long long)per_sm * device_sm_count() * warps;
+  const long long per_warp = (n_tiles + resident_warps - 1) / resident_warps;
+  const long long want_warps = per_warp > 0 ? (n_tiles + per_warp - 1) / per_warp : 1;
+  long long blocks = (want_warps + warps - 1) / warps;
   if (blocks < 1) blocks = 1;
   launch((int)blocks);
   return check_launch("product kernel");

@@ -1,4 +1,5 @@
 // Launchers for the 4-/6-bit kernels (instantiations of lw_qkern.cuh).
+#include <cstdlib>
 #include <mutex>
 #include <unordered_map>
 
@@ -10,7 +11,10 @@ namespace lw {
 
 namespace {
 
-constexpr int kWarps = 4;
+// One warp per CTA: tiles then spread evenly over the SMs, whatever the
+// matrix size (a persistent grid of 4-warp CTAs left some SMs with twice the
+// tiles of others on small matrices).
+constexpr int kWarps = 1;
 
 int ncmp_bucket(int span) { return span <= 4 ? 4 : (span <= 7 ? 7 : (span <= 8 ? 8 : 10)); }
 
@@ -65,6 +69,7 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   a.words = b->words;
   a.tile_off = b->tile_off;
   a.lane_bits = b->lane_bits;
+  a.lane_mid = twin ? nullptr : b->lane_mid;
   a.table = b->table;
   a.qparams = static_cast<const uint8_t*>(b->qparams);
   a.x = x;
@@ -79,8 +84,16 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   a.batch = batch;
   a.stage_rows = b->max_tile_rows + dev::kLookahead;
   const int qpb = qparam_tile_bytes(fmt);
-  a.stage_bytes = (a.stage_rows * 128 + qpb + bp * 1024 + 127) / 128 * 128;
-  const size_t smem = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
+  a.mid_offset = a.stage_rows * 128 + qpb + bp * 1024;
+  a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
+  // two stages per warp while that still leaves 16 resident warps per SM,
+  // else one stage (twice the warps; each warp then waits for its own next
+  // tile, other warps cover the wait)
+  const size_t smem2 = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
+  const size_t smem1 = (size_t)dev::kStageOff + kWarps * (size_t)a.stage_bytes;
+  a.nstage = resident_blocks((const void*)k, kWarps * 32, smem2) * kWarps >= 16 ? 2 : 1;
+  if (const char* e = getenv("LW_QSTAGES")) a.nstage = atoi(e) == 1 ? 1 : 2;
+  const size_t smem = a.nstage == 2 ? smem2 : smem1;
   return launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
     k<<<blocks, kWarps * 32, smem, st>>>(a);
   });
@@ -99,6 +112,7 @@ lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cu
   a.words = b->words;
   a.tile_off = b->tile_off;
   a.lane_bits = b->lane_bits;
+  a.lane_mid = b->lane_mid;
   a.table = b->table;
   a.out = static_cast<uint8_t*>(out);
   a.status = status;

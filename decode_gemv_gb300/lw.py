@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(HERE, "_build", "liblw.so")
 
 LW_FMT_Q4_PAIR, LW_FMT_Q6, LW_FMT_BF16_EXP = 1, 2, 3
 SECTION_NAMES = ["words", "tile_off", "lane_bits", "table", "qparams", "signman",
-                 "vflags", "vrow_off", "vexp"]
+                 "vflags", "vrow_off", "vexp", "lane_mid"]
 STATUS_NAMES = {0: "LW_OK", 1: "LW_ERR_INVALID_ARG", 2: "LW_ERR_SHAPE", 3: "LW_ERR_UNSUPPORTED",
                 4: "LW_ERR_ALLOC", 5: "LW_ERR_CORRUPT", 6: "LW_ERR_CUDA"}
 DEV_STATUS = {0: "ok", 1: "lane length", 2: "bad code", 3: "tile size", 4: "timeout",
@@ -42,7 +42,7 @@ class LwDesc(ctypes.Structure):
 
 
 class LwSections(ctypes.Structure):
-    _fields_ = [("ptr", ctypes.c_void_p * 9), ("bytes", ctypes.c_uint64 * 9),
+    _fields_ = [("ptr", ctypes.c_void_p * 10), ("bytes", ctypes.c_uint64 * 10),
                 ("coded_bytes", ctypes.c_uint64), ("n_tiles", ctypes.c_uint64),
                 ("n_verbatim", ctypes.c_int64), ("max_tile_rows", ctypes.c_int32),
                 ("max_len", ctypes.c_int32), ("min_len", ctypes.c_int32),
@@ -58,7 +58,7 @@ class LwDevBundle(ctypes.Structure):
                 ("lane_bits", ctypes.c_void_p), ("table", ctypes.c_void_p),
                 ("qparams", ctypes.c_void_p), ("signman", ctypes.c_void_p),
                 ("vflags", ctypes.c_void_p), ("vrow_off", ctypes.c_void_p),
-                ("vexp", ctypes.c_void_p)]
+                ("vexp", ctypes.c_void_p), ("lane_mid", ctypes.c_void_p)]
 
 
 _lib = None

@@ -68,7 +68,8 @@ typedef enum {
 /* device-side error codes written to *d_status */
 enum {
   LW_DEV_OK = 0,
-  LW_DEV_LANE_LENGTH = 1,   /* a lane ended at a bit count other than lane_bits */
+  LW_DEV_LANE_LENGTH = 1,   /* a lane (or its first row) ended at a bit count
+                               other than lane_bits (lane_mid) */
   LW_DEV_BAD_CODE = 2,      /* a peek matched no codeword (incomplete table) */
   LW_DEV_TILE_SIZE = 3,     /* a tile is longer than max_tile_rows */
   LW_DEV_TIMEOUT = 4,       /* a bounded wait on an asynchronous copy ran out */
@@ -157,6 +158,10 @@ enum {
   LW_SEC_VROW_OFF,    /* BF16: uint32 [N + 1]: verbatim groups before row r. */
   LW_SEC_VEXP,        /* BF16: uint8 [n_verbatim][64]: raw exponent bytes of
                          each verbatim group, ordered by row, then group. */
+  LW_SEC_LANE_MID,    /* uint16 [n_tiles][32]: bit offset in each lane where
+                         its second row (2l+1) starts, so a decoder can run the
+                         lane's two rows as independent streams (coded bundles
+                         only; an extension of the per-tile lane offsets). */
   LW_NUM_SECTIONS
 };
 
@@ -198,6 +203,7 @@ typedef struct {
   const uint32_t* vflags;
   const uint32_t* vrow_off;
   const uint8_t* vexp;
+  const uint16_t* lane_mid;
 } lw_dev_bundle;
 
 /*

@@ -272,9 +272,21 @@ def encode(fmt: int, payload: np.ndarray) -> dict:
                            _p(tile_off), _p(lane_bits), _p(words))
     if rc:
         raise ValueError(f"pack failed {rc}")
+    # bit offset where each lane's second row starts: the code lengths of the
+    # symbols of its first row, summed
+    if fmt == Q4:
+        first = np.full(nsym.shape, 128)
+    elif fmt == Q6:
+        first = np.full(nsym.shape, 256)
+    else:
+        vl = lanes_from_rows(sp["verbatim"], 4).reshape(-1, 32, 8)
+        first = 64 * (4 - vl[:, :, :4].sum(axis=2))
+    in_first = np.arange(maxsym)[None, None, :] < first[:, :, None]
+    lane_mid = (length.astype(np.int64)[np.where(in_first, syms, 0)] * in_first).sum(axis=2)
+    lane_mid = lane_mid.astype(np.uint16)
     out = dict(fmt=fmt, rows=payload.shape[0], cols=payload.shape[1], code_len=length,
-               words=words, tile_off=tile_off, lane_bits=lane_bits, nsym=nsym,
-               histogram=used)
+               words=words, tile_off=tile_off, lane_bits=lane_bits, lane_mid=lane_mid,
+               nsym=nsym, histogram=used)
     if sp is not None:
         out.update(palette=sp["palette"], verbatim=sp["verbatim"], vexp=sp["vexp"],
                    sm=sp["sm"])

@@ -128,7 +128,7 @@ def test_oracle_built_bundle_decodes_on_gpu():
     table = lw.lw_table_from_lengths(lw.LW_FMT_Q4_PAIR, ob["code_len"])
     tf = lw.table_fields(table)
     secs = dict(words=ob["words"], tile_off=ob["tile_off"], lane_bits=ob["lane_bits"],
-                table=table, qparams=hb.sections["qparams"])
+                table=table, qparams=hb.sections["qparams"], lane_mid=ob["lane_mid"])
     wt = int(np.diff(ob["tile_off"]).max())
     lw.lw_validate_sections(lw.LW_FMT_Q4_PAIR, n, k, secs, wt)
     db = lw.DeviceBundle(lw.LW_FMT_Q4_PAIR, False, n, k, secs, wt, tf["lmin"], tf["lmax"], DEV)

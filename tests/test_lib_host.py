@@ -36,7 +36,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lw.EXPORTED)
-    assert lw.load().lw_version() == 1
+    assert lw.load().lw_version() == 2
 
 
 def _q4(seed, rows, cols, sd=1.6):
@@ -59,6 +59,11 @@ def test_q4_library_bundle_decodes_with_oracle(sd):
     assert bits_lib == bits_or
     hist = ob["histogram"]
     assert int((hist * tb["code_len"]).sum()) == bits_or
+    # per-lane second-row offsets: the library's code lengths summed over the
+    # first row's symbols (lane order from the oracle)
+    syms = oracle.lanes_from_rows(oracle.q4_pair_symbols(m["codes"]), 128)
+    want_mid = tb["code_len"].astype(np.int64)[syms[:, :, :128]].sum(axis=2)
+    assert np.array_equal(hb.view("lane_mid", np.uint16).reshape(-1, 32), want_mid)
     # the oracle's lane bit counts agree with the library's per lane
     _, used = oracle.decode_lanes(tb["code_len"], words, toff, np.full((len(toff) - 1, 32), 256, np.int32), 256)
     assert np.array_equal(used, hb.view("lane_bits", np.uint16).reshape(-1, 32).astype(np.uint32))
@@ -96,7 +101,7 @@ def test_oracle_bundle_passes_library_validation_and_table_rebuild():
     qp = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"]).sections["qparams"]
     wt = np.diff(ob["tile_off"]).max()
     secs = dict(words=ob["words"], tile_off=ob["tile_off"], lane_bits=ob["lane_bits"],
-                table=table, qparams=qp)
+                table=table, qparams=qp, lane_mid=ob["lane_mid"])
     lw.lw_validate_sections(lw.LW_FMT_Q4_PAIR, 128, 512, secs, int(wt))
     bad = dict(secs, tile_off=ob["tile_off"].copy())
     bad["tile_off"][3] += 1
@@ -180,6 +185,10 @@ def test_bf16_sections_against_oracle():
     assert np.array_equal(out, m["bits"])
     ob = oracle.encode(oracle.BF16, m["bits"])
     assert int(hb.view("lane_bits", np.uint16).astype(np.int64).sum()) == int(ob["lane_bits"].astype(np.int64).sum())
+    # second-row offsets: the same wherever the two optimal codes agree on
+    # the first row's length (always, if the code lengths coincide)
+    if np.array_equal(tb["code_len"][:16], ob["code_len"]):
+        assert np.array_equal(hb.view("lane_mid", np.uint16).reshape(-1, 32), ob["lane_mid"])
 
 
 def test_encode_rejects_bad_arguments():

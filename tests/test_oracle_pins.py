@@ -209,6 +209,9 @@ def test_lane_layout_brute_force_q4():
         assert b["tile_off"][t + 1] - b["tile_off"][t] == wt
         for l, x in enumerate(strs):
             assert b["lane_bits"][t, l] == len(x)
+            first_row = [int(codes[64 * s + 2 * l, k]) | int(codes[64 * s + 2 * l, k + 1]) << 4
+                         for k in range(256 * kt, 256 * kt + 256, 2)]
+            assert b["lane_mid"][t, l] == len(expected_lane_bits(first_row, L, C))
             x = x.ljust(32 * wt, "0")
             for j in range(wt):
                 word = b["words"][(b["tile_off"][t] + j) * 32 + l]
