@@ -66,7 +66,8 @@ lw_status check_dev_bundle(const lw_dev_bundle* b, bool want_twin, bool product)
     return fail(LW_ERR_SHAPE, "matrix too large");
   if (want_twin && !b->twin) return fail(LW_ERR_INVALID_ARG, "expected a twin bundle");
   if (!want_twin && product && b->twin) return fail(LW_ERR_INVALID_ARG, "expected a coded bundle, got a twin");
-  if (!b->words || !b->tile_off || !b->lane_bits || !b->table)
+  // words may be absent only when no tile has a coded row (all verbatim)
+  if ((!b->words && b->max_tile_rows > 0) || !b->tile_off || !b->lane_bits || !b->table)
     return fail(LW_ERR_INVALID_ARG, "missing words/tile_off/lane_bits/table");
   if (!b->twin && !b->lane_mid) return fail(LW_ERR_INVALID_ARG, "missing lane_mid");
   if (!aligned16(b->words)) return fail(LW_ERR_INVALID_ARG, "words must be 16-byte aligned");
@@ -107,9 +108,12 @@ static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, f
   if (ws_bytes < lw_workspace_bytes(b, batch))
     return fail(LW_ERR_INVALID_ARG, "workspace of %zu bytes < %zu", ws_bytes, lw_workspace_bytes(b, batch));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (b->fmt == LW_FMT_BF16_EXP)
+  if (b->fmt == LW_FMT_BF16_EXP) {
+    if ((reinterpret_cast<uintptr_t>(X) & 15u) != 0)
+      return fail(LW_ERR_INVALID_ARG, "x must be 16-byte aligned");
     return launch_bf16_product(b, static_cast<const uint16_t*>(X), batch, Y,
                                static_cast<float*>(ws), d_status, st);
+  }
   // activation rows in chunks of up to 8 (each chunk decodes the matrix once)
   for (int b0 = 0; b0 < batch; b0 += 8) {
     const int nb = batch - b0 < 8 ? batch - b0 : 8;

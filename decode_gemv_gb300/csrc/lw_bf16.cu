@@ -1,17 +1,109 @@
-// BF16 exponent-coded weights: kernels and launchers (placeholder until the
-// BF16 path lands).
+// Launchers for the BF16 exponent-coded kernels (lw_bkern.cuh).
+#include "lw_bkern.cuh"
 #include "lw_internal.h"
 #include "lw_launch.h"
 
 namespace lw {
 
-lw_status launch_bf16_product(const lw_dev_bundle*, const uint16_t*, int, float*, float*, int32_t*,
-                              cudaStream_t) {
-  return fail(LW_ERR_UNSUPPORTED, "BF16 products are not built yet");
+namespace {
+
+using BKernel = void (*)(const dev::BArgs);
+
+int ncmp_bucket_b(int span) { return span <= 4 ? 4 : (span <= 8 ? 8 : 10); }
+
+template <bool TWIN, int BP>
+BKernel pick_b_product(int ncmp) {
+  if (TWIN) return dev::b_product_kernel<true, BP, 0>;
+  switch (ncmp) {
+    case 4: return dev::b_product_kernel<false, BP, 4>;
+    case 8: return dev::b_product_kernel<false, BP, 8>;
+    default: return dev::b_product_kernel<false, BP, 10>;
+  }
 }
 
-lw_status launch_bf16_decode(const lw_dev_bundle*, void*, int32_t*, cudaStream_t) {
-  return fail(LW_ERR_UNSUPPORTED, "BF16 decode is not built yet");
+template <bool TWIN>
+BKernel pick_b_product_bp(int bp, int ncmp) {
+  switch (bp) {
+    case 1: return pick_b_product<TWIN, 1>(ncmp);
+    case 2: return pick_b_product<TWIN, 2>(ncmp);
+    case 4: return pick_b_product<TWIN, 4>(ncmp);
+    default: return pick_b_product<TWIN, 8>(ncmp);
+  }
+}
+
+BKernel pick_b_decode(bool twin, int ncmp) {
+  if (twin) return dev::b_decode_kernel<true, 0>;
+  switch (ncmp) {
+    case 4: return dev::b_decode_kernel<false, 4>;
+    case 8: return dev::b_decode_kernel<false, 8>;
+    default: return dev::b_decode_kernel<false, 10>;
+  }
+}
+
+dev::BArgs common_args(const lw_dev_bundle* b) {
+  dev::BArgs a{};
+  a.words = b->words;
+  a.tile_off = b->tile_off;
+  a.lane_bits = b->lane_bits;
+  a.lane_mid = b->twin ? nullptr : b->lane_mid;
+  a.table = b->table;
+  a.signman = b->signman;
+  a.vflags = b->vflags;
+  a.vrow_off = b->vrow_off;
+  a.vexp = b->vexp;
+  a.TK = (int)(b->cols / 256);
+  a.N = (int)b->rows;
+  a.K = (int)b->cols;
+  a.GW = (int)((b->cols / 64 + 31) / 32);
+  a.n_tiles = (int)tiles_of(b->rows, b->cols);
+  a.stage_rows = b->max_tile_rows + dev::kLookahead;
+  return a;
+}
+
+}  // namespace
+
+lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
+                              float* ws, int32_t* status, cudaStream_t st) {
+  const bool twin = b->twin != 0;
+  const int ncmp = twin ? 0 : ncmp_bucket_b(b->lmax - b->lmin);
+  for (int b0 = 0; b0 < batch; b0 += 8) {
+    const int nb = batch - b0 < 8 ? batch - b0 : 8;
+    const int bp = nb <= 1 ? 1 : (nb <= 2 ? 2 : (nb <= 4 ? 4 : 8));
+    BKernel k = twin ? pick_b_product_bp<true>(bp, ncmp) : pick_b_product_bp<false>(bp, ncmp);
+    dev::BArgs a = common_args(b);
+    a.x = x + (size_t)b0 * b->cols;
+    a.ws = ws;
+    a.counters = workspace_counters(b, ws);
+    a.y = y + (size_t)b0 * b->rows;
+    a.status = status;
+    a.batch = nb;
+    // stage: coded rows | activations bf16 (bp x 512 B) | lane_mid (64 B) |
+    // activations fp32 (bp x 1 KB)
+    a.x_offset = a.stage_rows * 128;
+    a.mid_offset = a.x_offset + bp * 512;
+    a.xf_offset = a.mid_offset + 128;
+    a.stage_bytes = (a.xf_offset + bp * 1024 + 127) / 128 * 128;
+    const size_t smem = (size_t)dev::kBStageOff + (size_t)a.stage_bytes;
+    lw_status s = launch_persistent((const void*)k, 1, smem, a.n_tiles, st, [&](int blocks) {
+      k<<<blocks, 32, smem, st>>>(a);
+    });
+    if (s != LW_OK) return s;
+  }
+  return LW_OK;
+}
+
+lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st) {
+  const bool twin = b->twin != 0;
+  BKernel k = pick_b_decode(twin, twin ? 0 : ncmp_bucket_b(b->lmax - b->lmin));
+  dev::BArgs a = common_args(b);
+  a.out = static_cast<uint16_t*>(out);
+  a.status = status;
+  a.mid_offset = a.stage_rows * 128;
+  a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
+  const size_t smem = (size_t)dev::kBStageOff + (size_t)a.stage_bytes;
+  return launch_persistent((const void*)k, 1, smem, a.n_tiles, st, [&](int blocks) {
+    k<<<blocks, 32, smem, st>>>(a);
+  });
 }
 
 }  // namespace lw
