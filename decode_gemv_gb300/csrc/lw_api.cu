@@ -91,9 +91,10 @@ using namespace lw;
 
 extern "C" size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch) {
   if (!b || batch < 1 || b->rows <= 0 || b->cols <= 0) return 0;
-  // partials for up to 8 activation rows (the counters sit after the 8-row
-  // partials so that every batch size finds them at the same place)
-  return workspace_partials_bytes(b, 8) + (size_t)(b->rows / 64) * sizeof(uint32_t);
+  size_t part = workspace_partials_bytes(b, 8);
+  if (b->fmt == LW_FMT_BF16_EXP && !b->twin && batch >= 16 && workspace_tc_bytes(b) > part)
+    part = workspace_tc_bytes(b);
+  return workspace_counter_bytes(b) + part;
 }
 
 static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, float* Y, void* ws,
@@ -102,7 +103,7 @@ static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, f
   lw_status s = check_dev_bundle(b, twin, true);
   if (s != LW_OK) return s;
   if (!X || !Y || !ws) return fail(LW_ERR_INVALID_ARG, "NULL x/y/workspace");
-  if (batch < 1 || batch > 64) return fail(LW_ERR_INVALID_ARG, "batch %d outside 1..64", batch);
+  if (batch < 1 || batch > 256) return fail(LW_ERR_INVALID_ARG, "batch %d outside 1..256", batch);
   if (!aligned16(X) || (reinterpret_cast<uintptr_t>(Y) & 7u) || !aligned16(ws))
     return fail(LW_ERR_INVALID_ARG, "x/workspace must be 16-byte aligned, y 8-byte aligned");
   if (ws_bytes < lw_workspace_bytes(b, batch))
@@ -111,14 +112,26 @@ static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, f
   if (b->fmt == LW_FMT_BF16_EXP) {
     if ((reinterpret_cast<uintptr_t>(X) & 15u) != 0)
       return fail(LW_ERR_INVALID_ARG, "x must be 16-byte aligned");
-    return launch_bf16_product(b, static_cast<const uint16_t*>(X), batch, Y,
-                               static_cast<float*>(ws), d_status, st);
+    const uint16_t* xb = static_cast<const uint16_t*>(X);
+    if (!b->twin && batch >= 16) {
+      // tensor cores (tcgen05) for up to 64 activation rows per launch
+      for (int b0 = 0; b0 < batch; b0 += 64) {
+        const int nb = batch - b0 < 64 ? batch - b0 : 64;
+        s = nb >= 16 ? launch_bf16_tc_product(b, xb + (size_t)b0 * b->cols, nb,
+                                              Y + (size_t)b0 * b->rows, ws, d_status, st)
+                     : launch_bf16_product(b, xb + (size_t)b0 * b->cols, nb,
+                                           Y + (size_t)b0 * b->rows, ws, d_status, st);
+        if (s != LW_OK) return s;
+      }
+      return LW_OK;
+    }
+    return launch_bf16_product(b, xb, batch, Y, ws, d_status, st);
   }
   // activation rows in chunks of up to 8 (each chunk decodes the matrix once)
   for (int b0 = 0; b0 < batch; b0 += 8) {
     const int nb = batch - b0 < 8 ? batch - b0 : 8;
     s = launch_q_product(b, static_cast<const float*>(X) + (size_t)b0 * b->cols, nb,
-                         Y + (size_t)b0 * b->rows, static_cast<float*>(ws), d_status, st);
+                         Y + (size_t)b0 * b->rows, ws, d_status, st);
     if (s != LW_OK) return s;
   }
   return LW_OK;

@@ -1,5 +1,5 @@
 // Launchers for the BF16 exponent-coded kernels (lw_bkern.cuh).
-#include "lw_bkern.cuh"
+#include "lw_btc.cuh"
 #include "lw_internal.h"
 #include "lw_launch.h"
 
@@ -60,10 +60,59 @@ dev::BArgs common_args(const lw_dev_bundle* b) {
   return a;
 }
 
+BKernel pick_b_tc(int ncmp) {
+  switch (ncmp) {
+    case 4: return dev::b_tc_kernel<4>;
+    case 8: return dev::b_tc_kernel<8>;
+    default: return dev::b_tc_kernel<10>;
+  }
+}
+
 }  // namespace
 
+// Tensor-core product for 16..64 activation rows (one launch).
+lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
+                                 void* ws, int32_t* status, cudaStream_t st) {
+  BKernel k = pick_b_tc(ncmp_bucket_b(b->lmax - b->lmin));
+  dev::BArgs a = common_args(b);
+  a.x = x;
+  a.y = y;
+  a.ws = workspace_partials(b, ws);
+  a.counters = workspace_counters(b, ws);
+  a.status = status;
+  a.batch = batch;
+  a.bpad = (batch + 15) / 16 * 16;
+  a.tmem_cols = a.bpad * 2 <= 32 ? 32 : (a.bpad * 2 <= 64 ? 64 : 128);
+  a.mid_offset = a.stage_rows * 128;
+  a.stage_bytes = (a.mid_offset + 128 + 127) / 128 * 128;
+  a.slab_off = 1024;
+  a.xs_off = a.slab_off + 2 * dev::kSlots * dev::kSlabBytes;
+  a.wstage_off = a.xs_off + a.bpad * 512;
+  size_t smem = (size_t)a.wstage_off + 4 * (size_t)a.stage_bytes;
+  // at most 512 / tmem_cols resident CTAs per SM, so tensor memory never runs out
+  int dev_id = 0, per_sm_smem = 0;
+  cudaGetDevice(&dev_id);
+  cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev_id);
+  const int max_ctas = 512 / a.tmem_cols;
+  const size_t floor_smem = (size_t)per_sm_smem / (size_t)(max_ctas + 1) + 1;
+  if (smem < floor_smem) smem = floor_smem;
+  const int per_sm = resident_blocks((const void*)k, 128, smem);
+  if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
+  const int n_blocks = (int)((b->rows / 64 + 3) / 4);
+  const int slots = per_sm * device_sm_count();
+  int nsplit = (slots + n_blocks - 1) / n_blocks;
+  if (nsplit > kTcMaxSplit) nsplit = kTcMaxSplit;
+  if (nsplit > a.TK) nsplit = a.TK;
+  if (nsplit < 1) nsplit = 1;
+  a.nsplit = nsplit;
+  int grid = n_blocks * nsplit;
+  if (grid > slots) grid = slots;
+  k<<<grid, 128, smem, st>>>(a);
+  return check_launch("tensor-core product kernel");
+}
+
 lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
-                              float* ws, int32_t* status, cudaStream_t st) {
+                              void* ws, int32_t* status, cudaStream_t st) {
   const bool twin = b->twin != 0;
   const int ncmp = twin ? 0 : ncmp_bucket_b(b->lmax - b->lmin);
   for (int b0 = 0; b0 < batch; b0 += 8) {
@@ -72,7 +121,7 @@ lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int bat
     BKernel k = twin ? pick_b_product_bp<true>(bp, ncmp) : pick_b_product_bp<false>(bp, ncmp);
     dev::BArgs a = common_args(b);
     a.x = x + (size_t)b0 * b->cols;
-    a.ws = ws;
+    a.ws = workspace_partials(b, ws);
     a.counters = workspace_counters(b, ws);
     a.y = y + (size_t)b0 * b->rows;
     a.status = status;

@@ -44,6 +44,8 @@ struct BArgs {
   int n_tiles, TK, N, K, GW, batch;
   int stage_rows, stage_bytes;
   int x_offset, mid_offset, xf_offset;   // byte offsets inside a stage
+  // tensor-core product only
+  int nsplit, bpad, tmem_cols, slab_off, xs_off, wstage_off;
 };
 
 // shared-memory map (bytes) for the BF16 kernels

@@ -42,21 +42,38 @@ lw_status launch_persistent(const void* kernel, int warps, size_t smem, int n_ti
   return check_launch("product kernel");
 }
 
-// Partial sums fp32 [K/256][min(batch, 8)][N], then one uint32 counter per
-// 64-row strip (16-byte aligned).
+// Workspace layout: one uint32 split-K counter per 64-row strip (padded to
+// 256 bytes), then fp32 partial sums -- [K/256][min(batch, 8)][N] for the
+// CUDA-core products, [split <= kTcMaxSplit][64][N] for the tensor-core BF16
+// product.  The counters sit first so that every path finds them at the same
+// place; every call that completes leaves them at zero.
+constexpr int kTcMaxSplit = 8;
+inline size_t workspace_counter_bytes(const lw_dev_bundle* b) {
+  return ((size_t)(b->rows / 64) * sizeof(uint32_t) + 255) / 256 * 256;
+}
 inline size_t workspace_partials_bytes(const lw_dev_bundle* b, int batch) {
   const size_t chunk = batch > 8 ? 8 : (size_t)batch;
-  return ((size_t)(b->cols / 256) * chunk * (size_t)b->rows * sizeof(float) + 15) / 16 * 16;
+  return (size_t)(b->cols / 256) * chunk * (size_t)b->rows * sizeof(float);
+}
+inline size_t workspace_tc_bytes(const lw_dev_bundle* b) {
+  return (size_t)kTcMaxSplit * 64 * (size_t)b->rows * sizeof(float);
 }
 inline uint32_t* workspace_counters(const lw_dev_bundle* b, void* ws) {
-  return reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + workspace_partials_bytes(b, 8));
+  (void)b;
+  return static_cast<uint32_t*>(ws);
+}
+inline float* workspace_partials(const lw_dev_bundle* b, void* ws) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + workspace_counter_bytes(b));
 }
 
-lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, float* ws,
+// ws: the caller's whole workspace (counters, then partial sums)
+lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
                            int32_t* status, cudaStream_t st);
 lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);
 lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
-                              float* ws, int32_t* status, cudaStream_t st);
+                              void* ws, int32_t* status, cudaStream_t st);
 lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);
+lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
+                                 void* ws, int32_t* status, cudaStream_t st);
 
 }  // namespace lw

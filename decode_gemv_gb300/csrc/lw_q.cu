@@ -54,7 +54,7 @@ QKernel pick_decode(int ncmp) {
 
 }  // namespace
 
-lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, float* ws,
+lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
                            int32_t* status, cudaStream_t st) {
   const int fmt = b->fmt;
   const bool twin = b->twin != 0;
@@ -73,7 +73,7 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   a.table = b->table;
   a.qparams = static_cast<const uint8_t*>(b->qparams);
   a.x = x;
-  a.ws = ws;
+  a.ws = workspace_partials(b, ws);
   a.counters = workspace_counters(b, ws);
   a.y = y;
   a.status = status;

@@ -280,9 +280,16 @@ lw_status lw_decode_gemv(const lw_dev_bundle* b, const void* x, float* y,
 
 /*
  * Fused decode + small-batch product: Y[b][r] = sum_k W[r][k] X[b][k],
- * X [batch][K] row-major (fp32, or bf16 for BF16), Y fp32 [batch][N].
- * Same order as lw_decode_gemv per activation row.  batch 1..64; the BF16
- * format uses tensor cores (tcgen05, BF16 x BF16 -> FP32) for batch >= 16.
+ * X [batch][K] row-major (fp32, or bf16 for BF16), Y fp32 [batch][N],
+ * batch 1..256.  The 4-/6-bit formats work on CUDA cores, up to 8 activation
+ * rows per pass (larger batches in passes of 8), each row in the order of
+ * lw_decode_gemv.  The BF16 format takes the same CUDA-core path for fewer
+ * than 16 rows; from 16 rows on it rebuilds BF16 weights in shared memory and
+ * multiplies on the tensor cores (tcgen05.mma, BF16 x BF16 -> FP32 in tensor
+ * memory; up to 64 rows per pass), [UW] "How reconstructive matmul works":
+ * the order within the tensor core is the hardware's, then K-splits are added
+ * in ascending order -- deterministic, but not bitwise equal to the CUDA-core
+ * path.  The workspace must hold lw_workspace_bytes(b, batch) bytes.
  */
 lw_status lw_decode_gemm(const lw_dev_bundle* b, const void* X, int32_t batch,
                          float* Y, void* ws, size_t ws_bytes,

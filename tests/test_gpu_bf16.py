@@ -149,3 +149,37 @@ def test_full_size_llama_mlp(index):
     assert st == 0
     Y1, _ = run_product(upload(m["bits"])[1], m["x"][:1])
     assert np.array_equal(Y1.view(np.uint32), Yt.view(np.uint32))
+
+
+@pytest.mark.parametrize("shape,batch", [((256, 1024), 16), ((192, 768), 17), ((512, 512), 32),
+                                         ((256, 2048), 48), ((320, 1024), 64), ((128, 256), 64),
+                                         ((256, 1024), 80)])
+def test_bf16_tensor_core_batches(shape, batch):
+    """Batches >= 16 take the tcgen05 path (BF16 rebuilt in shared memory,
+    FP32 accumulation in tensor memory); checked against the oracle and
+    against the CUDA-core path fed 8 activation rows at a time."""
+    n, k = shape
+    m = inputs.small_bf16(5 * n + batch, n, k, batch=batch)
+    _, db = upload(m["bits"])
+    Y, st = run_product(db, m["x"])
+    assert st == 0
+    ref = oracle.reference_output(oracle.BF16, m)
+    absprod = oracle.abs_row_products(oracle.BF16, m)
+    assert_close(Y, ref, absprod)
+    Yc = np.concatenate([run_product(db, m["x"][b: b + 8])[0] for b in range(0, batch, 8)])
+    assert_close(Y, Yc, absprod)
+    Y2, st = run_product(db, m["x"])           # twice in a row: counters reset
+    assert st == 0 and np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+
+
+def test_bf16_tensor_core_full_size_down():
+    spec = inputs.workload_specs(inputs.LLAMA_MLP_BF16)[2]
+    m = inputs.make_matrix(inputs.LLAMA_MLP_BF16, spec, 0, 2, batch=64)
+    _, db = upload(m["bits"])
+    rows = np.unique(np.concatenate([np.arange(0, spec.rows, 97), [spec.rows - 1]]))
+    sub = dict(bits=m["bits"][rows], x=m["x"])
+    for b in (16, 64):
+        Y, st = run_product(db, m["x"][:b])
+        assert st == 0
+        assert_close(Y[:, rows], oracle.reference_output(oracle.BF16, dict(sub, x=m["x"][:b])),
+                     oracle.abs_row_products(oracle.BF16, dict(sub, x=m["x"][:b])))
