@@ -133,7 +133,7 @@ lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int bat
     a.xf_offset = a.mid_offset + 128;
     a.stage_bytes = (a.xf_offset + bp * 1024 + 127) / 128 * 128;
     const size_t smem = (size_t)dev::kBStageOff + (size_t)a.stage_bytes;
-    lw_status s = launch_persistent((const void*)k, 1, smem, a.n_tiles, st, [&](int blocks) {
+    lw_status s = launch_persistent((const void*)k, 32, smem, a.n_tiles, st, [&](int blocks) {
       k<<<blocks, 32, smem, st>>>(a);
     });
     if (s != LW_OK) return s;
@@ -150,7 +150,7 @@ lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status,
   a.mid_offset = a.stage_rows * 128;
   a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
   const size_t smem = (size_t)dev::kBStageOff + (size_t)a.stage_bytes;
-  return launch_persistent((const void*)k, 1, smem, a.n_tiles, st, [&](int blocks) {
+  return launch_persistent((const void*)k, 32, smem, a.n_tiles, st, [&](int blocks) {
     k<<<blocks, 32, smem, st>>>(a);
   });
 }

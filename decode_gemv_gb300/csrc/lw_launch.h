@@ -21,22 +21,21 @@ inline lw_status check_launch(const char* what) {
   return LW_OK;
 }
 
-// Launch a persistent grid: as many blocks as are resident on the device, but
-// no more than there are tiles to share among `warps`-warp blocks.
+// Launch a persistent grid of `threads`-thread blocks that each own one tile
+// at a time: as many blocks as are resident on the device, but no more than
+// it takes to give every block the same number of tiles.
 template <class Launch>
-lw_status launch_persistent(const void* kernel, int warps, size_t smem, int n_tiles,
+lw_status launch_persistent(const void* kernel, int threads, size_t smem, int n_tiles,
                             cudaStream_t st, Launch&& launch) {
   (void)st;
-  const int per_sm = resident_blocks(kernel, warps * 32, smem);
+  const int per_sm = resident_blocks(kernel, threads, smem);
   if (per_sm < 1)
     return fail(LW_ERR_UNSUPPORTED, "kernel does not fit on an SM (%zu bytes of shared memory)",
                 smem);
-  // every warp gets the same number of tiles: the fewest warps that still
-  // take ceil(n_tiles / resident warps) tiles each
-  const long long resident_warps = (long long)per_sm * device_sm_count() * warps;
-  const long long per_warp = (n_tiles + resident_warps - 1) / resident_warps;
-  const long long want_warps = per_warp > 0 ? (n_tiles + per_warp - 1) / per_warp : 1;
-  long long blocks = (want_warps + warps - 1) / warps;
+  // the fewest blocks that still take ceil(n_tiles / resident blocks) tiles each
+  const long long resident = (long long)per_sm * device_sm_count();
+  const long long per_block = (n_tiles + resident - 1) / resident;
+  long long blocks = per_block > 0 ? (n_tiles + per_block - 1) / per_block : 1;
   if (blocks < 1) blocks = 1;
   launch((int)blocks);
   return check_launch("product kernel");

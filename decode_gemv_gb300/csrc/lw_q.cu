@@ -11,23 +11,18 @@ namespace lw {
 
 namespace {
 
-// One warp per CTA: tiles then spread evenly over the SMs, whatever the
-// matrix size (a persistent grid of 4-warp CTAs left some SMs with twice the
-// tiles of others on small matrices).
-constexpr int kWarps = 1;
-
 int ncmp_bucket(int span) { return span <= 4 ? 4 : (span <= 7 ? 7 : (span <= 8 ? 8 : 10)); }
 
 using QKernel = void (*)(const dev::QArgs);
 
 template <int FMT, bool TWIN, int BP>
 QKernel pick_product(int ncmp) {
-  if (TWIN) return dev::q_product_kernel<FMT, true, BP, 0, kWarps>;
+  if (TWIN) return dev::q_product_kernel<FMT, true, BP, 0>;
   switch (ncmp) {
-    case 4: return dev::q_product_kernel<FMT, false, BP, 4, kWarps>;
-    case 7: return dev::q_product_kernel<FMT, false, BP, 7, kWarps>;
-    case 8: return dev::q_product_kernel<FMT, false, BP, 8, kWarps>;
-    default: return dev::q_product_kernel<FMT, false, BP, 10, kWarps>;
+    case 4: return dev::q_product_kernel<FMT, false, BP, 4>;
+    case 7: return dev::q_product_kernel<FMT, false, BP, 7>;
+    case 8: return dev::q_product_kernel<FMT, false, BP, 8>;
+    default: return dev::q_product_kernel<FMT, false, BP, 10>;
   }
 }
 
@@ -43,12 +38,12 @@ QKernel pick_product_b(int bp, int ncmp) {
 
 template <int FMT, bool TWIN>
 QKernel pick_decode(int ncmp) {
-  if (TWIN) return dev::q_decode_kernel<FMT, true, 0, kWarps>;
+  if (TWIN) return dev::q_decode_kernel<FMT, true, 0>;
   switch (ncmp) {
-    case 4: return dev::q_decode_kernel<FMT, false, 4, kWarps>;
-    case 7: return dev::q_decode_kernel<FMT, false, 7, kWarps>;
-    case 8: return dev::q_decode_kernel<FMT, false, 8, kWarps>;
-    default: return dev::q_decode_kernel<FMT, false, 10, kWarps>;
+    case 4: return dev::q_decode_kernel<FMT, false, 4>;
+    case 7: return dev::q_decode_kernel<FMT, false, 7>;
+    case 8: return dev::q_decode_kernel<FMT, false, 8>;
+    default: return dev::q_decode_kernel<FMT, false, 10>;
   }
 }
 
@@ -86,16 +81,16 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   const int qpb = qparam_tile_bytes(fmt);
   a.mid_offset = a.stage_rows * 128 + qpb + bp * 1024;
   a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
-  // two stages per warp while that still leaves 16 resident warps per SM,
-  // else one stage (twice the warps; each warp then waits for its own next
-  // tile, other warps cover the wait)
-  const size_t smem2 = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
-  const size_t smem1 = (size_t)dev::kStageOff + kWarps * (size_t)a.stage_bytes;
-  a.nstage = resident_blocks((const void*)k, kWarps * 32, smem2) * kWarps >= 16 ? 2 : 1;
+  // two stages per CTA while that still leaves 16 resident warps per SM,
+  // else one stage (more resident CTAs; a CTA then waits for its own next
+  // tile, other CTAs cover the wait)
+  const size_t smem2 = (size_t)dev::kStageOff + 2 * (size_t)a.stage_bytes;
+  const size_t smem1 = (size_t)dev::kStageOff + (size_t)a.stage_bytes;
+  a.nstage = resident_blocks((const void*)k, dev::kQThreads, smem2) * (dev::kQThreads / 32) >= 16 ? 2 : 1;
   if (const char* e = getenv("LW_QSTAGES")) a.nstage = atoi(e) == 1 ? 1 : 2;
   const size_t smem = a.nstage == 2 ? smem2 : smem1;
-  return launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
-    k<<<blocks, kWarps * 32, smem, st>>>(a);
+  return launch_persistent((const void*)k, dev::kQThreads, smem, a.n_tiles, st, [&](int blocks) {
+    k<<<blocks, dev::kQThreads, smem, st>>>(a);
   });
 }
 
@@ -112,7 +107,7 @@ lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cu
   a.words = b->words;
   a.tile_off = b->tile_off;
   a.lane_bits = b->lane_bits;
-  a.lane_mid = b->lane_mid;
+  a.lane_mid = twin ? nullptr : b->lane_mid;
   a.table = b->table;
   a.out = static_cast<uint8_t*>(out);
   a.status = status;
@@ -121,10 +116,11 @@ lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cu
   a.K = (int)b->cols;
   a.n_tiles = (int)tiles_of(b->rows, b->cols);
   a.stage_rows = b->max_tile_rows + dev::kLookahead;
-  a.stage_bytes = (a.stage_rows * 128 + 127) / 128 * 128;
-  const size_t smem = (size_t)dev::kStageOff + 2 * kWarps * (size_t)a.stage_bytes;
-  return launch_persistent((const void*)k, kWarps, smem, a.n_tiles, st, [&](int blocks) {
-    k<<<blocks, kWarps * 32, smem, st>>>(a);
+  a.mid_offset = a.stage_rows * 128;
+  a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
+  const size_t smem = (size_t)dev::kStageOff + 2 * (size_t)a.stage_bytes;
+  return launch_persistent((const void*)k, dev::kQThreads, smem, a.n_tiles, st, [&](int blocks) {
+    k<<<blocks, dev::kQThreads, smem, st>>>(a);
   });
 }
 

@@ -9,11 +9,15 @@
 // decode fused into the GEMV; the fixed-width twin).
 //
 // GB300 mapping (ours, not the pages'):
-//  * one warp owns one tile at a time; lane l decodes lane stream l;
-//  * a persistent grid; each warp double-buffers its tiles in shared memory,
-//    filled by bulk asynchronous copies (TMA engine, no multicast) completed
-//    on an mbarrier: the tile's coded rows, its scales/mins and the matching
-//    256-column slice of every activation row;
+//  * a persistent grid of two-warp CTAs; a CTA owns one tile at a time and
+//    lane l of warp h decodes row 2l + h of the tile: lane l's first row
+//    from the start of its stream, its second from the recorded mid offset,
+//    so the tile's 64 rows run as 64 independent streams;
+//  * each CTA stages its tiles in shared memory (one or two buffers), filled
+//    by bulk asynchronous copies (TMA engine, no multicast) completed on an
+//    mbarrier: the tile's coded rows, its scales/mins, the lanes' mid offsets
+//    and the matching 256-column slice of every activation row; the decoder
+//    table arrives the same way, once per CTA, and is checked lane-parallel;
 //  * the interleave puts word j of lane l at shared word 32j + l, so every
 //    lane's refill hits bank l: conflict-free however far lanes drift apart;
 //  * a lane keeps three stream words in registers; one 32-bit window serves
@@ -58,8 +62,8 @@ struct QArgs {
   int n_tiles, TK, N, K, batch;
   int stage_rows;        // rows of 128 B per stage buffer = max_tile_rows + 3
   int stage_bytes;       // bytes per stage buffer (multiple of 128)
-  int nstage;            // stage buffers per warp: 2 (prefetch the next tile
-                         // while decoding) or 1 (more resident warps)
+  int nstage;            // stage buffers per CTA: 2 (prefetch the next tile
+                         // while decoding) or 1 (more resident CTAs)
   int mid_offset;        // byte offset of the tile's lane_mid copy in a stage
 };
 
@@ -74,29 +78,33 @@ template <> struct QFmt<LW_FMT_Q6> {
 };
 
 // shared-memory map (bytes)
-constexpr int kOffOff = 0;       // uint32[16]: symbol-table base address per length index
-constexpr int kFlagOff = 64;     // int: table rejected
-constexpr int kTabOff = 128;     // symbol values: float2[256] (4-bit) / float[64]
-constexpr int kBarOff = 2176;    // uint64 mbarriers, 2 per warp (<= 8 warps)
-constexpr int kStageOff = 2304;  // per warp: one or two stage buffers
-constexpr int kLookahead = 3;    // stream words a lane holds in registers
+constexpr int kOffOff = 0;        // 64 B: symbol-table entry address per length index (put_off)
+constexpr int kFlagOff = 64;      // int: "this CTA adds the strip's partials" broadcast
+constexpr int kTabOff = 128;      // symbol values: float2[256] (4-bit) / float[64]; decode: uint32[256]
+constexpr int kBarOff = 2176;     // uint64 mbarriers: stage 0, stage 1, table
+constexpr int kRawTabOff = 2304;  // the bundle's lw_table, bulk-copied once per CTA
+constexpr int kStageOff = 3328;   // one or two stage buffers
+constexpr int kLookahead = 3;     // stream words a lane holds in registers
+constexpr int kQThreads = 64;     // two warps per CTA, one per row of each lane
+static_assert(kRawTabOff + (int)sizeof(lw_table) <= kStageOff, "shared-memory map");
 
 __host__ __device__ constexpr int q_x_offset(int stage_rows, int qp_bytes) {
   return stage_rows * 128 + qp_bytes;
 }
 
 // Issue the copies of tile t, whose coded rows are [r0, r1), into one stage
-// (whole warp; lane 0 issues).  Returns false if the tile is longer than the stage allows (the other copies
-// are still issued, so the barrier completes).
+// (thread `lead` issues; every caller gets the result).  Returns false if the
+// tile is longer than the stage allows (the other copies are still issued,
+// so the barrier completes).
 template <int FMT, bool PRODUCT>
 __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint32_t r0, uint32_t r1,
-                                        uint8_t* stage, uint64_t* bar, int lane) {
+                                        uint8_t* stage, uint64_t* bar, bool lead) {
   const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(a.stage_rows - kLookahead);
-  if (lane == 0) {
+  if (lead) {
     const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
     constexpr uint32_t qpb = PRODUCT ? QFmt<FMT>::qp_bytes : 0u;
     const uint32_t xbytes = PRODUCT ? (uint32_t)a.batch * 1024u : 0u;
-    const uint32_t mbytes = (PRODUCT && a.lane_mid) ? 64u : 0u;
+    const uint32_t mbytes = a.lane_mid ? 64u : 0u;
     mbar_arrive_expect_tx(bar, wbytes + qpb + xbytes + mbytes);
     if (wbytes) bulk_g2s(stage, a.words + (size_t)r0 * 32, wbytes, bar);
     if (PRODUCT) {
@@ -105,10 +113,48 @@ __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint32_t r0, uint
       uint8_t* xs = stage + q_x_offset(a.stage_rows, qpb);
       for (int b = 0; b < a.batch; ++b)
         bulk_g2s(xs + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024, bar);
-      if (mbytes) bulk_g2s(stage + a.mid_offset, a.lane_mid + (size_t)t * 32, 64, bar);
     }
+    if (mbytes) bulk_g2s(stage + a.mid_offset, a.lane_mid + (size_t)t * 32, 64, bar);
   }
   return fits;
+}
+
+// Start the bulk copy of the decoder table into shared memory (thread 0).
+__device__ __forceinline__ void table_issue(uint8_t* smem, const lw_table* tb, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, (uint32_t)sizeof(lw_table));
+  bulk_g2s(smem + kRawTabOff, tb, (uint32_t)sizeof(lw_table), bar);
+}
+
+// Checks of a staged table by one warp (every warp of a CTA may run them;
+// they agree): the format, the length span fits the launch's comparator
+// count, limits ascend, every limit below the longest length is even in
+// 11-bit peek space (the comparator tests 10-bit peeks against limit / 2),
+// and every window maps to an index inside the symbol table.  Lane j checks
+// length index j.  True if the table is good.
+__device__ __forceinline__ bool table_ok_warp(const lw_table* tb, int want_fmt, int want_alpha,
+                                              int ncmp, int lane) {
+  const int lmin = tb->lmin, lmax = tb->lmax;
+  const int n_entries = tb->n_sym + (tb->phantom ? 1 : 0);
+  bool ok = tb->fmt == want_fmt && tb->alpha == want_alpha && lmin >= 1 &&
+            lmax <= LW_MAX_CODE_LEN && lmin <= lmax && lmax - lmin <= ncmp &&
+            n_entries >= 1 && n_entries <= want_alpha;
+  if (ok && lane < 12) {
+    const int nl = lmax - lmin, j = lane;
+    const uint32_t hi = tb->lim_m1[j];
+    if (j >= nl) ok = ok && hi == 0xFFFFFFFFu;
+    if (j < nl) ok = ok && ((((hi + 1u) >> 21) & 1u) == 0u);
+    if (j <= nl) {
+      const int L = lmin + j;
+      const uint32_t prev_hi = j > 0 ? tb->lim_m1[j - 1] : 0u;
+      if (j > 0) ok = ok && hi >= prev_hi && prev_hi != 0xFFFFFFFFu;
+      const uint32_t cmax = hi >> (32 - L);
+      const uint32_t cmin = j == 0 ? 0u : (prev_hi + 1u) >> (32 - L);
+      const long long lo_idx = (long long)tb->off[j] + cmin;
+      const long long hi_idx = (long long)tb->off[j] + cmax;
+      ok = ok && lo_idx >= 0 && hi_idx < n_entries;
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Lane bit reader over a staged tile.  Registers cur:nxt:nx2 hold stream
@@ -169,12 +215,19 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cas
 // The comparator thresholds of a table as fp16 pairs.  Every limit below the
 // longest length is even in the 11-bit peek space, so the first 10 window
 // bits p decide each test exactly: with v = 1024 + p and T = 1024 + limit/2
-// (both exact in fp16), the saturating sum v + (1 - T) = p - limit/2 + 1,
-// clamped to [0, 1], is 1 exactly when the peek reaches the limit.  One
-// fp16x2 add tests two limits; unused slots hold a limit no peek reaches.
+// (both exact in fp16), v >= T exactly when the peek reaches the limit.  One
+// fp16x2 compare tests two limits and yields a 0xFFFF / 0 mask per half;
+// unused slots hold T = 2048, which no peek reaches.  The masks are merged by
+// bit selects into one word in which every reached limit owns the same
+// number of set bits (kScale), so one population count gives kScale times
+// the number of limits reached -- which is also the byte offset of that
+// length's entry in the offset table (entries kScale bytes apart).
 template <int NP>
 struct Cmp {
-  uint32_t c[NP > 0 ? NP : 1];   // fp16x2: (1 - T_2k, 1 - T_2k+1)
+  static constexpr int kScale = NP <= 1 ? 16 : (NP == 2 ? 8 : 4);
+  static constexpr int kShift = NP <= 1 ? 4 : (NP == 2 ? 3 : 2);
+  static_assert(NP <= 5, "at most 10 limits");
+  uint32_t c[NP > 0 ? NP : 1];   // fp16x2: (T_2k, T_2k+1)
   __device__ __forceinline__ void load(const lw_table* tb, int ncmp) {
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
@@ -184,40 +237,57 @@ struct Cmp {
         const int q = 2 * k + h;
         // lim_m1 = (limit << 21) - 1  ->  limit / 2 = (lim_m1 + 1) >> 22
         const uint32_t half_lim = q < ncmp ? ((tb->lim_m1[q] + 1u) >> 22) : 1024u;
-        lohi[h] = __half_as_ushort(__float2half_rn(1.f - (1024.f + (float)half_lim)));
+        lohi[h] = __half_as_ushort(__float2half_rn(1024.f + (float)half_lim));
       }
       c[k] = lohi[0] | (lohi[1] << 16);
     }
   }
-  // number of limits the window's code reaches (0 .. 2*NP)
-  __device__ __forceinline__ int count(uint32_t w) const {
+  static __device__ __forceinline__ uint32_t sel(uint32_t a, uint32_t b, uint32_t k) {
+    return (a & k) | (b & ~k);
+  }
+  // kScale * (number of limits the window's code reaches)
+  __device__ __forceinline__ uint32_t count(uint32_t w) const {
     const __half2 v = as_h2((w >> 22) * 0x00010001u + 0x64006400u);
-    __half2 s[NP > 0 ? NP : 1];
+    uint32_t m[NP > 0 ? NP : 1];
 #pragma unroll
-    for (int k = 0; k < NP; ++k) s[k] = __hadd2_sat(v, as_h2(c[k]));
-#pragma unroll
-    for (int step = 1; step < NP; step *= 2)
-#pragma unroll
-      for (int k = 0; k + step < NP; k += 2 * step) s[k] = __hadd2(s[k], s[k + step]);
-    // low half: 1024 + s.lo + s.hi  ->  bits 0x6400 + count
-    const __half2 r = __hadd2(__hadd2(s[0], as_h2(0x00006400u)), __lowhigh2highlow(s[0]));
-    return (int)(h2_bits(r) & 0xFFFFu) - 0x6400;
+    for (int k = 0; k < NP; ++k) m[k] = __hge2_mask(v, as_h2(c[k]));
+    if constexpr (NP <= 1) {
+      return __popc(m[0]);
+    } else if constexpr (NP == 2) {
+      return __popc(sel(m[0], m[1], 0x55555555u));
+    } else if constexpr (NP == 3) {
+      return __popc(sel(sel(m[0], m[1], 0x55555555u), m[2] & 0x55555555u, 0x33333333u));
+    } else {
+      const uint32_t z = sel(sel(m[0], m[1], 0x55555555u), sel(m[2], m[3], 0x55555555u),
+                             0x33333333u);
+      if constexpr (NP == 4) return __popc(z);
+      else return __popc(z) + (__popc(m[4]) >> 2);
+    }
   }
 };
+
+// Write the offset-table entry of length index c (count() returns its byte
+// offset from the table start).
+template <int NP>
+__device__ __forceinline__ void put_off(uint8_t* smem, int c, uint32_t v) {
+  constexpr int S = Cmp<NP>::kScale;
+  if (c * S < 64) *reinterpret_cast<uint32_t*>(smem + kOffOff + c * S) = v;
+}
 
 // Decode two symbols from one window.  Returns the shared addresses of their
 // symbol-table entries (entry size ESZ bytes).
 template <int NP, int ESZ>
 __device__ __forceinline__ void q_decode2(LaneBits& lb, const Cmp<NP>& cmp, int lmin, uint32_t s_off,
                                           uint32_t& e0, uint32_t& e1) {
+  constexpr int SH = Cmp<NP>::kShift;
   const uint32_t w = lb.window();
-  const int c0 = cmp.count(w);
-  const int L0 = lmin + c0;
+  const uint32_t z0 = cmp.count(w);
+  const int L0 = lmin + (int)(z0 >> SH);
   const uint32_t w1 = w << L0;
-  const int c1 = cmp.count(w1);
-  const int L1 = lmin + c1;
-  e0 = lds_u32(s_off + 4u * (uint32_t)c0) + __funnelshift_l(w, 0u, L0) * ESZ;
-  e1 = lds_u32(s_off + 4u * (uint32_t)c1) + __funnelshift_l(w1, 0u, L1) * ESZ;
+  const uint32_t z1 = cmp.count(w1);
+  const int L1 = lmin + (int)(z1 >> SH);
+  e0 = lds_u32(s_off + z0) + __funnelshift_l(w, 0u, L0) * ESZ;
+  e1 = lds_u32(s_off + z1) + __funnelshift_l(w1, 0u, L1) * ESZ;
   lb.advance(L0 + L1);
 }
 
@@ -271,11 +341,12 @@ __device__ __forceinline__ uint32_t atom_inc_acq_rel(uint32_t* p, uint32_t wrap)
   return old;
 }
 
-// Partial sums of rows (row0, row0+1) for tile (strip, kt) -> workspace; the
+// One-warp version (a warp owns a tile; lane l holds rows 2l and 2l+1):
+// partial sums of rows (row0, row0+1) for tile (strip, kt) -> workspace; the
 // last tile of the strip to arrive adds all partials of the strip in
 // ascending tile order and writes y.
 template <int BP>
-__device__ __forceinline__ void q_commit(const QArgs& a, int strip, int kt, int lane,
+__device__ __forceinline__ void warp_commit(const QArgs& a, int strip, int kt, int lane,
                                          const float (&p0)[BP], const float (&p1)[BP]) {
   const int row0 = strip * 64 + 2 * lane;
 #pragma unroll
@@ -308,49 +379,97 @@ __device__ __forceinline__ void q_commit(const QArgs& a, int strip, int kt, int 
   }
 }
 
-// ---------------------------------------------------------------------------
-// Fused product kernel: one persistent grid of WARPS-warp CTAs.
-// ---------------------------------------------------------------------------
-// resident warps per SM the register budget is sized for (more activation
-// rows need more accumulator registers)
-__host__ __device__ constexpr int q_target_warps(int bp) { return bp <= 4 ? 16 : 12; }
+// Partial sums of row `row` (row 2l + h of strip `strip`) for tile column kt
+// -> workspace; then the CTA's thread 0 counts the tile in, and the CTA that
+// completes the strip adds all of its partials in ascending tile order and
+// writes y.  Ends with the stage released (the barrier follows every read of
+// it).
+template <int BP>
+__device__ __forceinline__ void q_commit(const QArgs& a, uint8_t* smem, int strip, int kt, int row,
+                                         const float (&part)[BP]) {
+#pragma unroll
+  for (int b = 0; b < BP; ++b)
+    if (b < a.batch) a.ws[((size_t)kt * a.batch + b) * a.N + row] = part[b];
+  // the barrier orders both warps' partials before thread 0's release; the
+  // last arriver's acquire (then the barrier) orders the reads after it
+  __syncthreads();
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
+  if (threadIdx.x == 0)
+    *flag = atom_inc_acq_rel(a.counters + strip, (unsigned)(a.TK - 1)) == (uint32_t)(a.TK - 1);
+  __syncthreads();
+  if (!*flag) return;
+  const size_t step = (size_t)a.batch * a.N;
+  for (int b = 0; b < a.batch; ++b) {
+    const float* base = a.ws + (size_t)b * a.N + row;
+    float s = __ldcg(base);
+    for (int k0 = 1; k0 < a.TK; k0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.TK) v[i] = __ldcg(base + (size_t)(k0 + i) * step);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.TK) s += v[i];
+    }
+    a.y[(size_t)b * a.N + row] = s;
+  }
+}
 
-template <int FMT, bool TWIN, int BP, int NCMP, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32, q_target_warps(BP) / WARPS)
-    q_product_kernel(const QArgs a) {
+// Stage the symbol table and the offsets of a checked table (whole CTA).
+// ESZ = bytes per symbol entry; VAL converts a symbol to its entry.
+template <int NP, int ESZ, class Val>
+__device__ __forceinline__ void table_stage(uint8_t* smem, const lw_table* tb, int alpha, Val val) {
+  const uint32_t s_tab = smem_addr(smem) + kTabOff;
+  if (threadIdx.x < 16)
+    put_off<NP>(smem, threadIdx.x,
+                s_tab + (uint32_t)(ESZ * (threadIdx.x < 12 ? tb->off[threadIdx.x] : 0)));
+  for (int i = threadIdx.x; i < alpha; i += blockDim.x) val(i, (uint32_t)tb->sym[i]);
+}
+
+// ---------------------------------------------------------------------------
+// Fused product kernel: one persistent grid of two-warp CTAs.
+// ---------------------------------------------------------------------------
+// resident CTAs per SM the register budget is sized for (more activation
+// rows need more accumulator registers)
+__host__ __device__ constexpr int q_min_ctas(int bp) { return bp <= 4 ? 16 : 12; }
+
+template <int FMT, bool TWIN, int BP, int NCMP>
+__global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(const QArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   using F = QFmt<FMT>;
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t s_off = sbase + kOffOff;
-  const uint32_t s_tab = sbase + kTabOff;
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int xoff = q_x_offset(a.stage_rows, F::qp_bytes);
+  constexpr int NP = (NCMP + 1) / 2;
   constexpr int ESZ = FMT == kQ4 ? 8 : 4;
+  const uint32_t s_off = smem_addr(smem) + kOffOff;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kRawTabOff);
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool lead = threadIdx.x == 0;
+  const int xoff = q_x_offset(a.stage_rows, F::qp_bytes);
 
   const bool two = a.nstage == 2;
-  uint8_t* stage0 = smem + kStageOff + (a.nstage * warp) * a.stage_bytes;
+  uint8_t* stage0 = smem + kStageOff;
   uint8_t* stage1 = two ? stage0 + a.stage_bytes : stage0;
-  uint64_t* bar = s_bar + 2 * warp;
-  const int nw = gridDim.x * WARPS;
-  int t = blockIdx.x * WARPS + warp;
+  const int nw = gridDim.x;
+  int t = blockIdx.x;
   // activation rows beyond `batch` stay zero in every stage
-  for (int i = a.batch * 256 + lane; i < BP * 256; i += 32) {
+  for (int i = a.batch * 256 + threadIdx.x; i < BP * 256; i += kQThreads) {
     reinterpret_cast<float*>(stage0 + xoff)[i] = 0.f;
     reinterpret_cast<float*>(stage1 + xoff)[i] = 0.f;
   }
-  if (lane == 0) {
+  if (lead) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
     fence_barrier_init();
   }
-  __syncwarp();
-  // the first tile's copy starts before the table is staged
+  __syncthreads();
+  // the table and the first tile are copied at once
+  if (!TWIN && lead) table_issue(smem, a.table, &bar[2]);
   uint32_t par0 = 0u, par1 = 0u;
   bool fit0 = true, fit1 = true;
   if (t < a.n_tiles)
     fit0 = q_issue<FMT, true>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), stage0,
-                              &bar[0], lane);
+                              &bar[0], lead);
   // row range of the next tile to issue (t + nw), loaded one tile ahead
   uint32_t nr0 = 0, nr1 = 0;
   if (t + nw < a.n_tiles) {
@@ -358,33 +477,27 @@ __global__ void __launch_bounds__(WARPS * 32, q_target_warps(BP) / WARPS)
     nr1 = __ldg(a.tile_off + t + nw + 1);
   }
 
+  Cmp<NP> cmp;
+  int lmin = 1;
   if (!TWIN) {
-    if (threadIdx.x == 0)
-      *reinterpret_cast<int*>(smem + kFlagOff) = table_ok(a.table, FMT, F::alpha, NCMP) ? 0 : 1;
-    if (threadIdx.x < 16)
-      reinterpret_cast<uint32_t*>(smem + kOffOff)[threadIdx.x] =
-          s_tab + (uint32_t)(ESZ * (threadIdx.x < 12 ? a.table->off[threadIdx.x] : 0));
-    for (int i = threadIdx.x; i < F::alpha; i += blockDim.x) {
-      const uint32_t sy = a.table->sym[i];
+    const bool got = __syncthreads_and(mbar_wait(&bar[2], 0u));
+    const bool ok = got && __syncthreads_and(table_ok_warp(tb, FMT, F::alpha, NCMP, lane));
+    if (!ok) {
+      if (lead) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
+      if (!got) mbar_wait(&bar[2], 0u);        // let the copies in flight land
+      if (t < a.n_tiles) mbar_wait(&bar[0], 0u);
+      return;
+    }
+    table_stage<NP, ESZ>(smem, tb, F::alpha, [&](int i, uint32_t sy) {
       if (FMT == kQ4)
         reinterpret_cast<float2*>(smem + kTabOff)[i] =
             make_float2(16.f + (float)(sy & 15u), 16.f + (float)((sy >> 4) & 15u));
       else
         reinterpret_cast<float*>(smem + kTabOff)[i] = 64.f + (float)(sy & 63u);
-    }
-  }
-  __syncthreads();
-  if (!TWIN && *reinterpret_cast<volatile int*>(smem + kFlagOff)) {
-    if (threadIdx.x == 0) report(a.status, LW_DEV_BAD_TABLE);
-    if (t < a.n_tiles) mbar_wait(&bar[0], 0u);   // let the first copy land
-    return;
-  }
-  constexpr int NP = (NCMP + 1) / 2;
-  Cmp<NP> cmp;
-  int lmin = 1;
-  if (!TWIN) {
-    cmp.load(a.table, a.table->lmax - a.table->lmin);
-    lmin = a.table->lmin;
+    });
+    cmp.load(tb, tb->lmax - tb->lmin);
+    lmin = tb->lmin;
+    __syncthreads();
   }
 
   for (int it = 0; t < a.n_tiles; ++it, t += nw) {
@@ -395,16 +508,16 @@ __global__ void __launch_bounds__(WARPS * 32, q_target_warps(BP) / WARPS)
       nr0 = __ldg(a.tile_off + t + 2 * nw);
       nr1 = __ldg(a.tile_off + t + 2 * nw + 1);
     }
+    // two stages: the other one was released by the barrier that closed the
+    // previous tile
     if (two && more) {
-      __syncwarp();
-      fence_proxy_async();
-      if (odd) fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lane);
-      else fit1 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage1, &bar[1], lane);
+      if (odd) fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lead);
+      else fit1 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage1, &bar[1], lead);
     }
     uint8_t* st = odd ? stage1 : stage0;
-    const bool ok = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
-    if (!ok) {
-      if (lane == 0) report(a.status, LW_DEV_TIMEOUT);
+    const bool got = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
+    if (!__syncthreads_and(got)) {
+      if (lead) report(a.status, LW_DEV_TIMEOUT);
       if (two && more) {   // let the copy in flight land before leaving
         if (odd) mbar_wait(&bar[0], par0);
         else mbar_wait(&bar[1], par1);
@@ -414,164 +527,103 @@ __global__ void __launch_bounds__(WARPS * 32, q_target_warps(BP) / WARPS)
     if (odd) par1 ^= 1u; else par0 ^= 1u;
     const bool fit = odd ? fit1 : fit0;
     const int strip = t / a.TK, kt = t % a.TK;
-    float part0[BP], part1[BP];   // rows 2l and 2l+1
+    float part[BP];
 #pragma unroll
-    for (int b = 0; b < BP; ++b) part0[b] = part1[b] = 0.f;
-    if (!fit) {
-      if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
-      if (!two && more) {
-        __syncwarp();
-        fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lane);
-      }
-      q_commit<BP>(a, strip, kt, lane, part0, part1);
-      continue;
-    }
+    for (int b = 0; b < BP; ++b) part[b] = 0.f;
     const uint32_t wb = smem_addr(st);
     const uint32_t qp = wb + (uint32_t)a.stage_rows * 128u;
     const uint32_t sx = wb + (uint32_t)xoff;
-
-    LaneBits lb;
-    if (!TWIN) lb.init(wb, lane, a.stage_rows);
-
-    if (FMT == kQ4) {
+    if (!fit) {
+      if (lead) report(a.status, LW_DEV_TILE_SIZE);
+    } else if (FMT == kQ4) {
       float S[BP];
 #pragma unroll
       for (int b = 0; b < BP; ++b) S[b] = tile_sum256(sx + 1024u * b, lane);
-      const uint2 q2 = lds_u2(qp + 8u * (uint32_t)lane);   // rows 2l, 2l+1: (scale | min<<16)
-      if (!TWIN) {
-        // rows 2l and 2l+1 are decoded as two independent streams (the second
-        // starts at the lane's recorded mid offset); 64 symbol pairs each,
-        // the table entries of pair j read while pair j+1 is decoded
-        const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
-        LaneBits lr;
-        lr.init_at(wb, lane, a.stage_rows, mid);
-        float2 acc0[BP], acc1[BP];
+      const uint32_t q2 = lds_u32(qp + 4u * (uint32_t)(2 * lane + h));   // scale | min << 16
+      float2 acc[BP];
 #pragma unroll
-        for (int b = 0; b < BP; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
-        uint32_t a0, a1, c0, c1;
-        q_decode2<NP, 8>(lb, cmp, lmin, s_off, a0, a1);
-        q_decode2<NP, 8>(lr, cmp, lmin, s_off, c0, c1);
-#pragma unroll 2
+      for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
+      if (!TWIN) {
+        // this lane's row as one stream: 128 pair symbols decoded two at a
+        // time, the table entries of step j read while step j+1 is decoded
+        const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
+        LaneBits lb;
+        lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
+        uint32_t e0, e1;
+        q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
+#pragma unroll 4
         for (int j = 0; j < 64; ++j) {
-          const float2 va0 = lds_f2(a0), va1 = lds_f2(a1), vc0 = lds_f2(c0), vc1 = lds_f2(c1);
-          if (j < 63) {
-            q_decode2<NP, 8>(lb, cmp, lmin, s_off, a0, a1);
-            q_decode2<NP, 8>(lr, cmp, lmin, s_off, c0, c1);
-          }
+          const float2 v0 = lds_f2(e0), v1 = lds_f2(e1);
+          if (j < 63) q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float4 xv = lds_f4(sx + 1024u * b + 16u * (uint32_t)j);
-            acc0[b] = __ffma2_rn(va0, make_float2(xv.x, xv.y), acc0[b]);
-            acc0[b] = __ffma2_rn(va1, make_float2(xv.z, xv.w), acc0[b]);
-            acc1[b] = __ffma2_rn(vc0, make_float2(xv.x, xv.y), acc1[b]);
-            acc1[b] = __ffma2_rn(vc1, make_float2(xv.z, xv.w), acc1[b]);
+            acc[b] = __ffma2_rn(v0, make_float2(xv.x, xv.y), acc[b]);
+            acc[b] = __ffma2_rn(v1, make_float2(xv.z, xv.w), acc[b]);
           }
         }
-        const float sc0 = __half2float(__ushort_as_half((unsigned short)(q2.x & 0xFFFFu)));
-        const float mn0 = __half2float(__ushort_as_half((unsigned short)(q2.x >> 16)));
-        const float sc1 = __half2float(__ushort_as_half((unsigned short)(q2.y & 0xFFFFu)));
-        const float mn1 = __half2float(__ushort_as_half((unsigned short)(q2.y >> 16)));
-#pragma unroll
-        for (int b = 0; b < BP; ++b) {
-          part0[b] = fmaf(sc0, (acc0[b].x + acc0[b].y) - 16.f * S[b], mn0 * S[b]);
-          part1[b] = fmaf(sc1, (acc1[b].x + acc1[b].y) - 16.f * S[b], mn1 * S[b]);
-        }
-        if (lb.consumed() != mid || lr.consumed() != (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane))
-          report(a.status, LW_DEV_LANE_LENGTH);
+        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
+        if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
       } else {
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float2 acc[BP];
-#pragma unroll
-          for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
 #pragma unroll 2
-          for (int jj = 0; jj < 32; ++jj) {
-            const uint32_t w = lds_u32(wb + (uint32_t)((32 * h + jj) * 128 + 4 * lane));
-            const float2 v0 = make_float2(q4_twin_val<9>(w), q4_twin_val<5>(w));
-            const float2 v1 = make_float2(q4_twin_val<1>(w), q4_twin_val<-3>(w));
-            const float2 v2 = make_float2(q4_twin_val<-7>(w), q4_twin_val<-11>(w));
-            const float2 v3 = make_float2(q4_twin_val<-15>(w), q4_twin_val<-19>(w));
-#pragma unroll
-            for (int b = 0; b < BP; ++b) {
-              const float4 xa = lds_f4(sx + 1024u * b + 32u * jj);
-              const float4 xb = lds_f4(sx + 1024u * b + 32u * jj + 16u);
-              acc[b] = __ffma2_rn(v0, make_float2(xa.x, xa.y), acc[b]);
-              acc[b] = __ffma2_rn(v1, make_float2(xa.z, xa.w), acc[b]);
-              acc[b] = __ffma2_rn(v2, make_float2(xb.x, xb.y), acc[b]);
-              acc[b] = __ffma2_rn(v3, make_float2(xb.z, xb.w), acc[b]);
-            }
-          }
-          const uint32_t qv = h ? q2.y : q2.x;
-          const float sc = __half2float(__ushort_as_half((unsigned short)(qv & 0xFFFFu)));
-          const float mn = __half2float(__ushort_as_half((unsigned short)(qv >> 16)));
+        for (int jj = 0; jj < 32; ++jj) {
+          const uint32_t w = lds_u32(wb + (uint32_t)((32 * h + jj) * 128 + 4 * lane));
+          const float2 v0 = make_float2(q4_twin_val<9>(w), q4_twin_val<5>(w));
+          const float2 v1 = make_float2(q4_twin_val<1>(w), q4_twin_val<-3>(w));
+          const float2 v2 = make_float2(q4_twin_val<-7>(w), q4_twin_val<-11>(w));
+          const float2 v3 = make_float2(q4_twin_val<-15>(w), q4_twin_val<-19>(w));
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
-            const float A = (acc[b].x + acc[b].y) - 16.f * S[b];
-            const float v = fmaf(sc, A, mn * S[b]);
-            if (h) part1[b] = v; else part0[b] = v;
+            const float4 xa = lds_f4(sx + 1024u * b + 32u * jj);
+            const float4 xb = lds_f4(sx + 1024u * b + 32u * jj + 16u);
+            acc[b] = __ffma2_rn(v0, make_float2(xa.x, xa.y), acc[b]);
+            acc[b] = __ffma2_rn(v1, make_float2(xa.z, xa.w), acc[b]);
+            acc[b] = __ffma2_rn(v2, make_float2(xb.x, xb.y), acc[b]);
+            acc[b] = __ffma2_rn(v3, make_float2(xb.z, xb.w), acc[b]);
           }
         }
       }
+      const float sc = __half2float(__ushort_as_half((unsigned short)(q2 & 0xFFFFu)));
+      const float mn = __half2float(__ushort_as_half((unsigned short)(q2 >> 16)));
+#pragma unroll
+      for (int b = 0; b < BP; ++b) part[b] = fmaf(sc, (acc[b].x + acc[b].y) - 16.f * S[b], mn * S[b]);
     } else {  // 6-bit
       float X[BP];
 #pragma unroll
       for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
       if (!TWIN) {
-        // both rows as independent streams, group by group
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
-        LaneBits lr;
-        lr.init_at(wb, lane, a.stage_rows, mid);
-        float rowp0[BP], rowp1[BP];
-#pragma unroll
-        for (int b = 0; b < BP; ++b) rowp0[b] = rowp1[b] = 0.f;
-        uint32_t a0, a1, c0, c1;
-        q_decode2<NP, 4>(lb, cmp, lmin, s_off, a0, a1);
-        q_decode2<NP, 4>(lr, cmp, lmin, s_off, c0, c1);
+        LaneBits lb;
+        lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
+        uint32_t e0, e1;
+        q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll 1
         for (int g = 0; g < 16; ++g) {
-          float2 acc0[BP], acc1[BP];
+          float2 acc[BP];
 #pragma unroll
-          for (int b = 0; b < BP; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+          for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
-            const float2 v0 = make_float2(lds_f32(a0), lds_f32(a1));
-            const float2 v1 = make_float2(lds_f32(c0), lds_f32(c1));
-            if (g < 15 || m < 7) {
-              q_decode2<NP, 4>(lb, cmp, lmin, s_off, a0, a1);
-              q_decode2<NP, 4>(lr, cmp, lmin, s_off, c0, c1);
-            }
+            const float2 v = make_float2(lds_f32(e0), lds_f32(e1));
+            if (g < 15 || m < 7) q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll
-            for (int b = 0; b < BP; ++b) {
-              const float2 xv = lds_f2(sx + 1024u * b + 64u * g + 8u * m);
-              acc0[b] = __ffma2_rn(v0, xv, acc0[b]);
-              acc1[b] = __ffma2_rn(v1, xv, acc1[b]);
-            }
+            for (int b = 0; b < BP; ++b)
+              acc[b] = __ffma2_rn(v, lds_f2(sx + 1024u * b + 64u * g + 8u * m), acc[b]);
           }
-          const uint32_t sa0 = qp + (uint32_t)((((g >> 3) * 32) + lane) * 16 + 2 * (g & 7));
-          const uint32_t sa1 = qp + (uint32_t)((((2 + (g >> 3)) * 32) + lane) * 16 + 2 * (g & 7));
-          const float s0 = __half2float(__ushort_as_half((unsigned short)lds_u16(sa0)));
-          const float s1 = __half2float(__ushort_as_half((unsigned short)lds_u16(sa1)));
+          // scale of group g of row 2l + h: chunk 2h + g/8, position g%8
+          const uint32_t sa = qp + (uint32_t)((((2 * h + (g >> 3)) * 32) + lane) * 16 + 2 * (g & 7));
+          const float sc = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], g);
-            rowp0[b] = fmaf(s0, (acc0[b].x + acc0[b].y) - 96.f * Xg, rowp0[b]);
-            rowp1[b] = fmaf(s1, (acc1[b].x + acc1[b].y) - 96.f * Xg, rowp1[b]);
+            part[b] = fmaf(sc, (acc[b].x + acc[b].y) - 96.f * Xg, part[b]);
           }
         }
-#pragma unroll
-        for (int b = 0; b < BP; ++b) {
-          part0[b] = rowp0[b];
-          part1[b] = rowp1[b];
-        }
-        if (lb.consumed() != mid || lr.consumed() != (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane))
-          report(a.status, LW_DEV_LANE_LENGTH);
+        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
+        if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
       } else {
-        float rowp[BP];
-#pragma unroll
-        for (int b = 0; b < BP; ++b) rowp[b] = 0.f;
 #pragma unroll 1
-        for (int G = 0; G < 32; ++G) {          // group g = G % 16 of row h = G / 16
-          const int h = G >> 4, g = G & 15;
+        for (int g = 0; g < 16; ++g) {
           float2 acc[BP];
 #pragma unroll
           for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
@@ -593,99 +645,90 @@ __global__ void __launch_bounds__(WARPS * 32, q_target_warps(BP) / WARPS)
             for (int b = 0; b < BP; ++b)
               acc[b] = __ffma2_rn(make_float2(v[2 * m], v[2 * m + 1]),
                                   lds_f2(sx + 1024u * b + 64u * g + 8u * m), acc[b]);
-          // scale of group g of row h: chunk (2h + g/8), position g%8
           const uint32_t sa = qp + (uint32_t)((((2 * h + (g >> 3)) * 32) + lane) * 16 + 2 * (g & 7));
           const float sc = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], g);
-            rowp[b] = fmaf(sc, (acc[b].x + acc[b].y) - 96.f * Xg, rowp[b]);
-          }
-          if (g == 15) {
-#pragma unroll
-            for (int b = 0; b < BP; ++b) {
-              if (h) part1[b] = rowp[b]; else part0[b] = rowp[b];
-              rowp[b] = 0.f;
-            }
+            part[b] = fmaf(sc, (acc[b].x + acc[b].y) - 96.f * Xg, part[b]);
           }
         }
       }
     }
-    if (!two && more) {   // single stage: refill it now, overlapping the commit
-      __syncwarp();
-      fence_proxy_async();
-      fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lane);
-    }
-    q_commit<BP>(a, strip, kt, lane, part0, part1);
+    // this thread's reads of the stage come before the next bulk copy into it
+    fence_proxy_async();
+    q_commit<BP>(a, smem, strip, kt, strip * 64 + 2 * lane + h, part);
+    if (!two && more)   // single stage: refill it now (released by the commit's barrier)
+      fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lead);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Decode only: restore fixed-width codes to HBM.
 //  Q4 -> packed bytes [N][K/2] (low nibble = even column); Q6 -> uint8 [N][K].
+//  Two-warp CTAs; lane l of warp h restores row 2l + h of each tile.
 // ---------------------------------------------------------------------------
-template <int FMT, bool TWIN, int NCMP, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
+template <int FMT, bool TWIN, int NCMP>
+__global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   using F = QFmt<FMT>;
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t s_off = sbase + kOffOff;
-  const uint32_t s_sym = sbase + kTabOff;   // uint32 per canonical index
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int n_sym = 0;
-  if (!TWIN) {
-    if (threadIdx.x == 0)
-      *reinterpret_cast<int*>(smem + kFlagOff) = table_ok(a.table, FMT, F::alpha, NCMP) ? 0 : 1;
-    if (threadIdx.x < 16)
-      reinterpret_cast<uint32_t*>(smem + kOffOff)[threadIdx.x] =
-          s_sym + (uint32_t)(4 * (threadIdx.x < 12 ? a.table->off[threadIdx.x] : 0));
-    for (int i = threadIdx.x; i < 256; i += blockDim.x)
-      reinterpret_cast<uint32_t*>(smem + kTabOff)[i] = a.table->sym[i];
-    n_sym = a.table->n_sym;
-  }
-  uint8_t* stage0 = smem + kStageOff + (2 * warp) * a.stage_bytes;
+  constexpr int NP = (NCMP + 1) / 2;
+  const uint32_t s_off = smem_addr(smem) + kOffOff;
+  const uint32_t s_sym = smem_addr(smem) + kTabOff;   // uint32 per canonical index
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kRawTabOff);
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool lead = threadIdx.x == 0;
+  uint8_t* stage0 = smem + kStageOff;
   uint8_t* stage1 = stage0 + a.stage_bytes;
-  uint64_t* bar = s_bar + 2 * warp;
-  if (lane == 0) {
+  const int nw = gridDim.x;
+  int t = blockIdx.x;
+  if (lead) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
     fence_barrier_init();
   }
   __syncthreads();
-  if (!TWIN && *reinterpret_cast<volatile int*>(smem + kFlagOff)) {
-    if (threadIdx.x == 0) report(a.status, LW_DEV_BAD_TABLE);
-    return;
-  }
-  constexpr int NP = (NCMP + 1) / 2;
-  Cmp<NP> cmp;
-  int lmin = 1;
-  if (!TWIN) {
-    cmp.load(a.table, a.table->lmax - a.table->lmin);
-    lmin = a.table->lmin;
-  }
-  const uint32_t first_bad = s_sym + 4u * (uint32_t)n_sym;   // entries at or past it are phantom
-  const int nw = gridDim.x * WARPS;
-  int t = blockIdx.x * WARPS + warp;
+  if (!TWIN && lead) table_issue(smem, a.table, &bar[2]);
   uint32_t par0 = 0u, par1 = 0u;
   bool fit0 = true, fit1 = true;
   if (t < a.n_tiles)
     fit0 = q_issue<FMT, false>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), stage0,
-                               &bar[0], lane);
+                               &bar[0], lead);
+  Cmp<NP> cmp;
+  int lmin = 1;
+  uint32_t first_bad = 0u;   // table entries at or past it are phantom
+  if (!TWIN) {
+    const bool got = __syncthreads_and(mbar_wait(&bar[2], 0u));
+    const bool ok = got && __syncthreads_and(table_ok_warp(tb, FMT, F::alpha, NCMP, lane));
+    if (!ok) {
+      if (lead) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
+      if (!got) mbar_wait(&bar[2], 0u);        // let the copies in flight land
+      if (t < a.n_tiles) mbar_wait(&bar[0], 0u);
+      return;
+    }
+    table_stage<NP, 4>(smem, tb, 256, [&](int i, uint32_t sy) {
+      reinterpret_cast<uint32_t*>(smem + kTabOff)[i] = sy;
+    });
+    cmp.load(tb, tb->lmax - tb->lmin);
+    lmin = tb->lmin;
+    first_bad = s_sym + 4u * (uint32_t)tb->n_sym;
+    __syncthreads();
+  }
   for (int it = 0; t < a.n_tiles; ++it, t += nw) {
     const bool odd = it & 1;
-    if (t + nw < a.n_tiles) {
-      __syncwarp();
-      fence_proxy_async();
+    const bool more = t + nw < a.n_tiles;
+    if (more) {   // the other stage was released by the barrier closing the previous tile
       const uint32_t ir0 = __ldg(a.tile_off + t + nw), ir1 = __ldg(a.tile_off + t + nw + 1);
-      if (odd) fit0 = q_issue<FMT, false>(a, t + nw, ir0, ir1, stage0, &bar[0], lane);
-      else fit1 = q_issue<FMT, false>(a, t + nw, ir0, ir1, stage1, &bar[1], lane);
+      if (odd) fit0 = q_issue<FMT, false>(a, t + nw, ir0, ir1, stage0, &bar[0], lead);
+      else fit1 = q_issue<FMT, false>(a, t + nw, ir0, ir1, stage1, &bar[1], lead);
     }
     uint8_t* st = odd ? stage1 : stage0;
-    const bool ok = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
-    if (!ok) {
-      if (lane == 0) report(a.status, LW_DEV_TIMEOUT);
-      if (t + nw < a.n_tiles) {
+    const bool got = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
+    if (!__syncthreads_and(got)) {
+      if (lead) report(a.status, LW_DEV_TIMEOUT);
+      if (more) {
         if (odd) mbar_wait(&bar[0], par0);
         else mbar_wait(&bar[1], par1);
       }
@@ -693,19 +736,18 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
     }
     if (odd) par1 ^= 1u; else par0 ^= 1u;
     if (!(odd ? fit1 : fit0)) {
-      if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
-      continue;
-    }
-    const uint32_t wb = smem_addr(st);
-    const int strip = t / a.TK, kt = t % a.TK;
-    LaneBits lb;
-    if (!TWIN) lb.init(wb, lane, a.stage_rows);
-    bool bad_len = false;
-    bool bad = false;
-    for (int h = 0; h < 2; ++h) {
-      if (!TWIN && h == 1 && lb.consumed() != (uint32_t)__ldg(a.lane_mid + (size_t)t * 32 + lane))
-        bad_len = true;
+      if (lead) report(a.status, LW_DEV_TILE_SIZE);
+    } else {
+      const uint32_t wb = smem_addr(st);
+      const int strip = t / a.TK, kt = t % a.TK;
       const size_t r = (size_t)strip * 64 + 2 * lane + h;
+      LaneBits lb;
+      uint32_t mid = 0;
+      if (!TWIN) {
+        mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
+        lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
+      }
+      bool bad = false;
       if (FMT == kQ4) {
         uint32_t* o = reinterpret_cast<uint32_t*>(a.out + r * (a.K / 2) + (size_t)kt * 128);
         for (int q = 0; q < 32; ++q) {
@@ -754,12 +796,14 @@ __global__ void __launch_bounds__(WARPS * 32) q_decode_kernel(const QArgs a) {
           o[q] = packed;
         }
       }
+      if (!TWIN) {
+        if (bad) report(a.status, LW_DEV_BAD_CODE);
+        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
+        if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
+      }
     }
-    if (!TWIN) {
-      if (bad) report(a.status, LW_DEV_BAD_CODE);
-      if (bad_len || lb.consumed() != (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane))
-        report(a.status, LW_DEV_LANE_LENGTH);
-    }
+    fence_proxy_async();
+    __syncthreads();   // both warps are done with this stage
   }
 }
 
