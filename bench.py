@@ -47,6 +47,10 @@ def parse():
     p.add_argument("--copies", type=int, default=0, help="layer copies to rotate (0 = auto)")
     p.add_argument("--twin", action="store_true",
                    help="time the fixed-width twin in the main loop instead (profiling)")
+    p.add_argument("--workload", default="mistral",
+                   choices=["mistral", "tiny", "phi3", "llama_mlp", "stack", "stack_bf16mlp"],
+                   help="mistral: the headline line; the others print one line each with "
+                        "per-batch rows (coded, twin and dense BF16 times)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip twin / bf16 / cpu baseline / e2e legs (profiling)")
     return p.parse_args()
@@ -501,10 +505,155 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
                                       f"GEMV, {reps} timed passes"}
 
 
+# ----------------------------------------------------------------------------
+# Per-workload sweeps (--workload): every synthetic workload, each batch
+# ----------------------------------------------------------------------------
+
+SWEEPS = {
+    # name: (workload id, label, batches, layers)
+    "tiny": (0, "tiny_q4_256x1024", [1], 1),
+    "phi3": (2, "phi3mini_layer_q6", [1, 2, 4, 8], 1),
+    "llama_mlp": (3, "llama31_8b_mlp_bf16exp", [1, 4, 16, 64], 1),
+    "stack": (4, "stack32_mistral_q4", [1, 2, 4, 8, 16, 32], 32),
+    "stack_bf16mlp": (4, "stack32_q4attn_bf16exp_mlp", [1, 2, 4, 8, 16, 32], 32),
+}
+
+
+def _fmt_of(spec_fmt):
+    from decode_gemv_gb300 import lw
+    return {1: lw.LW_FMT_Q4_PAIR, 2: lw.LW_FMT_Q6, 3: lw.LW_FMT_BF16_EXP}[spec_fmt]
+
+
+def _encode_job(job):
+    """Spawned worker: draw one matrix and encode it (coded and twin);
+    returns picklable bundle descriptions."""
+    workload, layer, index, spec = job
+    sys.path.insert(0, ROOT)
+    from decode_gemv_gb300 import inputs, lw
+    m = inputs.make_matrix(workload, spec, layer, index)
+    fmt = _fmt_of(spec.fmt)
+    payload = m["bits"] if spec.fmt == inputs.BF16 else m["codes"]
+    out = {}
+    for twin in (False, True):
+        hb = lw.lw_encode_bundle(fmt, payload, m.get("scales"), m.get("mins"), twin=twin)
+        out[twin] = (fmt, twin, spec.rows, spec.cols, hb.sections, hb.stats.max_tile_rows,
+                     hb.stats.min_len, hb.stats.max_len, hb.stats.coded_bytes)
+    return spec, out
+
+
+def sweep_specs(name):
+    from decode_gemv_gb300 import inputs
+    wid, _, _, layers = SWEEPS[name]
+    jobs = []
+    for layer in range(layers):
+        specs = inputs.workload_specs(wid)
+        if name == "stack_bf16mlp":
+            # attention projections 4-bit as the stack; MLP as the BF16 workload
+            mlp = inputs.workload_specs(inputs.LLAMA_MLP_BF16)
+            jobs += [(wid, layer, i, s) for i, s in enumerate(specs[:4])]
+            jobs += [(inputs.LLAMA_MLP_BF16, layer, i, s) for i, s in enumerate(mlp)]
+        else:
+            jobs += [(wid, layer, i, s) for i, s in enumerate(specs)]
+    return jobs
+
+
+def run_sweep(args):
+    """Time the coded path, the fixed-width twin and a dense BF16 GEMV/GEMM
+    (cuBLAS, same shapes) for every batch of one workload."""
+    import multiprocessing as mp
+    wid, label, batches, layers = SWEEPS[args.workload]
+    jobs = sweep_specs(args.workload)
+    t_prep = time.perf_counter()
+    if len(jobs) > 8:
+        with mp.get_context("spawn").Pool(min(16, os.cpu_count() or 4)) as pool:
+            built = pool.map(_encode_job, jobs, chunksize=1)
+    else:
+        built = [_encode_job(j) for j in jobs]
+    t_prep = time.perf_counter() - t_prep
+    import torch
+    from decode_gemv_gb300 import lw
+    lw.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    coded_total = sum(o[False][8] for _, o in built)
+    copies = max(1, math.ceil(4 * l2 / coded_total)) if coded_total < 4 * l2 else 1
+    mats = []
+    for spec, o in built:
+        mats.append(dict(spec=spec, fmt=o[False][0],
+                         db=[lw.DeviceBundle(*o[False][:8], device=dev, coded_bytes=o[False][8])
+                             for _ in range(copies)],
+                         tw=lw.DeviceBundle(*o[True][:8], device=dev, coded_bytes=o[True][8])))
+    del built
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    # dense comparator: random bf16 weights of the same shapes (cuBLAS time
+    # depends on the shape only)
+    dense = [torch.randn(m["spec"].rows, m["spec"].cols, device=dev, generator=gen,
+                         dtype=torch.bfloat16) for m in mats]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = peaks()
+    weights = sum(m["spec"].rows * m["spec"].cols for m in mats)
+    rows_out = []
+    clk = ClockSampler(0)
+    clk.start()
+    for B in batches:
+        xs, ys = [], []
+        for m in mats:
+            dt = torch.bfloat16 if m["fmt"] == lw.LW_FMT_BF16_EXP else torch.float32
+            xs.append(torch.randn(B, m["spec"].cols, device=dev, generator=gen).to(dt))
+            ys.append(torch.empty(B, m["spec"].rows, device=dev, dtype=torch.float32))
+        wsb = max(lw.lw_workspace_bytes(m["db"][0], B) for m in mats)
+        ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device=dev)
+        x_bytes = sum(x.numel() * x.element_size() for x in xs)
+        coded_step = sum(m["db"][0].coded_bytes for m in mats) + x_bytes
+        twin_step = sum(m["tw"].coded_bytes for m in mats) + x_bytes
+
+        def coded_calls(c):
+            return [(lambda d=m["db"][c], x=x, y=y: lw.lw_decode_gemm(d, x, B, y, ws, st))
+                    for m, x, y in zip(mats, xs, ys)]
+        graphs = [layer_graph(torch, coded_calls(c)) for c in range(copies)]
+        one = time_steps(torch, stream, lambda c: graphs[c].replay(), 3, 2, copies)
+        steps = max(10, min(args.steps, int(2000.0 / max(one, 1e-3))))
+        t_coded = time_steps(torch, stream, lambda c: graphs[c].replay(), steps, 5, copies)
+        del graphs
+        tg = layer_graph(torch, [(lambda d=m["tw"], x=x, y=y: lw.lw_twin_gemm(d, x, B, y, ws, st))
+                                 for m, x, y in zip(mats, xs, ys)])
+        t_twin = time_steps(torch, stream, lambda c: tg.replay(), steps, 5, 1)
+        del tg
+        xb = [x.to(torch.bfloat16) for x in xs]
+        yb = [torch.empty(B, w.shape[0], device=dev, dtype=torch.bfloat16) for w in dense]
+        bg = layer_graph(torch, [(lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y))
+                                 for w, x, y in zip(dense, xb, yb)])
+        t_bf16 = time_steps(torch, stream, lambda c: bg.replay(), steps, 5, 1)
+        del bg
+        gbs = coded_step / (t_coded * 1e-3) / 1e9
+        rows_out.append({"batch": B, "ms_per_step": t_coded, "coded_gbs": gbs,
+                         "frac_of_hbm": gbs / peak, "b_eff_gbs": 2.0 * weights / (t_coded * 1e-3) / 1e9,
+                         "twin_ms": t_twin, "twin_gbs": twin_step / (t_twin * 1e-3) / 1e9,
+                         "speedup_vs_twin": t_twin / t_coded,
+                         "bf16_ms": t_bf16, "speedup_vs_bf16": t_bf16 / t_coded,
+                         "coded_bytes_per_step": coded_step, "steps": steps})
+    clocks = clk.stop()
+    line = {"metric": METRIC, "workload": label, "value": rows_out[0]["coded_gbs"], "unit": "GB/s",
+            "n_gpus": 1, "higher_is_better": True, "dtype": "f32" if mats[0]["fmt"] != lw.LW_FMT_BF16_EXP else "bf16",
+            "data": "synthetic", "peak_gbs": peak, "peak_kind": peak_kind,
+            "config": {"workload": label, "layers": layers, "matrices": len(mats), "weights": weights,
+                       "l2": f"rotate {copies} device copies" if copies > 1 else "working set > 4x L2",
+                       "dense_comparator": "torch.matmul on random bf16 weights of the same shapes (cuBLAS)",
+                       "host_prep_s": round(t_prep, 1)},
+            "rows": rows_out, "clocks": clocks, "device_status": int(st.item())}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "mistral":
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -82,22 +82,41 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   a.status = status;
   a.batch = batch;
   a.bpad = (batch + 15) / 16 * 16;
-  a.tmem_cols = a.bpad * 2 <= 32 ? 32 : (a.bpad * 2 <= 64 ? 64 : 128);
+  const int need = dev::tc_tmem_need(a.bpad);
+  a.tmem_cols = need <= 32 ? 32 : (need <= 64 ? 64 : (need <= 128 ? 128 : 256));
   a.mid_offset = a.stage_rows * 128;
   a.stage_bytes = (a.mid_offset + 128 + 127) / 128 * 128;
-  a.slab_off = 1024;
-  a.xs_off = a.slab_off + 2 * dev::kSlots * dev::kSlabBytes;
-  a.wstage_off = a.xs_off + a.bpad * 512;
-  size_t smem = (size_t)a.wstage_off + 4 * (size_t)a.stage_bytes;
-  // at most 512 / tmem_cols resident CTAs per SM, so tensor memory never runs out
+  // header | X^T halves (2 x bpad x 256 B) | tile stages (4 strips x 2)
+  a.xs_off = dev::kTcXsOff;
+  a.wstage_off = a.xs_off + 2 * a.bpad * 256;
+  size_t smem = (size_t)a.wstage_off + 8 * (size_t)a.stage_bytes;
   int dev_id = 0, per_sm_smem = 0;
   cudaGetDevice(&dev_id);
   cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev_id);
+  // at most 512 / tmem_cols resident CTAs per SM (shared memory sees to it),
+  // so a tensor-memory allocation never has to wait
   const int max_ctas = 512 / a.tmem_cols;
   const size_t floor_smem = (size_t)per_sm_smem / (size_t)(max_ctas + 1) + 1;
   if (smem < floor_smem) smem = floor_smem;
-  const int per_sm = resident_blocks((const void*)k, 128, smem);
-  if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
+  if (resident_blocks((const void*)k, dev::kTcThreads, smem) < 1)   // also raises the smem limit
+    return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
+  // resident CTAs per SM from the kernel's own budgets (registers, shared
+  // memory, tensor-memory columns); the runtime's occupancy query answers 1
+  // for this kernel whatever its shared memory
+  int per_sm = max_ctas;
+  {
+    cudaFuncAttributes fa{};
+    int regs_sm = 65536, reserved = 1024;
+    cudaFuncGetAttributes(&fa, (const void*)k);
+    cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev_id);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev_id);
+    const int warp_regs = ((fa.numRegs + 7) / 8 * 8 * 32 + 255) / 256 * 256;
+    const int by_regs = regs_sm / (warp_regs * (dev::kTcThreads / 32));
+    const int by_smem = (int)((size_t)per_sm_smem / (smem + (size_t)reserved));
+    per_sm = by_regs < per_sm ? by_regs : per_sm;
+    per_sm = by_smem < per_sm ? by_smem : per_sm;
+    if (per_sm < 1) per_sm = 1;
+  }
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
   const int slots = per_sm * device_sm_count();
   int nsplit = (slots + n_blocks - 1) / n_blocks;
@@ -107,7 +126,7 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   a.nsplit = nsplit;
   int grid = n_blocks * nsplit;
   if (grid > slots) grid = slots;
-  k<<<grid, 128, smem, st>>>(a);
+  k<<<grid, dev::kTcThreads, smem, st>>>(a);
   return check_launch("tensor-core product kernel");
 }
 

@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(32, 12) b_product_kernel(const BArgs a) {
   if (!TWIN) {
     if (lane == 0) *reinterpret_cast<int*>(smem + kFlagOff) = table_ok(a.table, LW_FMT_BF16_EXP, 16, NCMP) ? 0 : 1;
     if (lane < 16) {
-      put_off<(NCMP + 1) / 2>(smem, lane,
+      put_off<(NCMP + 1) / 2>(reinterpret_cast<uint32_t*>(smem + kOffOff), lane,
           s_tab + (uint32_t)(4 * (lane < 12 ? a.table->off[lane] : 0)));
       const uint32_t sy = a.table->sym[lane] & 15u;
       reinterpret_cast<uint32_t*>(smem + kBTabOff)[lane] = (uint32_t)a.table->palette[sy] << 23;
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(32) b_decode_kernel(const BArgs a) {
   if (!TWIN) {
     if (lane == 0) *reinterpret_cast<int*>(smem + kFlagOff) = table_ok(a.table, LW_FMT_BF16_EXP, 16, NCMP) ? 0 : 1;
     if (lane < 16) {
-      put_off<(NCMP + 1) / 2>(smem, lane,
+      put_off<(NCMP + 1) / 2>(reinterpret_cast<uint32_t*>(smem + kOffOff), lane,
           s_tab + (uint32_t)(4 * (lane < 12 ? a.table->off[lane] : 0)));
       const uint32_t sy = a.table->sym[lane] & 15u;
       reinterpret_cast<uint32_t*>(smem + kBTabOff)[lane] = (uint32_t)a.table->palette[sy] << 23;

@@ -1,27 +1,37 @@
 // BF16 exponent-coded weights times a batch of 16..64 activation rows on the
-// 5th-generation tensor cores: decode, rebuild BF16 in shared memory, feed
+// 5th-generation tensor cores: decode, rebuild BF16 on chip, feed
 // tcgen05.mma (BF16 x BF16 -> FP32 in tensor memory).
 //
 // "Unweight: Compressing LLM Weights for Faster Inference", "How
 // reconstructive matmul works": compressed data is loaded, BF16 values are
-// reconstructed in shared memory and fed to the tensor cores without a trip
-// through main memory.  The Hopper producer/consumer/WGMMA design of the page
+// reconstructed on chip and fed to the tensor cores without a trip through
+// main memory.  The Hopper producer/consumer/WGMMA design of the page
 // becomes, on sm_103a:
-//  * a CTA of 4 warps owns 256 output rows (4 row strips) and a range of
-//    256-column tile columns; warp w decodes the tile of strip w;
-//  * the lane's two rows are decoded in 16-column chunks; after each chunk
-//    the 4 warps have written a 256 x 16 slab of BF16 weights into shared
-//    memory in the tensor core's K-major, no-swizzle layout (8x8 core
-//    matrices); one thread then issues two tcgen05.mma (M = 128 each, N =
-//    the padded batch, K = 16) against the matching slice of X^T, staged per
-//    tile column in the same layout, accumulating in tensor memory;
-//  * tcgen05.commit on a per-slot mbarrier tells the decoders when a slab
-//    buffer may be rewritten (a ring of kSlots slabs);
-//  * the accumulators are read back with tcgen05.ld (warp w reads tensor
-//    memory lanes 32w..32w+31); split-K partials are added in ascending
-//    split order by the last CTA of each 256-row block.
+//  * a CTA of 8 warps owns 256 output rows (4 row strips) and a range of
+//    256-column tile columns; warp w decodes row 2l + h (h = w / 4) of lane l
+//    of the tile of strip w % 4, one stream per lane (the lane's second row
+//    starts at its recorded mid offset);
+//  * the rebuilt BF16 weights go straight into tensor memory (tcgen05.st):
+//    the CTA's rows form two M = 128 operand tiles, tile h holding row
+//    2l + h of strip s in tensor-memory lane 32 s + l -- exactly the lanes
+//    warp w may write; 16 columns (K = 16) per chunk, a ring of kSlots
+//    chunks per tile;
+//  * after each chunk one thread issues two tcgen05.mma (A from tensor
+//    memory, X^T from shared memory, N = the padded batch) accumulating in
+//    tensor memory, and a tcgen05.commit on the chunk's ring slot tells the
+//    decoders when the slot may be rewritten;
+//  * X^T is staged in 128-column halves, one half ahead (cp.async, two
+//    buffers, each released by a commit after the last MMA that reads it);
+//    each strip's
+//    next tile, the rows' verbatim flags and first sign+mantissa chunk are
+//    fetched while the current tile is decoded;
+//  * the accumulators are read back with tcgen05.ld by the warp that owns
+//    their lanes; split-K partials are added in ascending split order by the
+//    last CTA of each 256-row block;
+//  * the decoder table is bulk-copied into shared memory and checked
+//    lane-parallel.
 // Every wait is bounded; on a timeout the CTA reports LW_DEV_TIMEOUT, waits
-// (bounded) for its own MMAs, frees its tensor memory and returns.
+// (bounded) for its own MMAs and copies, frees its tensor memory and returns.
 #pragma once
 
 #include "lw_bkern.cuh"
@@ -29,8 +39,8 @@
 namespace lw {
 namespace dev {
 
-constexpr int kSlots = 4;            // slab ring depth
-constexpr int kSlabBytes = 128 * 16 * 2;   // M = 128 rows x K = 16 bf16
+constexpr int kSlots = 4;      // operand ring depth (chunks of K = 16)
+constexpr int kACols = 8;      // tensor-memory columns of one chunk: 16 bf16 per lane
 
 // ---- tcgen05 / tensor memory helpers (inline PTX) ---------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -68,6 +78,26 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
           smem_addr(bar))
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (BF16 inputs, FP32 accumulate)
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// this thread's 8 consecutive 32-bit columns of its tensor-memory lane
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -96,233 +126,269 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-// ---- the kernel -----------------------------------------------------------
+// 16-byte asynchronous copy global -> shared; zero-filled when src_bytes is 0
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Half hf of X^T of tile column kt (bpad rows x 128 columns of bf16, rows
+// >= batch zero) into `xs` in the K-major core-matrix layout: element (n, k)
+// at (n / 8) * 2048 + (k / 8) * 128 + (n % 8) * 16 + (k % 8) * 2.  Whole
+// CTA; one cp.async group per thread.
+__device__ __forceinline__ void stage_xt(const BArgs& a, uint32_t xs, int kt, int hf) {
+  for (int i = threadIdx.x; i < a.bpad * 16; i += blockDim.x) {
+    const int n = i >> 4, kb = i & 15;
+    const bool live = n < a.batch;
+    const uint16_t* src = a.x + (size_t)(live ? n : 0) * a.K + (size_t)kt * 256 + 128 * hf + 8 * kb;
+    cp_async16(xs + (uint32_t)((n >> 3) * 2048 + kb * 128 + (n & 7) * 16), src, live ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
+// shared-memory map of the tensor-core kernel (bytes; the X^T buffers and
+// tile stages follow at the launch's offsets)
+constexpr int kTcBarOff = 256;      // wbar[4 strips][2], sbar[kSlots], xbar[2], tbar
+constexpr int kTcSlotOff = 384;     // tensor-memory address, broadcast word
+constexpr int kTcRawTabOff = 1024;  // the bundle's lw_table
+constexpr int kTcXsOff = 2048;
+constexpr int kTcThreads = 256;
+
+// tensor-memory columns: D0, D1 (bpad each), then the two operand rings
+__host__ __device__ constexpr int tc_tmem_need(int bpad) { return 2 * bpad + 2 * kSlots * kACols; }
+
 template <int NCMP>
-__global__ void __launch_bounds__(128, 1) b_tc_kernel(const BArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int sq = warp & 3, h = warp >> 2;   // strip of the block, row of the lane
   const uint32_t sbase = smem_addr(smem);
   const uint32_t s_off = sbase + kOffOff;
   const uint32_t s_tab = sbase + kBTabOff;
-  uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + 256) + warp;   // this warp's tile copy
-  uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + 288);          // [kSlots] slab ring
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + 320);
-  volatile uint32_t* shared_word = reinterpret_cast<volatile uint32_t*>(smem + 324);
-  const uint32_t slab0 = sbase + (uint32_t)a.slab_off;   // [pair 2][slot][4 KB]
-  const uint32_t xs = sbase + (uint32_t)a.xs_off;        // X^T for one tile column
-  uint8_t* wstage = smem + a.wstage_off + warp * a.stage_bytes;
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + kTcBarOff) + 2 * sq;    // this strip's stages
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(smem + kTcBarOff) + 8;         // [kSlots] ring
+  uint64_t* xbar = sbar + kSlots;                                             // [2] X^T buffers
+  uint64_t* tbar = xbar + 2;                                                  // table copy
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kTcSlotOff);
+  volatile uint32_t* shared_word = tslot + 1;
+  const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kTcRawTabOff);
+  const uint32_t xs0 = sbase + (uint32_t)a.xs_off;       // [2][bpad * 256]: X^T halves
+  const uint32_t xs_bytes = (uint32_t)a.bpad * 256u;
+  uint8_t* wst0 = smem + a.wstage_off + (2 * sq) * a.stage_bytes;   // this strip's two stages
+  const bool lead = h == 0 && lane == 0;                 // issues this strip's tile copies
 
-  if (lane == 0) mbar_init(wbar, 1);
-  if (tid == 0)
-    for (int s = 0; s < kSlots; ++s) mbar_init(&sbar[s], 1);
+  if (warp < 4 && lane == 0) {
+    mbar_init(&wbar[0], 1);
+    mbar_init(&wbar[1], 1);
+  }
+  if (tid == 0) {
+    for (int q = 0; q < kSlots; ++q) mbar_init(&sbar[q], 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    mbar_init(tbar, 1);
+  }
   if (lane == 0) fence_barrier_init();
   if (warp == 0) {
     tmem_alloc(smem_addr(const_cast<uint32_t*>(tslot)), (uint32_t)a.tmem_cols);
     tmem_relinquish();
   }
-  if (warp == 0) {
-    if (lane == 0)
-      *reinterpret_cast<volatile int*>(smem + kFlagOff) =
-          table_ok(a.table, LW_FMT_BF16_EXP, 16, NCMP) ? 0 : 1;
-    if (lane < 16) {
-      put_off<(NCMP + 1) / 2>(smem, lane,
-          s_tab + (uint32_t)(4 * (lane < 12 ? a.table->off[lane] : 0)));
-      const uint32_t sy = a.table->sym[lane] & 15u;
-      reinterpret_cast<uint32_t*>(smem + kBTabOff)[lane] = (uint32_t)a.table->palette[sy] << 23;
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  bool failed = false;      // stop: rejected table or a wait that ran out
-  bool timed_out = false;   // a wait ran out (reported as LW_DEV_TIMEOUT)
-  bool copy_pending = false;  // this warp's tile copy may still be in flight
-  uint32_t pending_par = 0;   // ... on this phase of wbar
-  uint32_t gchunk = 0;   // slab commits issued by this CTA so far (uniform)
-  if (*reinterpret_cast<volatile int*>(smem + kFlagOff)) {
-    if (tid == 0) report(a.status, LW_DEV_BAD_TABLE);
+  const uint32_t t_lane = (uint32_t)(32 * sq) << 16;      // this warp's lane quarter
+  const uint32_t col_a = (uint32_t)(2 * a.bpad);          // first operand-ring column
+  if (tid == 0) table_issue(smem + kTcRawTabOff, a.table, tbar);
+  bool failed = false;        // stop: rejected table or a wait that ran out
+  bool timed_out = false;     // a wait ran out (reported as LW_DEV_TIMEOUT)
+  // this strip's stages: copy not yet waited for / parity of the next wait
+  bool infl0 = false, infl1 = false;
+  uint32_t wpar0 = 0u, wpar1 = 0u;
+  const bool got = __syncthreads_and(mbar_wait(tbar, 0u));
+  if (!got || !__syncthreads_and(table_ok_warp(tb, LW_FMT_BF16_EXP, 16, NCMP, lane))) {
+    if (tid == 0) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
+    if (!got) mbar_wait(tbar, 0u);
     failed = true;
+  } else if (warp == 0 && lane < 16) {
+    put_off<(NCMP + 1) / 2>(reinterpret_cast<uint32_t*>(smem + kOffOff), lane,
+                            s_tab + (uint32_t)(4 * (lane < 12 ? tb->off[lane] : 0)));
+    const uint32_t sy = tb->sym[lane] & 15u;
+    reinterpret_cast<uint32_t*>(smem + kBTabOff)[lane] = (uint32_t)tb->palette[sy] << 23;
   }
   constexpr int NP = (NCMP + 1) / 2;
   Cmp<NP> cmp;
   int lmin = 1;
   if (!failed) {
-    cmp.load(a.table, a.table->lmax - a.table->lmin);
-    lmin = a.table->lmin;
+    cmp.load(tb, tb->lmax - tb->lmin);
+    lmin = tb->lmin;
   }
+  __syncthreads();
   const uint32_t idesc = idesc_bf16((uint32_t)a.bpad);
   const int n_strips = a.N / 64;
   const int n_blocks = (n_strips + 3) / 4;
   const int units = n_blocks * a.nsplit;
-  uint32_t wpar = 0;
+  uint32_t gchunk = 0;   // ring commits issued by this CTA so far (uniform)
+  uint32_t xk = 0;       // X^T halves consumed by this CTA so far (uniform): the
+                         // current half sits in buffer xk & 1
+  uint32_t ts = 0;       // tile columns this CTA has started (uniform)
 
   for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
     const int rb = u / a.nsplit, sp = u % a.nsplit;
     const int kt0 = (int)((long long)a.TK * sp / a.nsplit);
     const int kt1 = (int)((long long)a.TK * (sp + 1) / a.nsplit);
-    const int strip = rb * 4 + warp;
+    const int strip = rb * 4 + sq;
     const bool has = strip < n_strips;
-    const size_t r0 = (size_t)strip * 64 + 2 * lane;
+    const size_t r = (size_t)strip * 64 + 2 * lane + h;
+    // prologue: the unit's first tile, X^T and flags
+    bool fit_cur = true, fit_nxt = true;
+    if (has) {
+      const int t = strip * a.TK + kt0;
+      fit_cur = b_issue<false, false>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1),
+                                      wst0 + (ts & 1) * a.stage_bytes, &wbar[ts & 1],
+                                      lead ? 0 : 1);
+      if (ts & 1) infl1 = true; else infl0 = true;
+    }
+    if (xk >= 2 && !mbar_wait(&xbar[xk & 1], ((xk - 2) >> 1) & 1u)) timed_out = true;
+    if (__syncthreads_or(timed_out)) { failed = true; break; }
+    stage_xt(a, xs0 + (xk & 1) * xs_bytes, kt0, 0);
+    uint32_t fw = 0, vb = 0;
+    if (has) b_row_flags(a, r, kt0, fw, vb);
+    uint4 n_sm = make_uint4(0, 0, 0, 0), n_ve = n_sm;
+    if (has) {
+      n_sm = b_load_sm(a, strip * a.TK + kt0, lane, h, 0);
+      if (fw & 1u) n_ve = b_load_vexp(a, vb, 0);
+    }
     bool first = true;
     for (int kt = kt0; kt < kt1 && !failed; ++kt) {
       const int t = strip * a.TK + kt;
-      bool fit = true;
-      if (has)
-        fit = b_issue<false, false>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), wstage,
-                                    wbar, lane);
-      uint32_t fw0 = 0, vb0 = 0, fw1 = 0, vb1 = 0;
-      if (has) {
-        b_row_flags(a, r0, kt, fw0, vb0);
-        b_row_flags(a, r0 + 1, kt, fw1, vb1);
+      const bool more = kt + 1 < kt1;
+      const uint32_t cur = ts & 1;
+      uint8_t* wstage = wst0 + cur * a.stage_bytes;
+      // next tile into the other stage (both of its readers finished the
+      // previous tile before the barrier that closed it)
+      if (has && more) {
+        fit_nxt = b_issue<false, false>(a, t + 1, __ldg(a.tile_off + t + 1), __ldg(a.tile_off + t + 2),
+                                        wst0 + (cur ^ 1u) * a.stage_bytes, &wbar[cur ^ 1u],
+                                        lead ? 0 : 1);
+        if (cur) infl0 = true; else infl1 = true;
       }
-      // the X^T stage is rewritten only after the MMAs reading it are done
+      uint32_t nfw = 0, nvb = 0;   // flags of the next tile column
+      if (has && more) b_row_flags(a, r, kt + 1, nfw, nvb);
       bool to = false;
-      if (gchunk > 0) to = !mbar_wait(&sbar[(gchunk - 1) % kSlots], ((gchunk - 1) / kSlots) & 1u);
-      if (__syncthreads_or(to)) {
-        failed = timed_out = true;
-        copy_pending = has;
-        pending_par = wpar;
-        break;
-      }
-      for (int i = tid; i < a.bpad * 32; i += 128) {
-        const int n = i >> 5, kb = i & 31;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (n < a.batch)
-          v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * a.K + (size_t)kt * 256 + 8 * kb));
-        *reinterpret_cast<uint4*>(smem + a.xs_off + (n >> 3) * 4096 + kb * 128 + (n & 7) * 16) = v;
-      }
-      fence_proxy_async();
       if (has) {
-        to = !mbar_wait(wbar, wpar);
-        copy_pending = to;
-        pending_par = wpar;
-        wpar ^= 1u;
+        to = !mbar_wait(&wbar[cur], cur ? wpar1 : wpar0);
+        if (!to) {
+          if (cur) { wpar1 ^= 1u; infl1 = false; } else { wpar0 ^= 1u; infl0 = false; }
+        }
       }
       const uint32_t wb = smem_addr(wstage);
-      LaneBits la, lr;
+      LaneBits lb;
       uint32_t mid = 0;
-      const bool dec = has && fit && !to;
+      const bool dec = has && fit_cur && !to;
       if (dec) {
         mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
-        la.init(wb, lane, a.stage_rows);
-        lr.init_at(wb, lane, a.stage_rows, mid);
+        lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
       }
-      if (has && !fit && lane == 0) report(a.status, LW_DEV_TILE_SIZE);
-      uint4 n_sm0 = make_uint4(0, 0, 0, 0), n_sm1 = n_sm0, n_ve0 = n_sm0, n_ve1 = n_sm0;
-      if (dec) {
-        n_sm0 = b_load_sm(a, t, lane, 0, 0);
-        n_sm1 = b_load_sm(a, t, lane, 1, 0);
-        if (fw0 & 1u) n_ve0 = b_load_vexp(a, vb0, 0);
-        if (fw1 & 1u) n_ve1 = b_load_vexp(a, vb1, 0);
-      }
+      if (has && !fit_cur && lead) report(a.status, LW_DEV_TILE_SIZE);
       for (int k = 0; k < 16; ++k) {
-        const uint32_t s = gchunk % kSlots;
+        const uint32_t slot = gchunk % kSlots;
         bool to2 = to;
         if (gchunk >= (uint32_t)kSlots)
-          to2 |= !mbar_wait(&sbar[s], ((gchunk - kSlots) / kSlots) & 1u);
-        uint32_t W0[8], W1[8];   // bf16x2 of rows 2l and 2l+1, columns 16k .. 16k+15
+          to2 |= !mbar_wait(&sbar[slot], ((gchunk - kSlots) / kSlots) & 1u);
+        if ((k & 7) == 0) {   // this thread's part of the current X^T half
+          cp_async_wait_all();
+          fence_proxy_async();
+        }
+        if ((k & 7) == 4 && (k < 8 || more)) {
+          // the next X^T half into the other buffer, once the MMAs that last
+          // read it (the previous half) are done
+          if (xk >= 1 && !mbar_wait(&xbar[(xk + 1) & 1], ((xk - 1) >> 1) & 1u)) to2 = true;
+          else stage_xt(a, xs0 + ((xk + 1) & 1) * xs_bytes, k < 8 ? kt : kt + 1, k < 8 ? 1 : 0);
+        }
+        uint32_t W[8];   // bf16x2 of this lane's row, columns 16k .. 16k+15
         if (dec) {
-          const int g = k >> 2;
-          const bool v0 = (fw0 >> g) & 1u, v1 = (fw1 >> g) & 1u;
-          const uint4 sm0 = n_sm0, sm1 = n_sm1, ve0 = n_ve0, ve1 = n_ve1;
+          const bool v = (fw >> (k >> 2)) & 1u;
+          const uint4 sm = n_sm, ve = n_ve;
           if (k < 15) {
             const int k1 = k + 1, g1 = k1 >> 2;
-            n_sm0 = b_load_sm(a, t, lane, 0, k1);
-            n_sm1 = b_load_sm(a, t, lane, 1, k1);
-            if ((fw0 >> g1) & 1u) n_ve0 = b_load_vexp(a, vb0 + __popc(fw0 & ((1u << g1) - 1u)), k1 & 3);
-            if ((fw1 >> g1) & 1u) n_ve1 = b_load_vexp(a, vb1 + __popc(fw1 & ((1u << g1) - 1u)), k1 & 3);
+            n_sm = b_load_sm(a, t, lane, h, k1);
+            if ((fw >> g1) & 1u) n_ve = b_load_vexp(a, vb + __popc(fw & ((1u << g1) - 1u)), k1 & 3);
+          } else if (more) {   // first chunk of the next tile column
+            n_sm = b_load_sm(a, t + 1, lane, h, 0);
+            if (nfw & 1u) n_ve = b_load_vexp(a, nvb, 0);
           }
 #pragma unroll
           for (int p = 0; p < 8; ++p) {
-            uint32_t E[4];
-            const uint32_t wv0 = u4w(ve0, p >> 1), wv1 = u4w(ve1, p >> 1);
-            if (!v0) {
+            uint32_t E0, E1;
+            if (!v) {
               uint32_t e0, e1;
-              q_decode2<NP, 4>(la, cmp, lmin, s_off, e0, e1);
-              E[0] = lds_u32(e0);
-              E[1] = lds_u32(e1);
+              q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
+              E0 = lds_u32(e0);
+              E1 = lds_u32(e1);
             } else {
-              E[0] = (p & 1) ? b_vexp23<2>(wv0) : b_vexp23<0>(wv0);
-              E[1] = (p & 1) ? b_vexp23<3>(wv0) : b_vexp23<1>(wv0);
+              const uint32_t wv = u4w(ve, p >> 1);
+              E0 = (p & 1) ? b_vexp23<2>(wv) : b_vexp23<0>(wv);
+              E1 = (p & 1) ? b_vexp23<3>(wv) : b_vexp23<1>(wv);
             }
-            if (!v1) {
-              uint32_t e0, e1;
-              q_decode2<NP, 4>(lr, cmp, lmin, s_off, e0, e1);
-              E[2] = lds_u32(e0);
-              E[3] = lds_u32(e1);
-            } else {
-              E[2] = (p & 1) ? b_vexp23<2>(wv1) : b_vexp23<0>(wv1);
-              E[3] = (p & 1) ? b_vexp23<3>(wv1) : b_vexp23<1>(wv1);
-            }
-            const uint32_t s0 = u4w(sm0, p >> 1), s1 = u4w(sm1, p >> 1);
-            uint32_t f[4];
-            if (p & 1) {
-              f[0] = __float_as_uint(b_value<2>(s0, E[0]));
-              f[1] = __float_as_uint(b_value<3>(s0, E[1]));
-              f[2] = __float_as_uint(b_value<2>(s1, E[2]));
-              f[3] = __float_as_uint(b_value<3>(s1, E[3]));
-            } else {
-              f[0] = __float_as_uint(b_value<0>(s0, E[0]));
-              f[1] = __float_as_uint(b_value<1>(s0, E[1]));
-              f[2] = __float_as_uint(b_value<0>(s1, E[2]));
-              f[3] = __float_as_uint(b_value<1>(s1, E[3]));
-            }
-            W0[p] = __byte_perm(f[0], f[1], 0x7632);   // (bf16 of f1) << 16 | bf16 of f0
-            W1[p] = __byte_perm(f[2], f[3], 0x7632);
+            const uint32_t sw = u4w(sm, p >> 1);
+            const uint32_t f0 = __float_as_uint((p & 1) ? b_value<2>(sw, E0) : b_value<0>(sw, E0));
+            const uint32_t f1 = __float_as_uint((p & 1) ? b_value<3>(sw, E1) : b_value<1>(sw, E1));
+            W[p] = __byte_perm(f0, f1, 0x7632);   // (bf16 of f1) << 16 | bf16 of f0
           }
         } else {
 #pragma unroll
-          for (int p = 0; p < 8; ++p) W0[p] = W1[p] = 0u;
+          for (int p = 0; p < 8; ++p) W[p] = 0u;
         }
-        // rows m = 64 (warp & 1) + 2 lane + h of pair (warp >> 1)'s slab
-        const uint32_t slab = slab0 + (uint32_t)(((warp >> 1) * kSlots + (int)s) * kSlabBytes);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t* W = h ? W1 : W0;
-          const uint32_t m = (uint32_t)(64 * (warp & 1) + 2 * lane + h);
-          uint8_t* row = smem + (slab - sbase) + (m >> 3) * 256 + (m & 7) * 16;
-          *reinterpret_cast<uint4*>(row) = make_uint4(W[0], W[1], W[2], W[3]);
-          *reinterpret_cast<uint4*>(row + 128) = make_uint4(W[4], W[5], W[6], W[7]);
-        }
+        tmem_st8(tmem + t_lane + col_a + (uint32_t)((h * kSlots + (int)slot) * kACols), W);
+        tmem_st_wait();
         fence_proxy_async();
+        tc_fence_before();
         if (__syncthreads_or(to2)) { failed = timed_out = true; break; }
         if (tid == 0) {
           tc_fence_after();
-          const uint64_t bd = sdesc(xs + 256u * (uint32_t)k, 128u, 4096u);
-          umma_bf16(tmem, sdesc(slab0 + s * kSlabBytes, 128u, 256u), bd, idesc, first ? 0u : 1u);
-          umma_bf16(tmem + (uint32_t)a.bpad, sdesc(slab0 + (kSlots + s) * kSlabBytes, 128u, 256u), bd,
-                    idesc, first ? 0u : 1u);
-          umma_commit(&sbar[s]);
+          const uint64_t bd = sdesc(xs0 + (xk & 1) * xs_bytes + 256u * (uint32_t)(k & 7), 128u, 2048u);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            umma_bf16_ta(tmem + (uint32_t)(hh * a.bpad),
+                         tmem + col_a + (uint32_t)((hh * kSlots + (int)slot) * kACols), bd, idesc,
+                         first ? 0u : 1u);
+          umma_commit(&sbar[slot]);
+          if ((k & 7) == 7) umma_commit(&xbar[xk & 1]);   // X^T half free after these
         }
         first = false;
         ++gchunk;
+        if ((k & 7) == 7) ++xk;
       }
-      if (dec && (la.consumed() != mid ||
-                  lr.consumed() != (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane)))
-        report(a.status, LW_DEV_LANE_LENGTH);
+      if (failed) break;
+      if (dec) {
+        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
+        if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
+      }
+      ++ts;
+      fit_cur = fit_nxt;
+      fw = nfw;
+      vb = nvb;
     }
     if (failed) break;
-    // all MMAs of this unit done -> read the accumulators
+    // all MMAs of this unit done -> read the accumulators (warp w: tile h,
+    // lanes of strip sq)
     bool to3 = !mbar_wait(&sbar[(gchunk - 1) % kSlots], ((gchunk - 1) / kSlots) & 1u);
     if (__syncthreads_or(to3)) { failed = timed_out = true; break; }
     tc_fence_after();
-    const size_t rows0 = (size_t)rb * 256 + 32 * warp + lane;   // D0 row; D1 row = +128
     const size_t step = (size_t)a.batch * a.N;
-    for (int p = 0; p < 2; ++p) {
-      const size_t row = rows0 + 128 * p;
-      for (int j = 0; j < a.bpad; j += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(p * a.bpad + j), r);
-        tmem_ld_wait();
-        if (row < (size_t)a.N) {
+    for (int j = 0; j < a.bpad; j += 16) {
+      uint32_t rr[16];
+      tmem_ld16(tmem + t_lane + (uint32_t)(h * a.bpad + j), rr);
+      tmem_ld_wait();
+      if (has) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int b = j + i;
-            if (b < a.batch) {
-              if (a.nsplit == 1) a.y[(size_t)b * a.N + row] = __uint_as_float(r[i]);
-              else a.ws[(size_t)sp * step + (size_t)b * a.N + row] = __uint_as_float(r[i]);
-            }
+        for (int i = 0; i < 16; ++i) {
+          const int b = j + i;
+          if (b < a.batch) {
+            if (a.nsplit == 1) a.y[(size_t)b * a.N + r] = __uint_as_float(rr[i]);
+            else a.ws[(size_t)sp * step + (size_t)b * a.N + r] = __uint_as_float(rr[i]);
           }
         }
       }
@@ -336,7 +402,7 @@ __global__ void __launch_bounds__(128, 1) b_tc_kernel(const BArgs a) {
       const bool last = *shared_word == (uint32_t)(a.nsplit - 1);
       __syncthreads();
       if (last) {
-        for (int i = tid; i < 256 * a.batch; i += 128) {
+        for (int i = tid; i < 256 * a.batch; i += kTcThreads) {
           const int b = i >> 8;
           const size_t row = (size_t)rb * 256 + (i & 255);
           if (row >= (size_t)a.N) continue;
@@ -350,10 +416,12 @@ __global__ void __launch_bounds__(128, 1) b_tc_kernel(const BArgs a) {
   }
   if (timed_out) {
     if (tid == 0) report(a.status, LW_DEV_TIMEOUT);
-    // let this CTA's own MMAs and tile copy finish (bounded) before leaving
+    // let this CTA's own MMAs and copies finish (bounded) before leaving
     if (gchunk > 0) mbar_wait(&sbar[(gchunk - 1) % kSlots], ((gchunk - 1) / kSlots) & 1u);
-    if (copy_pending) mbar_wait(wbar, pending_par);
+    if (infl0) mbar_wait(&wbar[0], wpar0);
+    if (infl1) mbar_wait(&wbar[1], wpar1);
   }
+  cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

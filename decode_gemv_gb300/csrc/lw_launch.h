@@ -21,22 +21,25 @@ inline lw_status check_launch(const char* what) {
   return LW_OK;
 }
 
-// Launch a persistent grid of `threads`-thread blocks that each own one tile
-// at a time: as many blocks as are resident on the device, but no more than
-// it takes to give every block the same number of tiles.
+// Blocks of a persistent grid of `threads`-thread blocks that each own one
+// tile at a time: every resident block, but no more blocks than tiles (more
+// resident warps hide more of the decoder's dependency latency than an
+// even tile count per block would gain).
+inline long long persistent_blocks(const void* kernel, int threads, size_t smem, int n_tiles) {
+  const int per_sm = resident_blocks(kernel, threads, smem);
+  if (per_sm < 1) return 0;
+  const long long resident = (long long)per_sm * device_sm_count();
+  return resident < n_tiles ? resident : (n_tiles > 0 ? n_tiles : 1);
+}
+
 template <class Launch>
 lw_status launch_persistent(const void* kernel, int threads, size_t smem, int n_tiles,
                             cudaStream_t st, Launch&& launch) {
   (void)st;
-  const int per_sm = resident_blocks(kernel, threads, smem);
-  if (per_sm < 1)
+  const long long blocks = persistent_blocks(kernel, threads, smem, n_tiles);
+  if (blocks < 1)
     return fail(LW_ERR_UNSUPPORTED, "kernel does not fit on an SM (%zu bytes of shared memory)",
                 smem);
-  // the fewest blocks that still take ceil(n_tiles / resident blocks) tiles each
-  const long long resident = (long long)per_sm * device_sm_count();
-  const long long per_block = (n_tiles + resident - 1) / resident;
-  long long blocks = per_block > 0 ? (n_tiles + per_block - 1) / per_block : 1;
-  if (blocks < 1) blocks = 1;
   launch((int)blocks);
   return check_launch("product kernel");
 }

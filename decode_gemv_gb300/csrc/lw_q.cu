@@ -1,5 +1,4 @@
 // Launchers for the 4-/6-bit kernels (instantiations of lw_qkern.cuh).
-#include <cstdlib>
 #include <mutex>
 #include <unordered_map>
 
@@ -81,13 +80,12 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   const int qpb = qparam_tile_bytes(fmt);
   a.mid_offset = a.stage_rows * 128 + qpb + bp * 1024;
   a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
-  // two stages per CTA while that still leaves 16 resident warps per SM,
-  // else one stage (more resident CTAs; a CTA then waits for its own next
-  // tile, other CTAs cover the wait)
-  const size_t smem2 = (size_t)dev::kStageOff + 2 * (size_t)a.stage_bytes;
+  // one stage per CTA (the most resident CTAs) unless the grid leaves each
+  // CTA three or more tiles, where prefetching the next tile pays
   const size_t smem1 = (size_t)dev::kStageOff + (size_t)a.stage_bytes;
-  a.nstage = resident_blocks((const void*)k, dev::kQThreads, smem2) * (dev::kQThreads / 32) >= 16 ? 2 : 1;
-  if (const char* e = getenv("LW_QSTAGES")) a.nstage = atoi(e) == 1 ? 1 : 2;
+  const size_t smem2 = smem1 + (size_t)a.stage_bytes;
+  const long long blocks1 = persistent_blocks((const void*)k, dev::kQThreads, smem1, a.n_tiles);
+  a.nstage = blocks1 > 0 && a.n_tiles >= 3 * blocks1 ? 2 : 1;
   const size_t smem = a.nstage == 2 ? smem2 : smem1;
   return launch_persistent((const void*)k, dev::kQThreads, smem, a.n_tiles, st, [&](int blocks) {
     k<<<blocks, dev::kQThreads, smem, st>>>(a);

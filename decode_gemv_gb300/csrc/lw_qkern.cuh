@@ -78,7 +78,7 @@ template <> struct QFmt<LW_FMT_Q6> {
 };
 
 // shared-memory map (bytes)
-constexpr int kOffOff = 0;        // 64 B: symbol-table entry address per length index (put_off)
+constexpr int kOffOff = 0;        // 64 B: offset table (BF16 kernels; the 4-/6-bit kernels keep it in static shared memory)
 constexpr int kFlagOff = 64;      // int: "this CTA adds the strip's partials" broadcast
 constexpr int kTabOff = 128;      // symbol values: float2[256] (4-bit) / float[64]; decode: uint32[256]
 constexpr int kBarOff = 2176;     // uint64 mbarriers: stage 0, stage 1, table
@@ -119,10 +119,11 @@ __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint32_t r0, uint
   return fits;
 }
 
-// Start the bulk copy of the decoder table into shared memory (thread 0).
-__device__ __forceinline__ void table_issue(uint8_t* smem, const lw_table* tb, uint64_t* bar) {
+// Start the bulk copy of the decoder table into shared memory at `dst`
+// (one thread).
+__device__ __forceinline__ void table_issue(uint8_t* dst, const lw_table* tb, uint64_t* bar) {
   mbar_arrive_expect_tx(bar, (uint32_t)sizeof(lw_table));
-  bulk_g2s(smem + kRawTabOff, tb, (uint32_t)sizeof(lw_table), bar);
+  bulk_g2s(dst, tb, (uint32_t)sizeof(lw_table), bar);
 }
 
 // Checks of a staged table by one warp (every warp of a CTA may run them;
@@ -161,33 +162,25 @@ __device__ __forceinline__ bool table_ok_warp(const lw_table* tb, int want_fmt, 
 // words j, j+1, j+2 where j = consumed / 32; pos = consumed % 32.
 struct LaneBits {
   uint32_t cur, nxt, nx2;
-  uint32_t wp;      // shared address of word j + 3 of this lane
+  uint32_t wp;      // shared address of word j + 3 of this lane (may run past the stage)
+  uint32_t w0;      // shared address of word 0 of this lane
   uint32_t wlast;   // last row this lane may read (clamp for corrupt streams)
-  int pos, nref;
+  int pos;
   __device__ __forceinline__ void init(uint32_t wb, int lane, int stage_rows) {
-    const uint32_t base = wb + 4u * (uint32_t)lane;
-    cur = lds_u32(base);
-    nxt = lds_u32(base + 128u);
-    nx2 = lds_u32(base + 256u);
-    wp = base + 384u;
-    wlast = base + (uint32_t)(stage_rows - 1) * 128u;
-    pos = 0;
-    nref = 0;
+    init_at(wb, lane, stage_rows, 0u);
   }
   // start at stream bit `bit` (clamped so that every read stays inside the
   // stage; a lane whose start was clamped fails its length check)
   __device__ __forceinline__ void init_at(uint32_t wb, int lane, int stage_rows, uint32_t bit) {
     uint32_t j0 = bit >> 5;
     if (j0 > (uint32_t)(stage_rows - kLookahead)) j0 = (uint32_t)(stage_rows - kLookahead);
-    const uint32_t base = wb + 4u * (uint32_t)lane;
-    cur = lds_u32(base + 128u * j0);
-    nxt = lds_u32(base + 128u * (j0 + 1));
-    nx2 = lds_u32(base + 128u * (j0 + 2));
-    wp = base + 128u * (j0 + 3);
-    wlast = base + (uint32_t)(stage_rows - 1) * 128u;
-    if (wp > wlast) wp = wlast;
+    w0 = wb + 4u * (uint32_t)lane;
+    cur = lds_u32(w0 + 128u * j0);
+    nxt = lds_u32(w0 + 128u * (j0 + 1));
+    nx2 = lds_u32(w0 + 128u * (j0 + 2));
+    wp = w0 + 128u * (j0 + 3);
+    wlast = w0 + (uint32_t)(stage_rows - 1) * 128u;
     pos = (int)(bit & 31u);
-    nref = (int)j0;
   }
   __device__ __forceinline__ uint32_t window() const { return __funnelshift_l(nxt, cur, pos); }
   // consume n (< 32) bits
@@ -197,13 +190,27 @@ struct LaneBits {
       pos -= 32;
       cur = nxt;
       nxt = nx2;
-      nx2 = lds_u32(wp);
-      wp = min(wp + 128u, wlast);
-      ++nref;
+      nx2 = lds_u32(min(wp, wlast));
+      wp += 128u;
     }
   }
-  __device__ __forceinline__ uint32_t consumed() const { return (uint32_t)nref * 32u + (uint32_t)pos; }
+  __device__ __forceinline__ uint32_t consumed() const {
+    return ((wp - w0) >> 7) * 32u + (uint32_t)pos - 96u;
+  }
 };
+
+// hi32(a * b) + c and hi32(a * b) (multiply-high: the FMA pipe, not the
+// integer ALU pipe)
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
 __device__ __forceinline__ __half2 as_h2(uint32_t b) {
   __half2 h;
@@ -247,7 +254,7 @@ struct Cmp {
   }
   // kScale * (number of limits the window's code reaches)
   __device__ __forceinline__ uint32_t count(uint32_t w) const {
-    const __half2 v = as_h2((w >> 22) * 0x00010001u + 0x64006400u);
+    const __half2 v = as_h2(mul_hi(w, 1u << 10) * 0x00010001u + 0x64006400u);   // 1024 + w >> 22
     uint32_t m[NP > 0 ? NP : 1];
 #pragma unroll
     for (int k = 0; k < NP; ++k) m[k] = __hge2_mask(v, as_h2(c[k]));
@@ -267,11 +274,11 @@ struct Cmp {
 };
 
 // Write the offset-table entry of length index c (count() returns its byte
-// offset from the table start).
+// offset from the table start; the table spans 64 bytes).
 template <int NP>
-__device__ __forceinline__ void put_off(uint8_t* smem, int c, uint32_t v) {
+__device__ __forceinline__ void put_off(uint32_t* tab, int c, uint32_t v) {
   constexpr int S = Cmp<NP>::kScale;
-  if (c * S < 64) *reinterpret_cast<uint32_t*>(smem + kOffOff + c * S) = v;
+  if (c * S < 64) tab[c * S / 4] = v;
 }
 
 // Decode two symbols from one window.  Returns the shared addresses of their
@@ -279,13 +286,13 @@ __device__ __forceinline__ void put_off(uint8_t* smem, int c, uint32_t v) {
 template <int NP, int ESZ>
 __device__ __forceinline__ void q_decode2(LaneBits& lb, const Cmp<NP>& cmp, int lmin, uint32_t s_off,
                                           uint32_t& e0, uint32_t& e1) {
-  constexpr int SH = Cmp<NP>::kShift;
+  constexpr uint32_t M = 1u << (32 - Cmp<NP>::kShift);   // count = hi32(z * M)
   const uint32_t w = lb.window();
   const uint32_t z0 = cmp.count(w);
-  const int L0 = lmin + (int)(z0 >> SH);
+  const int L0 = (int)mad_hi(z0, M, (uint32_t)lmin);
   const uint32_t w1 = w << L0;
   const uint32_t z1 = cmp.count(w1);
-  const int L1 = lmin + (int)(z1 >> SH);
+  const int L1 = (int)mad_hi(z1, M, (uint32_t)lmin);
   e0 = lds_u32(s_off + z0) + __funnelshift_l(w, 0u, L0) * ESZ;
   e1 = lds_u32(s_off + z1) + __funnelshift_l(w1, 0u, L1) * ESZ;
   lb.advance(L0 + L1);
@@ -418,10 +425,11 @@ __device__ __forceinline__ void q_commit(const QArgs& a, uint8_t* smem, int stri
 // Stage the symbol table and the offsets of a checked table (whole CTA).
 // ESZ = bytes per symbol entry; VAL converts a symbol to its entry.
 template <int NP, int ESZ, class Val>
-__device__ __forceinline__ void table_stage(uint8_t* smem, const lw_table* tb, int alpha, Val val) {
+__device__ __forceinline__ void table_stage(uint8_t* smem, uint32_t* offtab, const lw_table* tb,
+                                            int alpha, Val val) {
   const uint32_t s_tab = smem_addr(smem) + kTabOff;
   if (threadIdx.x < 16)
-    put_off<NP>(smem, threadIdx.x,
+    put_off<NP>(offtab, threadIdx.x,
                 s_tab + (uint32_t)(ESZ * (threadIdx.x < 12 ? tb->off[threadIdx.x] : 0)));
   for (int i = threadIdx.x; i < alpha; i += blockDim.x) val(i, (uint32_t)tb->sym[i]);
 }
@@ -439,7 +447,9 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
   using F = QFmt<FMT>;
   constexpr int NP = (NCMP + 1) / 2;
   constexpr int ESZ = FMT == kQ4 ? 8 : 4;
-  const uint32_t s_off = smem_addr(smem) + kOffOff;
+  // offsets in static shared memory: their address is a link-time constant
+  __shared__ __align__(16) uint32_t offtab[16];
+  const uint32_t s_off = smem_addr(offtab);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kRawTabOff);
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -464,7 +474,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
   }
   __syncthreads();
   // the table and the first tile are copied at once
-  if (!TWIN && lead) table_issue(smem, a.table, &bar[2]);
+  if (!TWIN && lead) table_issue(smem + kRawTabOff, a.table, &bar[2]);
   uint32_t par0 = 0u, par1 = 0u;
   bool fit0 = true, fit1 = true;
   if (t < a.n_tiles)
@@ -488,7 +498,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
       if (t < a.n_tiles) mbar_wait(&bar[0], 0u);
       return;
     }
-    table_stage<NP, ESZ>(smem, tb, F::alpha, [&](int i, uint32_t sy) {
+    table_stage<NP, ESZ>(smem, offtab, tb, F::alpha, [&](int i, uint32_t sy) {
       if (FMT == kQ4)
         reinterpret_cast<float2*>(smem + kTabOff)[i] =
             make_float2(16.f + (float)(sy & 15u), 16.f + (float)((sy >> 4) & 15u));
@@ -551,7 +561,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
         uint32_t e0, e1;
         q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
-#pragma unroll 4
+#pragma unroll 8
         for (int j = 0; j < 64; ++j) {
           const float2 v0 = lds_f2(e0), v1 = lds_f2(e1);
           if (j < 63) q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
@@ -673,7 +683,9 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   using F = QFmt<FMT>;
   constexpr int NP = (NCMP + 1) / 2;
-  const uint32_t s_off = smem_addr(smem) + kOffOff;
+  // offsets in static shared memory: their address is a link-time constant
+  __shared__ __align__(16) uint32_t offtab[16];
+  const uint32_t s_off = smem_addr(offtab);
   const uint32_t s_sym = smem_addr(smem) + kTabOff;   // uint32 per canonical index
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kRawTabOff);
@@ -690,7 +702,7 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
     fence_barrier_init();
   }
   __syncthreads();
-  if (!TWIN && lead) table_issue(smem, a.table, &bar[2]);
+  if (!TWIN && lead) table_issue(smem + kRawTabOff, a.table, &bar[2]);
   uint32_t par0 = 0u, par1 = 0u;
   bool fit0 = true, fit1 = true;
   if (t < a.n_tiles)
@@ -708,7 +720,7 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
       if (t < a.n_tiles) mbar_wait(&bar[0], 0u);
       return;
     }
-    table_stage<NP, 4>(smem, tb, 256, [&](int i, uint32_t sy) {
+    table_stage<NP, 4>(smem, offtab, tb, 256, [&](int i, uint32_t sy) {
       reinterpret_cast<uint32_t*>(smem + kTabOff)[i] = sy;
     });
     cmp.load(tb, tb->lmax - tb->lmin);
