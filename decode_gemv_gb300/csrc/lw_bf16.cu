@@ -120,7 +120,7 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
   const int slots = per_sm * device_sm_count();
   int nsplit = (slots + n_blocks - 1) / n_blocks;
-  if (nsplit > kTcMaxSplit) nsplit = kTcMaxSplit;
+  if (nsplit > tc_max_split(b)) nsplit = tc_max_split(b);
   if (nsplit > a.TK) nsplit = a.TK;
   if (nsplit < 1) nsplit = 1;
   a.nsplit = nsplit;
@@ -151,9 +151,9 @@ lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int bat
     a.mid_offset = a.x_offset + bp * 512;
     a.xf_offset = a.mid_offset + 128;
     a.stage_bytes = (a.xf_offset + bp * 1024 + 127) / 128 * 128;
-    const size_t smem = (size_t)dev::kBStageOff + (size_t)a.stage_bytes;
-    lw_status s = launch_persistent((const void*)k, 32, smem, a.n_tiles, st, [&](int blocks) {
-      k<<<blocks, 32, smem, st>>>(a);
+    const size_t smem = (size_t)dev::kStageOff + (size_t)a.stage_bytes;
+    lw_status s = launch_persistent((const void*)k, 64, smem, a.n_tiles, st, [&](int blocks) {
+      k<<<blocks, 64, smem, st>>>(a);
     });
     if (s != LW_OK) return s;
   }
@@ -168,9 +168,9 @@ lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status,
   a.status = status;
   a.mid_offset = a.stage_rows * 128;
   a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
-  const size_t smem = (size_t)dev::kBStageOff + (size_t)a.stage_bytes;
-  return launch_persistent((const void*)k, 32, smem, a.n_tiles, st, [&](int blocks) {
-    k<<<blocks, 32, smem, st>>>(a);
+  const size_t smem = (size_t)dev::kStageOff + (size_t)a.stage_bytes;
+  return launch_persistent((const void*)k, 64, smem, a.n_tiles, st, [&](int blocks) {
+    k<<<blocks, 64, smem, st>>>(a);
   });
 }
 

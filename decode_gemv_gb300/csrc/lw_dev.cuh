@@ -121,37 +121,5 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-// Table checks run by one thread per CTA before any decoding: the length
-// span fits the launch's comparator count, limits are ordered, and every
-// window maps to an index inside the symbol table.  Returns true if good.
-__device__ inline bool table_ok(const lw_table* tb, int want_fmt, int want_alpha, int ncmp) {
-  const int lmin = tb->lmin, lmax = tb->lmax;
-  if (tb->fmt != want_fmt || tb->alpha != want_alpha) return false;
-  if (lmin < 1 || lmax > LW_MAX_CODE_LEN || lmin > lmax || lmax - lmin > ncmp) return false;
-  const int n_entries = tb->n_sym + (tb->phantom ? 1 : 0);
-  if (n_entries < 1 || n_entries > want_alpha) return false;
-  const int nl = lmax - lmin;
-  for (int j = nl; j < 12; ++j)
-    if (tb->lim_m1[j] != 0xFFFFFFFFu) return false;
-  // every limit below the longest length is even in 11-bit peek space (the
-  // kernels compare 10-bit peeks against limit / 2)
-  for (int j = 0; j < nl; ++j)
-    if (((tb->lim_m1[j] + 1u) >> 21) & 1u) return false;
-  uint32_t prev_hi = 0;
-  for (int j = 0; j <= nl; ++j) {
-    const int L = lmin + j;
-    const uint32_t hi = tb->lim_m1[j];          // largest window of length <= L
-    if (j > 0 && hi < prev_hi) return false;
-    const uint32_t cmax = hi >> (32 - L);
-    const uint32_t cmin = j == 0 ? 0u : (prev_hi + 1u) >> (32 - L);
-    const long long lo_idx = (long long)tb->off[j] + cmin;
-    const long long hi_idx = (long long)tb->off[j] + cmax;
-    if (j > 0 && prev_hi == 0xFFFFFFFFu) return false;
-    if (lo_idx < 0 || hi_idx >= n_entries) return false;
-    prev_hi = hi;
-  }
-  return true;
-}
-
 }  // namespace dev
 }  // namespace lw

@@ -46,10 +46,15 @@ lw_status launch_persistent(const void* kernel, int threads, size_t smem, int n_
 
 // Workspace layout: one uint32 split-K counter per 64-row strip (padded to
 // 256 bytes), then fp32 partial sums -- [K/256][min(batch, 8)][N] for the
-// CUDA-core products, [split <= kTcMaxSplit][64][N] for the tensor-core BF16
+// CUDA-core products, [split <= tc_max_split][64][N] for the tensor-core BF16
 // product.  The counters sit first so that every path finds them at the same
 // place; every call that completes leaves them at zero.
-constexpr int kTcMaxSplit = 8;
+// K splits of the tensor-core product: at most one per two tile columns,
+// and 32
+inline int tc_max_split(const lw_dev_bundle* b) {
+  const int half_tk = (int)(b->cols / 512);
+  return half_tk < 1 ? 1 : (half_tk > 32 ? 32 : half_tk);
+}
 inline size_t workspace_counter_bytes(const lw_dev_bundle* b) {
   return ((size_t)(b->rows / 64) * sizeof(uint32_t) + 255) / 256 * 256;
 }
@@ -58,7 +63,7 @@ inline size_t workspace_partials_bytes(const lw_dev_bundle* b, int batch) {
   return (size_t)(b->cols / 256) * chunk * (size_t)b->rows * sizeof(float);
 }
 inline size_t workspace_tc_bytes(const lw_dev_bundle* b) {
-  return (size_t)kTcMaxSplit * 64 * (size_t)b->rows * sizeof(float);
+  return (size_t)tc_max_split(b) * 64 * (size_t)b->rows * sizeof(float);
 }
 inline uint32_t* workspace_counters(const lw_dev_bundle* b, void* ws) {
   (void)b;
