@@ -51,6 +51,8 @@ def parse():
                    choices=["mistral", "tiny", "phi3", "llama_mlp", "stack", "stack_bf16mlp"],
                    help="mistral: the headline line; the others print one line each with "
                         "per-batch rows (coded, twin and dense BF16 times)")
+    p.add_argument("--batches", default="",
+                   help="comma list of batch sizes for --workload sweeps (default: the workload's)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip twin / bf16 / cpu baseline / e2e legs (profiling)")
     return p.parse_args()
@@ -562,7 +564,12 @@ def run_sweep(args):
     (cuBLAS, same shapes) for every batch of one workload."""
     import multiprocessing as mp
     wid, label, batches, layers = SWEEPS[args.workload]
+    if args.batches:
+        batches = [int(b) for b in args.batches.split(",") if b]
     jobs = sweep_specs(args.workload)
+    names = [n for n in args.only.split(",") if n]
+    if names:
+        jobs = [j for j in jobs if j[3].name in names]
     t_prep = time.perf_counter()
     if len(jobs) > 8:
         with mp.get_context("spawn").Pool(min(16, os.cpu_count() or 4)) as pool:
@@ -583,18 +590,35 @@ def run_sweep(args):
         mats.append(dict(spec=spec, fmt=o[False][0],
                          db=[lw.DeviceBundle(*o[False][:8], device=dev, coded_bytes=o[False][8])
                              for _ in range(copies)],
-                         tw=lw.DeviceBundle(*o[True][:8], device=dev, coded_bytes=o[True][8])))
+                         tw=[lw.DeviceBundle(*o[True][:8], device=dev, coded_bytes=o[True][8])
+                             for _ in range(copies)]))
     del built
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234)
     # dense comparator: random bf16 weights of the same shapes (cuBLAS time
-    # depends on the shape only)
-    dense = [torch.randn(m["spec"].rows, m["spec"].cols, device=dev, generator=gen,
-                         dtype=torch.bfloat16) for m in mats]
+    # depends on the shape only), as many copies as the coded layer
+    dense = [[torch.randn(m["spec"].rows, m["spec"].cols, device=dev, generator=gen,
+                          dtype=torch.bfloat16) for m in mats] for _ in range(copies)]
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     peak, peak_kind = peaks()
     weights = sum(m["spec"].rows * m["spec"].cols for m in mats)
+    # tiny layers: each CUDA graph holds `group` consecutive steps (each on
+    # the next copy), so the host's replay cost does not dominate
+    group = 64 if copies >= 128 else 1
+    ngraph = max(1, copies // group)
+
+    def timed(calls_of_copy, steps=None):
+        graphs = [layer_graph(torch, [f for c in range(g * group, (g + 1) * group)
+                                      for f in calls_of_copy(c)]) for g in range(ngraph)]
+        if steps is None:
+            one = time_steps(torch, stream, lambda i: graphs[i].replay(), 3, 2, ngraph) / group
+            steps = max(10, min(args.steps, int(2000.0 / max(one, 1e-3))))
+        reps = max(3, steps // group)
+        t = time_steps(torch, stream, lambda i: graphs[i].replay(), reps, 5, ngraph) / group
+        del graphs
+        return t, steps
+
     rows_out = []
     clk = ClockSampler(0)
     clk.start()
@@ -608,26 +632,15 @@ def run_sweep(args):
         ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device=dev)
         x_bytes = sum(x.numel() * x.element_size() for x in xs)
         coded_step = sum(m["db"][0].coded_bytes for m in mats) + x_bytes
-        twin_step = sum(m["tw"].coded_bytes for m in mats) + x_bytes
-
-        def coded_calls(c):
-            return [(lambda d=m["db"][c], x=x, y=y: lw.lw_decode_gemm(d, x, B, y, ws, st))
-                    for m, x, y in zip(mats, xs, ys)]
-        graphs = [layer_graph(torch, coded_calls(c)) for c in range(copies)]
-        one = time_steps(torch, stream, lambda c: graphs[c].replay(), 3, 2, copies)
-        steps = max(10, min(args.steps, int(2000.0 / max(one, 1e-3))))
-        t_coded = time_steps(torch, stream, lambda c: graphs[c].replay(), steps, 5, copies)
-        del graphs
-        tg = layer_graph(torch, [(lambda d=m["tw"], x=x, y=y: lw.lw_twin_gemm(d, x, B, y, ws, st))
-                                 for m, x, y in zip(mats, xs, ys)])
-        t_twin = time_steps(torch, stream, lambda c: tg.replay(), steps, 5, 1)
-        del tg
+        twin_step = sum(m["tw"][0].coded_bytes for m in mats) + x_bytes
+        t_coded, steps = timed(lambda c: [(lambda d=m["db"][c], x=x, y=y: lw.lw_decode_gemm(d, x, B, y, ws, st))
+                                          for m, x, y in zip(mats, xs, ys)])
+        t_twin, _ = timed(lambda c: [(lambda d=m["tw"][c], x=x, y=y: lw.lw_twin_gemm(d, x, B, y, ws, st))
+                                     for m, x, y in zip(mats, xs, ys)], steps)
         xb = [x.to(torch.bfloat16) for x in xs]
-        yb = [torch.empty(B, w.shape[0], device=dev, dtype=torch.bfloat16) for w in dense]
-        bg = layer_graph(torch, [(lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y))
-                                 for w, x, y in zip(dense, xb, yb)])
-        t_bf16 = time_steps(torch, stream, lambda c: bg.replay(), steps, 5, 1)
-        del bg
+        yb = [torch.empty(B, m["spec"].rows, device=dev, dtype=torch.bfloat16) for m in mats]
+        t_bf16, _ = timed(lambda c: [(lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y))
+                                     for w, x, y in zip(dense[c], xb, yb)], steps)
         gbs = coded_step / (t_coded * 1e-3) / 1e9
         rows_out.append({"batch": B, "ms_per_step": t_coded, "coded_gbs": gbs,
                          "frac_of_hbm": gbs / peak, "b_eff_gbs": 2.0 * weights / (t_coded * 1e-3) / 1e9,
@@ -640,7 +653,8 @@ def run_sweep(args):
             "n_gpus": 1, "higher_is_better": True, "dtype": "f32" if mats[0]["fmt"] != lw.LW_FMT_BF16_EXP else "bf16",
             "data": "synthetic", "peak_gbs": peak, "peak_kind": peak_kind,
             "config": {"workload": label, "layers": layers, "matrices": len(mats), "weights": weights,
-                       "l2": f"rotate {copies} device copies" if copies > 1 else "working set > 4x L2",
+                       "l2": (f"rotate {copies} device copies ({group} steps per CUDA graph)"
+                              if copies > 1 else "working set > 4x L2"),
                        "dense_comparator": "torch.matmul on random bf16 weights of the same shapes (cuBLAS)",
                        "host_prep_s": round(t_prep, 1)},
             "rows": rows_out, "clocks": clocks, "device_status": int(st.item())}

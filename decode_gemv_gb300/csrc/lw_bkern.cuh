@@ -123,6 +123,34 @@ __device__ __forceinline__ uint32_t b_vexp23(uint32_t w) {
   return ((w >> (8 * K)) & 0xFFu) << 23;
 }
 
+// Exponent fields (exp << 23) of weights 2p, 2p+1 of chunk k of this lane's
+// row h: from the verbatim bytes `ve` in a verbatim group (v), else decoded
+// (coded) or read as a palette index (twin).  Branch-free in v: the coded
+// stream is read in every lane and advances only in coded groups.  Returns
+// the larger of the two table addresses used (phantom-entry check).
+template <bool TWIN, int NP>
+__device__ __forceinline__ uint32_t b_exponents(LaneBits& lb, const Cmp<NP>& cmp, int lmin,
+                                                uint32_t s_off, uint32_t s_tab, uint32_t wb, int h,
+                                                int lane, int k, int p, bool v, const uint4& ve,
+                                                uint32_t& E0, uint32_t& E1) {
+  uint32_t e0, e1;
+  if (!TWIN) {
+    q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1, v);
+  } else {
+    // direct palette: word j of the lane holds indices 8j..8j+7 (MSB first)
+    const int q0 = 16 * k + 2 * p;               // index within the row
+    const uint32_t wa = lds_u32(wb + (uint32_t)((32 * h + (q0 >> 3)) * 128 + 4 * lane));
+    const int sh = 28 - 4 * (q0 & 7);
+    e0 = s_tab + 4u * ((wa >> sh) & 15u);
+    e1 = s_tab + 4u * ((wa >> (sh - 4)) & 15u);
+  }
+  const uint32_t t0 = lds_u32(e0), t1 = lds_u32(e1);
+  const uint32_t wv = u4w(ve, p >> 1);
+  E0 = v ? ((p & 1) ? b_vexp23<2>(wv) : b_vexp23<0>(wv)) : t0;
+  E1 = v ? ((p & 1) ? b_vexp23<3>(wv) : b_vexp23<1>(wv)) : t1;
+  return e0 > e1 ? e0 : e1;
+}
+
 // ---------------------------------------------------------------------------
 // Shared prologue of the CUDA-core BF16 kernels (two-warp CTAs): barriers,
 // the table copy and check, the exponent table.  Returns false (after
@@ -213,9 +241,12 @@ __global__ void __launch_bounds__(64, 12) b_product_kernel(const BArgs a) {
     }
     const int strip = t / a.TK, kt = t % a.TK;
     const size_t r = (size_t)strip * 64 + 2 * lane + h;
-    // this row's verbatim flags (global loads overlap the copy in flight)
+    // this row's verbatim flags and first sign+mantissa chunk (global loads
+    // overlap the copy in flight)
     uint32_t fw, vb;
     b_row_flags(a, r, kt, fw, vb);
+    uint4 n_sm = b_load_sm(a, t, lane, h, 0);
+    uint4 n_ve = (fw & 1u) ? b_load_vexp(a, vb, 0) : make_uint4(0, 0, 0, 0);
     if (!__syncthreads_and(mbar_wait(&bar[0], par))) {
       if (lead) report(a.status, LW_DEV_TIMEOUT);
       return;
@@ -252,8 +283,6 @@ __global__ void __launch_bounds__(64, 12) b_product_kernel(const BArgs a) {
       for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
       // 16 chunks of 16 weights (chunk k: group k/4, part k%4); the next
       // chunk's bytes are loaded while this one is processed
-      uint4 n_sm = b_load_sm(a, t, lane, h, 0);
-      uint4 n_ve = (fw & 1u) ? b_load_vexp(a, vb, 0) : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
       for (int k = 0; k < 16; ++k) {
         const bool v = (fw >> (k >> 2)) & 1u;
@@ -266,23 +295,7 @@ __global__ void __launch_bounds__(64, 12) b_product_kernel(const BArgs a) {
 #pragma unroll
         for (int p = 0; p < 8; ++p) {       // weights 2p, 2p+1 of the chunk
           uint32_t E0, E1;                   // exp << 23
-          const uint32_t wv = u4w(ve, p >> 1);
-          if (v) {
-            E0 = (p & 1) ? b_vexp23<2>(wv) : b_vexp23<0>(wv);
-            E1 = (p & 1) ? b_vexp23<3>(wv) : b_vexp23<1>(wv);
-          } else if (!TWIN) {
-            uint32_t e0, e1;
-            q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
-            E0 = lds_u32(e0);
-            E1 = lds_u32(e1);
-          } else {
-            // direct palette: word j of the lane holds indices 8j..8j+7 (MSB first)
-            const int q0 = 16 * k + 2 * p;               // index within the row
-            const uint32_t wa = lds_u32(wb + (uint32_t)((32 * h + (q0 >> 3)) * 128 + 4 * lane));
-            const int sh = 28 - 4 * (q0 & 7);
-            E0 = lds_u32(s_tab + 4u * ((wa >> sh) & 15u));
-            E1 = lds_u32(s_tab + 4u * ((wa >> (sh - 4)) & 15u));
-          }
+          b_exponents<TWIN, NP>(lb, cmp, lmin, s_off, s_tab, wb, h, lane, k, p, v, ve, E0, E1);
           const uint32_t sw = u4w(sm, p >> 1);
           const float2 f = (p & 1) ? make_float2(b_value<2>(sw, E0), b_value<3>(sw, E1))
                                    : make_float2(b_value<0>(sw, E0), b_value<1>(sw, E1));
@@ -371,23 +384,9 @@ __global__ void __launch_bounds__(64) b_decode_kernel(const BArgs a) {
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           uint32_t E0, E1;
-          const uint32_t wv = u4w(ve, p >> 1);
-          if (v) {
-            E0 = (p & 1) ? b_vexp23<2>(wv) : b_vexp23<0>(wv);
-            E1 = (p & 1) ? b_vexp23<3>(wv) : b_vexp23<1>(wv);
-          } else if (!TWIN) {
-            uint32_t e0, e1;
-            q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
-            bad |= (e0 >= first_bad) | (e1 >= first_bad);
-            E0 = lds_u32(e0);
-            E1 = lds_u32(e1);
-          } else {
-            const int q0 = 16 * k + 2 * p;
-            const uint32_t wa = lds_u32(wb + (uint32_t)((32 * h + (q0 >> 3)) * 128 + 4 * lane));
-            const int sh = 28 - 4 * (q0 & 7);
-            E0 = lds_u32(s_tab + 4u * ((wa >> sh) & 15u));
-            E1 = lds_u32(s_tab + 4u * ((wa >> (sh - 4)) & 15u));
-          }
+          const uint32_t e = b_exponents<TWIN, NP>(lb, cmp, lmin, s_off, s_tab, wb, h, lane, k, p, v, ve,
+                                                   E0, E1);
+          if (!TWIN) bad |= !v && e >= first_bad;
           const uint32_t sw = u4w(sm, p >> 1);
           const uint32_t f0 = (p & 1) ? __float_as_uint(b_value<2>(sw, E0)) : __float_as_uint(b_value<0>(sw, E0));
           const uint32_t f1 = (p & 1) ? __float_as_uint(b_value<3>(sw, E1)) : __float_as_uint(b_value<1>(sw, E1));

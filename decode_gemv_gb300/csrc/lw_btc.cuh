@@ -274,8 +274,13 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
                                         lead ? 0 : 1);
         if (cur) infl0 = true; else infl1 = true;
       }
-      uint32_t nfw = 0, nvb = 0;   // flags of the next tile column
-      if (has && more) b_row_flags(a, r, kt + 1, nfw, nvb);
+      // flags of the next tile column: its flag word now (used at its start),
+      // its first verbatim index = this column's plus this column's count
+      uint32_t nword = 0;
+      if (has && more) nword = __ldg(a.vflags + r * (size_t)a.GW + (4 * (kt + 1)) / 32);
+      const uint32_t nvb = vb + __popc(fw);
+      uint4 p_sm = make_uint4(0, 0, 0, 0);   // the next column's first chunk
+      uint32_t nfw = 0;
       bool to = false;
       if (has) {
         to = !mbar_wait(&wbar[cur], cur ? wpar1 : wpar0);
@@ -307,6 +312,10 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
           if (xk >= 1 && !mbar_wait(&xbar[(xk + 1) & 1], ((xk - 1) >> 1) & 1u)) to2 = true;
           else stage_xt(a, xs0 + ((xk + 1) & 1) * xs_bytes, k < 8 ? kt : kt + 1, k < 8 ? 1 : 0);
         }
+        if (k == 8 && more && has) {
+          p_sm = b_load_sm(a, t + 1, lane, h, 0);
+          nfw = (nword >> ((4 * (kt + 1)) % 32)) & 15u;
+        }
         uint32_t W[8];   // bf16x2 of this lane's row, columns 16k .. 16k+15
         if (dec) {
           const bool v = (fw >> (k >> 2)) & 1u;
@@ -316,22 +325,14 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
             n_sm = b_load_sm(a, t, lane, h, k1);
             if ((fw >> g1) & 1u) n_ve = b_load_vexp(a, vb + __popc(fw & ((1u << g1) - 1u)), k1 & 3);
           } else if (more) {   // first chunk of the next tile column
-            n_sm = b_load_sm(a, t + 1, lane, h, 0);
+            n_sm = p_sm;
             if (nfw & 1u) n_ve = b_load_vexp(a, nvb, 0);
           }
+
 #pragma unroll
           for (int p = 0; p < 8; ++p) {
             uint32_t E0, E1;
-            if (!v) {
-              uint32_t e0, e1;
-              q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
-              E0 = lds_u32(e0);
-              E1 = lds_u32(e1);
-            } else {
-              const uint32_t wv = u4w(ve, p >> 1);
-              E0 = (p & 1) ? b_vexp23<2>(wv) : b_vexp23<0>(wv);
-              E1 = (p & 1) ? b_vexp23<3>(wv) : b_vexp23<1>(wv);
-            }
+            b_exponents<false, NP>(lb, cmp, lmin, s_off, s_tab, wb, h, lane, k, p, v, ve, E0, E1);
             const uint32_t sw = u4w(sm, p >> 1);
             const uint32_t f0 = __float_as_uint((p & 1) ? b_value<2>(sw, E0) : b_value<0>(sw, E0));
             const uint32_t f1 = __float_as_uint((p & 1) ? b_value<3>(sw, E1) : b_value<1>(sw, E1));

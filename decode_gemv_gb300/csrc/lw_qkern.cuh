@@ -283,9 +283,12 @@ __device__ __forceinline__ void put_off(uint32_t* tab, int c, uint32_t v) {
 
 // Decode two symbols from one window.  Returns the shared addresses of their
 // symbol-table entries (entry size ESZ bytes).
+// With `hold` set the reader does not advance (the lane's symbols come from
+// elsewhere this step); the entries returned are then meaningless but valid
+// shared addresses, so a warp decodes without branching on `hold`.
 template <int NP, int ESZ>
 __device__ __forceinline__ void q_decode2(LaneBits& lb, const Cmp<NP>& cmp, int lmin, uint32_t s_off,
-                                          uint32_t& e0, uint32_t& e1) {
+                                          uint32_t& e0, uint32_t& e1, bool hold = false) {
   constexpr uint32_t M = 1u << (32 - Cmp<NP>::kShift);   // count = hi32(z * M)
   const uint32_t w = lb.window();
   const uint32_t z0 = cmp.count(w);
@@ -295,7 +298,7 @@ __device__ __forceinline__ void q_decode2(LaneBits& lb, const Cmp<NP>& cmp, int 
   const int L1 = (int)mad_hi(z1, M, (uint32_t)lmin);
   e0 = lds_u32(s_off + z0) + __funnelshift_l(w, 0u, L0) * ESZ;
   e1 = lds_u32(s_off + z1) + __funnelshift_l(w1, 0u, L1) * ESZ;
-  lb.advance(L0 + L1);
+  lb.advance(hold ? 0 : L0 + L1);
 }
 
 // fp32 value 16 + c of a 4-bit code: shift the code to bits 19..22 (SH > 0:
