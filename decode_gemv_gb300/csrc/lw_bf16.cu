@@ -126,7 +126,7 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   a.nsplit = nsplit;
   int grid = n_blocks * nsplit;
   if (grid > slots) grid = slots;
-  k<<<grid, dev::kTcThreads, smem, st>>>(a);
+  launch_pdl(k, grid, dev::kTcThreads, smem, st, a);
   return check_launch("tensor-core product kernel");
 }
 
@@ -153,7 +153,7 @@ lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int bat
     a.stage_bytes = (a.xf_offset + bp * 1024 + 127) / 128 * 128;
     const size_t smem = (size_t)dev::kStageOff + (size_t)a.stage_bytes;
     lw_status s = launch_persistent((const void*)k, 64, smem, a.n_tiles, st, [&](int blocks) {
-      k<<<blocks, 64, smem, st>>>(a);
+      launch_pdl(k, blocks, 64, smem, st, a);
     });
     if (s != LW_OK) return s;
   }
@@ -170,7 +170,7 @@ lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status,
   a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
   const size_t smem = (size_t)dev::kStageOff + (size_t)a.stage_bytes;
   return launch_persistent((const void*)k, 64, smem, a.n_tiles, st, [&](int blocks) {
-    k<<<blocks, 64, smem, st>>>(a);
+    launch_pdl(k, blocks, 64, smem, st, a);
   });
 }
 

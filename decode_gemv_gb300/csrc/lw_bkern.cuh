@@ -56,9 +56,20 @@ constexpr int kBTabOff = 128;     // uint32 exp << 23 per canonical index (16) /
 
 // Copies of tile t (coded rows [r0, r1)): its words, activations (bf16) and
 // second-row offsets.
+// Copies of tile t's activation rows (bf16) on a barrier whose expected
+// bytes already include them (lane 0).
+__device__ __forceinline__ void b_issue_x(const BArgs& a, int t, uint8_t* stage, uint64_t* bar,
+                                          int lane) {
+  if (lane != 0) return;
+  const int kt = t % a.TK;
+  for (int b = 0; b < a.batch; ++b)
+    bulk_g2s(stage + a.x_offset + b * 512, a.x + (size_t)b * a.K + (size_t)kt * 256, 512, bar);
+}
+
 template <bool PRODUCT, bool TWIN>
 __device__ __forceinline__ bool b_issue(const BArgs& a, int t, uint32_t r0, uint32_t r1,
-                                        uint8_t* stage, uint64_t* bar, int lane) {
+                                        uint8_t* stage, uint64_t* bar, int lane,
+                                        bool with_x = true) {
   const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(a.stage_rows - kLookahead);
   if (lane == 0) {
     const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
@@ -66,13 +77,9 @@ __device__ __forceinline__ bool b_issue(const BArgs& a, int t, uint32_t r0, uint
     const uint32_t mbytes = TWIN ? 0u : 64u;
     mbar_arrive_expect_tx(bar, wbytes + xbytes + mbytes);
     if (wbytes) bulk_g2s(stage, a.words + (size_t)r0 * 32, wbytes, bar);
-    if (PRODUCT) {
-      const int kt = t % a.TK;
-      for (int b = 0; b < a.batch; ++b)
-        bulk_g2s(stage + a.x_offset + b * 512, a.x + (size_t)b * a.K + (size_t)kt * 256, 512, bar);
-    }
     if (mbytes) bulk_g2s(stage + a.mid_offset, a.lane_mid + (size_t)t * 32, 64, bar);
   }
+  if (PRODUCT && with_x) b_issue_x(a, t, stage, bar, lane);
   return fits;
 }
 
@@ -169,15 +176,19 @@ __device__ __forceinline__ bool b_prologue(const BArgs& a, uint8_t* smem, uint64
   __syncthreads();
   if (lead) table_issue(smem + kRawTabOff, a.table, &bar[2]);
   fit = true;
-  if (t < a.n_tiles)
+  if (t < a.n_tiles)   // the bundle part now, the activations after the wait below
     fit = b_issue<PRODUCT, TWIN>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1),
-                                 smem + kStageOff, &bar[0], lead ? 0 : 1);
+                                 smem + kStageOff, &bar[0], lead ? 0 : 1, false);
   const bool got = __syncthreads_and(mbar_wait(&bar[2], 0u));
   const bool ok = got && (TWIN || __syncthreads_and(table_ok_warp(tb, LW_FMT_BF16_EXP, 16, NCMP, lane)));
   if (!ok) {
     if (lead) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
     if (!got) mbar_wait(&bar[2], 0u);
-    if (t < a.n_tiles) mbar_wait(&bar[0], 0u);
+    if (t < a.n_tiles) {   // (the first tile's barrier expects the activations too)
+      pdl_wait();
+      if (PRODUCT) b_issue_x(a, t, smem + kStageOff, &bar[0], lead ? 0 : 1);
+      mbar_wait(&bar[0], 0u);
+    }
     return false;
   }
   // coded: offsets and exp << 23 per canonical index; twin: per palette index
@@ -194,6 +205,8 @@ __device__ __forceinline__ bool b_prologue(const BArgs& a, uint8_t* smem, uint64
     }
   }
   __syncthreads();
+  pdl_wait();
+  if (PRODUCT && t < a.n_tiles) b_issue_x(a, t, smem + kStageOff, &bar[0], lead ? 0 : 1);
   return true;
 }
 
@@ -313,6 +326,7 @@ __global__ void __launch_bounds__(64, 12) b_product_kernel(const BArgs a) {
     } else if (lead) {
       report(a.status, LW_DEV_TILE_SIZE);
     }
+    if (!more) pdl_trigger();   // last tile decoded (see q_product_kernel)
     fence_proxy_async();
     q_commit<BP>(qa, smem, strip, kt, (int)r, part);
     if (more)   // refill the stage (released by the commit's barrier)
@@ -401,6 +415,7 @@ __global__ void __launch_bounds__(64) b_decode_kernel(const BArgs a) {
     } else if (lead) {
       report(a.status, LW_DEV_TILE_SIZE);
     }
+    if (!more) pdl_trigger();
     fence_proxy_async();
     __syncthreads();   // both warps are done with the stage
     if (more) fit = b_issue<false, TWIN>(a, t + nw, nr0, nr1, stage, &bar[0], lead ? 0 : 1);

@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
     lmin = tb->lmin;
   }
   __syncthreads();
+  pdl_wait();
   const uint32_t idesc = idesc_bf16((uint32_t)a.bpad);
   const int n_strips = a.N / 64;
   const int n_blocks = (n_strips + 3) / 4;
@@ -373,6 +374,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       vb = nvb;
     }
     if (failed) break;
+    if (u + (int)gridDim.x >= units) pdl_trigger();   // last unit decoded
     // all MMAs of this unit done -> read the accumulators (warp w: tile h,
     // lanes of strip sq)
     bool to3 = !mbar_wait(&sbar[(gchunk - 1) % kSlots], ((gchunk - 1) / kSlots) & 1u);

@@ -117,6 +117,19 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t a) {
   return v;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled once every CTA of this one has issued the trigger (each CTA
+// issues it when its last tile is decoded; the next kernel then runs its
+// prologue while this one drains), and wait here for the previous kernel to
+// complete before touching anything it may write (activations, workspace,
+// outputs).  Before the wait a kernel reads bundle sections only, which no
+// library call writes.  A CTA that exits without the trigger counts as
+// triggered.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

@@ -15,6 +15,26 @@ int device_sm_count();
 // Cached per (kernel, smem).  0 if it cannot run.
 int resident_blocks(const void* kernel, int threads, size_t smem);
 
+// Launch kernel `k` with programmatic stream serialisation allowed: it may
+// be scheduled while the previous kernel of the stream drains, and waits
+// for it in-kernel (pdl_wait) before touching data that kernel may write.
+// Errors surface through cudaGetLastError (check_launch).
+template <class Arg>
+inline void launch_pdl(void (*k)(Arg), int grid, int block, size_t smem, cudaStream_t st,
+                       const Arg& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  (void)cudaLaunchKernelEx(&cfg, k, a);
+}
+
 inline lw_status check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(LW_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));

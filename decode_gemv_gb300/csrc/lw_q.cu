@@ -88,7 +88,7 @@ lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, fl
   a.nstage = blocks1 > 0 && a.n_tiles >= 3 * blocks1 ? 2 : 1;
   const size_t smem = a.nstage == 2 ? smem2 : smem1;
   return launch_persistent((const void*)k, dev::kQThreads, smem, a.n_tiles, st, [&](int blocks) {
-    k<<<blocks, dev::kQThreads, smem, st>>>(a);
+    launch_pdl(k, blocks, dev::kQThreads, smem, st, a);
   });
 }
 
@@ -118,7 +118,7 @@ lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cu
   a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
   const size_t smem = (size_t)dev::kStageOff + 2 * (size_t)a.stage_bytes;
   return launch_persistent((const void*)k, dev::kQThreads, smem, a.n_tiles, st, [&](int blocks) {
-    k<<<blocks, dev::kQThreads, smem, st>>>(a);
+    launch_pdl(k, blocks, dev::kQThreads, smem, st, a);
   });
 }
 

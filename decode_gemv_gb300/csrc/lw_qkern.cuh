@@ -96,9 +96,22 @@ __host__ __device__ constexpr int q_x_offset(int stage_rows, int qp_bytes) {
 // (thread `lead` issues; every caller gets the result).  Returns false if the
 // tile is longer than the stage allows (the other copies are still issued,
 // so the barrier completes).
+// Copies of tile t's activation slices (products), on a barrier whose
+// expected bytes already include them (thread `lead`).
+template <int FMT>
+__device__ __forceinline__ void q_issue_x(const QArgs& a, int t, uint8_t* stage, uint64_t* bar,
+                                          bool lead) {
+  if (!lead) return;
+  const int kt = t % a.TK;
+  uint8_t* xs = stage + q_x_offset(a.stage_rows, QFmt<FMT>::qp_bytes);
+  for (int b = 0; b < a.batch; ++b)
+    bulk_g2s(xs + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024, bar);
+}
+
 template <int FMT, bool PRODUCT>
 __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint32_t r0, uint32_t r1,
-                                        uint8_t* stage, uint64_t* bar, bool lead) {
+                                        uint8_t* stage, uint64_t* bar, bool lead,
+                                        bool with_x = true) {
   const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(a.stage_rows - kLookahead);
   if (lead) {
     const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
@@ -107,15 +120,10 @@ __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint32_t r0, uint
     const uint32_t mbytes = a.lane_mid ? 64u : 0u;
     mbar_arrive_expect_tx(bar, wbytes + qpb + xbytes + mbytes);
     if (wbytes) bulk_g2s(stage, a.words + (size_t)r0 * 32, wbytes, bar);
-    if (PRODUCT) {
-      bulk_g2s(stage + a.stage_rows * 128, a.qparams + (size_t)t * qpb, qpb, bar);
-      const int kt = t % a.TK;
-      uint8_t* xs = stage + q_x_offset(a.stage_rows, qpb);
-      for (int b = 0; b < a.batch; ++b)
-        bulk_g2s(xs + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024, bar);
-    }
+    if (PRODUCT) bulk_g2s(stage + a.stage_rows * 128, a.qparams + (size_t)t * qpb, qpb, bar);
     if (mbytes) bulk_g2s(stage + a.mid_offset, a.lane_mid + (size_t)t * 32, 64, bar);
   }
+  if (PRODUCT && with_x) q_issue_x<FMT>(a, t, stage, bar, lead);
   return fits;
 }
 
@@ -480,9 +488,9 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
   if (!TWIN && lead) table_issue(smem + kRawTabOff, a.table, &bar[2]);
   uint32_t par0 = 0u, par1 = 0u;
   bool fit0 = true, fit1 = true;
-  if (t < a.n_tiles)
+  if (t < a.n_tiles)   // the bundle part now, the activations after the wait below
     fit0 = q_issue<FMT, true>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), stage0,
-                              &bar[0], lead);
+                              &bar[0], lead, false);
   // row range of the next tile to issue (t + nw), loaded one tile ahead
   uint32_t nr0 = 0, nr1 = 0;
   if (t + nw < a.n_tiles) {
@@ -498,7 +506,11 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
     if (!ok) {
       if (lead) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
       if (!got) mbar_wait(&bar[2], 0u);        // let the copies in flight land
-      if (t < a.n_tiles) mbar_wait(&bar[0], 0u);
+      if (t < a.n_tiles) {                     // (the first tile's barrier expects x too)
+        pdl_wait();
+        q_issue_x<FMT>(a, t, stage0, &bar[0], lead);
+        mbar_wait(&bar[0], 0u);
+      }
       return;
     }
     table_stage<NP, ESZ>(smem, offtab, tb, F::alpha, [&](int i, uint32_t sy) {
@@ -512,6 +524,8 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
     lmin = tb->lmin;
     __syncthreads();
   }
+  pdl_wait();
+  if (t < a.n_tiles) q_issue_x<FMT>(a, t, stage0, &bar[0], lead);
 
   for (int it = 0; t < a.n_tiles; ++it, t += nw) {
     const bool odd = two && (it & 1);
@@ -668,6 +682,9 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
         }
       }
     }
+    // the next kernel may start its prologue once every CTA has decoded its
+    // last tile (earlier, its CTAs would crowd into the slots this grid leaves)
+    if (!more) pdl_trigger();
     // this thread's reads of the stage come before the next bulk copy into it
     fence_proxy_async();
     q_commit<BP>(a, smem, strip, kt, strip * 64 + 2 * lane + h, part);
@@ -731,6 +748,8 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
     first_bad = s_sym + 4u * (uint32_t)tb->n_sym;
     __syncthreads();
   }
+  pdl_wait();
+  if (t >= a.n_tiles) pdl_trigger();
   for (int it = 0; t < a.n_tiles; ++it, t += nw) {
     const bool odd = it & 1;
     const bool more = t + nw < a.n_tiles;
@@ -817,6 +836,7 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
         if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
       }
     }
+    if (!more) pdl_trigger();   // last tile decoded (see q_product_kernel)
     fence_proxy_async();
     __syncthreads();   // both warps are done with this stage
   }

@@ -35,7 +35,14 @@
  * library never allocates or frees device memory and never synchronises a
  * stream.  Device calls are asynchronous on `stream` (a cudaStream_t passed
  * as void*; NULL = the legacy default stream) and deterministic: a fixed
- * reduction order, no floating-point atomics.
+ * reduction order, no floating-point atomics.  Kernels are launched with
+ * programmatic stream serialisation: a call may be scheduled while the
+ * previous library kernel on the stream drains and then reads only the
+ * bundle's sections until that kernel has completed (activations, the
+ * workspace, outputs and *d_status are touched after it).  So bundle
+ * sections must not be written by a kernel that allows early launch of its
+ * successor and runs immediately before the call; ordinary kernels and
+ * copies (and every library call) are waited for in full.
  *
  * Errors.  Argument, shape and format checks run on the host before any
  * launch and return a status; a failed launch returns LW_ERR_CUDA.  A kernel
