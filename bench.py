@@ -207,6 +207,27 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------
 
+# ----------------------------------------------------------------------------
+# replicas (one process per GPU, no data-path collective)
+# ----------------------------------------------------------------------------
+
+def max_over_ranks(ms, device=None):
+    """The slowest rank's time (every rank gets it); `ms` unchanged with one
+    process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank, world, t_max_ms):
+    """Every rank's bytes over the slowest rank's time (weak scaling)."""
+    return bytes_per_rank * world / (t_max_ms * 1e-3) / 1e9
+
+
 def build_layer(names):
     from decode_gemv_gb300 import lw
     mats = []
@@ -382,17 +403,13 @@ def run_ours(args):
         torch.distributed.barrier()
     clocks = clk.stop()
     ms = ev0.elapsed_time(ev1) / args.steps
-    t_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms, dev)
     status = int(st.item())
     # diagnostic: each matrix's call alone (one graph per call, events around)
     per_mat = per_call_ms(torch, stream, [[(lambda c=c, j=j: call(c, j)) for j in range(n_mat)]
                                           for c in range(min(copies, 4))])
 
-    value = coded_step * world / (t_max * 1e-3) / 1e9
+    value = whole_job_gbs(coded_step, world, t_max)
     peak, peak_kind = peaks()
     launches_per_step = n_mat            # one fused kernel per matrix
     # dominant kernel (the fused decode+GEMV launch, 97 % of the step's GPU
