@@ -53,6 +53,30 @@ int resident_blocks(const void* kernel, int threads, size_t smem) {
   return n;
 }
 
+int tc_resident_blocks(const void* kernel, int threads, size_t& smem, int tmem_cols) {
+  int d = 0, per_sm_smem = 0, regs_sm = 65536, reserved = 1024;
+  cudaGetDevice(&d);
+  cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
+  cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, d);
+  cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, d);
+  const int max_ctas = 512 / tmem_cols;
+  const size_t floor_smem = (size_t)per_sm_smem / (size_t)(max_ctas + 1) + 1;
+  if (smem < floor_smem) smem = floor_smem;
+  if (resident_blocks(kernel, threads, smem) < 1) return 0;   // also raises the smem limit
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int warp_regs = ((fa.numRegs + 7) / 8 * 8 * 32 + 255) / 256 * 256;
+  int per_sm = max_ctas;
+  const int by_regs = regs_sm / (warp_regs * (threads / 32));
+  const int by_smem = (int)((size_t)per_sm_smem / (smem + (size_t)reserved));
+  per_sm = by_regs < per_sm ? by_regs : per_sm;
+  per_sm = by_smem < per_sm ? by_smem : per_sm;
+  return per_sm < 1 ? 1 : per_sm;
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 lw_status check_dev_bundle(const lw_dev_bundle* b, bool want_twin, bool product) {
@@ -93,8 +117,8 @@ using namespace lw;
 extern "C" size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch) {
   if (!b || batch < 1 || b->rows <= 0 || b->cols <= 0) return 0;
   size_t part = workspace_partials_bytes(b, 8);
-  if (b->fmt == LW_FMT_BF16_EXP && !b->twin && batch >= 16 && workspace_tc_bytes(b) > part)
-    part = workspace_tc_bytes(b);
+  const bool tc = !b->twin && (b->fmt == LW_FMT_BF16_EXP ? batch >= 16 : batch >= kQtMinRows);
+  if (tc && workspace_tc_bytes(b) > part) part = workspace_tc_bytes(b);
   return workspace_counter_bytes(b) + part;
 }
 
@@ -128,12 +152,19 @@ static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, f
     }
     return launch_bf16_product(b, xb, batch, Y, ws, d_status, st);
   }
-  // activation rows in chunks of up to 8 (each chunk decodes the matrix once)
-  for (int b0 = 0; b0 < batch; b0 += 8) {
-    const int nb = batch - b0 < 8 ? batch - b0 : 8;
-    s = launch_q_product(b, static_cast<const float*>(X) + (size_t)b0 * b->cols, nb,
-                         Y + (size_t)b0 * b->rows, ws, d_status, st);
+  // tensor cores for passes of kQtMinRows..32 activation rows, CUDA cores
+  // for passes of up to 8 (each pass decodes the matrix once)
+  const float* xf = static_cast<const float*>(X);
+  for (int b0 = 0; b0 < batch;) {
+    const int left = batch - b0;
+    const bool tc = !b->twin && left >= kQtMinRows;
+    const int nb = tc ? (left < 32 ? left : 32) : (left < 8 ? left : 8);
+    s = tc ? launch_q_tc_product(b, xf + (size_t)b0 * b->cols, nb, Y + (size_t)b0 * b->rows, ws,
+                                 d_status, st)
+           : launch_q_product(b, xf + (size_t)b0 * b->cols, nb, Y + (size_t)b0 * b->rows, ws,
+                              d_status, st);
     if (s != LW_OK) return s;
+    b0 += nb;
   }
   return LW_OK;
 }

@@ -90,33 +90,8 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   a.xs_off = dev::kTcXsOff;
   a.wstage_off = a.xs_off + 2 * a.bpad * 256;
   size_t smem = (size_t)a.wstage_off + 8 * (size_t)a.stage_bytes;
-  int dev_id = 0, per_sm_smem = 0;
-  cudaGetDevice(&dev_id);
-  cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev_id);
-  // at most 512 / tmem_cols resident CTAs per SM (shared memory sees to it),
-  // so a tensor-memory allocation never has to wait
-  const int max_ctas = 512 / a.tmem_cols;
-  const size_t floor_smem = (size_t)per_sm_smem / (size_t)(max_ctas + 1) + 1;
-  if (smem < floor_smem) smem = floor_smem;
-  if (resident_blocks((const void*)k, dev::kTcThreads, smem) < 1)   // also raises the smem limit
-    return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
-  // resident CTAs per SM from the kernel's own budgets (registers, shared
-  // memory, tensor-memory columns); the runtime's occupancy query answers 1
-  // for this kernel whatever its shared memory
-  int per_sm = max_ctas;
-  {
-    cudaFuncAttributes fa{};
-    int regs_sm = 65536, reserved = 1024;
-    cudaFuncGetAttributes(&fa, (const void*)k);
-    cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev_id);
-    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev_id);
-    const int warp_regs = ((fa.numRegs + 7) / 8 * 8 * 32 + 255) / 256 * 256;
-    const int by_regs = regs_sm / (warp_regs * (dev::kTcThreads / 32));
-    const int by_smem = (int)((size_t)per_sm_smem / (smem + (size_t)reserved));
-    per_sm = by_regs < per_sm ? by_regs : per_sm;
-    per_sm = by_smem < per_sm ? by_smem : per_sm;
-    if (per_sm < 1) per_sm = 1;
-  }
+  const int per_sm = tc_resident_blocks((const void*)k, dev::kTcThreads, smem, a.tmem_cols);
+  if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
   const int slots = per_sm * device_sm_count();
   int nsplit = (slots + n_blocks - 1) / n_blocks;

@@ -64,6 +64,14 @@ lw_status launch_persistent(const void* kernel, int threads, size_t smem, int n_
   return check_launch("product kernel");
 }
 
+// Resident CTAs per SM of a tensor-core kernel with `threads` threads and
+// `tmem_cols` tensor-memory columns per CTA, from its own budgets (registers,
+// shared memory, tensor memory): the runtime's occupancy query answers 1 for
+// these kernels whatever their shared memory.  Raises `smem` so that at most
+// 512 / tmem_cols CTAs fit on an SM (a tensor-memory allocation then never
+// waits) and the kernel's shared-memory limit to it.  0 if it cannot run.
+int tc_resident_blocks(const void* kernel, int threads, size_t& smem, int tmem_cols);
+
 // Workspace layout: one uint32 split-K counter per 64-row strip (padded to
 // 256 bytes), then fp32 partial sums -- [K/256][min(batch, 8)][N] for the
 // CUDA-core products, [split <= tc_max_split][64][N] for the tensor-core BF16
@@ -102,5 +110,11 @@ lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int bat
 lw_status launch_bf16_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);
 lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
                                  void* ws, int32_t* status, cudaStream_t st);
+// 4-/6-bit tensor-core product, kQtMinRows..32 activation rows per launch
+// (below kQtMinRows the CUDA-core kernel, whose cost grows with the rows, is
+// still faster)
+constexpr int kQtMinRows = 9;
+lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
+                              int32_t* status, cudaStream_t st);
 
 }  // namespace lw

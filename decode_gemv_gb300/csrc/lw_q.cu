@@ -5,6 +5,7 @@
 #include "lw_internal.h"
 #include "lw_launch.h"
 #include "lw_qkern.cuh"
+#include "lw_qtc.cuh"
 
 namespace lw {
 
@@ -46,7 +47,65 @@ QKernel pick_decode(int ncmp) {
   }
 }
 
+template <int FMT>
+QKernel pick_tc(int ncmp) {
+  switch (ncmp) {
+    case 4: return dev::q_tc_kernel<FMT, 4>;
+    case 7: return dev::q_tc_kernel<FMT, 7>;
+    case 8: return dev::q_tc_kernel<FMT, 8>;
+    default: return dev::q_tc_kernel<FMT, 10>;
+  }
+}
+
 }  // namespace
+
+lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
+                              int32_t* status, cudaStream_t st) {
+  const int fmt = b->fmt;
+  const int ncmp = ncmp_bucket(b->lmax - b->lmin);
+  QKernel k = fmt == LW_FMT_Q4_PAIR ? pick_tc<dev::kQ4>(ncmp) : pick_tc<dev::kQ6>(ncmp);
+  dev::QArgs a{};
+  a.words = b->words;
+  a.tile_off = b->tile_off;
+  a.lane_bits = b->lane_bits;
+  a.lane_mid = b->lane_mid;
+  a.table = b->table;
+  a.qparams = static_cast<const uint8_t*>(b->qparams);
+  a.x = x;
+  a.ws = workspace_partials(b, ws);
+  a.counters = workspace_counters(b, ws);
+  a.y = y;
+  a.status = status;
+  a.TK = (int)(b->cols / 256);
+  a.N = (int)b->rows;
+  a.K = (int)b->cols;
+  a.n_tiles = (int)tiles_of(b->rows, b->cols);
+  a.batch = batch;
+  a.stage_rows = b->max_tile_rows + dev::kLookahead;
+  // stage: coded rows | scales (and mins) | lane_mid
+  a.mid_offset = a.stage_rows * 128 + qparam_tile_bytes(fmt);
+  a.stage_bytes = (a.mid_offset + 64 + 127) / 128 * 128;
+  a.bpad = (batch + 15) / 16 * 16;
+  const int need = dev::qt_tmem_need(a.bpad);
+  a.tmem_cols = need <= 32 ? 32 : (need <= 64 ? 64 : (need <= 128 ? 128 : 256));
+  // header | X^T halves (2 x 2 bpad x 256 B) | tile stages (4 strips x 2)
+  a.xs_off = dev::kQtXsOff;
+  a.wstage_off = a.xs_off + 2 * a.bpad * 512;
+  size_t smem = (size_t)a.wstage_off + 8 * (size_t)a.stage_bytes;
+  const int per_sm = tc_resident_blocks((const void*)k, dev::kQtThreads, smem, a.tmem_cols);
+  if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
+  const int n_blocks = (int)((b->rows / 64 + 3) / 4);
+  const int slots = per_sm * device_sm_count();
+  int nsplit = (slots + n_blocks - 1) / n_blocks;
+  if (nsplit > tc_max_split(b)) nsplit = tc_max_split(b);
+  if (nsplit > a.TK) nsplit = a.TK;
+  if (nsplit < 1) nsplit = 1;
+  a.nsplit = nsplit;
+  int grid = n_blocks * nsplit;
+  if (grid > slots) grid = slots;
+  launch_pdl(k, grid, dev::kQtThreads, smem, st, a);
+  return check_launch("tensor-core product kernel");
+}
 
 lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
                            int32_t* status, cudaStream_t st) {

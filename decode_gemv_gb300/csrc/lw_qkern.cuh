@@ -65,6 +65,8 @@ struct QArgs {
   int nstage;            // stage buffers per CTA: 2 (prefetch the next tile
                          // while decoding) or 1 (more resident CTAs)
   int mid_offset;        // byte offset of the tile's lane_mid copy in a stage
+  // tensor-core product only
+  int nsplit, bpad, tmem_cols, xs_off, wstage_off;
 };
 
 constexpr int kQ4 = LW_FMT_Q4_PAIR, kQ6 = LW_FMT_Q6;
@@ -93,9 +95,11 @@ __host__ __device__ constexpr int q_x_offset(int stage_rows, int qp_bytes) {
 }
 
 // Issue the copies of tile t, whose coded rows are [r0, r1), into one stage
-// (thread `lead` issues; every caller gets the result).  Returns false if the
-// tile is longer than the stage allows (the other copies are still issued,
-// so the barrier completes).
+// (thread `lead` issues; every caller gets the result).  Activation slices
+// (products): xmode 1 = expected and copied now, 2 = expected, copied later
+// by q_issue_x, 0 = none (the tensor-core path stages them itself).  Returns
+// false if the tile is longer than the stage allows (the other copies are
+// still issued, so the barrier completes).
 // Copies of tile t's activation slices (products), on a barrier whose
 // expected bytes already include them (thread `lead`).
 template <int FMT>
@@ -111,19 +115,19 @@ __device__ __forceinline__ void q_issue_x(const QArgs& a, int t, uint8_t* stage,
 template <int FMT, bool PRODUCT>
 __device__ __forceinline__ bool q_issue(const QArgs& a, int t, uint32_t r0, uint32_t r1,
                                         uint8_t* stage, uint64_t* bar, bool lead,
-                                        bool with_x = true) {
+                                        int xmode = 1) {
   const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(a.stage_rows - kLookahead);
   if (lead) {
     const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
     constexpr uint32_t qpb = PRODUCT ? QFmt<FMT>::qp_bytes : 0u;
-    const uint32_t xbytes = PRODUCT ? (uint32_t)a.batch * 1024u : 0u;
+    const uint32_t xbytes = PRODUCT && xmode ? (uint32_t)a.batch * 1024u : 0u;
     const uint32_t mbytes = a.lane_mid ? 64u : 0u;
     mbar_arrive_expect_tx(bar, wbytes + qpb + xbytes + mbytes);
     if (wbytes) bulk_g2s(stage, a.words + (size_t)r0 * 32, wbytes, bar);
     if (PRODUCT) bulk_g2s(stage + a.stage_rows * 128, a.qparams + (size_t)t * qpb, qpb, bar);
     if (mbytes) bulk_g2s(stage + a.mid_offset, a.lane_mid + (size_t)t * 32, 64, bar);
   }
-  if (PRODUCT && with_x) q_issue_x<FMT>(a, t, stage, bar, lead);
+  if (PRODUCT && xmode == 1) q_issue_x<FMT>(a, t, stage, bar, lead);
   return fits;
 }
 
@@ -490,7 +494,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
   bool fit0 = true, fit1 = true;
   if (t < a.n_tiles)   // the bundle part now, the activations after the wait below
     fit0 = q_issue<FMT, true>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), stage0,
-                              &bar[0], lead, false);
+                              &bar[0], lead, 2);
   // row range of the next tile to issue (t + nw), loaded one tile ahead
   uint32_t nr0 = 0, nr1 = 0;
   if (t + nw < a.n_tiles) {

@@ -288,15 +288,22 @@ lw_status lw_decode_gemv(const lw_dev_bundle* b, const void* x, float* y,
 /*
  * Fused decode + small-batch product: Y[b][r] = sum_k W[r][k] X[b][k],
  * X [batch][K] row-major (fp32, or bf16 for BF16), Y fp32 [batch][N],
- * batch 1..256.  The 4-/6-bit formats work on CUDA cores, up to 8 activation
- * rows per pass (larger batches in passes of 8), each row in the order of
- * lw_decode_gemv.  The BF16 format takes the same CUDA-core path for fewer
- * than 16 rows; from 16 rows on it rebuilds BF16 weights in shared memory and
- * multiplies on the tensor cores (tcgen05.mma, BF16 x BF16 -> FP32 in tensor
- * memory; up to 64 rows per pass), [UW] "How reconstructive matmul works":
- * the order within the tensor core is the hardware's, then K-splits are added
- * in ascending order -- deterministic, but not bitwise equal to the CUDA-core
- * path.  The workspace must hold lw_workspace_bytes(b, batch) bytes.
+ * batch 1..256.  Passes (each decodes the matrix once):
+ *  - 4-/6-bit, up to 8 rows: CUDA cores, each row in the order of
+ *    lw_decode_gemv (bitwise equal to it and to the twin);
+ *  - 4-/6-bit, 9..32 rows: tensor cores -- each weight dequantised in fp32
+ *    and split exactly into a BF16 high part plus a BF16-rounded remainder,
+ *    each activation likewise; tcgen05.mma accumulates hi*x_hi + hi*x_lo +
+ *    lo*x_hi in FP32 tensor memory (relative error ~2^-16 per product);
+ *  - BF16, fewer than 16 rows: CUDA cores, passes of up to 8;
+ *  - BF16, 16..64 rows: tensor cores on the rebuilt BF16 weights
+ *    (tcgen05.mma, BF16 x BF16 -> FP32 in tensor memory), [UW] "How
+ *    reconstructive matmul works".
+ * Batches beyond one pass take as many passes as needed (the largest pass
+ * first).  On the tensor cores the order within an MMA is the hardware's,
+ * then K-splits are added in ascending order -- deterministic, but not
+ * bitwise equal to the CUDA-core path.  The workspace must hold
+ * lw_workspace_bytes(b, batch) bytes.
  */
 lw_status lw_decode_gemm(const lw_dev_bundle* b, const void* X, int32_t batch,
                          float* Y, void* ws, size_t ws_bytes,

@@ -98,7 +98,7 @@ def test_gemv_parity_and_twin_bitwise(fmt, shape):
     assert np.array_equal(y.view(np.uint32), yt.view(np.uint32)), "twin and coded kernel differ"
 
 
-@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8, 12])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("fmt", [lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6])
 def test_gemm_batches(fmt, batch):
     n, k = 192, 1024
@@ -116,6 +116,35 @@ def test_gemm_batches(fmt, batch):
     _, dt = upload(fmt, m, twin=True)
     Yt, stt = run_product(dt, m["x"], twin=True)
     assert stt == 0 and np.array_equal(Y.view(np.uint32), Yt.view(np.uint32))
+
+
+TC_CASES = [((192, 1024), 9), ((320, 512), 12), ((256, 3072), 16), ((64, 256), 32),
+            ((512, 2048), 33), ((256, 1024), 70)]
+
+
+@pytest.mark.parametrize("shape,batch", TC_CASES)
+@pytest.mark.parametrize("fmt", [lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6])
+def test_tensor_core_batches(fmt, shape, batch):
+    """Batches of 9 or more rows take the tcgen05 path (weights and
+    activations split into BF16 high and low parts, FP32 accumulation in
+    tensor memory): against the oracle, against the CUDA-core path fed 4
+    rows at a time, against the twin, and deterministic."""
+    n, k = shape
+    m = inputs.small_q4(3 * n + batch, n, k, batch=batch) if fmt == lw.LW_FMT_Q4_PAIR \
+        else inputs.small_q6(3 * n + batch, n, k, batch=batch)
+    _, db = upload(fmt, m)
+    Y, st = run_product(db, m["x"])
+    assert st == 0
+    absprod = oracle.abs_row_products(fmt, m)
+    assert_close(Y, oracle.reference_output(fmt, m), absprod)
+    Yc = np.concatenate([run_product(db, m["x"][b: b + 4])[0] for b in range(0, batch, 4)])
+    assert_close(Y, Yc, absprod)
+    _, dt = upload(fmt, m, twin=True)
+    Yt, stt = run_product(dt, m["x"], twin=True)
+    assert stt == 0
+    assert_close(Y, Yt, absprod)
+    Y2, st2 = run_product(db, m["x"])
+    assert st2 == 0 and np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
 
 
 def test_oracle_built_bundle_decodes_on_gpu():
@@ -260,6 +289,21 @@ def test_full_size_mistral_layer(index):
     _, dt = upload(spec.fmt, m, twin=True)
     yt, st = run_product(dt, m["x"], twin=True)
     assert st == 0 and np.array_equal(y.view(np.uint32), yt.view(np.uint32))
+
+
+@pytest.mark.parametrize("index", [4, 6])
+def test_full_size_mistral_tensor_core(index):
+    """gate (14336x4096) and down (4096x14336) at batch 16 and 32 on the
+    tensor cores, sampled rows against the oracle."""
+    spec = inputs.workload_specs(inputs.MISTRAL_LAYER)[index]
+    m = inputs.make_matrix(inputs.MISTRAL_LAYER, spec, 0, index, batch=32)
+    _, db = upload(spec.fmt, m)
+    rows = np.unique(np.concatenate([np.arange(0, spec.rows, 131), [spec.rows - 1]]))
+    ref, absprod = sampled_reference(spec.fmt, m, rows)
+    for b in (16, 32):
+        Y, st = run_product(db, m["x"][:b])
+        assert st == 0
+        assert_close(Y[:, rows], ref[:b], absprod[:b])
 
 
 @pytest.mark.parametrize("index", range(4))
