@@ -114,10 +114,21 @@ lw_status check_dev_bundle(const lw_dev_bundle* b, bool want_twin, bool product)
 
 using namespace lw;
 
+// Whether `rows` activation rows of a 4-/6-bit matrix go to the tensor-core
+// kernel.  It gives each CTA 256 rows x a range of tile columns, so it pays
+// from kQtMinRows rows on when the matrix has enough of those units to fill
+// the device (about 1.5 per SM); a smaller matrix stays on the CUDA-core
+// kernel (a CTA per tile) while one pass of 8 rows covers the batch.
+static bool q_use_tc(const lw_dev_bundle* b, int rows) {
+  if (b->twin || rows < kQtMinRows) return false;
+  const long long units = ((b->rows / 64 + 3) / 4) * (long long)tc_max_split(b);
+  return rows > 8 || 2 * units >= 3LL * device_sm_count();
+}
+
 extern "C" size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch) {
   if (!b || batch < 1 || b->rows <= 0 || b->cols <= 0) return 0;
   size_t part = workspace_partials_bytes(b, 8);
-  const bool tc = !b->twin && (b->fmt == LW_FMT_BF16_EXP ? batch >= 16 : batch >= kQtMinRows);
+  const bool tc = b->fmt == LW_FMT_BF16_EXP ? !b->twin && batch >= 16 : q_use_tc(b, batch);
   if (tc && workspace_tc_bytes(b) > part) part = workspace_tc_bytes(b);
   return workspace_counter_bytes(b) + part;
 }
@@ -157,7 +168,7 @@ static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, f
   const float* xf = static_cast<const float*>(X);
   for (int b0 = 0; b0 < batch;) {
     const int left = batch - b0;
-    const bool tc = !b->twin && left >= kQtMinRows;
+    const bool tc = q_use_tc(b, left);
     const int nb = tc ? (left < 32 ? left : 32) : (left < 8 ? left : 8);
     s = tc ? launch_q_tc_product(b, xf + (size_t)b0 * b->cols, nb, Y + (size_t)b0 * b->rows, ws,
                                  d_status, st)

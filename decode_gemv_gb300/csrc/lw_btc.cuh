@@ -112,6 +112,29 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Chunk hand-off without a CTA barrier: each of the `nwarps` decoding warps,
+// once its tensor-memory stores for the chunk are done (tcgen05.wait::st),
+// arrives on the chunk slot's counter, and the warp completing a group of
+// `nwarps` arrivals runs issue() on its lane 0.  The counter only grows: a
+// warp arrives on a slot again only after the MMAs of the slot's previous
+// chunk completed, i.e. after that chunk's group was full.  Ordering:
+// tcgen05 stores -> fence before thread sync -> (syncwarp, fence, atomic)
+// ... (atomic, fence) -> fence after thread sync -> tcgen05.mma.
+template <class Issue>
+__device__ __forceinline__ void chunk_arrive(uint32_t* cnt, uint32_t nwarps, int lane, Issue issue) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    if ((atomicAdd(cnt, 1u) + 1u) % nwarps == 0u) {
+      __threadfence_block();
+      tc_fence_after();
+      issue();
+    }
+  }
+  __syncwarp();
+}
+
 // Shared-memory matrix descriptor, K-major, no swizzle: 8x8 core matrices of
 // 16-byte rows; lbo = byte distance between core matrices adjacent along K,
 // sbo = along M/N; descriptor version 1 (sm_100 family), base offset 0.
@@ -151,7 +174,8 @@ __device__ __forceinline__ void stage_xt(const BArgs& a, uint32_t xs, int kt, in
 // shared-memory map of the tensor-core kernel (bytes; the X^T buffers and
 // tile stages follow at the launch's offsets)
 constexpr int kTcBarOff = 256;      // wbar[4 strips][2], sbar[kSlots], xbar[2], tbar
-constexpr int kTcSlotOff = 384;     // tensor-memory address, broadcast word
+constexpr int kTcSlotOff = 384;     // tensor-memory address, broadcast word, abort flag,
+                                    // chunk-slot arrival counters [kSlots]
 constexpr int kTcRawTabOff = 1024;  // the bundle's lw_table
 constexpr int kTcXsOff = 2048;
 constexpr int kTcThreads = 256;
@@ -173,6 +197,8 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   uint64_t* tbar = xbar + 2;                                                  // table copy
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kTcSlotOff);
   volatile uint32_t* shared_word = tslot + 1;
+  volatile uint32_t* abort_flag = tslot + 2;   // a wait ran out: stop at the next tile column
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + kTcSlotOff + 16);   // [kSlots]
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kTcRawTabOff);
   const uint32_t xs0 = sbase + (uint32_t)a.xs_off;       // [2][bpad * 256]: X^T halves
   const uint32_t xs_bytes = (uint32_t)a.bpad * 256u;
@@ -184,10 +210,14 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
     mbar_init(&wbar[1], 1);
   }
   if (tid == 0) {
-    for (int q = 0; q < kSlots; ++q) mbar_init(&sbar[q], 1);
+    for (int q = 0; q < kSlots; ++q) {
+      mbar_init(&sbar[q], 1);
+      cnt[q] = 0u;
+    }
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
     mbar_init(tbar, 1);
+    *abort_flag = 0u;
   }
   if (lane == 0) fence_barrier_init();
   if (warp == 0) {
@@ -262,13 +292,17 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       if (fw & 1u) n_ve = b_load_vexp(a, vb, 0);
     }
     bool first = true;
-    for (int kt = kt0; kt < kt1 && !failed; ++kt) {
+    for (int kt = kt0; kt < kt1; ++kt) {
+      // one CTA barrier per tile column: every warp is done with the previous
+      // column (its stage may be refilled), and a wait that ran out anywhere
+      // stops all warps here
+      if (__syncthreads_or(*abort_flag != 0u)) { failed = timed_out = true; break; }
       const int t = strip * a.TK + kt;
       const bool more = kt + 1 < kt1;
       const uint32_t cur = ts & 1;
       uint8_t* wstage = wst0 + cur * a.stage_bytes;
       // next tile into the other stage (both of its readers finished the
-      // previous tile before the barrier that closed it)
+      // previous tile before the barrier above)
       if (has && more) {
         fit_nxt = b_issue<false, false>(a, t + 1, __ldg(a.tile_off + t + 1), __ldg(a.tile_off + t + 2),
                                         wst0 + (cur ^ 1u) * a.stage_bytes, &wbar[cur ^ 1u],
@@ -298,21 +332,28 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
       }
       if (has && !fit_cur && lead) report(a.status, LW_DEV_TILE_SIZE);
+      if (to) *abort_flag = 1u;
       for (int k = 0; k < 16; ++k) {
         const uint32_t slot = gchunk % kSlots;
-        bool to2 = to;
-        if (gchunk >= (uint32_t)kSlots)
-          to2 |= !mbar_wait(&sbar[slot], ((gchunk - kSlots) / kSlots) & 1u);
+        // after an abort every wait is skipped and nothing is arrived on; the
+        // warps run to the barrier at the next tile column
+        // (`live` is kept warp-uniform: the tensor-memory stores and the
+        // hand-off below are warp-wide)
+        bool live = *abort_flag == 0u;
+        if (live && gchunk >= (uint32_t)kSlots)
+          live = mbar_wait(&sbar[slot], ((gchunk - kSlots) / kSlots) & 1u);
+        if (live && (k & 7) == 4 && (k < 8 || more) && xk >= 1)
+          // the next X^T half goes into the other buffer once the MMAs that
+          // last read it (the previous half) are done
+          live = mbar_wait(&xbar[(xk + 1) & 1], ((xk - 1) >> 1) & 1u);
+        live = __all_sync(0xFFFFFFFFu, live);
+        if (!live) *abort_flag = 1u;
         if ((k & 7) == 0) {   // this thread's part of the current X^T half
           cp_async_wait_all();
           fence_proxy_async();
         }
-        if ((k & 7) == 4 && (k < 8 || more)) {
-          // the next X^T half into the other buffer, once the MMAs that last
-          // read it (the previous half) are done
-          if (xk >= 1 && !mbar_wait(&xbar[(xk + 1) & 1], ((xk - 1) >> 1) & 1u)) to2 = true;
-          else stage_xt(a, xs0 + ((xk + 1) & 1) * xs_bytes, k < 8 ? kt : kt + 1, k < 8 ? 1 : 0);
-        }
+        if (live && (k & 7) == 4 && (k < 8 || more))
+          stage_xt(a, xs0 + ((xk + 1) & 1) * xs_bytes, k < 8 ? kt : kt + 1, k < 8 ? 1 : 0);
         if (k == 8 && more && has) {
           p_sm = b_load_sm(a, t + 1, lane, h, 0);
           nfw = (nword >> ((4 * (kt + 1)) % 32)) & 15u;
@@ -343,27 +384,27 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
 #pragma unroll
           for (int p = 0; p < 8; ++p) W[p] = 0u;
         }
-        tmem_st8(tmem + t_lane + col_a + (uint32_t)((h * kSlots + (int)slot) * kACols), W);
-        tmem_st_wait();
-        fence_proxy_async();
-        tc_fence_before();
-        if (__syncthreads_or(to2)) { failed = timed_out = true; break; }
-        if (tid == 0) {
-          tc_fence_after();
-          const uint64_t bd = sdesc(xs0 + (xk & 1) * xs_bytes + 256u * (uint32_t)(k & 7), 128u, 2048u);
+        if (live) {
+          tmem_st8(tmem + t_lane + col_a + (uint32_t)((h * kSlots + (int)slot) * kACols), W);
+          tmem_st_wait();
+          fence_proxy_async();
+          // the last of the 8 warps issues this chunk's MMAs
+          const bool fst = first;
+          chunk_arrive(&cnt[slot], 8u, lane, [&] {
+            const uint64_t bd = sdesc(xs0 + (xk & 1) * xs_bytes + 256u * (uint32_t)(k & 7), 128u, 2048u);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-            umma_bf16_ta(tmem + (uint32_t)(hh * a.bpad),
-                         tmem + col_a + (uint32_t)((hh * kSlots + (int)slot) * kACols), bd, idesc,
-                         first ? 0u : 1u);
-          umma_commit(&sbar[slot]);
-          if ((k & 7) == 7) umma_commit(&xbar[xk & 1]);   // X^T half free after these
+            for (int hh = 0; hh < 2; ++hh)
+              umma_bf16_ta(tmem + (uint32_t)(hh * a.bpad),
+                           tmem + col_a + (uint32_t)((hh * kSlots + (int)slot) * kACols), bd, idesc,
+                           fst ? 0u : 1u);
+            umma_commit(&sbar[slot]);
+            if ((k & 7) == 7) umma_commit(&xbar[xk & 1]);   // X^T half free after these
+          });
         }
         first = false;
         ++gchunk;
         if ((k & 7) == 7) ++xk;
       }
-      if (failed) break;
       if (dec) {
         const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
         if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
@@ -373,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       fw = nfw;
       vb = nvb;
     }
-    if (failed) break;
+    if (failed || __syncthreads_or(*abort_flag != 0u)) { failed = timed_out = true; break; }
     if (u + (int)gridDim.x >= units) pdl_trigger();   // last unit decoded
     // all MMAs of this unit done -> read the accumulators (warp w: tile h,
     // lanes of strip sq)

@@ -113,7 +113,7 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
 // 4-/6-bit tensor-core product, kQtMinRows..32 activation rows per launch
 // (below kQtMinRows the CUDA-core kernel, whose cost grows with the rows, is
 // still faster)
-constexpr int kQtMinRows = 9;
+constexpr int kQtMinRows = 6;
 lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
                               int32_t* status, cudaStream_t st);
 

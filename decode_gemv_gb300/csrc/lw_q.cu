@@ -88,11 +88,17 @@ lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch,
   a.bpad = (batch + 15) / 16 * 16;
   const int need = dev::qt_tmem_need(a.bpad);
   a.tmem_cols = need <= 32 ? 32 : (need <= 64 ? 64 : (need <= 128 ? 128 : 256));
-  // header | X^T halves (2 x 2 bpad x 256 B) | tile stages (4 strips x 2)
+  // header | X^T halves (2 x 2 bpad x 256 B) | tile stages (4 strips x 1 or
+  // 2): two stages per strip unless one stage lets more CTAs reside
   a.xs_off = dev::kQtXsOff;
   a.wstage_off = a.xs_off + 2 * a.bpad * 512;
-  size_t smem = (size_t)a.wstage_off + 8 * (size_t)a.stage_bytes;
-  const int per_sm = tc_resident_blocks((const void*)k, dev::kQtThreads, smem, a.tmem_cols);
+  size_t smem2 = (size_t)a.wstage_off + 8 * (size_t)a.stage_bytes;
+  size_t smem1 = (size_t)a.wstage_off + 4 * (size_t)a.stage_bytes;
+  const int per_sm2 = tc_resident_blocks((const void*)k, dev::kQtThreads, smem2, a.tmem_cols);
+  const int per_sm1 = tc_resident_blocks((const void*)k, dev::kQtThreads, smem1, a.tmem_cols);
+  a.nstage = per_sm1 > per_sm2 ? 1 : 2;
+  const int per_sm = a.nstage == 1 ? per_sm1 : per_sm2;
+  const size_t smem = a.nstage == 1 ? smem1 : smem2;
   if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
   const int slots = per_sm * device_sm_count();

@@ -1,4 +1,4 @@
-// 4-bit (pair-coded) and 6-bit Huffman-coded weights times a batch of 9..32
+// 4-bit (pair-coded) and 6-bit Huffman-coded weights times a batch of 6..32
 // fp32 activation rows on the 5th-generation tensor cores.
 //
 // The codes and their tiles follow "LazyWeights: Decode-on-Demand Edge
@@ -39,7 +39,8 @@ constexpr int kQtMaxRows = 32;      // activation rows per pass
 // dynamic shared-memory map (bytes)
 constexpr int kQtTabOff = 0;        // symbol values: float2[256] (c0, c1) / float[64] (c - 32)
 constexpr int kQtBarOff = 2048;     // wbar[4 strips][2], sbar[kQtSlots], xbar[2], tbar
-constexpr int kQtSlotOff = 2176;    // tensor-memory address, broadcast word
+constexpr int kQtSlotOff = 2176;    // tensor-memory address, broadcast word, abort flag,
+                                    // chunk-slot arrival counters [kQtSlots]
 constexpr int kQtRawTabOff = 2304;  // the bundle's lw_table
 constexpr int kQtXsOff = 3328;      // X^T halves: 2 x [2 bpad rows][128 columns] bf16
 static_assert(kQtRawTabOff + (int)sizeof(lw_table) <= kQtXsOff, "shared-memory map");
@@ -113,10 +114,14 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
   uint64_t* tbar = xbar + 2;                                                 // table copy
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kQtSlotOff);
   volatile uint32_t* shared_word = tslot + 1;
+  volatile uint32_t* abort_flag = tslot + 2;   // a wait ran out: stop at the next tile column
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + kQtSlotOff + 16);   // [kQtSlots]
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kQtRawTabOff);
   uint8_t* xs0 = smem + a.xs_off;                        // [2][2 bpad x 128] bf16
   const int xs_bytes = a.bpad * 512;
-  uint8_t* wst0 = smem + a.wstage_off + (2 * sq) * a.stage_bytes;   // this strip's two stages
+  // this strip's stages: two (the next tile prefetched) or one (more CTAs fit)
+  uint8_t* wst0 = smem + a.wstage_off + (a.nstage * sq) * a.stage_bytes;
+  const bool two = a.nstage == 2;
   const bool lead = h == 0 && lane == 0;                 // issues this strip's tile copies
 
   if (warp < 4 && lane == 0) {
@@ -124,10 +129,14 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
     mbar_init(&wbar[1], 1);
   }
   if (tid == 0) {
-    for (int q = 0; q < kQtSlots; ++q) mbar_init(&sbar[q], 1);
+    for (int q = 0; q < kQtSlots; ++q) {
+      mbar_init(&sbar[q], 1);
+      cnt[q] = 0u;
+    }
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
     mbar_init(tbar, 1);
+    *abort_flag = 0u;
   }
   if (lane == 0) fence_barrier_init();
   if (warp == 0) {
@@ -190,7 +199,7 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
     const bool has = strip < n_strips;
     const size_t r = (size_t)strip * 64 + 2 * lane + h;
     bool fit_cur = true, fit_nxt = true;
-    if (has) {
+    if (has && two) {
       const int t = strip * a.TK + kt0;
       fit_cur = q_issue<FMT, true>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1),
                                    wst0 + (ts & 1) * a.stage_bytes, &wbar[ts & 1], lead, 0);
@@ -203,12 +212,21 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
     qt_x_store(a, xs0 + (xk & 1) * xs_bytes, xv);
     fence_proxy_async();
     bool first = true;
-    for (int kt = kt0; kt < kt1 && !failed; ++kt) {
+    for (int kt = kt0; kt < kt1; ++kt) {
+      // one CTA barrier per tile column: every warp is done with the previous
+      // column (its stage may be refilled), and a wait that ran out anywhere
+      // stops all warps here
+      if (__syncthreads_or(*abort_flag != 0u)) { failed = timed_out = true; break; }
       const int t = strip * a.TK + kt;
       const bool more = kt + 1 < kt1;
-      const uint32_t cur = ts & 1;
+      const uint32_t cur = two ? ts & 1 : 0u;
       uint8_t* wstage = wst0 + cur * a.stage_bytes;
-      if (has && more) {   // the next tile into the other stage
+      if (has && !two) {   // one stage: this tile now (its last readers are past the barrier)
+        fit_cur = q_issue<FMT, true>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), wstage,
+                                     &wbar[0], lead, 0);
+        infl0 = true;
+      }
+      if (has && two && more) {   // the next tile into the other stage
         fit_nxt = q_issue<FMT, true>(a, t + 1, __ldg(a.tile_off + t + 1), __ldg(a.tile_off + t + 2),
                                      wst0 + (cur ^ 1u) * a.stage_bytes, &wbar[cur ^ 1u], lead, 0);
         if (cur) infl0 = true; else infl1 = true;
@@ -236,22 +254,26 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
         }
       }
       if (has && !fit_cur && lead) report(a.status, LW_DEV_TILE_SIZE);
+      if (to) *abort_flag = 1u;
       for (int k = 0; k < 16; ++k) {
         const uint32_t slot = gchunk % kQtSlots;
-        bool to2 = to;
-        if (gchunk >= (uint32_t)kQtSlots)
-          to2 |= !mbar_wait(&sbar[slot], ((gchunk - kQtSlots) / kQtSlots) & 1u);
         const bool next_half = k < 8 || more;
+        // after an abort every wait is skipped and nothing is arrived on; the
+        // warps run to the barrier at the next tile column.  `live` is kept
+        // warp-uniform (the tensor-memory stores and the hand-off are warp-wide)
+        bool live = *abort_flag == 0u;
+        if (live && gchunk >= (uint32_t)kQtSlots)
+          live = mbar_wait(&sbar[slot], ((gchunk - kQtSlots) / kQtSlots) & 1u);
+        if (live && (k & 7) == 4 && next_half && xk >= 1)
+          // the next X^T half goes into the other buffer once the MMAs that
+          // last read it (the previous half) are done
+          live = mbar_wait(&xbar[(xk + 1) & 1], ((xk - 1) >> 1) & 1u);
+        live = __all_sync(0xFFFFFFFFu, live);
+        if (!live) *abort_flag = 1u;
         if ((k & 7) == 2 && next_half) qt_x_load(a, k < 8 ? kt : kt + 1, k < 8 ? 1 : 0, xv);
-        if ((k & 7) == 4 && next_half) {
-          // the next X^T half into the other buffer, once the MMAs that last
-          // read it (the previous half) are done
-          if (xk >= 1 && !mbar_wait(&xbar[(xk + 1) & 1], ((xk - 1) >> 1) & 1u)) {
-            to2 = true;
-          } else {
-            qt_x_store(a, xs0 + ((xk + 1) & 1) * xs_bytes, xv);
-            fence_proxy_async();
-          }
+        if (live && (k & 7) == 4 && next_half) {
+          qt_x_store(a, xs0 + ((xk + 1) & 1) * xs_bytes, xv);
+          fence_proxy_async();
         }
         uint32_t WH[8], WL[8];   // this lane's row, columns 16k .. 16k+15: hi and lo halves
         if (dec) {
@@ -278,40 +300,40 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
 #pragma unroll
           for (int p = 0; p < 8; ++p) WH[p] = WL[p] = 0u;
         }
-        const uint32_t rs = (uint32_t)((h * kQtSlots + (int)slot) * kACols);
-        tmem_st8(tmem + t_lane + col_hi + rs, WH);
-        tmem_st8(tmem + t_lane + col_lo + rs, WL);
-        tmem_st_wait();
-        fence_proxy_async();
-        tc_fence_before();
-        if (__syncthreads_or(to2)) { failed = timed_out = true; break; }
-        if (tid == 0) {
-          tc_fence_after();
-          const uint64_t bd = sdesc(smem_addr(xs0) + (xk & 1) * (uint32_t)xs_bytes + 256u * (uint32_t)(k & 7),
-                                    128u, 2048u);
+        if (live) {
+          const uint32_t rs = (uint32_t)((h * kQtSlots + (int)slot) * kACols);
+          tmem_st8(tmem + t_lane + col_hi + rs, WH);
+          tmem_st8(tmem + t_lane + col_lo + rs, WL);
+          tmem_st_wait();
+          fence_proxy_async();
+          // the last of the 8 warps issues this chunk's MMAs
+          const bool fst = first;
+          chunk_arrive(&cnt[slot], 8u, lane, [&] {
+            const uint64_t bd = sdesc(smem_addr(xs0) + (xk & 1) * (uint32_t)xs_bytes +
+                                          256u * (uint32_t)(k & 7), 128u, 2048u);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t d = tmem + (uint32_t)(hh * 2 * a.bpad);
-            const uint32_t ra = (uint32_t)((hh * kQtSlots + (int)slot) * kACols);
-            umma_bf16_ta(d, tmem + col_hi + ra, bd, idesc2, first ? 0u : 1u);
-            umma_bf16_ta(d, tmem + col_lo + ra, bd, idesc1, 1u);
-          }
-          umma_commit(&sbar[slot]);
-          if ((k & 7) == 7) umma_commit(&xbar[xk & 1]);   // X^T half free after these
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t d = tmem + (uint32_t)(hh * 2 * a.bpad);
+              const uint32_t ra = (uint32_t)((hh * kQtSlots + (int)slot) * kACols);
+              umma_bf16_ta(d, tmem + col_hi + ra, bd, idesc2, fst ? 0u : 1u);
+              umma_bf16_ta(d, tmem + col_lo + ra, bd, idesc1, 1u);
+            }
+            umma_commit(&sbar[slot]);
+            if ((k & 7) == 7) umma_commit(&xbar[xk & 1]);   // X^T half free after these
+          });
         }
         first = false;
         ++gchunk;
         if ((k & 7) == 7) ++xk;
       }
-      if (failed) break;
       if (dec) {
         const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
         if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
       }
       ++ts;
-      fit_cur = fit_nxt;
+      if (two) fit_cur = fit_nxt;
     }
-    if (failed) break;
+    if (failed || __syncthreads_or(*abort_flag != 0u)) { failed = timed_out = true; break; }
     if (u + (int)gridDim.x >= units) pdl_trigger();   // last unit decoded
     // all MMAs of this unit done -> read the accumulators (warp w: tile h,
     // lanes of strip sq); y = hi-part columns + lo-part columns

@@ -289,9 +289,11 @@ lw_status lw_decode_gemv(const lw_dev_bundle* b, const void* x, float* y,
  * Fused decode + small-batch product: Y[b][r] = sum_k W[r][k] X[b][k],
  * X [batch][K] row-major (fp32, or bf16 for BF16), Y fp32 [batch][N],
  * batch 1..256.  Passes (each decodes the matrix once):
- *  - 4-/6-bit, up to 8 rows: CUDA cores, each row in the order of
+ *  - 4-/6-bit, up to 5 rows (up to 8 for matrices too small to fill the
+ *    device's tensor-core CTAs): CUDA cores, each row in the order of
  *    lw_decode_gemv (bitwise equal to it and to the twin);
- *  - 4-/6-bit, 9..32 rows: tensor cores -- each weight dequantised in fp32
+ *  - 4-/6-bit, otherwise up to 32 rows: tensor cores -- each weight
+ *    dequantised in fp32
  *    and split exactly into a BF16 high part plus a BF16-rounded remainder,
  *    each activation likewise; tcgen05.mma accumulates hi*x_hi + hi*x_lo +
  *    lo*x_hi in FP32 tensor memory (relative error ~2^-16 per product);
