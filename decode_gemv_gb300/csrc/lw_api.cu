@@ -190,6 +190,48 @@ extern "C" lw_status lw_decode_gemm(const lw_dev_bundle* b, const void* X, int32
   return product(b, X, batch, Y, ws, ws_bytes, d_status, stream, false);
 }
 
+static size_t group_slice(const lw_dev_bundle* b) {
+  return (lw_workspace_bytes(b, 1) + 255) / 256 * 256;
+}
+
+extern "C" size_t lw_workspace_bytes_group(const lw_dev_bundle* const* b, int32_t n) {
+  if (!b || n < 1 || n > LW_MAX_GROUP) return 0;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!b[i]) return 0;
+    total += group_slice(b[i]);
+  }
+  return total;
+}
+
+extern "C" lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t n,
+                                          const void* const* x, float* const* y, void* ws,
+                                          size_t ws_bytes, int32_t* d_status, void* stream) {
+  clear_error();
+  if (!b || !x || !y || n < 1 || n > LW_MAX_GROUP)
+    return fail(LW_ERR_INVALID_ARG, "group of %d matrices (1..%d) or NULL arrays", n, LW_MAX_GROUP);
+  if (!ws || !aligned16(ws)) return fail(LW_ERR_INVALID_ARG, "workspace NULL or not 16-byte aligned");
+  const float* xs[LW_MAX_GROUP];
+  float* ys[LW_MAX_GROUP];
+  void* wss[LW_MAX_GROUP];
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    lw_status s = check_dev_bundle(b[i], false, true);
+    if (s != LW_OK) return s;
+    if (b[i]->fmt == LW_FMT_BF16_EXP)
+      return fail(LW_ERR_UNSUPPORTED, "groups take 4-/6-bit bundles");
+    if (b[i]->fmt != b[0]->fmt) return fail(LW_ERR_INVALID_ARG, "mixed formats in a group");
+    if (!x[i] || !y[i] || !aligned16(x[i]) || (reinterpret_cast<uintptr_t>(y[i]) & 7u))
+      return fail(LW_ERR_INVALID_ARG, "matrix %d: x must be 16-byte aligned, y 8-byte aligned", i);
+    xs[i] = static_cast<const float*>(x[i]);
+    ys[i] = y[i];
+    wss[i] = static_cast<char*>(ws) + off;
+    off += group_slice(b[i]);
+  }
+  if (ws_bytes < off) return fail(LW_ERR_INVALID_ARG, "workspace of %zu bytes < %zu", ws_bytes, off);
+  return launch_q_products(b, n, xs, 1, ys, wss, d_status, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" lw_status lw_twin_gemv(const lw_dev_bundle* b, const void* x, float* y, void* ws,
                                   size_t ws_bytes, int32_t* d_status, void* stream) {
   return product(b, x, 1, y, ws, ws_bytes, d_status, stream, true);

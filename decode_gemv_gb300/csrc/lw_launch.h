@@ -104,6 +104,8 @@ inline float* workspace_partials(const lw_dev_bundle* b, void* ws) {
 // ws: the caller's whole workspace (counters, then partial sums)
 lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,
                            int32_t* status, cudaStream_t st);
+lw_status launch_q_products(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,
+                            float* const* y, void* const* ws, int32_t* status, cudaStream_t st);
 lw_status launch_q_decode(const lw_dev_bundle* b, void* out, int32_t* status, cudaStream_t st);
 lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
                               void* ws, int32_t* status, cudaStream_t st);

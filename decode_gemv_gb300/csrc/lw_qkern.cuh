@@ -69,6 +69,24 @@ struct QArgs {
   int nsplit, bpad, tmem_cols, xs_off, wstage_off;
 };
 
+// The product kernel's launch: one matrix, or a group of independent
+// matrices of one format decoded in one grid (their tiles concatenated, in
+// order).  Passed as a grid constant: per-matrix fields are read from the
+// constant bank by index.
+constexpr int kMaxGroup = 8;
+struct QLaunch {
+  QArgs m[kMaxGroup];          // stage_rows, stage_bytes, nstage, mid_offset, batch
+                               // and status agree across the group
+  int first[kMaxGroup + 1];    // first global tile of each matrix; first[n] = total
+  int n;
+};
+
+// Advance `m` to the matrix holding global tile t (t never decreases).
+__device__ __forceinline__ int group_seek(const QLaunch& g, int t, int m) {
+  while (m + 1 < g.n && t >= g.first[m + 1]) ++m;
+  return m;
+}
+
 constexpr int kQ4 = LW_FMT_Q4_PAIR, kQ6 = LW_FMT_Q6;
 
 template <int FMT> struct QFmt;
@@ -457,7 +475,8 @@ __device__ __forceinline__ void table_stage(uint8_t* smem, uint32_t* offtab, con
 __host__ __device__ constexpr int q_min_ctas(int bp) { return bp <= 4 ? 16 : 12; }
 
 template <int FMT, bool TWIN, int BP, int NCMP>
-__global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(const QArgs a) {
+__global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
+    q_product_kernel(const __grid_constant__ QLaunch g) {
   extern __shared__ __align__(128) uint8_t smem[];
   using F = QFmt<FMT>;
   constexpr int NP = (NCMP + 1) / 2;
@@ -469,15 +488,17 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kRawTabOff);
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool lead = threadIdx.x == 0;
-  const int xoff = q_x_offset(a.stage_rows, F::qp_bytes);
+  const QArgs& u = g.m[0];   // fields shared by the group
+  const int xoff = q_x_offset(u.stage_rows, F::qp_bytes);
+  const int total = g.first[g.n];
 
-  const bool two = a.nstage == 2;
+  const bool two = u.nstage == 2;
   uint8_t* stage0 = smem + kStageOff;
-  uint8_t* stage1 = two ? stage0 + a.stage_bytes : stage0;
+  uint8_t* stage1 = two ? stage0 + u.stage_bytes : stage0;
   const int nw = gridDim.x;
   int t = blockIdx.x;
   // activation rows beyond `batch` stay zero in every stage
-  for (int i = a.batch * 256 + threadIdx.x; i < BP * 256; i += kQThreads) {
+  for (int i = u.batch * 256 + threadIdx.x; i < BP * 256; i += kQThreads) {
     reinterpret_cast<float*>(stage0 + xoff)[i] = 0.f;
     reinterpret_cast<float*>(stage1 + xoff)[i] = 0.f;
   }
@@ -488,62 +509,80 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
     fence_barrier_init();
   }
   __syncthreads();
+  // matrices of tiles t, t + nw, t + 2 nw
+  int cm = group_seek(g, t, 0);
+  int cn = group_seek(g, t + nw, cm);
   // the table and the first tile are copied at once
-  if (!TWIN && lead) table_issue(smem + kRawTabOff, a.table, &bar[2]);
-  uint32_t par0 = 0u, par1 = 0u;
+  if (!TWIN && lead) table_issue(smem + kRawTabOff, g.m[cm].table, &bar[2]);
+  uint32_t par0 = 0u, par1 = 0u, tpar = 0u;
   bool fit0 = true, fit1 = true;
-  if (t < a.n_tiles)   // the bundle part now, the activations after the wait below
-    fit0 = q_issue<FMT, true>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1), stage0,
+  if (t < total) {   // the bundle part now, the activations after the wait below
+    const QArgs& a = g.m[cm];
+    const int lt = t - g.first[cm];
+    fit0 = q_issue<FMT, true>(a, lt, __ldg(a.tile_off + lt), __ldg(a.tile_off + lt + 1), stage0,
                               &bar[0], lead, 2);
+  }
   // row range of the next tile to issue (t + nw), loaded one tile ahead
   uint32_t nr0 = 0, nr1 = 0;
-  if (t + nw < a.n_tiles) {
-    nr0 = __ldg(a.tile_off + t + nw);
-    nr1 = __ldg(a.tile_off + t + nw + 1);
+  if (t + nw < total) {
+    const QArgs& a = g.m[cn];
+    const int lt = t + nw - g.first[cn];
+    nr0 = __ldg(a.tile_off + lt);
+    nr1 = __ldg(a.tile_off + lt + 1);
   }
 
   Cmp<NP> cmp;
   int lmin = 1;
-  if (!TWIN) {
-    const bool got = __syncthreads_and(mbar_wait(&bar[2], 0u));
-    const bool ok = got && __syncthreads_and(table_ok_warp(tb, FMT, F::alpha, NCMP, lane));
-    if (!ok) {
-      if (lead) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
-      if (!got) mbar_wait(&bar[2], 0u);        // let the copies in flight land
-      if (t < a.n_tiles) {                     // (the first tile's barrier expects x too)
-        pdl_wait();
-        q_issue_x<FMT>(a, t, stage0, &bar[0], lead);
-        mbar_wait(&bar[0], 0u);
-      }
-      return;
-    }
-    table_stage<NP, ESZ>(smem, offtab, tb, F::alpha, [&](int i, uint32_t sy) {
-      if (FMT == kQ4)
-        reinterpret_cast<float2*>(smem + kTabOff)[i] =
-            make_float2(16.f + (float)(sy & 15u), 16.f + (float)((sy >> 4) & 15u));
-      else
-        reinterpret_cast<float*>(smem + kTabOff)[i] = 64.f + (float)(sy & 63u);
-    });
-    cmp.load(tb, tb->lmax - tb->lmin);
-    lmin = tb->lmin;
-    __syncthreads();
-  }
+  int tab_m = -1;   // matrix whose table is staged
   pdl_wait();
-  if (t < a.n_tiles) q_issue_x<FMT>(a, t, stage0, &bar[0], lead);
+  if (t < total) q_issue_x<FMT>(g.m[cm], t - g.first[cm], stage0, &bar[0], lead);
 
-  for (int it = 0; t < a.n_tiles; ++it, t += nw) {
+  for (int it = 0; t < total; ++it, t += nw) {
+    const QArgs& a = g.m[cm];
+    const QArgs& an = g.m[cn];                 // matrix of tile t + nw
+    const int lt = t - g.first[cm];            // tile t within its matrix
+    const int ltn = t + nw - g.first[cn];
     const bool odd = two && (it & 1);
-    const bool more = t + nw < a.n_tiles;
+    const bool more = t + nw < total;
     const uint32_t ir0 = nr0, ir1 = nr1;     // rows of tile t + nw
-    if (t + 2 * nw < a.n_tiles) {
-      nr0 = __ldg(a.tile_off + t + 2 * nw);
-      nr1 = __ldg(a.tile_off + t + 2 * nw + 1);
+    const int c2 = group_seek(g, t + 2 * nw, cn);
+    if (t + 2 * nw < total) {
+      const QArgs& a2 = g.m[c2];
+      const int lt2 = t + 2 * nw - g.first[c2];
+      nr0 = __ldg(a2.tile_off + lt2);
+      nr1 = __ldg(a2.tile_off + lt2 + 1);
+    }
+    if (!TWIN && cm != tab_m) {
+      // this matrix's decoder table (copied now unless the prologue already
+      // did); every reader of the previous one is past the commit's barriers
+      if (tab_m >= 0 && lead) table_issue(smem + kRawTabOff, a.table, &bar[2]);
+      const bool got = __syncthreads_and(mbar_wait(&bar[2], tpar));
+      tpar ^= 1u;
+      const bool ok = got && __syncthreads_and(table_ok_warp(tb, FMT, F::alpha, NCMP, lane));
+      if (!ok) {
+        if (lead) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
+        if (!got) mbar_wait(&bar[2], tpar ^ 1u);   // let the copies in flight land
+        if (odd) mbar_wait(&bar[1], par1);
+        else mbar_wait(&bar[0], par0);
+        return;
+      }
+      table_stage<NP, ESZ>(smem, offtab, tb, F::alpha, [&](int i, uint32_t sy) {
+        if (FMT == kQ4)
+          reinterpret_cast<float2*>(smem + kTabOff)[i] =
+              make_float2(16.f + (float)(sy & 15u), 16.f + (float)((sy >> 4) & 15u));
+        else
+          reinterpret_cast<float*>(smem + kTabOff)[i] = 64.f + (float)(sy & 63u);
+      });
+      cmp.load(tb, tb->lmax - tb->lmin);
+      lmin = tb->lmin;
+      __syncthreads();
+      tab_m = cm;
     }
     // two stages: the other one was released by the barrier that closed the
     // previous tile
     if (two && more) {
-      if (odd) fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lead);
-      else fit1 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage1, &bar[1], lead);
+      if (odd) fit0 = q_issue<FMT, true>(an, ltn, ir0, ir1, stage0, &bar[0], lead);
+      else fit1 = q_issue<FMT, true>(an, ltn, ir0, ir1, stage1, &bar[1], lead);
     }
     uint8_t* st = odd ? stage1 : stage0;
     const bool got = odd ? mbar_wait(&bar[1], par1) : mbar_wait(&bar[0], par0);
@@ -557,7 +596,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
     }
     if (odd) par1 ^= 1u; else par0 ^= 1u;
     const bool fit = odd ? fit1 : fit0;
-    const int strip = t / a.TK, kt = t % a.TK;
+    const int strip = lt / a.TK, kt = lt % a.TK;
     float part[BP];
 #pragma unroll
     for (int b = 0; b < BP; ++b) part[b] = 0.f;
@@ -593,7 +632,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
             acc[b] = __ffma2_rn(v1, make_float2(xv.z, xv.w), acc[b]);
           }
         }
-        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
+        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)lt * 32 + lane) : mid;
         if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
       } else {
 #pragma unroll 2
@@ -650,7 +689,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
             part[b] = fmaf(sc, (acc[b].x + acc[b].y) - 96.f * Xg, part[b]);
           }
         }
-        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
+        const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)lt * 32 + lane) : mid;
         if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
       } else {
 #pragma unroll 1
@@ -693,7 +732,9 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP)) q_product_kernel(co
     fence_proxy_async();
     q_commit<BP>(a, smem, strip, kt, strip * 64 + 2 * lane + h, part);
     if (!two && more)   // single stage: refill it now (released by the commit's barrier)
-      fit0 = q_issue<FMT, true>(a, t + nw, ir0, ir1, stage0, &bar[0], lead);
+      fit0 = q_issue<FMT, true>(an, ltn, ir0, ir1, stage0, &bar[0], lead);
+    cm = cn;
+    cn = c2;
   }
 }
 

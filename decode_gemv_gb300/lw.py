@@ -27,7 +27,8 @@ TABLE_BYTES = 1024
 EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_table_from_lengths",
             "lw_validate_sections", "lw_workspace_bytes", "lw_decode", "lw_decode_gemv",
             "lw_decode_gemm", "lw_twin_gemv", "lw_twin_gemm", "lw_status_string",
-            "lw_last_error", "lw_version", "lw_decode_gemv_noalloc", "lw_noalloc_scratch_bytes"]
+            "lw_last_error", "lw_version", "lw_decode_gemv_noalloc", "lw_noalloc_scratch_bytes",
+            "lw_decode_gemv_group", "lw_workspace_bytes_group"]
 
 
 class LwError(RuntimeError):
@@ -90,6 +91,8 @@ def load():
         "lw_last_error": ([], ctypes.c_char_p),
         "lw_version": ([], i32),
         "lw_decode_gemv_noalloc": ([P, P, P, P, P], i32),
+        "lw_decode_gemv_group": ([P, i32, P, P, P, sz, P, P], i32),
+        "lw_workspace_bytes_group": ([P, i32], sz),
         "lw_noalloc_scratch_bytes": ([], sz),
     }
     for name, (args, res) in sig.items():
@@ -305,6 +308,26 @@ def lw_decode_gemv_noalloc(db: DeviceBundle, x, y, d_status, stream=None) -> Non
     caller workspace (allocates nothing)."""
     _check(load().lw_decode_gemv_noalloc(db.ref, _tp(x), _tp(y), _tp(d_status),
                                          _stream_ptr(stream)), "lw_decode_gemv_noalloc")
+
+
+def _views(dbs):
+    arr = (ctypes.c_void_p * len(dbs))(*[ctypes.addressof(d.view) for d in dbs])
+    return arr
+
+
+def lw_workspace_bytes_group(dbs) -> int:
+    return int(load().lw_workspace_bytes_group(_views(dbs), len(dbs)))
+
+
+def lw_decode_gemv_group(dbs, xs, ys, ws, d_status, stream=None) -> None:
+    """One launch for several 4-/6-bit matrices: ys[i] = W_i xs[i]."""
+    n = len(dbs)
+    xa = (ctypes.c_void_p * n)(*[_tp(x) for x in xs])
+    ya = (ctypes.c_void_p * n)(*[_tp(y) for y in ys])
+    _check(load().lw_decode_gemv_group(_views(dbs), n, xa, ya, _tp(ws),
+                                       ws.numel() * ws.element_size(), _tp(d_status),
+                                       _stream_ptr(stream)),
+           "lw_decode_gemv_group")
 
 
 def lw_noalloc_scratch_bytes() -> int:

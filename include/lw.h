@@ -327,6 +327,27 @@ lw_status lw_twin_gemm(const lw_dev_bundle* twin, const void* X, int32_t batch,
                        void* stream);
 
 /*
+ * Fused decode + GEMV of n (1..LW_MAX_GROUP) independent coded matrices of one
+ * 4-/6-bit format in ONE launch: y[i] = W_i x[i] for every i (e.g. a layer's
+ * q, k and v projections; the x[i] may alias).  [LW] runtime paragraph after
+ * Fig. 3: the decode work of a step fused into as few passes as possible.  A
+ * matrix with few tiles leaves most of the GPU idle when launched alone; the
+ * group's tiles are decoded by one grid.  Each y[i] is bitwise what
+ * lw_decode_gemv(b[i], x[i], y[i], ...) gives.  b, x, y: host arrays of n
+ * pointers (bundles, device activations fp32 [K_i], device outputs fp32
+ * [N_i]).  ws: one workspace of lw_workspace_bytes_group(b, n) bytes, zeroed
+ * before first use (the matrices' counters and partial sums in consecutive
+ * 256-byte-aligned slices).  Errors: LW_ERR_INVALID_ARG for n outside
+ * 1..LW_MAX_GROUP, NULL pointers, twins, mixed formats; LW_ERR_UNSUPPORTED for
+ * BF16 bundles.
+ */
+#define LW_MAX_GROUP 8
+lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t n, const void* const* x,
+                               float* const* y, void* ws, size_t ws_bytes, int32_t* d_status,
+                               void* stream);
+size_t lw_workspace_bytes_group(const lw_dev_bundle* const* b, int32_t n);
+
+/*
  * lw_decode_gemv without a caller workspace, for callers that cannot allocate
  * device memory: code running under CUDA-graph capture, engines whose pool
  * allocator owns all device memory, latency-critical paths that cannot afford

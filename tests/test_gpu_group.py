@@ -1,0 +1,100 @@
+"""One launch for several independent 4-/6-bit matrices
+(lw_decode_gemv_group): every output bitwise equal to its matrix's own
+lw_decode_gemv call and within tolerance of the oracle; matrices of different
+shapes, tables and tile sizes in one group; shared inputs; argument errors."""
+import numpy as np
+import pytest
+
+import oracle
+from decode_gemv_gb300 import inputs
+from decode_gemv_gb300 import lw
+from helpers import assert_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lw.load()
+
+
+def _mat(fmt, seed, n, k, sd=1.6):
+    return inputs.small_q4(seed, n, k, sd=sd) if fmt == lw.LW_FMT_Q4_PAIR else inputs.small_q6(seed, n, k)
+
+
+def _upload(fmt, m):
+    hb = lw.lw_encode_bundle(fmt, m["codes"], m["scales"], m.get("mins"))
+    return lw.DeviceBundle.upload(hb, DEV)
+
+
+def _single(db, x):
+    y = torch.full((db.rows,), float("nan"), device=DEV)
+    ws = torch.zeros(lw.lw_workspace_bytes(db, 1) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lw.lw_decode_gemv(db, x, y, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return y.cpu().numpy()
+
+
+SHAPES = [(1024, 4096), (64, 256), (256, 1024), (192, 3072), (512, 512), (320, 768), (128, 2048),
+          (64, 1024)]
+
+
+@pytest.mark.parametrize("fmt", [lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6])
+@pytest.mark.parametrize("n", [1, 3, 8])
+def test_group_equals_single_calls(fmt, n):
+    mats = [_mat(fmt, 100 * n + i, *SHAPES[i], sd=1.2 + 0.15 * i) for i in range(n)]
+    dbs = [_upload(fmt, m) for m in mats]
+    xs = [torch.from_numpy(m["x"][0]).to(DEV) for m in mats]
+    ys = [torch.full((d.rows,), float("nan"), device=DEV) for d in dbs]
+    ws = torch.zeros(lw.lw_workspace_bytes_group(dbs) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):   # twice: the counters are left at zero
+        lw.lw_decode_gemv_group(dbs, xs, ys, ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for m, d, x, y in zip(mats, dbs, xs, ys):
+            yg = y.cpu().numpy()
+            assert np.array_equal(yg.view(np.uint32), _single(d, x).view(np.uint32))
+            assert_close(yg[None], oracle.reference_output(fmt, m), oracle.abs_row_products(fmt, m))
+
+
+def test_group_of_a_layer_with_shared_input():
+    """q, k, v of a Mistral-shaped layer (full size) reading one x."""
+    specs = inputs.workload_specs(inputs.MISTRAL_LAYER)[:3]
+    mats = [inputs.make_matrix(inputs.MISTRAL_LAYER, s, 0, i) for i, s in enumerate(specs)]
+    dbs = [_upload(lw.LW_FMT_Q4_PAIR, m) for m in mats]
+    x = torch.from_numpy(mats[0]["x"][0]).to(DEV)
+    ys = [torch.empty(d.rows, device=DEV) for d in dbs]
+    ws = torch.zeros(lw.lw_workspace_bytes_group(dbs) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lw.lw_decode_gemv_group(dbs, [x, x, x], ys, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for d, y in zip(dbs, ys):
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), _single(d, x).view(np.uint32))
+
+
+def test_group_argument_errors():
+    m4 = _mat(lw.LW_FMT_Q4_PAIR, 1, 64, 256)
+    m6 = _mat(lw.LW_FMT_Q6, 2, 64, 256)
+    d4, d6 = _upload(lw.LW_FMT_Q4_PAIR, m4), _upload(lw.LW_FMT_Q6, m6)
+    x = torch.zeros(256, device=DEV)
+    y = torch.zeros(64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(1 << 20, device=DEV)
+    with pytest.raises(lw.LwError):
+        lw.lw_decode_gemv_group([d4, d6], [x, x], [y, y], ws, st)          # mixed formats
+    with pytest.raises(lw.LwError):
+        lw.lw_decode_gemv_group([d4] * 9, [x] * 9, [y] * 9, ws, st)         # too many
+    with pytest.raises(lw.LwError):
+        lw.lw_decode_gemv_group([d4, d4], [x, x], [y, y], ws[:4], st)      # workspace too small
+    hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m4["codes"], m4["scales"], m4["mins"], twin=True)
+    with pytest.raises(lw.LwError):
+        lw.lw_decode_gemv_group([lw.DeviceBundle.upload(hb, DEV)], [x], [y], ws, st)   # twin
+    assert int(st.item()) == 0
