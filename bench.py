@@ -53,6 +53,8 @@ def parse():
                         "per-batch rows (coded, twin and dense BF16 times)")
     p.add_argument("--batches", default="",
                    help="comma list of batch sizes for --workload sweeps (default: the workload's)")
+    p.add_argument("--ungrouped", action="store_true",
+                   help="one launch per matrix instead of one per group of independent matrices")
     p.add_argument("--no-extras", action="store_true",
                    help="skip twin / bf16 / cpu baseline / e2e legs (profiling)")
     return p.parse_args()
@@ -228,6 +230,25 @@ def whole_job_gbs(bytes_per_rank, world, t_max_ms):
     return bytes_per_rank * world / (t_max_ms * 1e-3) / 1e9
 
 
+# matrices of a decoder layer that read the same input and do not depend on
+# one another: each set is one grouped launch (q, k, v read the normalised
+# hidden state; gate and up read the normalised attention output)
+LAYER_GROUPS = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
+
+
+def layer_groups(names, ungrouped=False):
+    """Index lists, in layer order, of the launches of one step."""
+    if ungrouped:
+        return [[i] for i in range(len(names))]
+    out = []
+    for g in LAYER_GROUPS:
+        idx = [names.index(n) for n in g if n in names]
+        if idx:
+            out.append(idx)
+    assert sorted(i for g in out for i in g) == list(range(len(names)))
+    return out
+
+
 def build_layer(names):
     from decode_gemv_gb300 import lw
     mats = []
@@ -274,16 +295,18 @@ def kernel_source_digest():
     return h.hexdigest()
 
 
-def measured_traffic(names):
+def measured_traffic(names, launches):
     """DRAM bytes (read + write) per launch of the fused kernel on this
     workload, from the committed ncu capture -- only while the kernel source
-    is the one that was profiled, else None."""
+    and the step's launches are the ones that were profiled, else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic_q_product_kernel.json")) as f:
             d = json.load(f)
     except Exception:  # noqa: BLE001
         return None
     if d.get("source_sha256") != kernel_source_digest() or names:
+        return None
+    if d.get("launches") != launches:
         return None
     return d["bytes_per_launch"]
 
@@ -347,7 +370,9 @@ def run_ours(args):
     dbs = [[lw.DeviceBundle.upload(x[key], dev) for x in mats] for _ in range(copies)]
     xs = [torch.from_numpy(x["m"]["x"][0]).to(dev) for x in mats]
     ys = [torch.empty(x["spec"].rows, dtype=torch.float32, device=dev) for x in mats]
-    wsb = max(lw.lw_workspace_bytes(d, 1) for d in dbs[0])
+    groups = layer_groups([x["spec"].name for x in mats], args.ungrouped or args.twin)
+    wsb = max([lw.lw_workspace_bytes(d, 1) for d in dbs[0]] +
+              [lw.lw_workspace_bytes_group([dbs[0][j] for j in g]) for g in groups if len(g) > 1])
     ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -361,23 +386,28 @@ def run_ours(args):
         else:
             lw.lw_decode_gemv(dbs[c][j], xs[j], ys[j], ws, st)
 
-    # one CUDA graph per (layer copy, matrix): the host only replays graphs,
-    # so the timed region measures the device (the pages' runtime also
-    # captures each pass in CUDA graphs)
+    def launch(c, g):
+        if len(g) == 1:
+            call(c, g[0])
+        else:
+            lw.lw_decode_gemv_group([dbs[c][j] for j in g], [xs[j] for j in g],
+                                    [ys[j] for j in g], ws, st)
+
     for c in range(copies):
-        for j in range(len(mats)):
-            call(c, j)
+        for g in groups:
+            launch(c, g)
     torch.cuda.synchronize()
-    # one CUDA graph per layer copy (its seven fused launches): the host only
-    # replays graphs, so the timed region measures the device (the pages'
-    # runtime also captures each pass in CUDA graphs)
+    # one CUDA graph per layer copy (its fused launches, one per group of
+    # independent matrices): the host only replays graphs, so the timed region
+    # measures the device (the pages' runtime also captures each pass in CUDA
+    # graphs)
     graphs = []
     for c in range(copies):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for j in range(len(mats)):
-                call(c, j)
-        graphs.append(g)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            for g in groups:
+                launch(c, g)
+        graphs.append(cg)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     n_mat = len(mats)
@@ -411,12 +441,12 @@ def run_ours(args):
 
     value = whole_job_gbs(coded_step, world, t_max)
     peak, peak_kind = peaks()
-    launches_per_step = n_mat            # one fused kernel per matrix
+    launches_per_step = len(groups)      # one fused kernel per group
     # dominant kernel (the fused decode+GEMV launch, 97 % of the step's GPU
     # time): algorithmic bytes per launch over its average duration in the
     # timed region, i.e. the step time shared over its launches
-    mean_call_ms = t_max / n_mat
-    mean_call_bytes = coded_step / n_mat
+    mean_call_ms = t_max / launches_per_step
+    mean_call_bytes = coded_step / launches_per_step
     achieved = mean_call_bytes / (mean_call_ms * 1e-3) / 1e9
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max,
@@ -431,16 +461,19 @@ def run_ours(args):
             "b_eff_gbs": 2.0 * weights * world / (t_max * 1e-3) / 1e9,
             "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": measured_traffic(names),
+                         "frac": achieved / peak, "traffic": measured_traffic(names, [[mats[j]["spec"].name for j in g] for g in groups]),
                          "peak_kind": peak_kind,
-                         "kernel": "q_product_kernel (fused decode + GEMV + ordered split-K reduction), one launch per matrix",
+                         "kernel": "q_product_kernel (fused decode + GEMV + ordered split-K reduction), "
+                                   + ("one launch per matrix" if len(groups) == n_mat else
+                                      "one launch per group " + "/".join(
+                                          "+".join(mats[j]["spec"].name for j in g) for g in groups)),
                          "per_matrix_ms": {x["spec"].name: float(v) for x, v in zip(mats, per_mat)},
                          "per_matrix_note": "each call alone, one graph per call (diagnostic)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "device_status": status}
     if rank == 0 and not args.no_extras:
         extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, coded_step,
-               weights, t_max)
+               weights, t_max, groups)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -449,7 +482,7 @@ def run_ours(args):
 
 
 def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, coded_step,
-           weights, t_ours):
+           weights, t_ours, groups):
     """Comparators and the end-to-end leg (outside the timed region above)."""
     steps = max(10, min(args.steps, 400))
 
@@ -485,19 +518,25 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
     hx = [x.cpu().pin_memory() for x in xs]
     hy = [torch.empty(y.numel(), dtype=torch.float32).pin_memory() for y in ys]
     dbs = [lw.DeviceBundle.upload(x["hb"], dev) for x in mats]
+
+    def e2e_step():
+        for g in groups:
+            for j in g:
+                xs[j].copy_(hx[j], non_blocking=True)
+            if len(g) == 1:
+                lw.lw_decode_gemv(dbs[g[0]], xs[g[0]], ys[g[0]], ws, st, stream)
+            else:
+                lw.lw_decode_gemv_group([dbs[j] for j in g], [xs[j] for j in g],
+                                        [ys[j] for j in g], ws, st, stream)
+            for j in g:
+                hy[j].copy_(ys[j], non_blocking=True)
     for i in range(3):
-        for d, h, x, y, o in zip(dbs, hx, xs, ys, hy):
-            x.copy_(h, non_blocking=True)
-            lw.lw_decode_gemv(d, x, y, ws, st, stream)
-            o.copy_(y, non_blocking=True)
+        e2e_step()
         torch.cuda.synchronize()
     e_steps = max(10, min(args.steps, 200))
     t0 = time.perf_counter()
     for i in range(e_steps):
-        for d, h, x, y, o in zip(dbs, hx, xs, ys, hy):
-            x.copy_(h, non_blocking=True)
-            lw.lw_decode_gemv(d, x, y, ws, st, stream)
-            o.copy_(y, non_blocking=True)
+        e2e_step()
         torch.cuda.synchronize()
         _ = float(hy[0][0])
     dt = (time.perf_counter() - t0) / e_steps
