@@ -15,7 +15,7 @@
 // Same machinery as the 4-/6-bit kernels: two-warp CTAs (warp h decodes row
 // 2l + h of lane l), the tile's coded rows, activations and second-row
 // offsets staged in shared memory by bulk asynchronous copies, the table
-// bulk-copied and checked lane-parallel, the fp16x2 comparator, FFMA2
+// bulk-copied and checked lane-parallel, the multiply-add comparator, FFMA2
 // accumulation (even / odd columns), ordered split-K through the last tile
 // of each strip.  The twin reads a
 // fixed 4-bit palette index per weight ([UW] "direct palette").

@@ -24,9 +24,11 @@
 //    two symbols (a code is at most 11 bits, so after the first code at
 //    least 21 valid bits remain), and the words advance at most once per
 //    symbol pair;
-//  * comparator limits live in registers; per-length offsets (pre-scaled to
-//    shared addresses) and the symbol table (pre-converted to fp32) in shared
-//    memory, read with explicit ld.shared;
+//  * comparator limits live in registers, two per word, tested by integer
+//    multiply-adds on the FMA pipe (the integer ALU pipe, as busy, takes
+//    the merges); per-length offsets (pre-scaled to shared addresses) and
+//    the symbol table (pre-converted to fp32) in shared memory, read with
+//    explicit ld.shared;
 //  * dot products use packed fp32 FMA (FFMA2): even and odd columns in the
 //    two halves;
 //  * codes enter the FMA as the exact fp32 values 16 + c (4-bit) and 64 + c
@@ -242,64 +244,68 @@ __device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
   return d;
 }
 
-__device__ __forceinline__ __half2 as_h2(uint32_t b) {
-  __half2 h;
-  *reinterpret_cast<uint32_t*>(&h) = b;
-  return h;
-}
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-// The comparator thresholds of a table as fp16 pairs.  Every limit below the
-// longest length is even in the 11-bit peek space, so the first 10 window
-// bits p decide each test exactly: with v = 1024 + p and T = 1024 + limit/2
-// (both exact in fp16), v >= T exactly when the peek reaches the limit.  One
-// fp16x2 compare tests two limits and yields a 0xFFFF / 0 mask per half;
-// unused slots hold T = 2048, which no peek reaches.  The masks are merged by
-// bit selects into one word in which every reached limit owns the same
-// number of set bits (kScale), so one population count gives kScale times
-// the number of limits reached -- which is also the byte offset of that
-// length's entry in the offset table (entries kScale bytes apart).
+// The comparator: the number of per-length limits a window's code reaches.
+// Every limit below the longest length is even in the 11-bit peek space, so
+// the first 10 window bits p decide each test exactly: p reaches limit q
+// when p >= t_q, t_q = limit_q / 2 (unused slots hold t = 1024, which no
+// 10-bit peek reaches).  Two limits are tested by one integer multiply-add
+// (the FMA pipe): word k holds two 11-bit fields, at bits k and 16 + k,
+// each p + 1024 - t; such a field never exceeds 2047, so no field carries
+// into the next, and its top bit (bit 10 + k, resp. 26 + k) is set exactly
+// when p >= t.  The words' result bits sit at distinct positions; bit
+// selects merge them into one word, a mask clears the rest (each field's
+// low bits), and one population count gives the number of limits reached.
+// count() returns kScale = 4 times that number: the byte offset of that
+// length's entry in the offset table (32-bit entries).
 template <int NP>
 struct Cmp {
-  static constexpr int kScale = NP <= 1 ? 16 : (NP == 2 ? 8 : 4);
-  static constexpr int kShift = NP <= 1 ? 4 : (NP == 2 ? 3 : 2);
+  static constexpr int kScale = 4;
+  static constexpr int kShift = 2;
   static_assert(NP <= 5, "at most 10 limits");
-  uint32_t c[NP > 0 ? NP : 1];   // fp16x2: (T_2k, T_2k+1)
+  uint32_t c[NP > 0 ? NP : 1];   // word k: (1024 - t_2k) << k | (1024 - t_2k+1) << (16 + k)
   __device__ __forceinline__ void load(const lw_table* tb, int ncmp) {
 #pragma unroll
     for (int k = 0; k < NP; ++k) {
-      uint32_t lohi[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int q = 2 * k + h;
-        // lim_m1 = (limit << 21) - 1  ->  limit / 2 = (lim_m1 + 1) >> 22
-        const uint32_t half_lim = q < ncmp ? ((tb->lim_m1[q] + 1u) >> 22) : 1024u;
-        lohi[h] = __half_as_ushort(__float2half_rn(1024.f + (float)half_lim));
-      }
-      c[k] = lohi[0] | (lohi[1] << 16);
+      // lim_m1 = (limit << 21) - 1  ->  limit / 2 = (lim_m1 + 1) >> 22
+      const uint32_t tl = 2 * k < ncmp ? ((tb->lim_m1[2 * k] + 1u) >> 22) : 1024u;
+      const uint32_t th = 2 * k + 1 < ncmp ? ((tb->lim_m1[2 * k + 1] + 1u) >> 22) : 1024u;
+      c[k] = ((1024u - tl) << k) | ((1024u - th) << (16 + k));
     }
   }
   static __device__ __forceinline__ uint32_t sel(uint32_t a, uint32_t b, uint32_t k) {
     return (a & k) | (b & ~k);
   }
+  // a * B + c as one integer multiply-add
+  template <uint32_t B>
+  static __device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "n"(B), "r"(c));
+    return d;
+  }
   // kScale * (number of limits the window's code reaches)
   __device__ __forceinline__ uint32_t count(uint32_t w) const {
-    const __half2 v = as_h2(mul_hi(w, 1u << 10) * 0x00010001u + 0x64006400u);   // 1024 + w >> 22
-    uint32_t m[NP > 0 ? NP : 1];
-#pragma unroll
-    for (int k = 0; k < NP; ++k) m[k] = __hge2_mask(v, as_h2(c[k]));
+    const uint32_t p = w >> 22;
+    constexpr uint32_t R0 = (1u << 10) | (1u << 26);   // result bits of word 0
+    uint32_t r[NP > 0 ? NP : 1];
+    r[0] = imad<0x00010001u>(p, c[0]);
+    if constexpr (NP > 1) r[1] = imad<0x00020002u>(p, c[1]);
+    if constexpr (NP > 2) r[2] = imad<0x00040004u>(p, c[2]);
+    if constexpr (NP > 3) r[3] = imad<0x00080008u>(p, c[3]);
+    if constexpr (NP > 4) r[4] = imad<0x00100010u>(p, c[4]);
+    uint32_t z;
     if constexpr (NP <= 1) {
-      return __popc(m[0]);
+      z = r[0] & R0;
     } else if constexpr (NP == 2) {
-      return __popc(sel(m[0], m[1], 0x55555555u));
+      z = sel(r[1], r[0], R0 << 1) & (R0 * 3u);
     } else if constexpr (NP == 3) {
-      return __popc(sel(sel(m[0], m[1], 0x55555555u), m[2] & 0x55555555u, 0x33333333u));
+      z = sel(r[2], sel(r[1], r[0], R0 << 1), R0 << 2) & (R0 * 7u);
     } else {
-      const uint32_t z = sel(sel(m[0], m[1], 0x55555555u), sel(m[2], m[3], 0x55555555u),
-                             0x33333333u);
-      if constexpr (NP == 4) return __popc(z);
-      else return __popc(z) + (__popc(m[4]) >> 2);
+      z = sel(sel(r[1], r[0], R0 << 1), sel(r[3], r[2], R0 << 3), R0 * 3u);
+      if constexpr (NP == 5) z = sel(r[4], z, R0 << 4) & (R0 * 31u);
+      else z &= R0 * 15u;
     }
+    return __popc(z) << 2;
   }
 };
 
