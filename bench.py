@@ -491,13 +491,17 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
     twins = [[lw.DeviceBundle.upload(x["tw"], dev) for x in mats] for _ in range(ntw)]
     tcalls = [[(lambda d=d, x=x, y=y: lw.lw_twin_gemv(d, x, y, ws, st))
                for d, x, y in zip(twins[c], xs, ys)] for c in range(ntw)]
-    tg = [layer_graph(torch, calls) for calls in tcalls]
+    # the twin step makes the same launches as the coded step (one per group)
+    tsteps = [[(lambda c=c, g=g: lw.lw_twin_gemv_group([twins[c][j] for j in g], [xs[j] for j in g],
+                                                       [ys[j] for j in g], ws, st))
+               if len(g) > 1 else tcalls[c][g[0]] for g in groups] for c in range(ntw)]
+    tg = [layer_graph(torch, calls) for calls in tsteps]
 
     def tstep(c):
         tg[c].replay()
     t_twin = time_steps(torch, stream, tstep, steps, 5, ntw)
     tw_ms = per_call_ms(torch, stream, tcalls[: min(ntw, 4)])
-    del tg, twins, tcalls
+    del tg, twins, tcalls, tsteps
     # uncompressed BF16 GEMV (cuBLAS) on the dequantised weights, graphed
     wb = [dequant_bf16(x["m"]).to(dev) for x in mats]
     xb = [x.to(torch.bfloat16) for x in xs]
@@ -615,6 +619,25 @@ def sweep_specs(name):
     return jobs
 
 
+def sweep_groups(mats, lw):
+    """Launch groups of a sweep at batch 1: the 4-/6-bit matrices of one layer
+    that share an input (LAYER_GROUPS) and a format; every other matrix alone.
+    Index lists in the order of each group's first matrix."""
+    groups, seen = [], set()
+    for i, m in enumerate(mats):
+        if i in seen:
+            continue
+        g = [i]
+        if m["fmt"] != lw.LW_FMT_BF16_EXP:
+            for names in LAYER_GROUPS:
+                if m["spec"].name in names:
+                    g = [j for j, o in enumerate(mats) if o["layer"] == m["layer"]
+                         and o["spec"].name in names and o["fmt"] == m["fmt"]][:8]
+        seen.update(g)
+        groups.append(g)
+    return groups
+
+
 def run_sweep(args):
     """Time the coded path, the fixed-width twin and a dense BF16 GEMV/GEMM
     (cuBLAS, same shapes) for every batch of one workload."""
@@ -642,8 +665,8 @@ def run_sweep(args):
     coded_total = sum(o[False][8] for _, o in built)
     copies = max(1, math.ceil(4 * l2 / coded_total)) if coded_total < 4 * l2 else 1
     mats = []
-    for spec, o in built:
-        mats.append(dict(spec=spec, fmt=o[False][0],
+    for job, (spec, o) in zip(jobs, built):
+        mats.append(dict(spec=spec, fmt=o[False][0], layer=job[1],
                          db=[lw.DeviceBundle(*o[False][:8], device=dev, coded_bytes=o[False][8])
                              for _ in range(copies)],
                          tw=[lw.DeviceBundle(*o[True][:8], device=dev, coded_bytes=o[True][8])
@@ -675,6 +698,7 @@ def run_sweep(args):
         del graphs
         return t, steps
 
+    groups = sweep_groups(mats, lw)
     rows_out = []
     clk = ClockSampler(0)
     clk.start()
@@ -685,20 +709,33 @@ def run_sweep(args):
             xs.append(torch.randn(B, m["spec"].cols, device=dev, generator=gen).to(dt))
             ys.append(torch.empty(B, m["spec"].rows, device=dev, dtype=torch.float32))
         wsb = max(lw.lw_workspace_bytes(m["db"][0], B) for m in mats)
+        grouped = B == 1 and any(len(g) > 1 for g in groups)
+        if grouped:
+            wsb = max([wsb] + [lw.lw_workspace_bytes_group([mats[j]["db"][0] for j in g])
+                               for g in groups if len(g) > 1])
         ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device=dev)
         x_bytes = sum(x.numel() * x.element_size() for x in xs)
         coded_step = sum(m["db"][0].coded_bytes for m in mats) + x_bytes
         twin_step = sum(m["tw"][0].coded_bytes for m in mats) + x_bytes
-        t_coded, steps = timed(lambda c: [(lambda d=m["db"][c], x=x, y=y: lw.lw_decode_gemm(d, x, B, y, ws, st))
-                                          for m, x, y in zip(mats, xs, ys)])
-        t_twin, _ = timed(lambda c: [(lambda d=m["tw"][c], x=x, y=y: lw.lw_twin_gemm(d, x, B, y, ws, st))
-                                     for m, x, y in zip(mats, xs, ys)], steps)
+        def step_calls(c, key, one, group):
+            # batch 1: one launch per group of a layer's independent
+            # 4-/6-bit matrices; otherwise one call per matrix
+            if not grouped:
+                return [(lambda d=m[key][c], x=x, y=y: one(d, x, B, y, ws, st))
+                        for m, x, y in zip(mats, xs, ys)]
+            return [(lambda g=g: group([mats[j][key][c] for j in g], [xs[j] for j in g],
+                                       [ys[j] for j in g], ws, st)) if len(g) > 1 else
+                    (lambda d=mats[g[0]][key][c], x=xs[g[0]], y=ys[g[0]]: one(d, x, B, y, ws, st))
+                    for g in groups]
+        t_coded, steps = timed(lambda c: step_calls(c, "db", lw.lw_decode_gemm, lw.lw_decode_gemv_group))
+        t_twin, _ = timed(lambda c: step_calls(c, "tw", lw.lw_twin_gemm, lw.lw_twin_gemv_group), steps)
         xb = [x.to(torch.bfloat16) for x in xs]
         yb = [torch.empty(B, m["spec"].rows, device=dev, dtype=torch.bfloat16) for m in mats]
         t_bf16, _ = timed(lambda c: [(lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y))
                                      for w, x, y in zip(dense[c], xb, yb)], steps)
         gbs = coded_step / (t_coded * 1e-3) / 1e9
-        rows_out.append({"batch": B, "ms_per_step": t_coded, "coded_gbs": gbs,
+        rows_out.append({"batch": B, "launches": len(groups) if grouped else len(mats),
+                         "ms_per_step": t_coded, "coded_gbs": gbs,
                          "frac_of_hbm": gbs / peak, "b_eff_gbs": 2.0 * weights / (t_coded * 1e-3) / 1e9,
                          "twin_ms": t_twin, "twin_gbs": twin_step / (t_twin * 1e-3) / 1e9,
                          "speedup_vs_twin": t_twin / t_coded,
@@ -709,6 +746,8 @@ def run_sweep(args):
             "n_gpus": 1, "higher_is_better": True, "dtype": "f32" if mats[0]["fmt"] != lw.LW_FMT_BF16_EXP else "bf16",
             "data": "synthetic", "peak_gbs": peak, "peak_kind": peak_kind,
             "config": {"workload": label, "layers": layers, "matrices": len(mats), "weights": weights,
+                       "launches": "batch 1: one launch per group of a layer's independent 4-/6-bit "
+                                   "matrices (q+k+v, gate+up; coded and twin alike); else one per matrix",
                        "l2": (f"rotate {copies} device copies ({group} steps per CUDA graph)"
                               if copies > 1 else "working set > 4x L2"),
                        "dense_comparator": "torch.matmul on random bf16 weights of the same shapes (cuBLAS)",

@@ -204,9 +204,9 @@ extern "C" size_t lw_workspace_bytes_group(const lw_dev_bundle* const* b, int32_
   return total;
 }
 
-extern "C" lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t n,
-                                          const void* const* x, float* const* y, void* ws,
-                                          size_t ws_bytes, int32_t* d_status, void* stream) {
+static lw_status gemv_group(const lw_dev_bundle* const* b, int32_t n, const void* const* x,
+                            float* const* y, void* ws, size_t ws_bytes, int32_t* d_status,
+                            void* stream, bool twin) {
   clear_error();
   if (!b || !x || !y || n < 1 || n > LW_MAX_GROUP)
     return fail(LW_ERR_INVALID_ARG, "group of %d matrices (1..%d) or NULL arrays", n, LW_MAX_GROUP);
@@ -216,7 +216,7 @@ extern "C" lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t
   void* wss[LW_MAX_GROUP];
   size_t off = 0;
   for (int i = 0; i < n; ++i) {
-    lw_status s = check_dev_bundle(b[i], false, true);
+    lw_status s = check_dev_bundle(b[i], twin, true);
     if (s != LW_OK) return s;
     if (b[i]->fmt == LW_FMT_BF16_EXP)
       return fail(LW_ERR_UNSUPPORTED, "groups take 4-/6-bit bundles");
@@ -230,6 +230,18 @@ extern "C" lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t
   }
   if (ws_bytes < off) return fail(LW_ERR_INVALID_ARG, "workspace of %zu bytes < %zu", ws_bytes, off);
   return launch_q_products(b, n, xs, 1, ys, wss, d_status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t n,
+                                          const void* const* x, float* const* y, void* ws,
+                                          size_t ws_bytes, int32_t* d_status, void* stream) {
+  return gemv_group(b, n, x, y, ws, ws_bytes, d_status, stream, false);
+}
+
+extern "C" lw_status lw_twin_gemv_group(const lw_dev_bundle* const* b, int32_t n,
+                                        const void* const* x, float* const* y, void* ws,
+                                        size_t ws_bytes, int32_t* d_status, void* stream) {
+  return gemv_group(b, n, x, y, ws, ws_bytes, d_status, stream, true);
 }
 
 extern "C" lw_status lw_twin_gemv(const lw_dev_bundle* b, const void* x, float* y, void* ws,

@@ -28,7 +28,7 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_validate_sections", "lw_workspace_bytes", "lw_decode", "lw_decode_gemv",
             "lw_decode_gemm", "lw_twin_gemv", "lw_twin_gemm", "lw_status_string",
             "lw_last_error", "lw_version", "lw_decode_gemv_noalloc", "lw_noalloc_scratch_bytes",
-            "lw_decode_gemv_group", "lw_workspace_bytes_group"]
+            "lw_decode_gemv_group", "lw_workspace_bytes_group", "lw_twin_gemv_group"]
 
 
 class LwError(RuntimeError):
@@ -92,6 +92,7 @@ def load():
         "lw_version": ([], i32),
         "lw_decode_gemv_noalloc": ([P, P, P, P, P], i32),
         "lw_decode_gemv_group": ([P, i32, P, P, P, sz, P, P], i32),
+        "lw_twin_gemv_group": ([P, i32, P, P, P, sz, P, P], i32),
         "lw_workspace_bytes_group": ([P, i32], sz),
         "lw_noalloc_scratch_bytes": ([], sz),
     }
@@ -319,15 +320,22 @@ def lw_workspace_bytes_group(dbs) -> int:
     return int(load().lw_workspace_bytes_group(_views(dbs), len(dbs)))
 
 
-def lw_decode_gemv_group(dbs, xs, ys, ws, d_status, stream=None) -> None:
-    """One launch for several 4-/6-bit matrices: ys[i] = W_i xs[i]."""
+def _gemv_group(fn, dbs, xs, ys, ws, d_status, stream):
     n = len(dbs)
     xa = (ctypes.c_void_p * n)(*[_tp(x) for x in xs])
     ya = (ctypes.c_void_p * n)(*[_tp(y) for y in ys])
-    _check(load().lw_decode_gemv_group(_views(dbs), n, xa, ya, _tp(ws),
-                                       ws.numel() * ws.element_size(), _tp(d_status),
-                                       _stream_ptr(stream)),
-           "lw_decode_gemv_group")
+    _check(getattr(load(), fn)(_views(dbs), n, xa, ya, _tp(ws), ws.numel() * ws.element_size(),
+                               _tp(d_status), _stream_ptr(stream)), fn)
+
+
+def lw_decode_gemv_group(dbs, xs, ys, ws, d_status, stream=None) -> None:
+    """One launch for several 4-/6-bit matrices: ys[i] = W_i xs[i]."""
+    _gemv_group("lw_decode_gemv_group", dbs, xs, ys, ws, d_status, stream)
+
+
+def lw_twin_gemv_group(dbs, xs, ys, ws, d_status, stream=None) -> None:
+    """The fixed-width twin of lw_decode_gemv_group."""
+    _gemv_group("lw_twin_gemv_group", dbs, xs, ys, ws, d_status, stream)
 
 
 def lw_noalloc_scratch_bytes() -> int:

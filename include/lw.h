@@ -348,6 +348,18 @@ lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t n, const v
 size_t lw_workspace_bytes_group(const lw_dev_bundle* const* b, int32_t n);
 
 /*
+ * The fixed-width twin of lw_decode_gemv_group: n (1..LW_MAX_GROUP) twin
+ * bundles of one 4-/6-bit format in one launch ([LW] runtime paragraph after
+ * Fig. 3, the decode-free comparison), each y[i] bitwise what
+ * lw_twin_gemv(b[i], x[i], y[i], ...) gives.  Same arguments, workspace
+ * (lw_workspace_bytes_group) and errors, with every b[i] a twin (coded
+ * bundles are rejected with LW_ERR_INVALID_ARG).
+ */
+lw_status lw_twin_gemv_group(const lw_dev_bundle* const* b, int32_t n, const void* const* x,
+                             float* const* y, void* ws, size_t ws_bytes, int32_t* d_status,
+                             void* stream);
+
+/*
  * lw_decode_gemv without a caller workspace, for callers that cannot allocate
  * device memory: code running under CUDA-graph capture, engines whose pool
  * allocator owns all device memory, latency-critical paths that cannot afford

@@ -98,3 +98,33 @@ def test_group_argument_errors():
     with pytest.raises(lw.LwError):
         lw.lw_decode_gemv_group([lw.DeviceBundle.upload(hb, DEV)], [x], [y], ws, st)   # twin
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("fmt", [lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6])
+def test_twin_group_equals_single_twin_calls(fmt):
+    n = 5
+    mats = [_mat(fmt, 300 + i, *SHAPES[i]) for i in range(n)]
+    tws = [lw.DeviceBundle.upload(lw.lw_encode_bundle(fmt, m["codes"], m["scales"], m.get("mins"),
+                                                      twin=True), DEV) for m in mats]
+    dbs = [_upload(fmt, m) for m in mats]
+    xs = [torch.from_numpy(m["x"][0]).to(DEV) for m in mats]
+    ys = [torch.full((d.rows,), float("nan"), device=DEV) for d in tws]
+    ws = torch.zeros(lw.lw_workspace_bytes_group(tws) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lw.lw_twin_gemv_group(tws, xs, ys, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for d, t, x, y in zip(dbs, tws, xs, ys):
+        y1 = torch.empty(t.rows, device=DEV)
+        w1 = torch.zeros(lw.lw_workspace_bytes(t, 1) // 4 + 64, device=DEV)
+        lw.lw_twin_gemv(t, x, y1, w1, st)
+        torch.cuda.synchronize()
+        yg = y.cpu().numpy()
+        assert np.array_equal(yg.view(np.uint32), y1.cpu().numpy().view(np.uint32))
+        # the twin executes the coded kernel's floating-point operations
+        assert np.array_equal(yg.view(np.uint32), _single(d, x).view(np.uint32))
+    with pytest.raises(lw.LwError):
+        lw.lw_twin_gemv_group(dbs[:2], xs[:2], ys[:2], ws, st)        # coded bundles
+    with pytest.raises(lw.LwError):
+        lw.lw_twin_gemv_group([tws[0], dbs[1]], xs[:2], ys[:2], ws, st)   # mixed
+    assert int(st.item()) == 0
