@@ -20,7 +20,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "liblw.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU = ["lw_api.cu", "lw_q.cu", "lw_bf16.cu", "lw_noalloc.cu"]
-CPP = ["lw_host.cpp"]
+CPP = ["lw_host.cpp", "lw_file.cpp"]
 
 
 def _nvcc() -> str:

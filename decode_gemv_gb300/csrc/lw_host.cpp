@@ -18,6 +18,7 @@
 #include <thread>
 #include <vector>
 
+#include "lw_bundle.h"
 #include "lw_internal.h"
 
 namespace lw {
@@ -180,16 +181,6 @@ extern "C" lw_status lw_table_from_lengths(int32_t fmt, const uint8_t* code_len,
 // ---------------------------------------------------------------------------
 // Bundle
 // ---------------------------------------------------------------------------
-struct lw_bundle {
-  lw_desc desc{};
-  std::vector<uint32_t> words, tile_off;
-  std::vector<uint16_t> lane_bits, lane_mid, qparams;
-  lw_table table{};
-  std::vector<uint8_t> signman, vexp;
-  std::vector<uint32_t> vflags, vrow_off;
-  int32_t max_tile_rows = 0;
-  int64_t n_verbatim = 0;
-};
 
 namespace {
 
@@ -636,6 +627,7 @@ extern "C" const char* lw_status_string(lw_status s) {
     case LW_ERR_ALLOC: return "LW_ERR_ALLOC";
     case LW_ERR_CORRUPT: return "LW_ERR_CORRUPT";
     case LW_ERR_CUDA: return "LW_ERR_CUDA";
+    case LW_ERR_IO: return "LW_ERR_IO";
   }
   return "unknown lw_status";
 }

@@ -17,10 +17,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "liblw.so")
 
 LW_FMT_Q4_PAIR, LW_FMT_Q6, LW_FMT_BF16_EXP = 1, 2, 3
+(LW_OK, LW_ERR_INVALID_ARG, LW_ERR_SHAPE, LW_ERR_UNSUPPORTED, LW_ERR_ALLOC, LW_ERR_CORRUPT,
+ LW_ERR_CUDA, LW_ERR_IO) = range(8)
 SECTION_NAMES = ["words", "tile_off", "lane_bits", "table", "qparams", "signman",
                  "vflags", "vrow_off", "vexp", "lane_mid"]
 STATUS_NAMES = {0: "LW_OK", 1: "LW_ERR_INVALID_ARG", 2: "LW_ERR_SHAPE", 3: "LW_ERR_UNSUPPORTED",
-                4: "LW_ERR_ALLOC", 5: "LW_ERR_CORRUPT", 6: "LW_ERR_CUDA"}
+                4: "LW_ERR_ALLOC", 5: "LW_ERR_CORRUPT", 6: "LW_ERR_CUDA", 7: "LW_ERR_IO"}
 DEV_STATUS = {0: "ok", 1: "lane length", 2: "bad code", 3: "tile size", 4: "timeout",
               5: "bad table"}
 TABLE_BYTES = 1024
@@ -28,7 +30,9 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_validate_sections", "lw_workspace_bytes", "lw_decode", "lw_decode_gemv",
             "lw_decode_gemm", "lw_twin_gemv", "lw_twin_gemm", "lw_status_string",
             "lw_last_error", "lw_version", "lw_decode_gemv_noalloc", "lw_noalloc_scratch_bytes",
-            "lw_decode_gemv_group", "lw_workspace_bytes_group", "lw_twin_gemv_group"]
+            "lw_decode_gemv_group", "lw_workspace_bytes_group", "lw_twin_gemv_group",
+            "lw_bundle_desc", "lw_bundle_serialized_bytes", "lw_bundle_serialize",
+            "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load"]
 
 
 class LwError(RuntimeError):
@@ -95,6 +99,12 @@ def load():
         "lw_twin_gemv_group": ([P, i32, P, P, P, sz, P, P], i32),
         "lw_workspace_bytes_group": ([P, i32], sz),
         "lw_noalloc_scratch_bytes": ([], sz),
+        "lw_bundle_desc": ([P, P], i32),
+        "lw_bundle_serialized_bytes": ([P], sz),
+        "lw_bundle_serialize": ([P, P, sz], i32),
+        "lw_bundle_deserialize": ([P, sz, P], i32),
+        "lw_bundle_save": ([P, ctypes.c_char_p], i32),
+        "lw_bundle_load": ([ctypes.c_char_p, P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -184,6 +194,40 @@ def lw_encode_bundle(fmt: int, payload: np.ndarray, scales=None, mins=None,
     _check(load().lw_encode_bundle(ctypes.byref(desc), _np_ptr(payload), _np_ptr(sc),
                                    _np_ptr(mn), ctypes.byref(h)), "lw_encode_bundle")
     return HostBundle(h, desc)
+
+
+def _adopt(h) -> HostBundle:
+    """Wrap a bundle handle returned by the library."""
+    desc = LwDesc()
+    st = load().lw_bundle_desc(h, ctypes.byref(desc))
+    if st != 0:
+        load().lw_bundle_free(h)
+        raise LwError(st, "lw_bundle_desc")
+    return HostBundle(h, desc)
+
+
+def lw_bundle_serialize(hb: HostBundle) -> bytes:
+    """The bundle as one byte string (the bundle file format)."""
+    n = int(load().lw_bundle_serialized_bytes(hb._h))
+    buf = ctypes.create_string_buffer(n)
+    _check(load().lw_bundle_serialize(hb._h, buf, n), "lw_bundle_serialize")
+    return buf.raw
+
+
+def lw_bundle_deserialize(data: bytes) -> HostBundle:
+    h = ctypes.c_void_p()
+    _check(load().lw_bundle_deserialize(data, len(data), ctypes.byref(h)), "lw_bundle_deserialize")
+    return _adopt(h)
+
+
+def lw_bundle_save(hb: HostBundle, path) -> None:
+    _check(load().lw_bundle_save(hb._h, os.fsencode(path)), "lw_bundle_save")
+
+
+def lw_bundle_load(path) -> HostBundle:
+    h = ctypes.c_void_p()
+    _check(load().lw_bundle_load(os.fsencode(path), ctypes.byref(h)), "lw_bundle_load")
+    return _adopt(h)
 
 
 def lw_table_from_lengths(fmt: int, code_len, palette=None) -> np.ndarray:

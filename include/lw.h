@@ -69,7 +69,8 @@ typedef enum {
   LW_ERR_UNSUPPORTED = 3,
   LW_ERR_ALLOC = 4,       /* host allocation failed */
   LW_ERR_CORRUPT = 5,     /* malformed bundle or table detected on the host */
-  LW_ERR_CUDA = 6         /* launch or CUDA runtime error */
+  LW_ERR_CUDA = 6,        /* launch or CUDA runtime error */
+  LW_ERR_IO = 7           /* a bundle file could not be opened, read or written */
 } lw_status;
 
 /* device-side error codes written to *d_status */
@@ -233,6 +234,33 @@ lw_status lw_encode_bundle(const lw_desc* desc, const void* payload,
 lw_status lw_bundle_sections(const lw_bundle* b, lw_sections* out);
 
 void lw_bundle_free(lw_bundle* b);
+
+/* Format, twin flag and shape of a bundle (e.g. one just loaded). */
+lw_status lw_bundle_desc(const lw_bundle* b, lw_desc* out);
+
+/*
+ * Bundle files [UW "One Format, Two Purposes"]: the coded bundle is the
+ * distribution format -- shipped as a byte string, loaded back, then
+ * uploaded (or transcoded to the twin, lw_transcode_twin) at load time.
+ * The string: a 192-byte little-endian header ("LWBUNDLE", version 1, fmt,
+ * twin, rows, cols, max_tile_rows, section count, n_verbatim, the byte size
+ * of every section in lw_sections order), the sections in that order each
+ * at a multiple of 64 bytes, then a 64-bit FNV-1a checksum of everything
+ * before it.  lw_bundle_serialized_bytes: its length (0 for NULL).
+ * lw_bundle_serialize writes it into buf (cap >= that length; the caller
+ * owns buf).  lw_bundle_deserialize builds a new bundle (free with
+ * lw_bundle_free) after checking the header, the checksum, every section
+ * size against the shape and format, and everything lw_validate_sections
+ * checks; errors: LW_ERR_CORRUPT (any mismatch), LW_ERR_UNSUPPORTED (another
+ * version, a big-endian host), LW_ERR_ALLOC, LW_ERR_INVALID_ARG.
+ * lw_bundle_save / lw_bundle_load do the same through a file (LW_ERR_IO when
+ * it cannot be opened, read or written).
+ */
+size_t lw_bundle_serialized_bytes(const lw_bundle* b);
+lw_status lw_bundle_serialize(const lw_bundle* b, void* buf, size_t cap);
+lw_status lw_bundle_deserialize(const void* buf, size_t bytes, lw_bundle** out);
+lw_status lw_bundle_save(const lw_bundle* b, const char* path);
+lw_status lw_bundle_load(const char* path, lw_bundle** out);
 
 /*
  * Fill an lw_table from per-symbol code lengths (for bundles built or stored
