@@ -32,7 +32,8 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_last_error", "lw_version", "lw_decode_gemv_noalloc", "lw_noalloc_scratch_bytes",
             "lw_decode_gemv_group", "lw_workspace_bytes_group", "lw_twin_gemv_group",
             "lw_bundle_desc", "lw_bundle_serialized_bytes", "lw_bundle_serialize",
-            "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load"]
+            "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load", "lw_transcode_twin",
+            "lw_twin_tile_rows"]
 
 
 class LwError(RuntimeError):
@@ -105,6 +106,8 @@ def load():
         "lw_bundle_deserialize": ([P, sz, P], i32),
         "lw_bundle_save": ([P, ctypes.c_char_p], i32),
         "lw_bundle_load": ([ctypes.c_char_p, P], i32),
+        "lw_transcode_twin": ([P, P, P, P], i32),
+        "lw_twin_tile_rows": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -297,6 +300,22 @@ class DeviceBundle:
         self.view = v
 
     @classmethod
+    def from_tensors(cls, fmt, twin, rows, cols, tensors: dict, max_tile_rows, lmin, lmax):
+        """A view over device tensors that already hold the sections."""
+        self = cls.__new__(cls)
+        self.fmt, self.twin, self.rows, self.cols = fmt, bool(twin), rows, cols
+        self.tensors = dict(tensors)
+        self.coded_bytes = int(sum(t.numel() * t.element_size() for t in self.tensors.values()))
+        v = LwDevBundle()
+        v.fmt, v.twin, v.rows, v.cols = fmt, int(twin), rows, cols
+        v.max_tile_rows, v.lmin, v.lmax = max_tile_rows, lmin, lmax
+        for name in SECTION_NAMES:
+            t = self.tensors.get(name)
+            setattr(v, name, t.data_ptr() if t is not None else None)
+        self.view = v
+        return self
+
+    @classmethod
     def upload(cls, hb: HostBundle, device="cuda"):
         return cls(hb.desc.fmt, hb.desc.twin, hb.desc.rows, hb.desc.cols, hb.sections,
                    hb.stats.max_tile_rows, hb.stats.min_len, hb.stats.max_len, device,
@@ -324,6 +343,30 @@ def lw_workspace_bytes(db: DeviceBundle, batch: int = 1) -> int:
 
 def lw_decode(db: DeviceBundle, out, d_status, stream=None) -> None:
     _check(load().lw_decode(db.ref, _tp(out), _tp(d_status), _stream_ptr(stream)), "lw_decode")
+
+
+def lw_twin_tile_rows(fmt: int) -> int:
+    return int(load().lw_twin_tile_rows(fmt))
+
+
+def lw_transcode_twin(db: DeviceBundle, d_status, stream=None) -> DeviceBundle:
+    """Transcode a coded device bundle into its fixed-width twin on the
+    device: new words, tile offsets and lane bit counts; every other section
+    is the coded bundle's own tensor (shared, not copied)."""
+    import torch
+    dev = db.tensors["tile_off"].device
+    n_tiles = (db.rows // 64) * (db.cols // 256)
+    r2 = lw_twin_tile_rows(db.fmt)
+    t = {"words": torch.empty(n_tiles * r2 * 128, dtype=torch.uint8, device=dev),
+         "tile_off": torch.empty((n_tiles + 1) * 4, dtype=torch.uint8, device=dev),
+         "lane_bits": torch.empty(n_tiles * 64, dtype=torch.uint8, device=dev)}
+    for name in ("table", "qparams", "signman", "vflags", "vrow_off", "vexp"):
+        if name in db.tensors:
+            t[name] = db.tensors[name]
+    tw = DeviceBundle.from_tensors(db.fmt, True, db.rows, db.cols, t, r2, 0, 0)
+    _check(load().lw_transcode_twin(db.ref, tw.ref, _tp(d_status), _stream_ptr(stream)),
+           "lw_transcode_twin")
+    return tw
 
 
 def lw_decode_gemv(db: DeviceBundle, x, y, ws, d_status, stream=None) -> None:

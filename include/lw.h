@@ -388,6 +388,31 @@ lw_status lw_twin_gemv_group(const lw_dev_bundle* const* b, int32_t n, const voi
                              void* stream);
 
 /*
+ * Load-time transcode [UW "Four approaches to using compressed weights" (the
+ * palette pipelines), "One Format, Two Purposes"]: decode a coded bundle on
+ * the device into its fixed-width twin ([LW] runtime paragraph after Fig. 3),
+ * bit-exact with lw_encode_bundle(twin = 1) of the same weights.  Writes the
+ * twin's words, tile offsets and lane bit counts; every other twin section
+ * (table, qparams; BF16 signman, vflags, vrow_off, vexp) equals the coded
+ * bundle's and may point at the same device buffers.  `twin`: a view with
+ * twin = 1, the coded bundle's fmt, rows and cols, max_tile_rows =
+ * lw_twin_tile_rows(fmt), and caller-owned device buffers words
+ * (n_tiles * max_tile_rows * 128 bytes, 16-byte aligned, not overlapping the
+ * coded bundle), tile_off ((n_tiles + 1) uint32) and lane_bits
+ * (n_tiles * 32 uint16).  Runs in plain stream order and is followed by an
+ * empty plain-order kernel, so the next call on `stream` (whose kernels read
+ * bundle sections before waiting on their predecessor) sees the complete
+ * twin.  Device status as lw_decode (a corrupt stream is reported, the
+ * twin is then undefined).  Errors: LW_ERR_INVALID_ARG (views, shapes,
+ * alignment, overlap), LW_ERR_UNSUPPORTED, LW_ERR_CUDA.
+ */
+lw_status lw_transcode_twin(const lw_dev_bundle* coded, const lw_dev_bundle* twin,
+                            int32_t* d_status, void* stream);
+/* 128-byte word rows per tile of a format's twin: 64 (4-bit codes, BF16
+   palette index), 96 (6-bit codes); 0 for an unknown format. */
+int32_t lw_twin_tile_rows(int32_t fmt);
+
+/*
  * lw_decode_gemv without a caller workspace, for callers that cannot allocate
  * device memory: code running under CUDA-graph capture, engines whose pool
  * allocator owns all device memory, latency-critical paths that cannot afford
