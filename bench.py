@@ -699,6 +699,12 @@ def run_sweep(args):
         return t, steps
 
     groups = sweep_groups(mats, lw)
+    # decode buffers of the full-decode comparator (all-BF16 workloads only;
+    # one per matrix, rewritten every step)
+    wdec = None
+    if all(m["fmt"] == lw.LW_FMT_BF16_EXP for m in mats):
+        wdec = [torch.empty(m["spec"].rows, m["spec"].cols, device=dev, dtype=torch.bfloat16)
+                for m in mats]
     rows_out = []
     clk = ClockSampler(0)
     clk.start()
@@ -733,6 +739,13 @@ def run_sweep(args):
         yb = [torch.empty(B, m["spec"].rows, device=dev, dtype=torch.bfloat16) for m in mats]
         t_bf16, _ = timed(lambda c: [(lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y))
                                      for w, x, y in zip(dense[c], xb, yb)], steps)
+        # the pages' "full decode" pipeline (BF16 exponent bundles): restore
+        # the weights into HBM with lw_decode, then one cuBLAS product
+        t_full = None
+        if wdec is not None:
+            t_full, _ = timed(lambda c: [f for m, x, y, w in zip(mats, xb, yb, wdec) for f in (
+                (lambda d=m["db"][c], w=w: lw.lw_decode(d, w, st)),
+                (lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y)))], steps)
         gbs = coded_step / (t_coded * 1e-3) / 1e9
         rows_out.append({"batch": B, "launches": len(groups) if grouped else len(mats),
                          "ms_per_step": t_coded, "coded_gbs": gbs,
@@ -741,6 +754,9 @@ def run_sweep(args):
                          "speedup_vs_twin": t_twin / t_coded,
                          "bf16_ms": t_bf16, "speedup_vs_bf16": t_bf16 / t_coded,
                          "coded_bytes_per_step": coded_step, "steps": steps})
+        if t_full is not None:
+            rows_out[-1]["decode_cublas_ms"] = t_full
+            rows_out[-1]["speedup_vs_decode_cublas"] = t_full / t_coded
     clocks = clk.stop()
     line = {"metric": METRIC, "workload": label, "value": rows_out[0]["coded_gbs"], "unit": "GB/s",
             "n_gpus": 1, "higher_is_better": True, "dtype": "f32" if mats[0]["fmt"] != lw.LW_FMT_BF16_EXP else "bf16",

@@ -388,13 +388,15 @@ __global__ void __launch_bounds__(64) b_decode_kernel(const BArgs a) {
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
       }
       bool bad = false;
-      uint32_t* o = reinterpret_cast<uint32_t*>(a.out + r * a.K + (size_t)kt * 256);
+      // each lane writes its row's 16 weights of a chunk as two 16-byte stores
+      uint4* o = reinterpret_cast<uint4*>(a.out + r * a.K + (size_t)kt * 256);
       for (int k = 0; k < 16; ++k) {
         const int g = k >> 2;
         const bool v = (fw >> g) & 1u;
         const uint4 sm = b_load_sm(a, t, lane, h, k);
         const uint4 ve = v ? b_load_vexp(a, vb + __popc(fw & ((1u << g) - 1u)), k & 3)
                            : make_uint4(0, 0, 0, 0);
+        uint32_t pw[8];
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           uint32_t E0, E1;
@@ -404,8 +406,10 @@ __global__ void __launch_bounds__(64) b_decode_kernel(const BArgs a) {
           const uint32_t sw = u4w(sm, p >> 1);
           const uint32_t f0 = (p & 1) ? __float_as_uint(b_value<2>(sw, E0)) : __float_as_uint(b_value<0>(sw, E0));
           const uint32_t f1 = (p & 1) ? __float_as_uint(b_value<3>(sw, E1)) : __float_as_uint(b_value<1>(sw, E1));
-          o[8 * k + p] = (f0 >> 16) | (f1 & 0xFFFF0000u);
+          pw[p] = (f0 >> 16) | (f1 & 0xFFFF0000u);
         }
+        o[2 * k] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        o[2 * k + 1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
       }
       if (!TWIN) {
         if (bad) report(a.status, LW_DEV_BAD_CODE);

@@ -833,8 +833,11 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
       }
       bool bad = false;
+      // each lane writes its row in 16-byte stores (four packed words)
+      uint32_t pw[4];
       if (FMT == kQ4) {
-        uint32_t* o = reinterpret_cast<uint32_t*>(a.out + r * (a.K / 2) + (size_t)kt * 128);
+        uint4* o = reinterpret_cast<uint4*>(a.out + r * (a.K / 2) + (size_t)kt * 128);
+#pragma unroll 4
         for (int q = 0; q < 32; ++q) {
           uint32_t packed = 0;
           if (!TWIN) {
@@ -854,10 +857,12 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
               packed |= (ce | (co << 4)) << (8 * i);
             }
           }
-          o[q] = packed;
+          pw[q & 3] = packed;
+          if ((q & 3) == 3) o[q >> 2] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
       } else {
-        uint32_t* o = reinterpret_cast<uint32_t*>(a.out + r * a.K + (size_t)kt * 256);
+        uint4* o = reinterpret_cast<uint4*>(a.out + r * a.K + (size_t)kt * 256);
+#pragma unroll 4
         for (int q = 0; q < 64; ++q) {
           uint32_t packed = 0;
           if (!TWIN) {
@@ -878,7 +883,8 @@ __global__ void __launch_bounds__(kQThreads) q_decode_kernel(const QArgs a) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) packed |= ((win >> (26 - 6 * i)) & 63u) << (8 * i);
           }
-          o[q] = packed;
+          pw[q & 3] = packed;
+          if ((q & 3) == 3) o[q >> 2] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
       }
       if (!TWIN) {
