@@ -55,6 +55,8 @@ struct QArgs {
   const uint16_t* lane_mid;  // coded bundles: bit where each lane's second row starts
   const lw_table* table;
   const uint8_t* qparams;
+  const int32_t* strips; // products: 64-row strips to compute (n_tiles = entries x TK), or
+                         // nullptr for every strip
   const float* x;        // [batch][K] (products)
   float* ws;             // partials [TK][batch][N] (products)
   uint32_t* counters;    // [N/64] strip counters (products), zero between calls
@@ -82,6 +84,23 @@ struct QLaunch {
   int first[kMaxGroup + 1];    // first global tile of each matrix; first[n] = total
   int n;
 };
+
+// Tile of the bundle behind list tile lt: with a strip list, entry lt / TK
+// names the strip and lt % TK the tile column.  An entry outside the
+// matrix, or not above the previous entry, is invalid (ok = false): it maps
+// to a tile of strip 0, which is read but whose results are dropped.
+template <bool STRIPS>
+__device__ __forceinline__ int list_tile(const QArgs& a, int lt, bool& ok) {
+  if (!STRIPS) {
+    ok = true;
+    return lt;
+  }
+  const int si = lt / a.TK, kt = lt - si * a.TK;
+  const int st = __ldg(a.strips + si);
+  const int prev = si > 0 ? __ldg(a.strips + si - 1) : -1;
+  ok = st >= 0 && st < a.N / 64 && st > prev;
+  return ok ? st * a.TK + kt : kt;
+}
 
 // Advance `m` to the matrix holding global tile t (t never decreases).
 __device__ __forceinline__ int group_seek(const QLaunch& g, int t, int m) {
@@ -432,7 +451,11 @@ __device__ __forceinline__ void warp_commit(const QArgs& a, int strip, int kt, i
 // it).
 template <int BP>
 __device__ __forceinline__ void q_commit(const QArgs& a, uint8_t* smem, int strip, int kt, int row,
-                                         const float (&part)[BP]) {
+                                         const float (&part)[BP], bool valid = true) {
+  if (!valid) {   // an invalid strip-list entry: nothing to add (CTA-uniform)
+    __syncthreads();
+    return;
+  }
 #pragma unroll
   for (int b = 0; b < BP; ++b)
     if (b < a.batch) a.ws[((size_t)kt * a.batch + b) * a.N + row] = part[b];
@@ -480,7 +503,7 @@ __device__ __forceinline__ void table_stage(uint8_t* smem, uint32_t* offtab, con
 // rows need more accumulator registers)
 __host__ __device__ constexpr int q_min_ctas(int bp) { return bp <= 4 ? 16 : 12; }
 
-template <int FMT, bool TWIN, int BP, int NCMP>
+template <int FMT, bool TWIN, int BP, int NCMP, bool STRIPS = false>
 __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
     q_product_kernel(const __grid_constant__ QLaunch g) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -515,6 +538,9 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
     fence_barrier_init();
   }
   __syncthreads();
+  // a strip list is written by earlier work on the stream: read it only
+  // after that work is complete
+  if (STRIPS) pdl_wait();
   // matrices of tiles t, t + nw, t + 2 nw
   int cm = group_seek(g, t, 0);
   int cn = group_seek(g, t + nw, cm);
@@ -524,17 +550,19 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
   bool fit0 = true, fit1 = true;
   if (t < total) {   // the bundle part now, the activations after the wait below
     const QArgs& a = g.m[cm];
-    const int lt = t - g.first[cm];
-    fit0 = q_issue<FMT, true>(a, lt, __ldg(a.tile_off + lt), __ldg(a.tile_off + lt + 1), stage0,
+    bool ok;
+    const int rt = list_tile<STRIPS>(a, t - g.first[cm], ok);
+    fit0 = q_issue<FMT, true>(a, rt, __ldg(a.tile_off + rt), __ldg(a.tile_off + rt + 1), stage0,
                               &bar[0], lead, 2);
   }
   // row range of the next tile to issue (t + nw), loaded one tile ahead
   uint32_t nr0 = 0, nr1 = 0;
   if (t + nw < total) {
     const QArgs& a = g.m[cn];
-    const int lt = t + nw - g.first[cn];
-    nr0 = __ldg(a.tile_off + lt);
-    nr1 = __ldg(a.tile_off + lt + 1);
+    bool ok;
+    const int rt = list_tile<STRIPS>(a, t + nw - g.first[cn], ok);
+    nr0 = __ldg(a.tile_off + rt);
+    nr1 = __ldg(a.tile_off + rt + 1);
   }
 
   Cmp<NP> cmp;
@@ -546,15 +574,17 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
   for (int it = 0; t < total; ++it, t += nw) {
     const QArgs& a = g.m[cm];
     const QArgs& an = g.m[cn];                 // matrix of tile t + nw
-    const int lt = t - g.first[cm];            // tile t within its matrix
-    const int ltn = t + nw - g.first[cn];
+    bool valid, okn;
+    const int lt = list_tile<STRIPS>(a, t - g.first[cm], valid);   // tile t within its matrix
+    const int ltn = list_tile<STRIPS>(an, t + nw - g.first[cn], okn);
     const bool odd = two && (it & 1);
     const bool more = t + nw < total;
     const uint32_t ir0 = nr0, ir1 = nr1;     // rows of tile t + nw
     const int c2 = group_seek(g, t + 2 * nw, cn);
     if (t + 2 * nw < total) {
       const QArgs& a2 = g.m[c2];
-      const int lt2 = t + 2 * nw - g.first[c2];
+      bool ok2;
+      const int lt2 = list_tile<STRIPS>(a2, t + 2 * nw - g.first[c2], ok2);
       nr0 = __ldg(a2.tile_off + lt2);
       nr1 = __ldg(a2.tile_off + lt2 + 1);
     }
@@ -736,7 +766,8 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
     if (!more) pdl_trigger();
     // this thread's reads of the stage come before the next bulk copy into it
     fence_proxy_async();
-    q_commit<BP>(a, smem, strip, kt, strip * 64 + 2 * lane + h, part);
+    q_commit<BP>(a, smem, strip, kt, strip * 64 + 2 * lane + h, part, valid);
+    if (STRIPS && !valid && lead) report(a.status, LW_DEV_BAD_STRIPS);
     if (!two && more)   // single stage: refill it now (released by the commit's barrier)
       fit0 = q_issue<FMT, true>(an, ltn, ir0, ir1, stage0, &bar[0], lead);
     cm = cn;

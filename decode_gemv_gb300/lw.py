@@ -33,7 +33,7 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_decode_gemv_group", "lw_workspace_bytes_group", "lw_twin_gemv_group",
             "lw_bundle_desc", "lw_bundle_serialized_bytes", "lw_bundle_serialize",
             "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load", "lw_transcode_twin",
-            "lw_twin_tile_rows"]
+            "lw_twin_tile_rows", "lw_decode_gemm_strips"]
 
 
 class LwError(RuntimeError):
@@ -107,6 +107,7 @@ def load():
         "lw_bundle_save": ([P, ctypes.c_char_p], i32),
         "lw_bundle_load": ([ctypes.c_char_p, P], i32),
         "lw_transcode_twin": ([P, P, P, P], i32),
+        "lw_decode_gemm_strips": ([P, P, i32, P, i32, P, P, sz, P, P], i32),
         "lw_twin_tile_rows": ([i32], i32),
     }
     for name, (args, res) in sig.items():
@@ -343,6 +344,15 @@ def lw_workspace_bytes(db: DeviceBundle, batch: int = 1) -> int:
 
 def lw_decode(db: DeviceBundle, out, d_status, stream=None) -> None:
     _check(load().lw_decode(db.ref, _tp(out), _tp(d_status), _stream_ptr(stream)), "lw_decode")
+
+
+def lw_decode_gemm_strips(db: DeviceBundle, strips, X, batch, Y, ws, d_status, stream=None) -> None:
+    """Y = W X on the 64-row strips listed in `strips` (device int32 tensor,
+    ascending); the other rows of Y are left as they are."""
+    n = int(strips.numel()) if strips is not None else 0
+    _check(load().lw_decode_gemm_strips(db.ref, _tp(strips) if n else None, n, _tp(X), batch, _tp(Y),
+                                        _tp(ws), ws.numel() * ws.element_size(), _tp(d_status),
+                                        _stream_ptr(stream)), "lw_decode_gemm_strips")
 
 
 def lw_twin_tile_rows(fmt: int) -> int:

@@ -81,8 +81,10 @@ enum {
   LW_DEV_BAD_CODE = 2,      /* a peek matched no codeword (incomplete table) */
   LW_DEV_TILE_SIZE = 3,     /* a tile is longer than max_tile_rows */
   LW_DEV_TIMEOUT = 4,       /* a bounded wait on an asynchronous copy ran out */
-  LW_DEV_BAD_TABLE = 5      /* the device table fails its in-kernel checks, or
+  LW_DEV_BAD_TABLE = 5,     /* the device table fails its in-kernel checks, or
                                its length span exceeds what the launch expects */
+  LW_DEV_BAD_STRIPS = 6     /* a strip-list entry is outside the matrix or not
+                               above the entry before it (its tiles skipped) */
 };
 
 typedef enum {
@@ -386,6 +388,28 @@ size_t lw_workspace_bytes_group(const lw_dev_bundle* const* b, int32_t n);
 lw_status lw_twin_gemv_group(const lw_dev_bundle* const* b, int32_t n, const void* const* x,
                              float* const* y, void* ws, size_t ws_bytes, int32_t* d_status,
                              void* stream);
+
+/*
+ * Tile-skip launch list ["Software-Defined Bandwidth Expansion" §IV.C: an
+ * inactive tile is absent from a smaller launch grid, so it moves no
+ * weight bytes]: Y = W X for the n_strips 64-row strips listed in `strips`
+ * (device int32 array, strictly ascending strip indices in [0, N/64)),
+ * every row of every other strip of Y left as it was.  One launch per pass
+ * of up to 8 activation rows over the listed strips' tiles only (CUDA
+ * cores; 4-/6-bit coded bundles).  The list is read on the device after
+ * the previous kernel on `stream` has completed (it may be computed there).
+ * Same X, Y and workspace (lw_workspace_bytes(b, batch) suffices) as
+ * lw_decode_gemm, and the order of summation of its CUDA-core passes: the
+ * listed rows are bitwise what lw_decode_gemm gives on X in slices of up to
+ * 8 rows that stay on the CUDA cores (a pass it sends to the tensor cores
+ * sums in another order).  n_strips = 0 launches nothing.  A bad entry is
+ * reported as LW_DEV_BAD_STRIPS and its tiles are skipped.  Errors:
+ * LW_ERR_INVALID_ARG (NULL list with n_strips > 0, n_strips > N/64,
+ * alignment, workspace size), LW_ERR_UNSUPPORTED (BF16, twins).
+ */
+lw_status lw_decode_gemm_strips(const lw_dev_bundle* b, const int32_t* strips, int32_t n_strips,
+                                const void* X, int32_t batch, float* Y, void* ws, size_t ws_bytes,
+                                int32_t* d_status, void* stream);
 
 /*
  * Load-time transcode [UW "Four approaches to using compressed weights" (the
