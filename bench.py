@@ -53,6 +53,9 @@ def parse():
                         "per-batch rows (coded, twin and dense BF16 times)")
     p.add_argument("--batches", default="",
                    help="comma list of batch sizes for --workload sweeps (default: the workload's)")
+    p.add_argument("--keep", type=float, default=1.0,
+                   help="fraction of each matrix's 64-row strips to compute through a tile-skip "
+                        "launch list (lw_decode_gemm_strips; seeded random strips); 1 = all")
     p.add_argument("--ungrouped", action="store_true",
                    help="one launch per matrix instead of one per group of independent matrices")
     p.add_argument("--no-extras", action="store_true",
@@ -249,6 +252,17 @@ def layer_groups(names, ungrouped=False):
     return out
 
 
+def listed_bytes(hb, strips, cols):
+    """Bundle bytes the product reads for the listed strips: their tiles'
+    coded words, tile offsets, lane bits and mids, scales/mins, plus the
+    table."""
+    tk = cols // 256
+    toff = hb.view("tile_off", np.uint32).astype(np.int64)
+    per_tile = 4 + 64 + 64 + (len(hb.sections.get("qparams", b"")) // max(1, len(toff) - 1))
+    words = sum(int(toff[(s + 1) * tk] - toff[s * tk]) * 128 for s in strips)
+    return words + len(strips) * tk * per_tile + 1024
+
+
 def build_layer(names):
     from decode_gemv_gb300 import lw
     mats = []
@@ -370,7 +384,8 @@ def run_ours(args):
     dbs = [[lw.DeviceBundle.upload(x[key], dev) for x in mats] for _ in range(copies)]
     xs = [torch.from_numpy(x["m"]["x"][0]).to(dev) for x in mats]
     ys = [torch.empty(x["spec"].rows, dtype=torch.float32, device=dev) for x in mats]
-    groups = layer_groups([x["spec"].name for x in mats], args.ungrouped or args.twin)
+    keep = args.keep < 1.0 and not args.twin
+    groups = layer_groups([x["spec"].name for x in mats], args.ungrouped or args.twin or keep)
     wsb = max([lw.lw_workspace_bytes(d, 1) for d in dbs[0]] +
               [lw.lw_workspace_bytes_group([dbs[0][j] for j in g]) for g in groups if len(g) > 1])
     ws = torch.zeros(wsb // 4 + 64, dtype=torch.float32, device=dev)
@@ -378,11 +393,25 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     x_bytes = sum(t.numel() * 4 for t in xs)
     coded_step = layer_coded + x_bytes          # every byte the step must read
+    strip_lists = None
+    if keep:
+        # tile-skip launch lists: a seeded random `keep` fraction of each
+        # matrix's strips; the step then reads only their tiles
+        rk = np.random.default_rng(1234)
+        strip_lists, coded_keep = [], 0
+        for x in mats:
+            ns = x["spec"].rows // 64
+            lst = np.sort(rk.choice(ns, max(1, int(round(args.keep * ns))), replace=False))
+            strip_lists.append(torch.from_numpy(lst.astype(np.int32)).to(dev))
+            coded_keep += listed_bytes(x["hb"], lst, x["spec"].cols)
+        coded_step = coded_keep + x_bytes
     weights = sum(x["spec"].rows * x["spec"].cols for x in mats)
 
     def call(c, j):
         if args.twin:
             lw.lw_twin_gemv(dbs[c][j], xs[j], ys[j], ws, st)
+        elif strip_lists is not None:
+            lw.lw_decode_gemm_strips(dbs[c][j], strip_lists[j], xs[j], 1, ys[j], ws, st)
         else:
             lw.lw_decode_gemv(dbs[c][j], xs[j], ys[j], ws, st)
 
@@ -452,7 +481,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "matrices": [x["spec"].name for x in mats],
+            "config": {"workload": WORKLOAD + (f"_keep{args.keep:g}" if keep else ""),
+                       "matrices": [x["spec"].name for x in mats],
                        "weights": weights, "coded_bytes_per_step": coded_step,
                        "bits_per_weight": 8 * layer_coded / weights, "batch": 1,
                        "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -471,7 +501,11 @@ def run_ours(args):
                          "per_matrix_note": "each call alone, one graph per call (diagnostic)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "device_status": status}
-    if rank == 0 and not args.no_extras:
+    if keep:
+        line["config"]["tile_skip"] = (f"each matrix computes a seeded random {args.keep:g} of its "
+                                       f"64-row strips through lw_decode_gemm_strips; value counts "
+                                       f"the listed tiles' bytes only")
+    if rank == 0 and not args.no_extras and not keep:
         extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, coded_step,
                weights, t_max, groups, dbs)
     if rank == 0:
