@@ -1,0 +1,49 @@
+"""Huffman lanes against rANS lanes on the workloads' weight distributions
+(analysis, test infrastructure: uses the oracle only).  Prints a markdown
+table; `python oracle/compare_rans.py > profiles/rans_vs_huffman.md`."""
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import oracle                                   # noqa: E402
+from oracle import rans                         # noqa: E402
+from decode_gemv_gb300 import inputs            # noqa: E402
+
+
+def main():
+    n, k = 4096, 4096
+    cases = [("4-bit pair symbols, sd 1.2", oracle.Q4, inputs.small_q4(1, n, k, sd=1.2)["codes"]),
+             ("4-bit pair symbols, sd 1.6", oracle.Q4, inputs.small_q4(2, n, k, sd=1.6)["codes"]),
+             ("4-bit pair symbols, sd 2.2", oracle.Q4, inputs.small_q4(3, n, k, sd=2.2)["codes"]),
+             ("6-bit codes", oracle.Q6, inputs.small_q6(4, n, k)["codes"]),
+             ("BF16 exponent palette index", oracle.BF16, inputs.small_bf16(5, n, k)["bits"])]
+    print("# rANS against the Huffman lanes (same symbols, same lanes)\n")
+    print("Command: `python oracle/compare_rans.py` (CPU; the oracle's optimal 11-bit")
+    print("Huffman code and lane split; rANS with a 32-bit state, byte renormalisation,")
+    print(f"{rans.PREC}-bit frequencies and a 4-byte final state per stream). {n}x{k} matrices")
+    print("drawn as the workloads' (seeded). Bits exclude the per-matrix tables and the")
+    print("word/tile padding; \"per row\" gives every row its own stream (two final states")
+    print("per lane, as independent decoding of a lane's two rows needs).\n")
+    print("| symbols | Shannon bound bits/sym | Huffman bits/sym | rANS per lane | rANS vs Huffman | rANS per row | vs Huffman |")
+    print("|---|---|---|---|---|---|---|")
+    for name, fmt, payload in cases:
+        r = rans.compare(fmt, payload)
+        s = r["symbols"]
+        row = (f"| {name} | {r['entropy_bits'] / s:.4f} | {r['huffman_bits'] / s:.4f} | "
+               f"{r['rans_bits'] / s:.4f} | {100 * (r['rans_bits'] / r['huffman_bits'] - 1):+.2f} % |")
+        if r["rans_row_stream_bits"] is not None:
+            row += (f" {r['rans_row_stream_bits'] / s:.4f} | "
+                    f"{100 * (r['rans_row_stream_bits'] / r['huffman_bits'] - 1):+.2f} % |")
+        else:
+            row += " — | — |"
+        print(row)
+    print("\nReading: on these distributions the length-limited Huffman lanes stay within")
+    print("about 1-2 % of the Shannon bound, and rANS, although closer to the bound per")
+    print("symbol, loses it again to its final state per stream (32 bits per lane of a")
+    print("few hundred symbols): it is never smaller, as the LazyWeights page reports")
+    print("(\"Decoder hardware\", Huffman over rANS: 0.0 to +1.0 % more bits).")
+
+
+if __name__ == "__main__":
+    main()
