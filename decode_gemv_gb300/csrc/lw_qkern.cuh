@@ -250,20 +250,6 @@ struct LaneBits {
   }
 };
 
-// hi32(a * b) + c and hi32(a * b) (multiply-high: the FMA pipe, not the
-// integer ALU pipe)
-__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-
 // The comparator: the number of per-length limits a window's code reaches.
 // Every limit below the longest length is even in the 11-bit peek space, so
 // the first 10 window bits p decide each test exactly: p reaches limit q
@@ -274,13 +260,12 @@ __device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
 // into the next, and its top bit (bit 10 + k, resp. 26 + k) is set exactly
 // when p >= t.  The words' result bits sit at distinct positions; bit
 // selects merge them into one word, a mask clears the rest (each field's
-// low bits), and one population count gives the number of limits reached.
-// count() returns kScale = 4 times that number: the byte offset of that
-// length's entry in the offset table (32-bit entries).
+// low bits), and one population count gives the number of limits reached:
+// the length is lmin + that count, and kScale = 4 times it is the byte
+// offset of the length's entry in the offset table (32-bit entries).
 template <int NP>
 struct Cmp {
   static constexpr int kScale = 4;
-  static constexpr int kShift = 2;
   static_assert(NP <= 5, "at most 10 limits");
   uint32_t c[NP > 0 ? NP : 1];   // word k: (1024 - t_2k) << k | (1024 - t_2k+1) << (16 + k)
   __device__ __forceinline__ void load(const lw_table* tb, int ncmp) {
@@ -302,7 +287,7 @@ struct Cmp {
     asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "n"(B), "r"(c));
     return d;
   }
-  // kScale * (number of limits the window's code reaches)
+  // number of limits the window's code reaches
   __device__ __forceinline__ uint32_t count(uint32_t w) const {
     const uint32_t p = w >> 22;
     constexpr uint32_t R0 = (1u << 10) | (1u << 26);   // result bits of word 0
@@ -324,7 +309,7 @@ struct Cmp {
       if constexpr (NP == 5) z = sel(r[4], z, R0 << 4) & (R0 * 31u);
       else z &= R0 * 15u;
     }
-    return __popc(z) << 2;
+    return __popc(z);
   }
 };
 
@@ -344,15 +329,16 @@ __device__ __forceinline__ void put_off(uint32_t* tab, int c, uint32_t v) {
 template <int NP, int ESZ>
 __device__ __forceinline__ void q_decode2(LaneBits& lb, const Cmp<NP>& cmp, int lmin, uint32_t s_off,
                                           uint32_t& e0, uint32_t& e1, bool hold = false) {
-  constexpr uint32_t M = 1u << (32 - Cmp<NP>::kShift);   // count = hi32(z * M)
+  // on the dependency chain: count -> length (one add) -> next window;
+  // the offset-table address is scaled off the chain
   const uint32_t w = lb.window();
   const uint32_t z0 = cmp.count(w);
-  const int L0 = (int)mad_hi(z0, M, (uint32_t)lmin);
+  const int L0 = (int)z0 + lmin;
   const uint32_t w1 = w << L0;
   const uint32_t z1 = cmp.count(w1);
-  const int L1 = (int)mad_hi(z1, M, (uint32_t)lmin);
-  e0 = lds_u32(s_off + z0) + __funnelshift_l(w, 0u, L0) * ESZ;
-  e1 = lds_u32(s_off + z1) + __funnelshift_l(w1, 0u, L1) * ESZ;
+  const int L1 = (int)z1 + lmin;
+  e0 = lds_u32(s_off + (uint32_t)Cmp<NP>::kScale * z0) + __funnelshift_l(w, 0u, L0) * ESZ;
+  e1 = lds_u32(s_off + (uint32_t)Cmp<NP>::kScale * z1) + __funnelshift_l(w1, 0u, L1) * ESZ;
   lb.advance(hold ? 0 : L0 + L1);
 }
 
