@@ -17,7 +17,7 @@ What each function follows is cited in its docstring.  Sources:
 * "Software-Defined Bandwidth Expansion" (page 3): section IV.A (grouped
   low-bit storage, codec idempotence on its lattice), eq. (1) (B_eff).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 tile = 64 rows x 256 columns; lane l holds rows 2l and 2l+1, row 2l first,
 columns ascending; pair symbol = c[k] | c[k+1] << 4 for even k; codes MSB-first
 in 32-bit words; lanes zero-padded to the tile's longest lane; package-merge
