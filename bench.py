@@ -498,7 +498,10 @@ def run_ours(args):
                                       "one launch per group " + "/".join(
                                           "+".join(mats[j]["spec"].name for j in g) for g in groups)),
                          "per_matrix_ms": {x["spec"].name: float(v) for x, v in zip(mats, per_mat)},
-                         "per_matrix_note": "each call alone, one graph per call (diagnostic)"},
+                         "per_matrix_note": "each call alone, one graph per call (diagnostic)",
+                         "note": "bound in practice by instruction issue, not HBM: ~29 warp-instructions "
+                                 "per decoded pair symbol put the issue-rate ceiling near 1.05 TB/s of "
+                                 "coded bytes (profiles/q_product_kernel_gate_q4.md)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "device_status": status}
     if keep:
