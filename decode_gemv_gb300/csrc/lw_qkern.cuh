@@ -637,16 +637,16 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
       for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
       if (!TWIN) {
         // this lane's row as one stream: 128 pair symbols decoded two at a
-        // time, the table entries of step j read while step j+1 is decoded
+        // time (the unrolled steps overlap: a step's decode does not wait for
+        // the previous step's table reads)
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         LaneBits lb;
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
-        uint32_t e0, e1;
-        q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll 8
         for (int j = 0; j < 64; ++j) {
+          uint32_t e0, e1;
+          q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
           const float2 v0 = lds_f2(e0), v1 = lds_f2(e1);
-          if (j < 63) q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float4 xv = lds_f4(sx + 1024u * b + 16u * (uint32_t)j);
@@ -687,8 +687,6 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         LaneBits lb;
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
-        uint32_t e0, e1;
-        q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll 1
         for (int g = 0; g < 16; ++g) {
           float2 acc[BP];
@@ -696,8 +694,9 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
           for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
+            uint32_t e0, e1;
+            q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
             const float2 v = make_float2(lds_f32(e0), lds_f32(e1));
-            if (g < 15 || m < 7) q_decode2<NP, 4>(lb, cmp, lmin, s_off, e0, e1);
 #pragma unroll
             for (int b = 0; b < BP; ++b)
               acc[b] = __ffma2_rn(v, lds_f2(sx + 1024u * b + 64u * g + 8u * m), acc[b]);
