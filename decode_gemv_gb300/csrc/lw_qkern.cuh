@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         LaneBits lb;
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
-#pragma unroll 8
+#pragma unroll 16
         for (int j = 0; j < 64; ++j) {
           uint32_t e0, e1;
           q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
