@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(64, 12) b_product_kernel(const BArgs a) {
       for (int b = 0; b < BP; ++b) acc[b] = make_float2(0.f, 0.f);
       // 16 chunks of 16 weights (chunk k: group k/4, part k%4); the next
       // chunk's bytes are loaded while this one is processed
-#pragma unroll 1
+#pragma unroll 2
       for (int k = 0; k < 16; ++k) {
         const bool v = (fw >> (k >> 2)) & 1u;
         const uint4 sm = n_sm, ve = n_ve;

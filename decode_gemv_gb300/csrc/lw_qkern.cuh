@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         LaneBits lb;
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
-#pragma unroll 1
+#pragma unroll 2
         for (int g = 0; g < 16; ++g) {
           float2 acc[BP];
 #pragma unroll
