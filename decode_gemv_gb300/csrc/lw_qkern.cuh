@@ -496,6 +496,11 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
   using F = QFmt<FMT>;
   constexpr int NP = (NCMP + 1) / 2;
   constexpr int ESZ = FMT == kQ4 ? 8 : 4;
+  // unrolling of the decode loops: deeper for one activation row (more
+  // steps in flight), shallower for more rows (their accumulators need the
+  // registers)
+  constexpr int kUnrollQ4 = BP == 1 ? 16 : 8;
+  constexpr int kUnrollQ6 = BP == 1 ? 2 : 1;
   // offsets in static shared memory: their address is a link-time constant
   __shared__ __align__(16) uint32_t offtab[16];
   const uint32_t s_off = smem_addr(offtab);
@@ -642,7 +647,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         LaneBits lb;
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
-#pragma unroll 16
+#pragma unroll kUnrollQ4
         for (int j = 0; j < 64; ++j) {
           uint32_t e0, e1;
           q_decode2<NP, 8>(lb, cmp, lmin, s_off, e0, e1);
@@ -687,7 +692,7 @@ __global__ void __launch_bounds__(kQThreads, q_min_ctas(BP))
         const uint32_t mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         LaneBits lb;
         lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
-#pragma unroll 2
+#pragma unroll kUnrollQ6
         for (int g = 0; g < 16; ++g) {
           float2 acc[BP];
 #pragma unroll
