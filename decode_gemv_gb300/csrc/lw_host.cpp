@@ -634,4 +634,4 @@ extern "C" const char* lw_status_string(lw_status s) {
 
 extern "C" const char* lw_last_error(void) { return g_err.c_str(); }
 
-extern "C" int32_t lw_version(void) { return 2; }
+extern "C" int32_t lw_version(void) { return 3; }

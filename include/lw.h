@@ -459,7 +459,9 @@ size_t lw_noalloc_scratch_bytes(void);
 const char* lw_status_string(lw_status s);
 const char* lw_last_error(void);
 
-/* Library version, for the bundle file header and for checks. */
+/* ABI revision of this header: 3 (2 + grouped launches, strip lists, the
+   load-time transcode, bundle files, LW_ERR_IO, LW_DEV_BAD_STRIPS).  The
+   bundle file format carries its own version. */
 int32_t lw_version(void);
 
 #ifdef __cplusplus
