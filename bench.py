@@ -333,6 +333,21 @@ def dequant_bf16(m):
     return w.to(torch.bfloat16)
 
 
+def step_graph(torch, lw, calls, stream):
+    """The library calls of a step captured once as a CUDA graph of the
+    library's own (lw.StepGraph: nothing but the calls is replayed), after
+    one eager run."""
+    for f in calls:
+        f()
+    torch.cuda.synchronize()
+    g = lw.StepGraph(stream)
+    with g.capture():
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    return g
+
+
 def layer_graph(torch, calls):
     """One CUDA graph holding the given calls in order (after one eager run)."""
     for f in calls:
@@ -427,16 +442,17 @@ def run_ours(args):
             launch(c, g)
     torch.cuda.synchronize()
     # one CUDA graph per layer copy (its fused launches, one per group of
-    # independent matrices): the host only replays graphs, so the timed region
-    # measures the device (the pages' runtime also captures each pass in CUDA
-    # graphs)
+    # independent matrices), captured by the library's step-graph calls: the
+    # host only replays graphs, so the timed region measures the device (the
+    # pages' runtime also captures each pass in CUDA graphs)
+    cap = torch.cuda.Stream(dev)
     graphs = []
     for c in range(copies):
-        cg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(cg):
+        sg = lw.StepGraph(cap)
+        with sg.capture():
             for g in groups:
                 launch(c, g)
-        graphs.append(cg)
+        graphs.append(sg)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     n_mat = len(mats)
@@ -444,7 +460,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     for i in range(args.warmup):
-        graphs[i % copies].replay()
+        graphs[i % copies].launch(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -455,7 +471,7 @@ def run_ours(args):
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for i in range(args.steps):
-        graphs[i % copies].replay()
+        graphs[i % copies].launch(stream)
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -532,10 +548,11 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
     tsteps = [[(lambda c=c, g=g: lw.lw_twin_gemv_group([twins[c][j] for j in g], [xs[j] for j in g],
                                                        [ys[j] for j in g], ws, st))
                if len(g) > 1 else tcalls[c][g[0]] for g in groups] for c in range(ntw)]
-    tg = [layer_graph(torch, calls) for calls in tsteps]
+    cap = torch.cuda.Stream(dev)
+    tg = [step_graph(torch, lw, calls, cap) for calls in tsteps]
 
     def tstep(c):
-        tg[c].replay()
+        tg[c].launch(stream)
     t_twin = time_steps(torch, stream, tstep, steps, 5, ntw)
     tw_ms = per_call_ms(torch, stream, tcalls[: min(ntw, 4)])
     del tg, twins, tcalls, tsteps

@@ -1,6 +1,7 @@
 // Device-facing C-ABI calls of liblw: argument checks, then the launchers.
 #include <cstdint>
 #include <mutex>
+#include <new>
 #include <unordered_map>
 
 #include "lw_internal.h"
@@ -262,4 +263,55 @@ extern "C" lw_status lw_decode(const lw_dev_bundle* b, void* out, int32_t* d_sta
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (b->fmt == LW_FMT_BF16_EXP) return launch_bf16_decode(b, out, d_status, st);
   return launch_q_decode(b, out, d_status, st);
+}
+
+// ---------------------------------------------------------------------------
+// Step graphs: a decode step's calls captured once on a stream and replayed
+// (CUDA graphs; the programmatic launch dependencies become graph edges).
+// ---------------------------------------------------------------------------
+struct lw_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" lw_status lw_graph_begin(void* stream) {
+  clear_error();
+  if (!stream) return fail(LW_ERR_INVALID_ARG, "capture needs a created stream, not the default one");
+  const cudaError_t e = cudaStreamBeginCapture(static_cast<cudaStream_t>(stream),
+                                               cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return fail(LW_ERR_CUDA, "begin capture: %s", cudaGetErrorString(e));
+  return LW_OK;
+}
+
+extern "C" lw_status lw_graph_end(void* stream, lw_graph** out) {
+  clear_error();
+  if (!stream || !out) return fail(LW_ERR_INVALID_ARG, "NULL argument");
+  *out = nullptr;
+  lw_graph* g = new (std::nothrow) lw_graph;
+  if (!g) return fail(LW_ERR_ALLOC, "graph");
+  cudaError_t e = cudaStreamEndCapture(static_cast<cudaStream_t>(stream), &g->graph);
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+  if (e != cudaSuccess) {
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    cudaGetLastError();
+    return fail(LW_ERR_CUDA, "end capture / instantiate: %s", cudaGetErrorString(e));
+  }
+  *out = g;
+  return LW_OK;
+}
+
+extern "C" lw_status lw_graph_launch(const lw_graph* g, void* stream) {
+  clear_error();
+  if (!g || !g->exec) return fail(LW_ERR_INVALID_ARG, "NULL graph");
+  const cudaError_t e = cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(LW_ERR_CUDA, "graph launch: %s", cudaGetErrorString(e));
+  return LW_OK;
+}
+
+extern "C" void lw_graph_free(lw_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
 }

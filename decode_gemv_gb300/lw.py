@@ -33,7 +33,8 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_decode_gemv_group", "lw_workspace_bytes_group", "lw_twin_gemv_group",
             "lw_bundle_desc", "lw_bundle_serialized_bytes", "lw_bundle_serialize",
             "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load", "lw_transcode_twin",
-            "lw_twin_tile_rows", "lw_decode_gemm_strips"]
+            "lw_twin_tile_rows", "lw_decode_gemm_strips", "lw_graph_begin", "lw_graph_end",
+            "lw_graph_launch", "lw_graph_free"]
 
 
 class LwError(RuntimeError):
@@ -109,6 +110,10 @@ def load():
         "lw_transcode_twin": ([P, P, P, P], i32),
         "lw_decode_gemm_strips": ([P, P, i32, P, i32, P, P, sz, P, P], i32),
         "lw_twin_tile_rows": ([i32], i32),
+        "lw_graph_begin": ([P], i32),
+        "lw_graph_end": ([P, P], i32),
+        "lw_graph_launch": ([P, P], i32),
+        "lw_graph_free": ([P], None),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -380,6 +385,43 @@ class PreparedGemv:
     def __call__(self, stream=None) -> None:
         _check(self._fn(*self._args, self._ws, self._wsb, self._st, _stream_ptr(stream)),
                "prepared gemv")
+
+
+class StepGraph:
+    """Library calls captured once on a stream and replayed as one CUDA
+    graph (lw_graph_begin / lw_graph_end / lw_graph_launch).  Use as
+        g = StepGraph(stream)
+        with g.capture():
+            ...library calls on `stream` (e.g. with torch.cuda.stream(stream))...
+        g.launch()"""
+
+    def __init__(self, stream):
+        self.stream = stream
+        self._h = ctypes.c_void_p()
+
+    def capture(self):
+        import contextlib
+        import torch
+
+        @contextlib.contextmanager
+        def cm():
+            with torch.cuda.stream(self.stream):
+                _check(load().lw_graph_begin(_stream_ptr(self.stream)), "lw_graph_begin")
+                try:
+                    yield self
+                finally:
+                    _check(load().lw_graph_end(_stream_ptr(self.stream), ctypes.byref(self._h)),
+                           "lw_graph_end")
+        return cm()
+
+    def launch(self, stream=None) -> None:
+        _check(load().lw_graph_launch(self._h, _stream_ptr(stream if stream is not None else self.stream)),
+               "lw_graph_launch")
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.lw_graph_free(self._h)
+            self._h = ctypes.c_void_p()
 
 
 def lw_twin_tile_rows(fmt: int) -> int:

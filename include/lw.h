@@ -459,8 +459,29 @@ size_t lw_noalloc_scratch_bytes(void);
 const char* lw_status_string(lw_status s);
 const char* lw_last_error(void);
 
+/*
+ * Step graphs: the library calls of a decode step captured once on a
+ * stream and replayed as one CUDA graph ([LW] runtime: each pass captured in
+ * CUDA graphs; the programmatic launch dependencies between the library's
+ * kernels become graph edges).  lw_graph_begin starts a thread-local capture
+ * on `stream` (a created stream; the default stream cannot be captured);
+ * every library call on that stream until lw_graph_end is recorded, not run;
+ * lw_graph_end ends the capture and instantiates the graph (*out, owned by
+ * the caller, freed with lw_graph_free).  lw_graph_launch replays it on
+ * `stream` (asynchronous, like the calls it holds).  The buffers the calls
+ * named must stay allocated while the graph is used.  Errors:
+ * LW_ERR_INVALID_ARG, LW_ERR_CUDA (capture or launch refused, with the
+ * runtime's reason), LW_ERR_ALLOC.
+ */
+typedef struct lw_graph lw_graph;
+lw_status lw_graph_begin(void* stream);
+lw_status lw_graph_end(void* stream, lw_graph** out);
+lw_status lw_graph_launch(const lw_graph* g, void* stream);
+void lw_graph_free(lw_graph* g);
+
 /* ABI revision of this header: 3 (2 + grouped launches, strip lists, the
-   load-time transcode, bundle files, LW_ERR_IO, LW_DEV_BAD_STRIPS).  The
+   load-time transcode, bundle files, step graphs, LW_ERR_IO,
+   LW_DEV_BAD_STRIPS).  The
    bundle file format carries its own version. */
 int32_t lw_version(void);
 

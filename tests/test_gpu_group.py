@@ -152,3 +152,39 @@ def test_prepared_calls_equal_direct_calls():
             for j, y in zip(sel, ys):
                 ref = _single(dbs[j], xs[j])    # the twin gives the coded result bitwise
                 assert np.array_equal(y.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_step_graph_replays_the_calls():
+    """lw_graph_begin / lw_graph_end / lw_graph_launch: a step of library
+    calls (a group and a single matrix) captured once and replayed gives the
+    eager results bitwise; capture refuses the default stream."""
+    fmt = lw.LW_FMT_Q4_PAIR
+    mats = [_mat(fmt, 700 + i, *SHAPES[i]) for i in range(3)]
+    dbs = [_upload(fmt, m) for m in mats]
+    xs = [torch.from_numpy(m["x"][0]).to(DEV) for m in mats]
+    ys = [torch.full((d.rows,), float("nan"), device=DEV) for d in dbs]
+    ws = torch.zeros(lw.lw_workspace_bytes_group(dbs[:2]) // 4 + 64, device=DEV)
+    ws2 = torch.zeros(lw.lw_workspace_bytes(dbs[2], 1) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    calls = [lw.PreparedGemv(dbs[:2], xs[:2], ys[:2], ws, st), lw.PreparedGemv(dbs[2:], xs[2:], ys[2:], ws2, st)]
+    for c in calls:
+        c()                                   # eager once (launch attributes set up)
+    torch.cuda.synchronize()
+    ref = [y.cpu().numpy().copy() for y in ys]
+    for y in ys:
+        y.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    g = lw.StepGraph(s)
+    with g.capture():
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    assert all(torch.isnan(y).all() for y in ys)      # captured, not run
+    for _ in range(3):
+        g.launch()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for y, r in zip(ys, ref):
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), r.view(np.uint32))
+    with pytest.raises(lw.LwError):
+        lw._check(lw.load().lw_graph_begin(None), "lw_graph_begin")
