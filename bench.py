@@ -800,7 +800,10 @@ def run_sweep(args):
             xs.append(torch.randn(B, m["spec"].cols, device=dev, generator=gen).to(dt))
             ys.append(torch.empty(B, m["spec"].rows, device=dev, dtype=torch.float32))
         wsb = max(lw.lw_workspace_bytes(m["db"][0], B) for m in mats)
-        grouped = B == 1 and any(len(g) > 1 for g in groups)
+        # one launch per group of a layer's independent 4-/6-bit matrices while
+        # the batch stays on the CUDA cores (up to 5 rows: from 6 the large
+        # matrices take the tensor cores, one launch each)
+        grouped = B <= 5 and any(len(g) > 1 for g in groups)
         if grouped:
             wsb = max([wsb] + [lw.lw_workspace_bytes_group([mats[j]["db"][0] for j in g])
                                for g in groups if len(g) > 1])
@@ -818,8 +821,10 @@ def run_sweep(args):
                                        [ys[j] for j in g], ws, st)) if len(g) > 1 else
                     (lambda d=mats[g[0]][key][c], x=xs[g[0]], y=ys[g[0]]: one(d, x, B, y, ws, st))
                     for g in groups]
-        t_coded, steps = timed(lambda c: step_calls(c, "db", lw.lw_decode_gemm, lw.lw_decode_gemv_group))
-        t_twin, _ = timed(lambda c: step_calls(c, "tw", lw.lw_twin_gemm, lw.lw_twin_gemv_group), steps)
+        gc = lambda d, x, y, w, s_: lw.lw_decode_gemm_group(d, x, B, y, w, s_)
+        gt = lambda d, x, y, w, s_: lw.lw_twin_gemm_group(d, x, B, y, w, s_)
+        t_coded, steps = timed(lambda c: step_calls(c, "db", lw.lw_decode_gemm, gc))
+        t_twin, _ = timed(lambda c: step_calls(c, "tw", lw.lw_twin_gemm, gt), steps)
         xb = [x.to(torch.bfloat16) for x in xs]
         yb = [torch.empty(B, m["spec"].rows, device=dev, dtype=torch.bfloat16) for m in mats]
         t_bf16, _ = timed(lambda c: [(lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y))
@@ -847,7 +852,7 @@ def run_sweep(args):
             "n_gpus": 1, "higher_is_better": True, "dtype": "f32" if mats[0]["fmt"] != lw.LW_FMT_BF16_EXP else "bf16",
             "data": "synthetic", "peak_gbs": peak, "peak_kind": peak_kind,
             "config": {"workload": label, "layers": layers, "matrices": len(mats), "weights": weights,
-                       "launches": "batch 1: one launch per group of a layer's independent 4-/6-bit "
+                       "launches": "batch 1..5: one launch per group of a layer's independent 4-/6-bit "
                                    "matrices (q+k+v, gate+up; coded and twin alike); else one per matrix",
                        "l2": (f"rotate {copies} device copies ({group} steps per CUDA graph)"
                               if copies > 1 else "working set > 4x L2"),

@@ -205,12 +205,13 @@ extern "C" size_t lw_workspace_bytes_group(const lw_dev_bundle* const* b, int32_
   return total;
 }
 
-static lw_status gemv_group(const lw_dev_bundle* const* b, int32_t n, const void* const* x,
-                            float* const* y, void* ws, size_t ws_bytes, int32_t* d_status,
-                            void* stream, bool twin) {
+static lw_status gemm_group(const lw_dev_bundle* const* b, int32_t n, const void* const* x,
+                            int32_t batch, float* const* y, void* ws, size_t ws_bytes,
+                            int32_t* d_status, void* stream, bool twin) {
   clear_error();
   if (!b || !x || !y || n < 1 || n > LW_MAX_GROUP)
     return fail(LW_ERR_INVALID_ARG, "group of %d matrices (1..%d) or NULL arrays", n, LW_MAX_GROUP);
+  if (batch < 1 || batch > 8) return fail(LW_ERR_INVALID_ARG, "group batch %d outside 1..8", batch);
   if (!ws || !aligned16(ws)) return fail(LW_ERR_INVALID_ARG, "workspace NULL or not 16-byte aligned");
   const float* xs[LW_MAX_GROUP];
   float* ys[LW_MAX_GROUP];
@@ -230,19 +231,33 @@ static lw_status gemv_group(const lw_dev_bundle* const* b, int32_t n, const void
     off += group_slice(b[i]);
   }
   if (ws_bytes < off) return fail(LW_ERR_INVALID_ARG, "workspace of %zu bytes < %zu", ws_bytes, off);
-  return launch_q_products(b, n, xs, 1, ys, wss, d_status, static_cast<cudaStream_t>(stream));
+  return launch_q_products(b, n, xs, batch, ys, wss, d_status, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" lw_status lw_decode_gemv_group(const lw_dev_bundle* const* b, int32_t n,
                                           const void* const* x, float* const* y, void* ws,
                                           size_t ws_bytes, int32_t* d_status, void* stream) {
-  return gemv_group(b, n, x, y, ws, ws_bytes, d_status, stream, false);
+  return gemm_group(b, n, x, 1, y, ws, ws_bytes, d_status, stream, false);
 }
 
 extern "C" lw_status lw_twin_gemv_group(const lw_dev_bundle* const* b, int32_t n,
                                         const void* const* x, float* const* y, void* ws,
                                         size_t ws_bytes, int32_t* d_status, void* stream) {
-  return gemv_group(b, n, x, y, ws, ws_bytes, d_status, stream, true);
+  return gemm_group(b, n, x, 1, y, ws, ws_bytes, d_status, stream, true);
+}
+
+extern "C" lw_status lw_decode_gemm_group(const lw_dev_bundle* const* b, int32_t n,
+                                          const void* const* X, int32_t batch, float* const* Y,
+                                          void* ws, size_t ws_bytes, int32_t* d_status,
+                                          void* stream) {
+  return gemm_group(b, n, X, batch, Y, ws, ws_bytes, d_status, stream, false);
+}
+
+extern "C" lw_status lw_twin_gemm_group(const lw_dev_bundle* const* b, int32_t n,
+                                        const void* const* X, int32_t batch, float* const* Y,
+                                        void* ws, size_t ws_bytes, int32_t* d_status,
+                                        void* stream) {
+  return gemm_group(b, n, X, batch, Y, ws, ws_bytes, d_status, stream, true);
 }
 
 extern "C" lw_status lw_twin_gemv(const lw_dev_bundle* b, const void* x, float* y, void* ws,

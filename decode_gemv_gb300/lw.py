@@ -34,7 +34,7 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_bundle_desc", "lw_bundle_serialized_bytes", "lw_bundle_serialize",
             "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load", "lw_transcode_twin",
             "lw_twin_tile_rows", "lw_decode_gemm_strips", "lw_graph_begin", "lw_graph_end",
-            "lw_graph_launch", "lw_graph_free"]
+            "lw_graph_launch", "lw_graph_free", "lw_decode_gemm_group", "lw_twin_gemm_group"]
 
 
 class LwError(RuntimeError):
@@ -99,6 +99,8 @@ def load():
         "lw_decode_gemv_noalloc": ([P, P, P, P, P], i32),
         "lw_decode_gemv_group": ([P, i32, P, P, P, sz, P, P], i32),
         "lw_twin_gemv_group": ([P, i32, P, P, P, sz, P, P], i32),
+        "lw_decode_gemm_group": ([P, i32, P, i32, P, P, sz, P, P], i32),
+        "lw_twin_gemm_group": ([P, i32, P, i32, P, P, sz, P, P], i32),
         "lw_workspace_bytes_group": ([P, i32], sz),
         "lw_noalloc_scratch_bytes": ([], sz),
         "lw_bundle_desc": ([P, P], i32),
@@ -492,6 +494,23 @@ def _gemv_group(fn, dbs, xs, ys, ws, d_status, stream):
     ya = (ctypes.c_void_p * n)(*[_tp(y) for y in ys])
     _check(getattr(load(), fn)(_views(dbs), n, xa, ya, _tp(ws), ws.numel() * ws.element_size(),
                                _tp(d_status), _stream_ptr(stream)), fn)
+
+
+def _gemm_group(fn, dbs, Xs, batch, Ys, ws, d_status, stream):
+    n = len(dbs)
+    xa = (ctypes.c_void_p * n)(*[_tp(x) for x in Xs])
+    ya = (ctypes.c_void_p * n)(*[_tp(y) for y in Ys])
+    _check(getattr(load(), fn)(_views(dbs), n, xa, batch, ya, _tp(ws), ws.numel() * ws.element_size(),
+                               _tp(d_status), _stream_ptr(stream)), fn)
+
+
+def lw_decode_gemm_group(dbs, Xs, batch, Ys, ws, d_status, stream=None) -> None:
+    """One launch for several 4-/6-bit matrices, batch 1..8: Ys[i] = Xs[i] W_i^T."""
+    _gemm_group("lw_decode_gemm_group", dbs, Xs, batch, Ys, ws, d_status, stream)
+
+
+def lw_twin_gemm_group(dbs, Xs, batch, Ys, ws, d_status, stream=None) -> None:
+    _gemm_group("lw_twin_gemm_group", dbs, Xs, batch, Ys, ws, d_status, stream)
 
 
 def lw_decode_gemv_group(dbs, xs, ys, ws, d_status, stream=None) -> None:

@@ -390,6 +390,23 @@ lw_status lw_twin_gemv_group(const lw_dev_bundle* const* b, int32_t n, const voi
                              void* stream);
 
 /*
+ * The grouped launches for small batches: Y[i] = X[i] W_i^T for `batch` = 1..8
+ * activation rows (X[i] fp32 [batch][K_i], Y[i] fp32 [batch][N_i]) on the
+ * CUDA cores, one launch for the group; each Y[i] is bitwise what
+ * lw_decode_gemm / lw_twin_gemm gives for that matrix when its pass stays on
+ * the CUDA cores (below 6 rows always; a larger pass on a matrix that fills
+ * the device takes the tensor cores in lw_decode_gemm).  Same workspace
+ * (lw_workspace_bytes_group) and errors as lw_decode_gemv_group, plus
+ * LW_ERR_INVALID_ARG for a batch outside 1..8.
+ */
+lw_status lw_decode_gemm_group(const lw_dev_bundle* const* b, int32_t n, const void* const* X,
+                               int32_t batch, float* const* Y, void* ws, size_t ws_bytes,
+                               int32_t* d_status, void* stream);
+lw_status lw_twin_gemm_group(const lw_dev_bundle* const* b, int32_t n, const void* const* X,
+                             int32_t batch, float* const* Y, void* ws, size_t ws_bytes,
+                             int32_t* d_status, void* stream);
+
+/*
  * Tile-skip launch list ["Software-Defined Bandwidth Expansion" §IV.C: an
  * inactive tile is absent from a smaller launch grid, so it moves no
  * weight bytes]: Y = W X for the n_strips 64-row strips listed in `strips`

@@ -188,3 +188,39 @@ def test_step_graph_replays_the_calls():
         assert np.array_equal(y.cpu().numpy().view(np.uint32), r.view(np.uint32))
     with pytest.raises(lw.LwError):
         lw._check(lw.load().lw_graph_begin(None), "lw_graph_begin")
+
+
+@pytest.mark.parametrize("fmt", [lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6])
+@pytest.mark.parametrize("batch", [2, 3, 8])
+def test_gemm_group_equals_per_matrix_products(fmt, batch):
+    """lw_decode_gemm_group / lw_twin_gemm_group: batches of up to 8 rows in
+    one launch, each output bitwise what the per-matrix CUDA-core product
+    gives (these matrices stay on the CUDA cores up to 8 rows)."""
+    n = 4
+    mats = [(inputs.small_q4(900 + i, *SHAPES[i], batch=batch) if fmt == lw.LW_FMT_Q4_PAIR
+             else inputs.small_q6(900 + i, *SHAPES[i], batch=batch)) for i in range(n)]
+    dbs = [_upload(fmt, m) for m in mats]
+    tws = [lw.DeviceBundle.upload(lw.lw_encode_bundle(fmt, m["codes"], m["scales"], m.get("mins"),
+                                                      twin=True), DEV) for m in mats]
+    Xs = [torch.from_numpy(np.ascontiguousarray(m["x"][:batch])).to(DEV) for m in mats]
+    ws = torch.zeros(lw.lw_workspace_bytes_group(dbs) // 4 + 64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for bundles, group, one in ((dbs, lw.lw_decode_gemm_group, lw.lw_decode_gemm),
+                                (tws, lw.lw_twin_gemm_group, lw.lw_twin_gemm)):
+        Ys = [torch.full((batch, d.rows), float("nan"), device=DEV) for d in bundles]
+        group(bundles, Xs, batch, Ys, ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        for d, X, Y in zip(bundles, Xs, Ys):
+            Y1 = torch.empty(batch, d.rows, device=DEV)
+            w1 = torch.zeros(lw.lw_workspace_bytes(d, batch) // 4 + 64, device=DEV)
+            one(d, X, batch, Y1, w1, st)
+            torch.cuda.synchronize()
+            assert np.array_equal(Y.cpu().numpy().view(np.uint32), Y1.cpu().numpy().view(np.uint32))
+    for m, Y in zip(mats, Ys):
+        ref = oracle.reference_output(oracle.Q4 if fmt == lw.LW_FMT_Q4_PAIR else oracle.Q6, m)
+        scale = oracle.abs_row_products(oracle.Q4 if fmt == lw.LW_FMT_Q4_PAIR else oracle.Q6, m)
+        assert_close(Y.cpu().numpy(), ref, scale)
+    with pytest.raises(lw.LwError):
+        lw.lw_decode_gemm_group(dbs, Xs, 9, Ys, ws, st)
+    assert int(st.item()) == 0
