@@ -157,3 +157,15 @@ def test_transcode_argument_errors(lib):
         st, msg = status(lib, "lw_transcode_twin", ctypes.byref(c), ctypes.byref(t), None, None)
         assert st == lw.LW_ERR_INVALID_ARG, (st, msg)
         assert msg
+
+
+def test_gemm_group_batch_checks(lib):
+    vs = [view(), view(rows=256)]
+    arr = (ctypes.c_void_p * 2)(*[ctypes.addressof(v) for v in vs])
+    xs = (ctypes.c_void_p * 2)(FAKE + 0xA000000, FAKE + 0xA100000)
+    ys = (ctypes.c_void_p * 2)(FAKE + 0xB000000, FAKE + 0xB100000)
+    ws = P(FAKE + 0x9000000)
+    for fn in ("lw_decode_gemm_group", "lw_twin_gemm_group"):
+        for batch in (0, 9, -1):
+            st, msg = status(lib, fn, arr, 2, xs, batch, ys, ws, 1 << 40, None, None)
+            assert st == lw.LW_ERR_INVALID_ARG and msg, (fn, batch, st)
