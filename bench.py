@@ -258,9 +258,13 @@ def listed_bytes(hb, strips, cols):
     table."""
     tk = cols // 256
     toff = hb.view("tile_off", np.uint32).astype(np.int64)
-    per_tile = 4 + 64 + 64 + (len(hb.sections.get("qparams", b"")) // max(1, len(toff) - 1))
+    per_tile = 64 + 64 + (len(hb.sections.get("qparams", b"")) // max(1, len(toff) - 1))
     words = sum(int(toff[(s + 1) * tk] - toff[s * tk]) * 128 for s in strips)
-    return words + len(strips) * tk * per_tile + 1024
+    # tile offsets read: each listed tile's start and end entries
+    offsets = set()
+    for s in strips:
+        offsets.update(range(int(s) * tk, (int(s) + 1) * tk + 1))
+    return words + len(strips) * tk * per_tile + 4 * len(offsets) + 1024
 
 
 def build_layer(names):
