@@ -129,6 +129,9 @@ def decoder_tables(lengths) -> dict:
 # --------------------------------------------------------------------------
 
 def tile_grid(rows: int, cols: int):
+    """(tile rows, tile columns) of a matrix cut into 64 x 256 tiles (a
+    reading: LazyWeights "2 . Code them" and Fig. 3(a) code a matrix in
+    independently decodable tiles of 32 lanes but fix no tile shape)."""
     if rows % 64 or cols % 256 or rows <= 0 or cols <= 0:
         raise ValueError("shape must be a positive multiple of 64 x 256")
     return rows // 64, cols // 256
@@ -145,7 +148,9 @@ def lanes_from_rows(a: np.ndarray, per_row: int) -> np.ndarray:
     """[N][TK*per_row] row-major symbols -> [n_tiles][32][2*per_row].
 
     Tile t = s*TK + kt covers rows 64s..64s+63; lane l carries row 64s+2l then
-    row 64s+2l+1, each over the tile's columns in ascending order.
+    row 64s+2l+1, each over the tile's columns in ascending order (LazyWeights
+    Fig. 3(a): one Huffman stream per lane, 32 lanes per tile; the rows a lane
+    carries are a reading).
     """
     n = a.shape[0]
     tr, tk = n // 64, a.shape[1] // per_row
@@ -154,6 +159,8 @@ def lanes_from_rows(a: np.ndarray, per_row: int) -> np.ndarray:
 
 
 def rows_from_lanes(v: np.ndarray, n: int, per_row: int) -> np.ndarray:
+    """Inverse of lanes_from_rows: [n_tiles][32][2*per_row] -> [N][TK*per_row]
+    (the lane-to-row map of LazyWeights Fig. 3(a), read backwards)."""
     tr = n // 64
     tk = v.shape[0] // tr
     a = v.reshape(tr, tk, 32, 2, per_row).transpose(0, 2, 3, 1, 4)
@@ -175,6 +182,8 @@ def bf16_fields(bits: np.ndarray):
 
 
 def bf16_join(exp: np.ndarray, sm: np.ndarray) -> np.ndarray:
+    """Inverse of bf16_fields: exponent byte + sign/mantissa byte -> bf16
+    bits (Unweight, "Understanding BF16 weight structure")."""
     e = exp.astype(np.uint16)
     s = sm.astype(np.uint16)
     return ((s & 0x80) << 8) | (e << 7) | (s & 0x7F)
@@ -199,6 +208,10 @@ def bf16_verbatim_groups(exp: np.ndarray, palette: np.ndarray) -> np.ndarray:
 
 
 def bf16_split(bits: np.ndarray) -> dict:
+    """Everything the BF16 path stores besides the coded indices: exponent
+    and sign+mantissa bytes, the top-16 palette, the verbatim 64-column
+    groups with their raw exponents, and each weight's palette index
+    (Unweight, "The exponent's exploitable redundancy")."""
     exp, sm = bf16_fields(bits)
     pal = bf16_palette(exp)
     verb = bf16_verbatim_groups(exp, pal)
@@ -213,8 +226,10 @@ def bf16_split(bits: np.ndarray) -> dict:
 def bf16_lane_symbols(index: np.ndarray, verbatim: np.ndarray):
     """Palette indices in lane order, skipping verbatim groups.
 
-    Lane l of a tile walks row 2l then 2l+1; within a row the four 64-column
-    groups in ascending order; a verbatim group contributes no symbol.
+    Lane l of a tile walks row 2l then 2l+1 (the lane map of LazyWeights
+    Fig. 3(a)); within a row the four 64-column groups in ascending order; a
+    verbatim group contributes no symbol (Unweight, "The exponent's
+    exploitable redundancy": such rows of 64 bypass the code).
     Returns syms [n_tiles][32][512] (tail unused) and nsym [n_tiles][32].
     """
     n, k = index.shape
@@ -249,7 +264,10 @@ def _symbols(fmt: int, payload: np.ndarray):
 
 
 def encode(fmt: int, payload: np.ndarray) -> dict:
-    """Build the coded sections of one matrix.
+    """Build the coded sections of one matrix: one length-limited Huffman
+    code over the matrix's symbol histogram, each lane's codes packed
+    MSB-first into 32-bit words interleaved across the tile's 32 lanes, and
+    per-tile word offsets (LazyWeights "2 . Code them", Fig. 3(a)).
 
     payload: uint8 codes [N][K] (4- or 6-bit) or uint16 bf16 bits [N][K].
     Returns code_len, words, tile_off, lane_bits (+ BF16 side data).
@@ -312,7 +330,9 @@ def decode_lanes(code_len, words, tile_off, nsym, maxsym):
 
 def decode(fmt: int, rows: int, cols: int, code_len, words, tile_off,
            palette=None, verbatim=None, vexp=None, sm=None):
-    """Restore the fixed-width payload from the coded sections.
+    """Restore the fixed-width payload from the coded sections (LazyWeights
+    "3 . Decode on demand"; BF16 exponents through the palette and the
+    verbatim groups of Unweight, "The exponent's exploitable redundancy").
 
     Q4 -> packed bytes [N][K/2] (low nibble = even column), Q6 -> uint8
     [N][K], BF16 -> uint16 bits [N][K].
@@ -344,6 +364,8 @@ def decode(fmt: int, rows: int, cols: int, code_len, words, tile_off,
 
 
 def unpack_q4(packed: np.ndarray) -> np.ndarray:
+    """Packed 4-bit bytes [N][K/2] -> codes [N][K], low nibble = even column
+    (the pair order of q4_pair_symbols)."""
     out = np.empty((packed.shape[0], packed.shape[1] * 2), dtype=np.uint8)
     out[:, 0::2] = packed & 15
     out[:, 1::2] = packed >> 4
@@ -355,10 +377,14 @@ def unpack_q4(packed: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 
 def fp16_to_f64(bits) -> np.ndarray:
+    """IEEE binary16 bit patterns -> exact fp64 values (the stored scales
+    and minimums)."""
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 
 
 def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> exact fp64 values (bf16 is the top half of an
+    fp32; Unweight, "Understanding BF16 weight structure")."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return u.view(np.float32).astype(np.float64)
 
@@ -375,7 +401,8 @@ def dequant_q4(codes, scales, mins) -> np.ndarray:
 
 def dequant_q6(codes, scales) -> np.ndarray:
     """w = scale * (code - 32), one fp16 scale per 16 weights of a row
-    (Q6_K's code offset; the pages name Q6_K but print no formula)."""
+    (Q6_K's code offset; LazyWeights "1 . Select the codes" names llama.cpp's
+    Q6_K block format but prints no formula, so this is a reading)."""
     c = np.asarray(codes, dtype=np.float64)
     s = np.repeat(fp16_to_f64(scales), 16, axis=1)
     return s * (c - 32.0)
@@ -383,7 +410,8 @@ def dequant_q6(codes, scales) -> np.ndarray:
 
 def gemm(w: np.ndarray, x: np.ndarray) -> np.ndarray:
     """Y[b][r] = sum_k W[r][k] * X[b][k] in fp64, k ascending (plain loops in
-    C).  Shapes: W [N][K], X [B][K] -> Y [B][N]."""
+    C): the matrix-vector product of LazyWeights "3 . Decode on demand", one
+    row of X per batch entry.  Shapes: W [N][K], X [B][K] -> Y [B][N]."""
     w = np.ascontiguousarray(w, dtype=np.float64)
     x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float64)
     n, k = w.shape
@@ -402,7 +430,9 @@ def reference_output(fmt: int, m: dict) -> np.ndarray:
 
 
 def abs_row_products(fmt: int, m: dict) -> np.ndarray:
-    """sum_k |w_rk x_k| per output, the scale of the componentwise check."""
+    """sum_k |w_rk x_k| per output in fp64: the scale of the componentwise
+    check (the standard bound on a floating-point dot product's rounding
+    error is proportional to this sum, not to |y|)."""
     if fmt == Q4:
         w = dequant_q4(m["codes"], m["scales"], m["mins"])
         x = m["x"]
