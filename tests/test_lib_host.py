@@ -134,6 +134,17 @@ def test_twin_words_identical_to_oracle(fmt):
     assert np.array_equal(hb.view("tile_off", np.uint32), np.arange(5, dtype=np.uint32) * wt)
 
 
+def test_bf16_twin_against_oracle():
+    m = inputs.small_bf16(9, 128, 512, outlier_p=0.004)
+    hb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, m["bits"], twin=True)
+    assert np.array_equal(hb.view("words", np.uint32), oracle.twin_words(oracle.BF16, m["bits"]))
+    assert np.array_equal(hb.view("tile_off", np.uint32), np.arange(5, dtype=np.uint32) * 64)
+    sp = oracle.bf16_split(m["bits"])
+    tb = lw.table_fields(hb.sections["table"])
+    assert list(tb["palette"][: tb["n_palette"]]) == list(sp["palette"])
+    assert np.array_equal(hb.view("vexp", np.uint8).reshape(-1, 64), sp["vexp"])
+
+
 def test_q4_qparams_layout():
     m = _q4(6, 128, 768)
     hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"])

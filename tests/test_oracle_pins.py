@@ -422,3 +422,37 @@ def test_twin_layout_brute_force():
     assert w6.size == 96 * 32
     stream = "".join(format(int(v), "06b") for r in (2, 3) for v in m6["codes"][r])
     assert format(int(w6[7 * 32 + 1]), "032b") == stream[224:256]
+
+
+def test_bf16_twin_layout_brute_force():
+    """The BF16 twin: every weight's exponent as a 4-bit index into the
+    ascending top-16 palette, 0 throughout a verbatim 64-column group; the
+    palette and the verbatim groups counted here by hand."""
+    m = inputs.small_bf16(13, 64, 512, outlier_p=0.01)
+    bits = m["bits"]
+    exp = [[(int(v) >> 7) & 0xFF for v in row] for row in bits]
+    counts = {}
+    for row in exp:
+        for e in row:
+            counts[e] = counts.get(e, 0) + 1
+    palette = sorted(sorted(counts, key=lambda e: (-counts[e], e))[:16])
+    assert len(counts) > 16                       # some groups are verbatim
+    pos = {e: i for i, e in enumerate(palette)}
+    w = oracle.twin_words(oracle.BF16, bits)
+    assert w.size == 2 * 64 * 32                  # 2 tiles, 64 words per lane
+    n_verbatim = 0
+    for t in range(2):
+        for l in (0, 9, 31):
+            vals = []
+            for r in (2 * l, 2 * l + 1):
+                for g in range(4 * t, 4 * t + 4):
+                    grp = exp[r][64 * g: 64 * g + 64]
+                    if all(e in pos for e in grp):
+                        vals += [pos[e] for e in grp]
+                    else:
+                        vals += [0] * 64
+                        n_verbatim += 1
+            stream = "".join(format(v, "04b") for v in vals)
+            for j in range(64):
+                assert format(int(w[t * 64 * 32 + j * 32 + l]), "032b") == stream[32 * j: 32 * j + 32]
+    assert n_verbatim > 0
