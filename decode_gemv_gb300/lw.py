@@ -38,9 +38,14 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
 
 
 class LwError(RuntimeError):
-    def __init__(self, status: int, what: str):
+    """A failing call: `status` is the lw_status code.  `detail` replaces the
+    library's thread-local error text when the binding itself refused the
+    call before reaching the library."""
+
+    def __init__(self, status: int, what: str, detail: str | None = None):
         self.status = status
-        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}: {_last_error()}")
+        text = _last_error() if detail is None else detail
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}: {text}")
 
 
 class LwDesc(ctypes.Structure):
@@ -345,21 +350,151 @@ def _tp(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+# ----------------------------------------------------------------------------
+# device buffers, checked before their addresses cross the C ABI
+# ----------------------------------------------------------------------------
+# The C calls take bare device addresses: they cannot tell how large a buffer
+# is, whether it lives on the device or how it is strided.  A tensor that is
+# too small, on the host or strided would let a kernel read or write outside
+# it, so every tensor is checked here first (LW_ERR_INVALID_ARG, nothing
+# launched).  Sizes follow the view's shape; a shape the library refuses
+# anyway (not a multiple of 64 x 256) is left for it to report.
+
+def _refuse(fn: str, detail: str):
+    raise LwError(LW_ERR_INVALID_ARG, fn, detail)
+
+
+def _buf(fn: str, name: str, t, nbytes: int, dtypes=None):
+    """Address of tensor `t` after checking that it is a torch.Tensor of one
+    of `dtypes` (any if None), contiguous and at least `nbytes` bytes.  Its
+    device is checked afterwards (_on), once every buffer has passed."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        _refuse(fn, f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if dtypes is not None and t.dtype not in dtypes:
+        want = ", ".join(str(d).replace("torch.", "") for d in dtypes)
+        _refuse(fn, f"{name}: dtype {str(t.dtype).replace('torch.', '')}, expected {want}")
+    if not t.is_contiguous():
+        _refuse(fn, f"{name}: not contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        _refuse(fn, f"{name}: {have} bytes, the call needs {nbytes}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bundle_device(fn: str, db, name: str = "bundle"):
+    """The one CUDA device holding every section tensor of `db`."""
+    devs = {t.device for t in db.tensors.values()}
+    if len(devs) != 1:
+        _refuse(fn, f"{name}: sections on {sorted(map(str, devs)) or 'no device'}, "
+                    "expected one CUDA device")
+    dev = devs.pop()
+    if dev.type != "cuda":
+        _refuse(fn, f"{name}: sections on {dev}, expected a CUDA device")
+    if not all(t.is_contiguous() for t in db.tensors.values()):
+        _refuse(fn, f"{name}: a section tensor is not contiguous")
+    return dev
+
+
+def _on(fn: str, dev, *named):
+    """Every (name, tensor) pair is on the bundle's device `dev`."""
+    for name, t in named:
+        if t.device.type != "cuda":
+            _refuse(fn, f"{name}: on {t.device}, expected a CUDA device")
+        if t.device != dev:
+            _refuse(fn, f"{name}: on {t.device}, the bundle is on {dev}")
+
+
+def _dims(db):
+    """(N, K) of the view when the library accepts that shape, else (0, 0)."""
+    n, k = int(db.view.rows), int(db.view.cols)
+    return (n, k) if n > 0 and k > 0 and n % 64 == 0 and k % 256 == 0 else (0, 0)
+
+
+def _act_types(fmt: int):
+    """Activation dtypes and element size of a format (fp32; BF16 as
+    bfloat16 or its bits)."""
+    import torch
+    if fmt == LW_FMT_BF16_EXP:
+        return (torch.bfloat16, torch.int16) + ((torch.uint16,) if hasattr(torch, "uint16") else ()), 2
+    if fmt in (LW_FMT_Q4_PAIR, LW_FMT_Q6):
+        return (torch.float32,), 4
+    return None, 0
+
+
+def _decoded_bytes(fmt: int, n: int, k: int) -> int:
+    """Bytes lw_decode writes: packed pairs (4-bit), one byte per code
+    (6-bit), BF16 bits."""
+    return {LW_FMT_Q4_PAIR: n * k // 2, LW_FMT_Q6: n * k, LW_FMT_BF16_EXP: 2 * n * k}.get(fmt, 0)
+
+
+def _status_ptr(fn: str, d_status):
+    import torch
+    return _buf(fn, "d_status", d_status, 4, (torch.int32,))
+
+
+def _ws_ptr(fn: str, ws):
+    return _buf(fn, "ws", ws, 0), ctypes.c_size_t(ws.numel() * ws.element_size())
+
+
+def _product_bufs(fn: str, db, x, y, batch: int, xname="x", yname="y"):
+    """Checked addresses of one matrix's activations [batch][K] and outputs
+    fp32 [batch][N] (devices not yet checked)."""
+    import torch
+    n, k = _dims(db)
+    b = max(int(batch), 0)
+    types, esize = _act_types(int(db.view.fmt))
+    return (_buf(fn, xname, x, b * k * esize, types),
+            _buf(fn, yname, y, b * n * 4, (torch.float32,)))
+
+
+def _checked(fn: str, dbs, xs, ys, batch: int, ws, d_status, names=("x", "y"), indexed=False,
+             extra=()):
+    """Check a product call's buffers in two passes -- first every buffer's
+    type, dtype, layout and size, then that the bundles and every buffer sit
+    on one CUDA device -- and return the addresses: (x list, y list, ws,
+    ws bytes, d_status).  `extra`: further (name, tensor) pairs whose device
+    is checked."""
+    n = len(dbs)
+    if n < 1 or len(xs) != n or len(ys) != n:
+        _refuse(fn, f"{n} bundles, {len(xs)} activations, {len(ys)} outputs")
+    label = (lambda i: (f"{names[0]}[{i}]", f"{names[1]}[{i}]")) if indexed else (lambda i: names)
+    bufs = [_product_bufs(fn, d, x, y, batch, *label(i)) for i, (d, x, y) in enumerate(zip(dbs, xs, ys))]
+    wp, wb = _ws_ptr(fn, ws) if ws is not None else (None, None)
+    sp = _status_ptr(fn, d_status)
+    dev = _bundle_device(fn, dbs[0], "bundle[0]" if indexed else "bundle")
+    for i in range(1, n):
+        if _bundle_device(fn, dbs[i], f"bundle[{i}]") != dev:
+            _refuse(fn, f"bundle[{i}]: not on {dev} like bundle[0]")
+    named = [p for i in range(n) for p in zip(label(i), (xs[i], ys[i]))]
+    _on(fn, dev, *named, *((("ws", ws),) if ws is not None else ()), ("d_status", d_status), *extra)
+    return [b[0] for b in bufs], [b[1] for b in bufs], wp, wb, sp
+
+
 def lw_workspace_bytes(db: DeviceBundle, batch: int = 1) -> int:
     return int(load().lw_workspace_bytes(db.ref, batch))
 
 
 def lw_decode(db: DeviceBundle, out, d_status, stream=None) -> None:
-    _check(load().lw_decode(db.ref, _tp(out), _tp(d_status), _stream_ptr(stream)), "lw_decode")
+    fn = "lw_decode"
+    n, k = _dims(db)
+    o = _buf(fn, "out", out, _decoded_bytes(int(db.view.fmt), n, k))
+    sp = _status_ptr(fn, d_status)
+    _on(fn, _bundle_device(fn, db), ("out", out), ("d_status", d_status))
+    _check(load().lw_decode(db.ref, o, sp, _stream_ptr(stream)), fn)
 
 
 def lw_decode_gemm_strips(db: DeviceBundle, strips, X, batch, Y, ws, d_status, stream=None) -> None:
     """Y = W X on the 64-row strips listed in `strips` (device int32 tensor,
     ascending); the other rows of Y are left as they are."""
+    import torch
+    fn = "lw_decode_gemm_strips"
     n = int(strips.numel()) if strips is not None else 0
-    _check(load().lw_decode_gemm_strips(db.ref, _tp(strips) if n else None, n, _tp(X), batch, _tp(Y),
-                                        _tp(ws), ws.numel() * ws.element_size(), _tp(d_status),
-                                        _stream_ptr(stream)), "lw_decode_gemm_strips")
+    lp = _buf(fn, "strips", strips, 4 * n, (torch.int32,)) if n else None
+    (xp,), (yp,), wp, wb, sp = _checked(fn, [db], [X], [Y], batch, ws, d_status, ("X", "Y"),
+                                        extra=(("strips", strips),) if n else ())
+    _check(load().lw_decode_gemm_strips(db.ref, lp, n, xp, batch, yp, wp, wb, sp,
+                                        _stream_ptr(stream)), fn)
 
 
 class PreparedGemv:
@@ -370,18 +505,19 @@ class PreparedGemv:
 
     def __init__(self, dbs, xs, ys, ws, d_status, twin: bool = False):
         lib = load()
+        fn = "PreparedGemv"
         self._keep = (list(dbs), list(xs), list(ys), ws, d_status)
         n = len(dbs)
-        self._ws, self._wsb = _tp(ws), ctypes.c_size_t(ws.numel() * ws.element_size())
-        self._st = _tp(d_status)
+        xps, yps, self._ws, self._wsb, self._st = _checked(fn, dbs, xs, ys, 1, ws, d_status,
+                                                           indexed=True)
         if n == 1:
             self._fn = lib.lw_twin_gemv if twin else lib.lw_decode_gemv
-            self._args = (dbs[0].ref, _tp(xs[0]), _tp(ys[0]))
+            self._args = (dbs[0].ref, xps[0], yps[0])
         else:
             self._fn = lib.lw_twin_gemv_group if twin else lib.lw_decode_gemv_group
             self._views = _views(dbs)
-            self._xa = (ctypes.c_void_p * n)(*[_tp(x) for x in xs])
-            self._ya = (ctypes.c_void_p * n)(*[_tp(y) for y in ys])
+            self._xa = (ctypes.c_void_p * n)(*xps)
+            self._ya = (ctypes.c_void_p * n)(*yps)
             self._args = (self._views, n, self._xa, self._ya)
 
     def __call__(self, stream=None) -> None:
@@ -445,38 +581,45 @@ def lw_transcode_twin(db: DeviceBundle, d_status, stream=None) -> DeviceBundle:
         if name in db.tensors:
             t[name] = db.tensors[name]
     tw = DeviceBundle.from_tensors(db.fmt, True, db.rows, db.cols, t, r2, 0, 0)
-    _check(load().lw_transcode_twin(db.ref, tw.ref, _tp(d_status), _stream_ptr(stream)),
-           "lw_transcode_twin")
+    fn = "lw_transcode_twin"
+    sp = _status_ptr(fn, d_status)
+    _on(fn, _bundle_device(fn, db), ("d_status", d_status))
+    _check(load().lw_transcode_twin(db.ref, tw.ref, sp, _stream_ptr(stream)), fn)
     return tw
 
 
+def _gemv(fn, db, x, y, ws, d_status, stream):
+    (xp,), (yp,), wp, wb, sp = _checked(fn, [db], [x], [y], 1, ws, d_status)
+    _check(getattr(load(), fn)(db.ref, xp, yp, wp, wb, sp, _stream_ptr(stream)), fn)
+
+
+def _gemm(fn, db, X, batch, Y, ws, d_status, stream):
+    (xp,), (yp,), wp, wb, sp = _checked(fn, [db], [X], [Y], batch, ws, d_status, ("X", "Y"))
+    _check(getattr(load(), fn)(db.ref, xp, batch, yp, wp, wb, sp, _stream_ptr(stream)), fn)
+
+
 def lw_decode_gemv(db: DeviceBundle, x, y, ws, d_status, stream=None) -> None:
-    _check(load().lw_decode_gemv(db.ref, _tp(x), _tp(y), _tp(ws), ws.numel() * ws.element_size(),
-                                 _tp(d_status), _stream_ptr(stream)), "lw_decode_gemv")
+    _gemv("lw_decode_gemv", db, x, y, ws, d_status, stream)
 
 
 def lw_decode_gemm(db: DeviceBundle, X, batch, Y, ws, d_status, stream=None) -> None:
-    _check(load().lw_decode_gemm(db.ref, _tp(X), batch, _tp(Y), _tp(ws),
-                                 ws.numel() * ws.element_size(), _tp(d_status),
-                                 _stream_ptr(stream)), "lw_decode_gemm")
+    _gemm("lw_decode_gemm", db, X, batch, Y, ws, d_status, stream)
 
 
 def lw_twin_gemv(db: DeviceBundle, x, y, ws, d_status, stream=None) -> None:
-    _check(load().lw_twin_gemv(db.ref, _tp(x), _tp(y), _tp(ws), ws.numel() * ws.element_size(),
-                               _tp(d_status), _stream_ptr(stream)), "lw_twin_gemv")
+    _gemv("lw_twin_gemv", db, x, y, ws, d_status, stream)
 
 
 def lw_twin_gemm(db: DeviceBundle, X, batch, Y, ws, d_status, stream=None) -> None:
-    _check(load().lw_twin_gemm(db.ref, _tp(X), batch, _tp(Y), _tp(ws),
-                               ws.numel() * ws.element_size(), _tp(d_status),
-                               _stream_ptr(stream)), "lw_twin_gemm")
+    _gemm("lw_twin_gemm", db, X, batch, Y, ws, d_status, stream)
 
 
 def lw_decode_gemv_noalloc(db: DeviceBundle, x, y, d_status, stream=None) -> None:
     """lw_decode_gemv with the library's fixed device scratch instead of a
     caller workspace (allocates nothing)."""
-    _check(load().lw_decode_gemv_noalloc(db.ref, _tp(x), _tp(y), _tp(d_status),
-                                         _stream_ptr(stream)), "lw_decode_gemv_noalloc")
+    fn = "lw_decode_gemv_noalloc"
+    (xp,), (yp,), _, _, sp = _checked(fn, [db], [x], [y], 1, None, d_status)
+    _check(load().lw_decode_gemv_noalloc(db.ref, xp, yp, sp, _stream_ptr(stream)), fn)
 
 
 def _views(dbs):
@@ -489,19 +632,17 @@ def lw_workspace_bytes_group(dbs) -> int:
 
 
 def _gemv_group(fn, dbs, xs, ys, ws, d_status, stream):
+    xps, yps, wp, wb, sp = _checked(fn, dbs, xs, ys, 1, ws, d_status, indexed=True)
     n = len(dbs)
-    xa = (ctypes.c_void_p * n)(*[_tp(x) for x in xs])
-    ya = (ctypes.c_void_p * n)(*[_tp(y) for y in ys])
-    _check(getattr(load(), fn)(_views(dbs), n, xa, ya, _tp(ws), ws.numel() * ws.element_size(),
-                               _tp(d_status), _stream_ptr(stream)), fn)
+    xa, ya = (ctypes.c_void_p * n)(*xps), (ctypes.c_void_p * n)(*yps)
+    _check(getattr(load(), fn)(_views(dbs), n, xa, ya, wp, wb, sp, _stream_ptr(stream)), fn)
 
 
 def _gemm_group(fn, dbs, Xs, batch, Ys, ws, d_status, stream):
+    xps, yps, wp, wb, sp = _checked(fn, dbs, Xs, Ys, batch, ws, d_status, indexed=True)
     n = len(dbs)
-    xa = (ctypes.c_void_p * n)(*[_tp(x) for x in Xs])
-    ya = (ctypes.c_void_p * n)(*[_tp(y) for y in Ys])
-    _check(getattr(load(), fn)(_views(dbs), n, xa, batch, ya, _tp(ws), ws.numel() * ws.element_size(),
-                               _tp(d_status), _stream_ptr(stream)), fn)
+    xa, ya = (ctypes.c_void_p * n)(*xps), (ctypes.c_void_p * n)(*yps)
+    _check(getattr(load(), fn)(_views(dbs), n, xa, batch, ya, wp, wb, sp, _stream_ptr(stream)), fn)
 
 
 def lw_decode_gemm_group(dbs, Xs, batch, Ys, ws, d_status, stream=None) -> None:

@@ -73,8 +73,8 @@ def test_no_alloc_rejects_matrices_beyond_its_scratch():
     db = _bundle(m, lw.LW_FMT_Q4_PAIR)
     db.view.rows = 64 * 1024          # claims a matrix far larger than the scratch
     db.view.cols = 256 * 64
-    x = torch.zeros(256, dtype=torch.float32, device="cuda")
-    y = torch.zeros(64, dtype=torch.float32, device="cuda")
+    x = torch.zeros(db.view.cols, dtype=torch.float32, device="cuda")   # sized for the claim,
+    y = torch.zeros(db.view.rows, dtype=torch.float32, device="cuda")   # so only the scratch limit refuses
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(lw.LwError) as e:
         lw.lw_decode_gemv_noalloc(db, x, y, st)
