@@ -379,6 +379,28 @@ def time_steps(torch, stream, step_fn, steps, warmup, copies):
     return ev0.elapsed_time(ev1) / steps
 
 
+def percentiles(samples):
+    """p10, median and p90 of per-step times (linear interpolation between
+    order statistics, numpy's default)."""
+    a = np.asarray(samples, dtype=np.float64)
+    p10, med, p90 = np.percentile(a, [10, 50, 90])
+    return {"p10": float(p10), "median": float(med), "p90": float(p90), "steps": int(a.size)}
+
+
+def per_step_ms(torch, stream, step_fn, steps, copies):
+    """Each step timed alone: an event pair around every step on `stream`
+    (after the timed region; it does not enter `value`)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        step_fn(i % copies)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def run_ours(args):
     import torch
     from decode_gemv_gb300 import lw
@@ -484,6 +506,10 @@ def run_ours(args):
     ms = ev0.elapsed_time(ev1) / args.steps
     t_max = max_over_ranks(ms, dev)
     status = int(st.item())
+    # spread of the step time: every step timed alone, over as many steps
+    # as the timed region (at most 2000)
+    spread = percentiles(per_step_ms(torch, stream, lambda c: graphs[c].launch(stream),
+                                     max(1, min(args.steps, 2000)), copies))
     # diagnostic: each matrix's call alone (one graph per call, events around)
     per_mat = per_call_ms(torch, stream, [[(lambda c=c, j=j: call(c, j)) for j in range(n_mat)]
                                           for c in range(min(copies, 4))])
@@ -510,6 +536,8 @@ def run_ours(args):
                              f"({copies * layer_coded / 1e6:.0f} MB > 4x L2 {l2 / 1e6:.0f} MB)"},
             "b_eff_gbs": 2.0 * weights * world / (t_max * 1e-3) / 1e9,
             "hbm_frac_of_nominal_8tbs": value / world / 8000.0,
+            "step_ms_spread": dict(spread, note="each step timed alone with its own event pair, "
+                                                "after the timed region (not part of value)"),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": measured_traffic(names, [[mats[j]["spec"].name for j in g] for g in groups]),
                          "peak_kind": peak_kind,

@@ -46,3 +46,11 @@ def test_listed_bytes_counts_the_listed_tiles():
         words = sum(int(toff[(s + 1) * tk] - toff[s * tk]) * 128 for s in lst)
         per_tile = 64 + 64 + 256          # lane bits, lane mids, scales/mins
         assert bench.listed_bytes(hb, lst, k) == words + len(lst) * tk * per_tile + 4 * n_off + 1024
+
+
+def test_percentiles_of_step_times():
+    # 1..101 ms: the order statistics fall on whole values
+    s = bench.percentiles(np.arange(1, 102, dtype=np.float64)[::-1])
+    assert s == {"p10": 11.0, "median": 51.0, "p90": 91.0, "steps": 101}
+    one = bench.percentiles([0.25])
+    assert one["p10"] == one["median"] == one["p90"] == 0.25 and one["steps"] == 1
