@@ -54,3 +54,42 @@ def test_percentiles_of_step_times():
     assert s == {"p10": 11.0, "median": 51.0, "p90": 91.0, "steps": 101}
     one = bench.percentiles([0.25])
     assert one["p10"] == one["median"] == one["p90"] == 0.25 and one["steps"] == 1
+
+
+def _fake_layer():
+    rng = np.random.default_rng(0)
+    out = []
+    for name, n, k in (("a", 512, 256), ("b", 128, 1024), ("c", 256, 512)):
+        spec = SimpleNamespace(name=name, rows=n, cols=k)
+        m = dict(codes=rng.integers(0, 16, size=(n, k), dtype=np.uint8),
+                 scales=rng.integers(0, 1 << 14, size=(n, k // 256), dtype=np.uint16),
+                 mins=rng.integers(0, 1 << 14, size=(n, k // 256), dtype=np.uint16),
+                 x=rng.standard_normal((1, k)).astype(np.float32))
+        out.append((spec, m))
+    return out
+
+
+def test_oracle_shares_deal_every_strip_once():
+    mats = _fake_layer()
+    target = 3 * 64 * 1024 * 2          # two 64-row strips' worth of weights per matrix
+    one = bench.oracle_shares(mats, target, 1)[0]
+    for n in (1, 3, 5, 64):
+        shares = bench.oracle_shares(mats, target, n)
+        assert 1 <= len(shares) <= n
+        # per matrix, the strips dealt out are exactly the one-worker sample's rows
+        for j, (spec, m) in enumerate(mats):
+            got = np.concatenate([sub["codes"] for sh in shares for sub in sh
+                                  if sub["x"] is m["x"]] or [np.zeros((0, spec.cols), np.uint8)])
+            want = [sub["codes"] for sub in one if sub["x"] is m["x"]][0]
+            rows = sorted(map(bytes, got))
+            assert rows == sorted(map(bytes, want))
+        loads = [sum(sub["codes"].size for sub in sh) for sh in shares]
+        assert max(loads) - min(loads) <= 64 * max(s.cols for s, _ in mats)
+
+
+def test_oracle_all_cores_runs_every_share():
+    mats = _fake_layer()
+    r = bench.oracle_all_cores(mats, 3 * 64 * 1024, steps=1, warmup=0, cores=2)
+    assert r["cores"] == 2 and r["value"] > 0 and r["seconds_per_pass"] > 0
+    assert r["weights"] == sum(min(s.rows, max(64, (64 * 1024 // s.cols) // 64 * 64)) * s.cols
+                               for s, _ in mats)
