@@ -830,8 +830,10 @@ def extras(args, torch, lw, dev, mats, copies, xs, ys, ws, st, stream, line, cod
                    "note": f"wall clock per step: one packed H2D of the activations, the step's "
                            f"{len(groups)} library calls, one packed D2H of the results, a stream "
                            f"sync; rotating over the {copies} device copies of the layer"}
-    # the oracle on the host, bounded samples (a few seconds of work per core)
-    line["cpu_baseline"] = cpu_baseline_entry([(x["spec"], x["m"]) for x in mats])
+    # the oracle on the host, bounded samples (a few seconds of work per
+    # core); one process per GPU shares the host's cores, so only at N = 1
+    if int(os.environ.get("WORLD_SIZE", "1")) == 1:
+        line["cpu_baseline"] = cpu_baseline_entry([(x["spec"], x["m"]) for x in mats])
 
 
 # ----------------------------------------------------------------------------
