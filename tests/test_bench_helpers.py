@@ -93,3 +93,30 @@ def test_oracle_all_cores_runs_every_share():
     assert r["cores"] == 2 and r["value"] > 0 and r["seconds_per_pass"] > 0
     assert r["weights"] == sum(min(s.rows, max(64, (64 * 1024 // s.cols) // 64 * 64)) * s.cols
                                for s, _ in mats)
+
+
+def test_reference_arm_prints_one_json_line(monkeypatch, capsys):
+    """bench.py --impl reference on a small stand-in layer: one JSON line with
+    the contract's keys, the oracle on every host core and on one."""
+    import json
+    monkeypatch.setattr(bench, "layer_matrices", _fake_layer)
+    monkeypatch.setenv("RANK", "0")
+    args = SimpleNamespace(steps=2, warmup=1, gpus=1, impl="reference")
+    assert bench.run_reference(args) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 2
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["single_core"]["cores"] == 1 and cb["single_core"]["value"] > 0
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setattr(bench, "layer_matrices", lambda: (_ for _ in ()).throw(AssertionError))
+    assert bench.run_reference(SimpleNamespace(steps=2, warmup=1, gpus=2, impl="reference")) == 0
+    assert capsys.readouterr().out == ""
