@@ -589,6 +589,19 @@ extern "C" lw_status lw_validate_sections(const lw_desc* d, const lw_sections* s
     return fail(LW_ERR_CORRUPT, "word count does not match tile_off");
   const lw_table* tb = (const lw_table*)s->ptr[LW_SEC_TABLE];
   if (tb->fmt != d->fmt) return fail(LW_ERR_CORRUPT, "table format mismatch");
+  if (d->twin) {
+    // a twin reads no code from its table: only the alphabet and, for BF16,
+    // the palette that maps its 4-bit indices back to exponent bytes
+    const int alpha = d->fmt == LW_FMT_Q4_PAIR ? 256 : (d->fmt == LW_FMT_Q6 ? 64 : 16);
+    if (tb->alpha != alpha) return fail(LW_ERR_CORRUPT, "twin table alphabet %d", tb->alpha);
+    if (d->fmt == LW_FMT_BF16_EXP) {
+      if (tb->n_palette < 1 || tb->n_palette > 16)
+        return fail(LW_ERR_CORRUPT, "twin palette size %d", tb->n_palette);
+      for (int i = 1; i < tb->n_palette; ++i)
+        if (tb->palette[i] <= tb->palette[i - 1])
+          return fail(LW_ERR_CORRUPT, "twin palette not ascending");
+    }
+  }
   if (!d->twin) {
     lw_table chk;
     lw_status st = lw_table_from_lengths(tb->fmt, tb->code_len, tb->alpha, tb->palette,

@@ -277,10 +277,12 @@ lw_status lw_table_from_lengths(int32_t fmt, const uint8_t* code_len,
                                 int32_t n_palette, lw_table* out);
 
 /*
- * Check the host sections of a coded bundle for consistency (tile offsets
+ * Check the host sections of a bundle for consistency (tile offsets
  * non-decreasing and within the word count, lane bit counts within W_t*32,
- * table well formed, BF16 verbatim offsets consistent).  Returns LW_OK or
- * LW_ERR_CORRUPT with the reason in lw_last_error().
+ * the table equal to the one its code lengths define -- for a twin, its
+ * alphabet and, for BF16, an ascending palette of 1..16 entries -- BF16
+ * verbatim offsets consistent).  Returns LW_OK or LW_ERR_CORRUPT with the
+ * reason in lw_last_error().
  */
 lw_status lw_validate_sections(const lw_desc* desc, const lw_sections* s);
 
