@@ -228,3 +228,34 @@ def test_single_symbol_and_all_verbatim_bundles():
     bits = (exp << 7) | (k % 128).astype(np.uint16)
     hb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, bits)
     assert hb.stats.n_verbatim == 64 * 4 and hb.stats.max_tile_rows == 0
+
+
+def test_host_calls_from_many_threads():
+    """The host builder keeps no shared mutable state: bundles encoded on
+    eight threads at once (ctypes releases the interpreter lock during the
+    call) are byte-for-byte the ones encoded one after another, and each
+    thread's failing call reports its own error text."""
+    from concurrent.futures import ThreadPoolExecutor
+    mats = [inputs.small_q4(40 + i, 128, 1024, sd=1.2 + 0.1 * i) for i in range(8)]
+
+    def enc(m):
+        hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"])
+        return {k: v.tobytes() for k, v in hb.sections.items()}
+
+    want = [enc(m) for m in mats]
+    with ThreadPoolExecutor(8) as ex:
+        got = list(ex.map(enc, mats * 2))
+    assert got == want * 2
+
+    def bad(i):
+        codes = np.full((64, 256 * (i + 1)), 16 + i, np.uint8)       # out of range
+        try:
+            lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, codes, np.zeros((64, i + 1), np.uint16),
+                                np.zeros((64, i + 1), np.uint16))
+        except lw.LwError as e:
+            return str(e)
+        return ""
+    with ThreadPoolExecutor(8) as ex:
+        msgs = list(ex.map(bad, range(8)))
+    for i, msg in enumerate(msgs):
+        assert f"code {16 + i} out of range" in msg, msg
