@@ -352,13 +352,18 @@ def run_reference(args):
               "sample": f"first row strips of all 7 matrices of the layer: {weights} weights, "
                         f"{coded} coded bytes per step; decode + dequant + fp64 GEMV"}
     layer = sum(sp.rows * sp.cols for sp, _ in mats)
-    allc = oracle_all_cores(mats, int(min(layer, weights * host_cores())), max(1, args.steps),
-                            max(0, args.warmup))
+    try:
+        allc = oracle_all_cores(mats, int(min(layer, weights * host_cores())), max(1, args.steps),
+                                max(0, args.warmup))
+        sample = (f"first row strips of all 7 matrices of the layer: {allc['weights']} weights, "
+                  f"{allc['coded_bytes']} coded bytes per step, cut into 64-row strips over "
+                  f"{allc['cores']} spawned processes (one per host core, started together each "
+                  f"step); decode + dequant + fp64 GEMV")
+    except Exception as e:  # noqa: BLE001 -- the one-core run still stands as the value
+        allc = {"value": single["value"], "seconds_per_pass": dt1, "cores": 1,
+                "weights": weights}
+        sample = single["sample"] + f" (all-cores run unavailable: {e})"
     gbs, dt = allc["value"], allc["seconds_per_pass"]
-    sample = (f"first row strips of all 7 matrices of the layer: {allc['weights']} weights, "
-              f"{allc['coded_bytes']} coded bytes per step, cut into 64-row strips over "
-              f"{allc['cores']} spawned processes (one per host core, started together each "
-              f"step); decode + dequant + fp64 GEMV")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",

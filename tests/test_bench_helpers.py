@@ -120,3 +120,17 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
     monkeypatch.setattr(bench, "layer_matrices", lambda: (_ for _ in ()).throw(AssertionError))
     assert bench.run_reference(SimpleNamespace(steps=2, warmup=1, gpus=2, impl="reference")) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_falls_back_to_one_core(monkeypatch, capsys):
+    import json
+
+    def broken(*a, **k):
+        raise RuntimeError("no workers")
+    monkeypatch.setattr(bench, "layer_matrices", _fake_layer)
+    monkeypatch.setattr(bench, "oracle_all_cores", broken)
+    monkeypatch.setenv("RANK", "0")
+    assert bench.run_reference(SimpleNamespace(steps=1, warmup=0, gpus=1, impl="reference")) == 0
+    d = json.loads(capsys.readouterr().out.strip())
+    assert d["cpu_baseline"]["cores"] == 1 and d["value"] == d["cpu_baseline"]["single_core"]["value"]
+    assert "unavailable: no workers" in d["cpu_baseline"]["sample"]
