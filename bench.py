@@ -961,6 +961,8 @@ def run_sweep(args):
     group = 64 if copies >= 128 else 1
     ngraph = max(1, copies // group)
 
+    last = {}
+
     def timed(calls_of_copy, steps=None):
         graphs = [layer_graph(torch, [f for c in range(g * group, (g + 1) * group)
                                       for f in calls_of_copy(c)]) for g in range(ngraph)]
@@ -969,6 +971,9 @@ def run_sweep(args):
             steps = max(10, min(args.steps, int(2000.0 / max(one, 1e-3))))
         reps = max(3, steps // group)
         t = time_steps(torch, stream, lambda i: graphs[i].replay(), reps, 5, ngraph) / group
+        # spread: every replay timed alone afterwards (per step of the graph)
+        last["spread"] = percentiles([v / group for v in per_step_ms(
+            torch, stream, lambda i: graphs[i].replay(), reps, ngraph)])
         del graphs
         return t, steps
 
@@ -1013,6 +1018,7 @@ def run_sweep(args):
         gc = lambda d, x, y, w, s_: lw.lw_decode_gemm_group(d, x, B, y, w, s_)
         gt = lambda d, x, y, w, s_: lw.lw_twin_gemm_group(d, x, B, y, w, s_)
         t_coded, steps = timed(lambda c: step_calls(c, "db", lw.lw_decode_gemm, gc))
+        spread_coded = last["spread"]
         t_twin, _ = timed(lambda c: step_calls(c, "tw", lw.lw_twin_gemm, gt), steps)
         xb = [x.to(torch.bfloat16) for x in xs]
         yb = [torch.empty(B, m["spec"].rows, device=dev, dtype=torch.bfloat16) for m in mats]
@@ -1030,7 +1036,7 @@ def run_sweep(args):
                          "ms_per_step": t_coded, "coded_gbs": gbs,
                          "frac_of_hbm": gbs / peak, "b_eff_gbs": 2.0 * weights / (t_coded * 1e-3) / 1e9,
                          "twin_ms": t_twin, "twin_gbs": twin_step / (t_twin * 1e-3) / 1e9,
-                         "speedup_vs_twin": t_twin / t_coded,
+                         "speedup_vs_twin": t_twin / t_coded, "ms_spread": spread_coded,
                          "bf16_ms": t_bf16, "speedup_vs_bf16": t_bf16 / t_coded,
                          "coded_bytes_per_step": coded_step, "steps": steps})
         if t_full is not None:

@@ -134,3 +134,54 @@ def test_reference_arm_falls_back_to_one_core(monkeypatch, capsys):
     d = json.loads(capsys.readouterr().out.strip())
     assert d["cpu_baseline"]["cores"] == 1 and d["value"] == d["cpu_baseline"]["single_core"]["value"]
     assert "unavailable: no workers" in d["cpu_baseline"]["sample"]
+
+
+class _FakeCuda:
+    """Just enough of torch.cuda for bench's timing helpers on the CPU: events
+    read a counter that every step advances by the step's index + 1 ms."""
+
+    def __init__(self):
+        self.now = 0.0
+
+    def Event(self, enable_timing=True):
+        cuda = self
+
+        class E:
+            def record(self, stream=None):
+                self.t = cuda.now
+
+            def elapsed_time(self, other):
+                return other.t - self.t
+        return E()
+
+    def synchronize(self):
+        pass
+
+    def CUDAGraph(self):
+        return SimpleNamespace(replay=lambda: None)
+
+    def graph(self, g):
+        import contextlib
+        return contextlib.nullcontext()
+
+
+def test_timing_helpers_with_a_fake_device():
+    cuda = _FakeCuda()
+    torch = SimpleNamespace(cuda=cuda)
+    seen = []
+
+    def step(c):
+        seen.append(c)
+        cuda.now += 1.0 + c          # copy c takes c + 1 ms
+    # mean over steps rotating over 3 copies: (1 + 2 + 3) / 3
+    assert bench.time_steps(torch, None, step, steps=6, warmup=2, copies=3) == 2.0
+    assert seen[:2] == [0, 1] and seen[2:] == [0, 1, 2, 0, 1, 2]
+    ms = bench.per_step_ms(torch, None, step, steps=4, copies=2)
+    assert ms == [1.0, 2.0, 1.0, 2.0]
+    sp = bench.percentiles(ms)
+    assert sp["median"] == 1.5 and sp["steps"] == 4
+    # a layer graph: the calls run once eagerly, then once more, in order,
+    # under the capture
+    calls = []
+    bench.layer_graph(torch, [lambda: calls.append("a"), lambda: calls.append("b")])
+    assert calls == ["a", "b", "a", "b"]
