@@ -235,6 +235,8 @@ lw_status lw_encode_bundle(const lw_desc* desc, const void* payload,
 /* Section pointers and sizes of a bundle (valid until lw_bundle_free). */
 lw_status lw_bundle_sections(const lw_bundle* b, lw_sections* out);
 
+/* Free a bundle and every section it owns (NULL is allowed); pointers
+   obtained from lw_bundle_sections become invalid. */
 void lw_bundle_free(lw_bundle* b);
 
 /* Format, twin flag and shape of a bundle (e.g. one just loaded). */
@@ -286,8 +288,13 @@ lw_status lw_table_from_lengths(int32_t fmt, const uint8_t* code_len,
  */
 lw_status lw_validate_sections(const lw_desc* desc, const lw_sections* s);
 
-/* Device workspace the product calls need for `batch` activation rows: the
-   per-tile partial sums, fp32 [K/256][batch][N].  0 for lw_decode. */
+/* Bytes of device workspace a product call on this bundle needs for
+   `batch` activation rows: the per-strip counters (N/64 uint32, padded to
+   256 bytes; zeroed by the caller before first use and left at zero by
+   every call that completes), then the split-K partial sums (fp32
+   [K/256][min(batch, 8)][N], or the tensor-core path's K-split partials
+   where that is larger).  lw_decode takes no workspace.  0 for a NULL view,
+   batch < 1 or a non-positive shape. */
 size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch);
 
 /*
@@ -475,7 +482,12 @@ lw_status lw_decode_gemv_noalloc(const lw_dev_bundle* b, const void* x, float* y
                                  int32_t* d_status, void* stream);
 size_t lw_noalloc_scratch_bytes(void);
 
+/* The status's name ("LW_OK", "LW_ERR_SHAPE", ...; "unknown lw_status" for
+   other values): a static string, never NULL, not to be freed. */
 const char* lw_status_string(lw_status s);
+/* The calling thread's text for its last failing host call (the reason a
+   status was returned; calls that succeed may leave it unchanged).  Owned
+   by the library, valid until the thread's next library call. */
 const char* lw_last_error(void);
 
 /*
