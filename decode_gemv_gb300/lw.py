@@ -347,6 +347,8 @@ def _stream_ptr(stream):
 
 
 def _tp(t):
+    """A tensor's address, unchecked (for callers that drive the C functions
+    directly and check their buffers themselves)."""
     return ctypes.c_void_p(t.data_ptr())
 
 
