@@ -292,9 +292,10 @@ lw_status lw_validate_sections(const lw_desc* desc, const lw_sections* s);
    `batch` activation rows: the per-strip counters (N/64 uint32, padded to
    256 bytes; zeroed by the caller before first use and left at zero by
    every call that completes), then the split-K partial sums (fp32
-   [K/256][min(batch, 8)][N], or the tensor-core path's K-split partials
-   where that is larger).  lw_decode takes no workspace.  0 for a NULL view,
-   batch < 1 or a non-positive shape. */
+   [K/256][8][N]: room for a full CUDA-core pass of 8 rows whatever
+   `batch`, or the tensor-core path's K-split partials where that path is
+   taken and they are larger).  lw_decode takes no workspace.  0 for a NULL
+   view, batch < 1 or a non-positive shape. */
 size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch);
 
 /*

@@ -259,3 +259,29 @@ def test_host_calls_from_many_threads():
         msgs = list(ex.map(bad, range(8)))
     for i, msg in enumerate(msgs):
         assert f"code {16 + i} out of range" in msg, msg
+
+
+def test_workspace_bytes_follow_the_documented_layout():
+    """lw_workspace_bytes = per-strip counters (N/64 uint32, padded to 256
+    bytes) + fp32 partial sums [K/256][8][N]; BF16 products of 16 or more
+    rows use the tensor-core K-split partials [min(max(K/512, 1), 32)][64][N]
+    when larger.  Host arithmetic only: the view's addresses are never used."""
+    lib = lw.load()
+    for fmt in (lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6, lw.LW_FMT_BF16_EXP):
+        for n, k in ((64, 256), (192, 768), (4096, 4096), (14336, 4096), (4096, 14336)):
+            v = lw.LwDevBundle()
+            v.fmt, v.twin, v.rows, v.cols = fmt, 0, n, k
+            counters = (n // 64 * 4 + 255) // 256 * 256
+            part = (k // 256) * 8 * n * 4
+            for batch in (1, 2, 5):
+                assert lib.lw_workspace_bytes(ctypes.byref(v), batch) == counters + part
+            if fmt == lw.LW_FMT_BF16_EXP:
+                splits = min(max(k // 512, 1), 32)
+                want = counters + max(part, splits * 64 * n * 4)
+                assert lib.lw_workspace_bytes(ctypes.byref(v), 16) == want
+                v.twin = 1                      # the twin stays on the CUDA cores
+                assert lib.lw_workspace_bytes(ctypes.byref(v), 16) == counters + part
+    v = lw.LwDevBundle()
+    v.fmt, v.rows, v.cols = lw.LW_FMT_Q4_PAIR, 64, 256
+    assert lib.lw_workspace_bytes(ctypes.byref(v), 0) == 0
+    assert lib.lw_workspace_bytes(None, 1) == 0
