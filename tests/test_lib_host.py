@@ -285,3 +285,22 @@ def test_workspace_bytes_follow_the_documented_layout():
     v.fmt, v.rows, v.cols = lw.LW_FMT_Q4_PAIR, 64, 256
     assert lib.lw_workspace_bytes(ctypes.byref(v), 0) == 0
     assert lib.lw_workspace_bytes(None, 1) == 0
+
+
+def test_group_workspace_is_the_members_slices():
+    """lw_workspace_bytes_group = the sum over the members of their one-row
+    workspace rounded up to 256 bytes (consecutive slices); 0 for an empty,
+    oversized or NULL-holding group."""
+    lib = lw.load()
+    views = []
+    for n, k in ((4096, 4096), (1024, 4096), (192, 768)):
+        v = lw.LwDevBundle()
+        v.fmt, v.rows, v.cols = lw.LW_FMT_Q4_PAIR, n, k
+        views.append(v)
+    arr = (ctypes.c_void_p * 3)(*[ctypes.addressof(v) for v in views])
+    want = sum((lib.lw_workspace_bytes(ctypes.byref(v), 1) + 255) // 256 * 256 for v in views)
+    assert lib.lw_workspace_bytes_group(arr, 3) == want
+    assert lib.lw_workspace_bytes_group(arr, 0) == 0
+    assert lib.lw_workspace_bytes_group(arr, 9) == 0
+    arr[1] = None
+    assert lib.lw_workspace_bytes_group(arr, 3) == 0
