@@ -104,8 +104,8 @@ lw_status check_dev_bundle(const lw_dev_bundle* b, bool want_twin, bool product)
   if (b->fmt != LW_FMT_BF16_EXP) {
     if (product && (!b->qparams || !aligned16(b->qparams)))
       return fail(LW_ERR_INVALID_ARG, "qparams missing or not 16-byte aligned");
-  } else if (!b->signman || !b->vflags || !b->vrow_off || !aligned16(b->signman) ||
-             (!b->vexp && b->twin == 0 && false)) {
+  } else if (!b->signman || !b->vflags || !b->vrow_off || !aligned16(b->signman)) {
+    // vexp may be NULL: a matrix without verbatim groups has no such section
     return fail(LW_ERR_INVALID_ARG, "BF16 side sections missing or misaligned");
   }
   return LW_OK;
