@@ -1,7 +1,9 @@
 """Thin Python binding of liblw (the C ABI in include/lw.h).
 
-Argument marshalling only: every step of the path runs in liblw's host code or
-CUDA kernels.  PyTorch is used for device memory and streams.  If the compiled
+Argument marshalling and checks only: every step of the path runs in liblw's
+host code or CUDA kernels.  Each tensor is checked (dtype, contiguity, size,
+device) before its address crosses the ABI, since the C calls cannot see
+them.  PyTorch is used for device memory and streams.  If the compiled
 library is missing this module raises at load time -- there is no fallback.
 Functions carry the C names; see include/lw.h for the contract of each.
 """
