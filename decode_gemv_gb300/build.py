@@ -19,7 +19,8 @@ INC = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "liblw.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU = ["lw_api.cu", "lw_q.cu", "lw_bf16.cu", "lw_noalloc.cu", "lw_trans.cu", "lw_strips.cu"]
+CU = ["lw_api.cu", "lw_q.cu", "lw_qlut.cu", "lw_bf16.cu", "lw_noalloc.cu", "lw_trans.cu",
+      "lw_strips.cu"]
 CPP = ["lw_host.cpp", "lw_file.cpp"]
 
 

@@ -95,8 +95,9 @@ lw_status check_dev_bundle(const lw_dev_bundle* b, bool want_twin, bool product)
   if ((!b->words && b->max_tile_rows > 0) || !b->tile_off || !b->lane_bits || !b->table)
     return fail(LW_ERR_INVALID_ARG, "missing words/tile_off/lane_bits/table");
   if (!b->twin && !b->lane_mid) return fail(LW_ERR_INVALID_ARG, "missing lane_mid");
-  if (!aligned16(b->words) || !aligned16(b->table) || !aligned16(b->lane_mid))
-    return fail(LW_ERR_INVALID_ARG, "words, table and lane_mid must be 16-byte aligned");
+  if (!aligned16(b->words) || !aligned16(b->table) || !aligned16(b->lane_mid) ||
+      !aligned16(b->lane_bits))
+    return fail(LW_ERR_INVALID_ARG, "words, lane_bits, table and lane_mid must be 16-byte aligned");
   if (b->max_tile_rows < 0 || b->max_tile_rows > 1024)
     return fail(LW_ERR_INVALID_ARG, "max_tile_rows %d out of range", b->max_tile_rows);
   if (!b->twin && (b->lmin < 1 || b->lmax > LW_MAX_CODE_LEN || b->lmin > b->lmax))

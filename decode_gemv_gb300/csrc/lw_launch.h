@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include "lw_internal.h"
+#include "lw_lut.h"
 
 namespace lw {
 
@@ -100,6 +101,14 @@ inline uint32_t* workspace_counters(const lw_dev_bundle* b, void* ws) {
 inline float* workspace_partials(const lw_dev_bundle* b, void* ws) {
   return reinterpret_cast<float*>(static_cast<char*>(ws) + workspace_counter_bytes(b));
 }
+
+// Table-driven 4-/6-bit product kernel (and the fixed-width twins on the same
+// skeleton): usable for a coded bundle whose lut_entries hint is 1..kLutCap.
+bool lut_fits(const lw_dev_bundle* b);
+// With a strip list (device array of n_strips 64-row strips), n must be 1.
+lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,
+                       float* const* y, void* const* ws, int32_t* status, cudaStream_t st,
+                       const int32_t* strips = nullptr, int n_strips = 0);
 
 // ws: the caller's whole workspace (counters, then partial sums)
 lw_status launch_q_product(const lw_dev_bundle* b, const float* x, int batch, float* y, void* ws,

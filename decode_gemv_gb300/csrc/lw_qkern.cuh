@@ -85,13 +85,14 @@ struct QLaunch {
   int n;
 };
 
-// Tile of the bundle behind list tile lt: with a strip list, entry lt / TK
-// names the strip and lt % TK the tile column.  An entry outside the
+// Tile of the bundle behind list tile lt: with a strip list (a.strips not
+// NULL), entry lt / TK names the strip and lt % TK the tile column; without
+// one, lt itself.  An entry outside the
 // matrix, or not above the previous entry, is invalid (ok = false): it maps
 // to a tile of strip 0, which is read but whose results are dropped.
 template <bool STRIPS>
 __device__ __forceinline__ int list_tile(const QArgs& a, int lt, bool& ok) {
-  if (!STRIPS) {
+  if (!STRIPS || !a.strips) {
     ok = true;
     return lt;
   }

@@ -1,0 +1,152 @@
+// Launcher of the table-driven 4-/6-bit product kernel (lw_qlut.cuh) and of
+// its fixed-width-twin instantiations.
+#include <mutex>
+
+#include "lw_internal.h"
+#include "lw_launch.h"
+#include "lw_qlut.cuh"
+
+namespace lw {
+
+namespace {
+
+using LKernel = void (*)(const dev::LLaunch);
+
+template <int FMT, bool TWIN>
+LKernel pick_lut(int bp) {
+  switch (bp) {
+    case 1: return dev::q_lut_kernel<FMT, TWIN, 1>;
+    case 2: return dev::q_lut_kernel<FMT, TWIN, 2>;
+    case 4: return dev::q_lut_kernel<FMT, TWIN, 4>;
+    default: return dev::q_lut_kernel<FMT, TWIN, 8>;
+  }
+}
+
+// Largest dynamic shared memory a CTA may use on the current device.
+int max_dyn_smem() {
+  static std::mutex mu;
+  static int cache[128] = {0};
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 128) return 0;
+  std::lock_guard<std::mutex> g(mu);
+  if (!cache[d]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    cache[d] = v > 0 ? v : 1;
+  }
+  return cache[d];
+}
+
+}  // namespace
+
+bool lut_fits(const lw_dev_bundle* b) {
+  return b->twin || (b->lut_entries >= 1 && b->lut_entries <= kLutCap);
+}
+
+lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,
+                       float* const* y, void* const* ws, int32_t* status, cudaStream_t st,
+                       const int32_t* strips, int n_strips) {
+  const int fmt = bs[0]->fmt;
+  const bool twin = bs[0]->twin != 0;
+  const int bp = batch <= 1 ? 1 : (batch <= 2 ? 2 : (batch <= 4 ? 4 : 8));
+  LKernel k = fmt == LW_FMT_Q4_PAIR ? (twin ? pick_lut<dev::kQ4, true>(bp) : pick_lut<dev::kQ4, false>(bp))
+                                    : (twin ? pick_lut<dev::kQ6, true>(bp) : pick_lut<dev::kQ6, false>(bp));
+  int max_rows = 0;
+  long long total = 0;
+  // tiles of each matrix (with a strip list, a single matrix: its listed strips')
+  auto n_tiles = [&](int i) -> long long {
+    return strips ? (long long)n_strips * (bs[i]->cols / 256) : tiles_of(bs[i]->rows, bs[i]->cols);
+  };
+  for (int i = 0; i < n; ++i) {
+    max_rows = bs[i]->max_tile_rows > max_rows ? bs[i]->max_tile_rows : max_rows;
+    total += n_tiles(i);
+  }
+  if (total < 1) return LW_OK;
+  if (total > (1ll << 30)) return fail(LW_ERR_SHAPE, "group too large");
+  dev::LLaunch g{};
+  g.n = n;
+  // stage: coded rows (a stream reads up to two rows past its last word) |
+  // scales/mins | mid offsets | lane bit counts | activation slices | "fits"
+  // flag
+  g.stage_rows = max_rows + 2;
+  g.qp_off = g.stage_rows * 128;
+  g.mid_off = g.qp_off + qparam_tile_bytes(fmt);
+  g.lb_off = g.mid_off + 64;
+  g.x_off = g.mid_off + (twin ? 0 : 128);
+  g.stage_bytes = (g.x_off + bp * 1024 + 16 + 127) / 128 * 128;
+  g.ring_off = (dev::kLHdrBytes + 127) / 128 * 128;
+  // the decode table: the largest member's entries (the device checks each
+  // table against it), and at least the rows a corrupt stream of the last
+  // stage could read past it
+  int lut_cap = 0;
+  for (int i = 0; i < n; ++i) lut_cap = bs[i]->lut_entries > lut_cap ? bs[i]->lut_entries : lut_cap;
+  if (lut_cap < dev::kLGuardRows) lut_cap = dev::kLGuardRows;
+  g.lut_cap = lut_cap;
+  const int lut_bytes = twin ? 0 : lut_cap * 128;
+  const int budget = max_dyn_smem();
+  int S = (budget - g.ring_off - lut_bytes) / g.stage_bytes;
+  if (S > dev::kLMaxStages) S = dev::kLMaxStages;
+  S -= S % dev::kLProducers;   // every stage has one producer: stage s, producer s mod 4
+  if (S < 2 * dev::kLProducers)
+    return fail(LW_ERR_UNSUPPORTED, "tiles of %d rows do not fit the table-driven kernel", max_rows);
+  g.nstage = S;
+  g.lut_off = g.ring_off + S * g.stage_bytes;
+  const size_t smem = (size_t)g.lut_off + (size_t)lut_bytes;
+  // CTAs: one per SM, shared among the matrices in proportion to their tiles
+  const int G = device_sm_count();
+  int left = G;
+  int max_per_cta = 1;
+  g.cfirst[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    const long long t = n_tiles(i);
+    int c;
+    if (i == n - 1) {
+      c = left;
+    } else {
+      c = (int)((t * G + total / 2) / total);
+      const int reserve = n - 1 - i;   // at least one CTA for each later matrix
+      if (c > left - reserve) c = left - reserve;
+    }
+    if (c < 1) c = 1;
+    if (c > t) c = (int)t;   // no idle CTAs beyond one per tile
+    left -= c;
+    g.cfirst[i + 1] = g.cfirst[i] + c;
+    const int per = (int)((t + c - 1) / c);
+    max_per_cta = per > max_per_cta ? per : max_per_cta;
+  }
+  const int grid = g.cfirst[n];
+  // consumer warps: at most 16 and four fewer than stages (copies in flight
+  // while every warp decodes), and no more than a CTA has tiles; warps take tiles as they free
+  // up, so the tiles of a CTA need not divide evenly among them
+  int nw = S - 4 < 16 ? S - 4 : 16;
+  if (nw > max_per_cta) nw = max_per_cta;
+  if (nw < 1) nw = 1;
+  for (int i = 0; i < n; ++i) {
+    const lw_dev_bundle* b = bs[i];
+    dev::QArgs& a = g.m[i];
+    a.words = b->words;
+    a.tile_off = b->tile_off;
+    a.lane_bits = b->lane_bits;
+    a.lane_mid = twin ? nullptr : b->lane_mid;
+    a.table = b->table;
+    a.qparams = static_cast<const uint8_t*>(b->qparams);
+    a.strips = strips;
+    a.x = x[i];
+    a.ws = workspace_partials(b, ws[i]);
+    a.counters = workspace_counters(b, ws[i]);
+    a.y = y[i];
+    a.status = status;
+    a.TK = (int)(b->cols / 256);
+    a.N = (int)b->rows;
+    a.K = (int)b->cols;
+    a.n_tiles = (int)n_tiles(i);
+    a.batch = batch;
+  }
+  const int threads = (nw + dev::kLProducers) * 32;
+  if (resident_blocks((const void*)k, threads, smem) < 1)
+    return fail(LW_ERR_UNSUPPORTED, "table-driven kernel does not fit on an SM (%zu bytes)", smem);
+  launch_pdl(k, grid, threads, smem, st, g);
+  return check_launch("table-driven product kernel");
+}
+
+}  // namespace lw

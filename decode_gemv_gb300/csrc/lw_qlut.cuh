@@ -1,0 +1,665 @@
+// Table-driven fused decode + GEMV / small-batch GEMM for 4-bit (pair-coded)
+// and 6-bit Huffman-coded weights, and the same skeleton for their
+// fixed-width twins.
+//
+// Method: "LazyWeights: Decode-on-Demand Edge LLMs" -- "2 . Code them" and
+// Fig. 3(a) (64x256 tiles of 32 interleaved lanes of two rows), "3 . Decode on
+// demand" (per lane: an 11-bit peek of the stream selects the codeword; the
+// lane then shifts by its length) and the runtime paragraph after Fig. 3
+// (software decode fused into the GEMV; the fixed-width twin as the
+// decode-free comparator).
+//
+// GB300 mapping (ours):
+//  * one persistent CTA per SM: four producer warps and NW consumer warps.
+//    The producers fill a ring of S tile stages in shared memory with bulk
+//    asynchronous copies (TMA engine, no multicast) -- a tile's coded rows,
+//    its scales/mins, its lanes' mid offsets and bit counts and its slices of
+//    the activations -- each stage completing on a "full" mbarrier (four
+//    issuers: one thread's bulk copies alone reach about half of HBM's
+//    bandwidth); a consumer warp takes the next tile (a shared counter),
+//    waits for the stage to be announced for that tile and then for its
+//    barrier, decodes it and releases the stage on its "empty" mbarrier.
+//    Every wait is bounded.
+//  * a consumer warp decodes a whole tile: lane l runs the lane's two rows
+//    (2l from the start of its stream, 2l + 1 from its mid offset) as two
+//    interleaved streams, so both rows share the activation loads;
+//  * decoding is a lookup: the peek indexes a compact table (lw_lut.h) in
+//    shared memory that is replicated once per lane -- lane l's copy of an
+//    entry sits in bank l, so a warp's 32 lookups are one conflict-free
+//    shared-memory wavefront whatever symbols the lanes decode.  An entry
+//    holds the code length (bits 0..7), and the symbol's weights in the form
+//    the product consumes: 4-bit pairs carry the even column's code as a
+//    byte (bits 8..15, turned into the fp32 128 + c by one byte permute) and
+//    the odd column's code as the fp16 1024 + c (bits 16..31, turned into
+//    the exact fp32 c by one mixed-precision add, which runs on the FMA
+//    pipes and keeps the integer ALU pipe -- the decoder's bottleneck -- for
+//    the bit work); 6-bit codes carry only the fp16 form;
+//  * one 32-bit window serves two symbols (an 11-bit code leaves at least 21
+//    valid bits): window = funnel shift of two stream words by the bit
+//    position; the second peek comes from the window shifted by the first
+//    length; the position advances by both lengths and the words by at most
+//    one per step, branch-free (the next word is reloaded every step);
+//  * products in packed fp32 FMA (FFMA2): even and odd columns in the two
+//    halves, then per row and tile part = scale * ((acc.x - 128 X_even) +
+//    acc.y) + min * X (4-bit) or, per 16-weight group, scale * (acc.x +
+//    acc.y - 32 X_group) (6-bit), in a fixed order; the twin executes the
+//    same floating-point operations on the same values, so the twin's y is
+//    bitwise equal to the coded y;
+//  * split-K: each tile's partial sums go to the workspace; the last tile of
+//    a 64-row strip to finish (an atomicInc counter that wraps back to zero)
+//    adds them in ascending tile order -- one launch, deterministic;
+//  * stream reads never leave shared memory: a stream starts inside its
+//    stage and advances at most one 128-byte row per two symbols, and the
+//    stages are followed by the table (or, without a table, by a guard), so
+//    even a corrupt stream reads only this CTA's shared memory; it then
+//    fails its length check.
+#pragma once
+
+#include "lw_dev.cuh"
+#include "lw_lut.h"
+#include "lw_qkern.cuh"
+
+namespace lw {
+namespace dev {
+
+// One launch: up to kMaxGroup matrices of one format; the CTAs are
+// partitioned among them (CTA c serves matrix m when cfirst[m] <= c <
+// cfirst[m + 1]), each CTA walking its matrix's tiles c', c' + cnt, ...
+struct LLaunch {
+  QArgs m[kMaxGroup];
+  int cfirst[kMaxGroup + 1];
+  int n;
+  int nstage;       // S: stages in the ring
+  int stage_bytes;  // bytes per stage (multiple of 128)
+  int stage_rows;   // rows of 128 B of coded words a stage holds
+  int qp_off;       // offsets inside a stage: scales/mins, mid offsets, activations
+  int mid_off;
+  int lb_off;       // lane bit counts (coded bundles)
+  int x_off;
+  int ring_off;     // shared-memory offset of stage 0
+  int lut_off;      // shared-memory offset of the decode table (coded bundles)
+  int lut_cap;      // entries it holds (>= every member's table)
+};
+
+// Shared-memory header (bytes).
+constexpr int kLHdrNext = 0;     // int: next local tile to hand out
+constexpr int kLHdrErr = 4;      // int: set when any warp gives up
+constexpr int kLHdrTab = 8;      // uint64 mbarrier: table copy
+constexpr int kLHdrBar = 64;     // uint64 mbarriers: full[S], then empty[S]
+constexpr int kLMaxStages = 32;
+constexpr int kLRawTab = kLHdrBar + 16 * kLMaxStages;   // 576: the staged lw_table
+constexpr int kLHdrTiles = kLRawTab + (int)sizeof(lw_table);   // int[S]: tile each stage is armed for
+constexpr int kLHdrBytes = kLHdrTiles + 4 * kLMaxStages;
+constexpr int kLGuardRows = 132;  // rows a corrupt 6-bit stream may read past its stage
+constexpr int kLProducers = 4;    // producer warps (each issues its own stages' copies)
+
+__device__ __forceinline__ uint32_t shf_l_wrap(uint32_t lo, uint32_t hi, uint32_t n) {
+  uint32_t d;
+  asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(lo), "r"(hi), "r"(n));
+  return d;
+}
+__device__ __forceinline__ uint32_t shf_r_clamp(uint32_t lo, uint32_t hi, uint32_t n) {
+  uint32_t d;
+  asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(lo), "r"(hi), "r"(n));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// exact fp32 value of the fp16 in the high half of e, plus c
+__device__ __forceinline__ float f16hi_plus(uint32_t e, float c) {
+  float f;
+  asm("{.reg .b16 h; mov.b32 {_, h}, %1; add.rn.f32.f16 %0, h, %2;}" : "=f"(f) : "r"(e), "f"(c));
+  return f;
+}
+__device__ __forceinline__ float f16lo_plus(uint32_t e, float c) {
+  float f;
+  asm("{.reg .b16 h; mov.b32 {h, _}, %1; add.rn.f32.f16 %0, h, %2;}" : "=f"(f) : "r"(e), "f"(c));
+  return f;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Table entry of a 4-bit pair symbol / a 6-bit code of length L.
+__device__ __forceinline__ uint32_t lut_entry(int fmt, uint32_t sym, int L) {
+  if (fmt == LW_FMT_Q4_PAIR)
+    return ((0x6400u | ((sym >> 4) & 15u)) << 16) | ((sym & 15u) << 8) | (uint32_t)L;
+  return ((0x6400u | (sym & 63u)) << 16) | (uint32_t)L;
+}
+
+// Build the replicated table of a checked, staged lw_table: consumer warp w
+// takes entries 32 w .. 32 w + 31, then 32 (w + NW) .., ...; lane j decodes
+// entry i0 + j, then every entry of the group is broadcast and each lane
+// stores its own copy (lane l's copy of entry i at table + 128 i + 4 l).
+__device__ __forceinline__ void lut_build(const lw_table* tb, const LutShape& sh, uint32_t lut,
+                                          int warp, int nw, int lane) {
+  const int lmin = tb->lmin, lmax = tb->lmax;
+  for (int i0 = warp * 32; i0 < sh.n; i0 += nw * 32) {
+    // lane j decodes entry i0 + j
+    uint32_t e = 0;
+    const int i = i0 + lane;
+    if (i < sh.n) {
+      const uint32_t win = (uint32_t)lut_peek(sh, i) << 21;
+      int L = lmin;
+      while (L < lmax && win > tb->lim_m1[L - lmin]) ++L;
+      const int idx = (int)(win >> (32 - L)) + tb->off[L - lmin];
+      e = lut_entry(tb->fmt, tb->sym[idx], L);
+    }
+    const int cnt = sh.n - i0 < 32 ? sh.n - i0 : 32;
+    for (int j = 0; j < cnt; ++j) {
+      const uint32_t v = __shfl_sync(0xFFFFFFFFu, e, j);
+      asm volatile("st.shared.u32 [%0], %1;" ::"r"(lut + (uint32_t)(i0 + j) * 128u + 4u * lane),
+                   "r"(v)
+                   : "memory");
+    }
+  }
+}
+
+// A lane's row stream: stream words cur (j), nxt (j + 1) and nx2 (j + 2),
+// bit position pos (bits 0..4; bits 8 and up collect the table entries'
+// other fields and are never read), wp = shared address of nx2.  The window
+// of a step needs only cur and nxt; nx2, loaded a step ahead, keeps the
+// shared-memory load off the decode's dependency chain.
+struct LStream {
+  uint32_t cur, nxt, nx2, pos, wp, w0;
+  __device__ __forceinline__ void init(uint32_t wb, int lane, int stage_rows, uint32_t bit) {
+    uint32_t j0 = bit >> 5;
+    if (j0 > (uint32_t)(stage_rows - 3)) j0 = (uint32_t)(stage_rows - 3);   // corrupt start
+    w0 = wb + 4u * (uint32_t)lane;
+    cur = lds_u32(w0 + 128u * j0);
+    nxt = lds_u32(w0 + 128u * (j0 + 1));
+    wp = w0 + 128u * (j0 + 2);
+    nx2 = lds_u32(wp);
+    pos = bit & 31u;
+  }
+  __device__ __forceinline__ uint32_t consumed() const {
+    return ((wp - w0) >> 7) * 32u - 64u + (pos & 31u);
+  }
+};
+
+// Per-table decode constants (registers).
+struct LDec {
+  uint32_t lutl;   // shared address of entry 0, lane's copy
+  int negC;
+  uint32_t sh;     // 21 + s
+};
+
+// Decode the next two symbols of a stream: their table entries.
+__device__ __forceinline__ void l_decode2(LStream& st, const LDec& d, uint32_t& e0, uint32_t& e1) {
+  const uint32_t w = shf_l_wrap(st.nxt, st.cur, st.pos);
+  const int i0 = __viaddmax_s32((int)(w >> 21), d.negC, (int)(w >> d.sh));
+  e0 = lds_u32(d.lutl + (uint32_t)i0 * 128u);
+  const uint32_t w1 = shf_l_wrap(0u, w, e0);
+  const int i1 = __viaddmax_s32((int)(w1 >> 21), d.negC, (int)(w1 >> d.sh));
+  e1 = lds_u32(d.lutl + (uint32_t)i1 * 128u);
+  const uint32_t p2 = st.pos + e0 + e1;
+  const uint32_t hb = p2 & 32u;   // 32 when the window moves on by a word
+  st.pos = p2 ^ hb;
+  st.cur = shf_r_clamp(st.cur, st.nxt, hb);
+  st.nxt = shf_r_clamp(st.nxt, st.nx2, hb);
+  st.wp += hb * 4u;
+  st.nx2 = lds_u32(st.wp);
+}
+
+// fp32 128 + c of the byte-sized code in byte 1 of e (the even column of a
+// 4-bit pair entry)
+__device__ __forceinline__ float even_val(uint32_t e) {
+  return __uint_as_float(prmt(e, 0x43u, 0x4155u));
+}
+
+// Sums of the tile's 256 activations of one row: over the even columns and
+// over all columns (fixed order: per lane 4 + 4 sequential, then a
+// butterfly; every lane gets the same values).
+__device__ __forceinline__ void tile_sums(uint32_t sx, int lane, float& xe, float& xall) {
+  const float4 u = lds_f4(sx + 32u * (uint32_t)lane);
+  const float4 v = lds_f4(sx + 32u * (uint32_t)lane + 16u);
+  float e = ((u.x + u.z) + v.x) + v.z;
+  float o = ((u.y + u.w) + v.y) + v.w;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    e += __shfl_xor_sync(0xFFFFFFFFu, e, m);
+    o += __shfl_xor_sync(0xFFFFFFFFu, o, m);
+  }
+  xe = e;
+  xall = e + o;
+}
+
+// Values of the four pairs of a 4-bit twin word (codes MSB-first in stream
+// order: code k at bits 28 - 4k .. 31 - 4k; even columns are codes 0, 2, 4,
+// 6), in the coded entries' forms: even 128 + c, odd c.
+__device__ __forceinline__ void q4_twin_word(uint32_t w, float2 (&v)[4]) {
+  const uint32_t E = (w >> 4) & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6 as bytes 3..0
+  const uint32_t O1 = (w & 0x000F000Fu) | 0x64006400u;  // fp16 1024 + code 3 | 1024 + code 7
+  const uint32_t O2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;   // 1024 + code 1 | 1024 + code 5
+  v[0] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4355u)), f16hi_plus(O2, -1024.f));
+  v[1] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4255u)), f16hi_plus(O1, -1024.f));
+  v[2] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4155u)), f16lo_plus(O2, -1024.f));
+  v[3] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4055u)), f16lo_plus(O1, -1024.f));
+}
+
+// fp32 value c of the 6-bit code at stream bit B of the lane's twin words
+// (row base address rb = stage + 4 lane; word j at rb + 128 j).
+template <int B>
+__device__ __forceinline__ float q6_twin_c(uint32_t w0, uint32_t w1) {
+  constexpr int o = B % 32;
+  uint32_t t;
+  if constexpr (o <= 26) t = w0 >> (26 - o);   // the code is bits 31-o..26-o of w0
+  else t = __funnelshift_l(w1, w0, o - 26);     // it continues into w1
+  return f16lo_plus((t & 63u) | 0x6400u, -1024.f);
+}
+
+// Split-K commit of a warp's tile, in three parts that the consumer loop
+// spreads over three tiles so that no warp waits for a round trip to L2:
+// l_store writes the partial sums of rows (2l, 2l + 1) of tile (strip, kt);
+// a tile later, l_count counts it in (lane 0: an acq_rel atomicInc that
+// wraps to zero -- its release covers every lane's stores, ordered by the
+// warp barrier, which by then have long landed); another tile later,
+// l_finish reads the count, and the warp that brought it to TK adds the
+// strip's partials in ascending tile order and writes y.
+template <int BP>
+__device__ __forceinline__ void l_store(const QArgs& a, int strip, int kt, int lane,
+                                        const float (&p0)[BP], const float (&p1)[BP]) {
+  const int row0 = strip * 64 + 2 * lane;
+#pragma unroll
+  for (int b = 0; b < BP; ++b)
+    if (b < a.batch)
+      *reinterpret_cast<float2*>(a.ws + ((size_t)kt * a.batch + b) * a.N + row0) =
+          make_float2(p0[b], p1[b]);
+}
+__device__ __forceinline__ uint32_t l_count(const QArgs& a, int strip, int lane) {
+  __syncwarp();
+  return lane == 0 ? atom_inc_acq_rel(a.counters + strip, (unsigned)(a.TK - 1)) : 0u;
+}
+__device__ __forceinline__ void l_finish(const QArgs& a, int strip, int lane, uint32_t old) {
+  if (__shfl_sync(0xFFFFFFFFu, old, 0) != (uint32_t)(a.TK - 1)) return;
+  __syncwarp();   // the last arriver's acquire (lane 0) orders the reads below
+  const int row0 = strip * 64 + 2 * lane;
+  const size_t step = (size_t)a.batch * a.N;
+  for (int b = 0; b < a.batch; ++b) {
+    const float* base = a.ws + (size_t)b * a.N + row0;
+    float2 s = __ldcg(reinterpret_cast<const float2*>(base));
+    for (int k0 = 1; k0 < a.TK; k0 += 8) {
+      float2 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.TK) v[i] = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(k0 + i) * step));
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.TK) { s.x += v[i].x; s.y += v[i].y; }
+    }
+    *reinterpret_cast<float2*>(a.y + (size_t)b * a.N + row0) = s;
+  }
+}
+
+template <int FMT, bool TWIN, int BP>
+__global__ void __launch_bounds__((16 + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int nthreads = blockDim.x;
+  const int nw = nthreads / 32 - kLProducers;   // consumer warps; warps nw.. produce
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool producer = warp >= nw;
+  int mi = 0;
+  while (mi + 1 < g.n && (int)blockIdx.x >= g.cfirst[mi + 1]) ++mi;
+  const QArgs& a = g.m[mi];
+  const int cnt = g.cfirst[mi + 1] - g.cfirst[mi];
+  const int c0 = (int)blockIdx.x - g.cfirst[mi];
+  const int n_local = c0 < a.n_tiles ? (a.n_tiles - c0 + cnt - 1) / cnt : 0;
+  const int S = g.nstage;
+  uint64_t* tbar = reinterpret_cast<uint64_t*>(smem + kLHdrTab);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kLHdrBar);
+  uint64_t* empty = full + kLMaxStages;
+  volatile int* err = reinterpret_cast<volatile int*>(smem + kLHdrErr);
+  const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kLRawTab);
+  const uint32_t sbase = smem_addr(smem);
+
+  // activation rows beyond `batch` stay zero in every stage
+  if (BP > 1) {
+    for (int s = 0; s < S; ++s)
+      for (int i = a.batch * 256 + threadIdx.x; i < BP * 256; i += nthreads)
+        reinterpret_cast<float*>(smem + g.ring_off + s * g.stage_bytes + g.x_off)[i] = 0.f;
+  }
+  int* stage_tile = reinterpret_cast<int*>(smem + kLHdrTiles);
+  if (threadIdx.x == 0) {
+    *reinterpret_cast<int*>(smem + kLHdrNext) = 0;
+    *err = 0;
+    mbar_init(tbar, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      stage_tile[s] = -1;
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (!TWIN && threadIdx.x == 0) table_issue(smem + kLRawTab, a.table, tbar);
+
+  // ---- producers: fill the ring ----
+  // kLProducers warps; producer p owns the stages s = p mod kLProducers and
+  // fills local tiles i = p, p + kLProducers, ... in order (one warp issuing
+  // bulk copies cannot keep HBM busy: each copy holds the issuing thread for
+  // a few hundred ns).  Lane j loads the row ranges of the warp's tiles
+  // 32 c + j of the current chunk c and the next (in flight a chunk ahead);
+  // lane 0 issues each tile's copies once its stage is free.
+  if (producer) {
+    pdl_wait();
+    constexpr uint32_t qpb = QFmt<FMT>::qp_bytes;
+    const int pw = warp - nw;                  // producer index
+    auto rows_of = [&](int k, uint32_t& r0, uint32_t& r1, int& t) {
+      const int i = pw + k * kLProducers;
+      r0 = r1 = 0u;
+      t = 0;
+      if (i < n_local) {
+        bool v;
+        t = list_tile<true>(a, c0 + i * cnt, v);
+        r0 = __ldg(a.tile_off + t);
+        r1 = __ldg(a.tile_off + t + 1);
+      }
+    };
+    uint32_t cr0, cr1, nr0, nr1;
+    int ct, nt, cb = 0;
+    rows_of(lane, cr0, cr1, ct);
+    rows_of(32 + lane, nr0, nr1, nt);
+    int issued = -1;   // last local tile this warp issued
+    for (int k = 0; pw + k * kLProducers < n_local; ++k) {
+      const int i = pw + k * kLProducers;
+      if (k == cb + 32) {   // move to the next chunk; start loading the one after
+        cr0 = nr0; cr1 = nr1; ct = nt;
+        cb += 32;
+        rows_of(cb + 32 + lane, nr0, nr1, nt);
+      }
+      const int s = i % S;
+      int ok = 1;
+      if (lane == 0 && i >= S) {   // stage s is free once tile i - S has been consumed
+        bool got = mbar_try_wait(&empty[s], ((i / S) - 1) & 1);
+        if (!got) {
+          const long long t0 = clock64();
+          while (!(got = mbar_try_wait(&empty[s], ((i / S) - 1) & 1)))
+            if (*err || clock64() - t0 > kWaitCycles) break;
+        }
+        if (!got && !*err) report(a.status, LW_DEV_TIMEOUT);
+        ok = got && !*err;
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+        if (lane == 0) *err = 1;
+        break;
+      }
+      const int j = k - cb;   // 0..31: lane j of the current chunk
+      const uint32_t r0 = __shfl_sync(0xFFFFFFFFu, cr0, j), r1 = __shfl_sync(0xFFFFFFFFu, cr1, j);
+      const int t = __shfl_sync(0xFFFFFFFFu, ct, j);
+      if (lane == 0) {
+        uint8_t* st = smem + g.ring_off + s * g.stage_bytes;
+        const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(g.stage_rows - 2);
+        const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
+        const uint32_t mbytes = TWIN ? 0u : 128u;   // mid offsets + lane bit counts
+        const uint32_t xbytes = (uint32_t)a.batch * 1024u;
+        // the stage records whether the tile fits (read by the consumer after
+        // the barrier completes, which orders this store before it)
+        *reinterpret_cast<volatile int*>(st + g.x_off + BP * 1024) = fits ? 1 : 0;
+        // announce which tile stage s now carries: its consumer waits for this
+        // before waiting on the barrier, so it never mistakes the stage's
+        // previous phase (same parity, two phases back) for its own
+        st_release(&stage_tile[s], i);
+        mbar_arrive_expect_tx(&full[s], wbytes + qpb + mbytes + xbytes);
+        if (wbytes) bulk_g2s(st, a.words + (size_t)r0 * 32, wbytes, &full[s]);
+        bulk_g2s(st + g.qp_off, a.qparams + (size_t)t * qpb, qpb, &full[s]);
+        if (!TWIN) {
+          bulk_g2s(st + g.mid_off, a.lane_mid + (size_t)t * 32, 64, &full[s]);
+          bulk_g2s(st + g.lb_off, a.lane_bits + (size_t)t * 32, 64, &full[s]);
+        }
+        const int kt = t % a.TK;
+        for (int b = 0; b < a.batch; ++b)
+          bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
+                   &full[s]);
+      }
+      issued = i;
+    }
+    // after an error: let this warp's copies still in flight land before leaving
+    if (lane == 0 && *err)
+      for (int i = issued; i >= 0 && i > issued - S; i -= kLProducers)
+        mbar_wait(&full[i % S], (i / S) & 1);
+    pdl_trigger();
+    return;
+  }
+
+  // ---- consumers ----
+  LDec dec{0u, 0, 21u};
+  if (!TWIN) {
+    const bool got = mbar_wait(tbar, 0u);
+    bool ok = got && table_ok_warp(tb, FMT, QFmt<FMT>::alpha, 10, lane);
+    LutShape sh{0, 0, 2048, 2048};
+    if (ok) {
+      sh = lut_shape(tb->lim_m1, tb->lmin, tb->lmax);
+      ok = sh.n <= g.lut_cap;
+    }
+    if (!ok) {
+      if (lane == 0 && warp == 0) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
+      *err = 1;
+    } else {
+      lut_build(tb, sh, sbase + (uint32_t)g.lut_off, warp, nw, lane);
+    }
+    dec.lutl = sbase + (uint32_t)g.lut_off + 4u * (uint32_t)lane;
+    dec.negC = -sh.C;
+    dec.sh = 21u + (uint32_t)sh.s;
+    // the table is complete before any warp decodes (consumer warps only)
+    asm volatile("bar.sync 1, %0;" ::"r"(nw * 32) : "memory");
+  }
+  pdl_wait();
+  int* next = reinterpret_cast<int*>(smem + kLHdrNext);
+  // commit pipeline: strip of the tile stored last (not yet counted), and
+  // the strip counted last with its pending count (-1: none)
+  int ps1 = -1, ps2 = -1;
+  uint32_t old2 = 0u;
+  while (true) {
+    int i = 0;
+    if (lane == 0) i = *err ? n_local : atomicAdd(next, 1);
+    i = __shfl_sync(0xFFFFFFFFu, i, 0);
+    if (i >= n_local) break;
+    const int s = i % S;
+    // first the producer's announcement that stage s carries tile i (then the
+    // barrier's phase i / S is the one in progress), then the barrier
+    bool got = ld_acquire(&stage_tile[s]) == i && mbar_try_wait(&full[s], (i / S) & 1);
+    if (!got) {
+      const long long t0 = clock64();
+      bool announced;
+      while (!(announced = ld_acquire(&stage_tile[s]) == i))
+        if (*err || clock64() - t0 > kWaitCycles) break;
+      if (announced)
+        while (!(got = mbar_try_wait(&full[s], (i / S) & 1)))
+          if (*err || clock64() - t0 > kWaitCycles) break;
+    }
+    got = __all_sync(0xFFFFFFFFu, got);
+    if (!got) {
+      if (lane == 0 && !*err) report(a.status, LW_DEV_TIMEOUT);
+      *err = 1;
+      break;
+    }
+    bool valid;
+    const int t = list_tile<true>(a, c0 + i * cnt, valid);   // a tile of the bundle
+    const int strip = t / a.TK, kt = t % a.TK;
+    const uint32_t wb = sbase + (uint32_t)(g.ring_off + s * g.stage_bytes);
+    const uint32_t qp = wb + (uint32_t)g.qp_off;
+    const uint32_t sx = wb + (uint32_t)g.x_off;
+    const bool fits = lds_s32(sx + BP * 1024) != 0;
+    float p0[BP], p1[BP];
+#pragma unroll
+    for (int b = 0; b < BP; ++b) p0[b] = p1[b] = 0.f;
+    if (!fits) {
+      if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
+    } else if (FMT == kQ4) {
+      float xe[BP], xa[BP];
+#pragma unroll
+      for (int b = 0; b < BP; ++b) tile_sums(sx + 1024u * b, lane, xe[b], xa[b]);
+      float2 acc0[BP], acc1[BP];
+#pragma unroll
+      for (int b = 0; b < BP; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+      if (!TWIN) {
+        const uint32_t mid = lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
+        LStream A, B;
+        A.init(wb, lane, g.stage_rows, 0u);
+        B.init(wb, lane, g.stage_rows, mid);
+#pragma unroll 4
+        for (int j = 0; j < 64; ++j) {
+          uint32_t a0, a1, b0, b1;
+          l_decode2(A, dec, a0, a1);
+          l_decode2(B, dec, b0, b1);
+          const float2 va0 = make_float2(even_val(a0), f16hi_plus(a0, -1024.f));
+          const float2 va1 = make_float2(even_val(a1), f16hi_plus(a1, -1024.f));
+          const float2 vb0 = make_float2(even_val(b0), f16hi_plus(b0, -1024.f));
+          const float2 vb1 = make_float2(even_val(b1), f16hi_plus(b1, -1024.f));
+#pragma unroll
+          for (int b = 0; b < BP; ++b) {
+            const float4 xv = lds_f4(sx + 1024u * b + 16u * (uint32_t)j);
+            acc0[b] = __ffma2_rn(va0, make_float2(xv.x, xv.y), acc0[b]);
+            acc0[b] = __ffma2_rn(va1, make_float2(xv.z, xv.w), acc0[b]);
+            acc1[b] = __ffma2_rn(vb0, make_float2(xv.x, xv.y), acc1[b]);
+            acc1[b] = __ffma2_rn(vb1, make_float2(xv.z, xv.w), acc1[b]);
+          }
+        }
+        const uint32_t end = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
+        if (A.consumed() != mid || B.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
+      } else {
+        // twin: row 2l in words 0..31 of lane l, row 2l + 1 in words 32..63
+        const uint32_t la = wb + 4u * (uint32_t)lane;
+#pragma unroll 2
+        for (int jj = 0; jj < 32; ++jj) {
+          float2 va[4], vb[4];
+          q4_twin_word(lds_u32(la + 128u * (uint32_t)jj), va);
+          q4_twin_word(lds_u32(la + 128u * (uint32_t)(32 + jj)), vb);
+#pragma unroll
+          for (int b = 0; b < BP; ++b) {
+            const float4 xa4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj);
+            const float4 xb4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj + 16u);
+            acc0[b] = __ffma2_rn(va[0], make_float2(xa4.x, xa4.y), acc0[b]);
+            acc0[b] = __ffma2_rn(va[1], make_float2(xa4.z, xa4.w), acc0[b]);
+            acc0[b] = __ffma2_rn(va[2], make_float2(xb4.x, xb4.y), acc0[b]);
+            acc0[b] = __ffma2_rn(va[3], make_float2(xb4.z, xb4.w), acc0[b]);
+            acc1[b] = __ffma2_rn(vb[0], make_float2(xa4.x, xa4.y), acc1[b]);
+            acc1[b] = __ffma2_rn(vb[1], make_float2(xa4.z, xa4.w), acc1[b]);
+            acc1[b] = __ffma2_rn(vb[2], make_float2(xb4.x, xb4.y), acc1[b]);
+            acc1[b] = __ffma2_rn(vb[3], make_float2(xb4.z, xb4.w), acc1[b]);
+          }
+        }
+      }
+      // scale | min << 16 of rows 2l and 2l + 1
+      const uint2 q = lds_u2(qp + 8u * (uint32_t)lane);
+      const float sc0 = __half2float(__ushort_as_half((unsigned short)(q.x & 0xFFFFu)));
+      const float mn0 = __half2float(__ushort_as_half((unsigned short)(q.x >> 16)));
+      const float sc1 = __half2float(__ushort_as_half((unsigned short)(q.y & 0xFFFFu)));
+      const float mn1 = __half2float(__ushort_as_half((unsigned short)(q.y >> 16)));
+#pragma unroll
+      for (int b = 0; b < BP; ++b) {
+        p0[b] = fmaf(sc0, (acc0[b].x - 128.f * xe[b]) + acc0[b].y, mn0 * xa[b]);
+        p1[b] = fmaf(sc1, (acc1[b].x - 128.f * xe[b]) + acc1[b].y, mn1 * xa[b]);
+      }
+    } else {  // 6-bit: 16 groups of 16 weights per row
+      float X[BP];
+#pragma unroll
+      for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
+      const uint32_t mid = TWIN ? 0u : lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
+      LStream A, B;
+      if (!TWIN) {
+        A.init(wb, lane, g.stage_rows, 0u);
+        B.init(wb, lane, g.stage_rows, mid);
+      }
+      const uint32_t la = wb + 4u * (uint32_t)lane;
+#pragma unroll 1
+      for (int gi = 0; gi < 16; ++gi) {
+        float2 acc0[BP], acc1[BP];
+#pragma unroll
+        for (int b = 0; b < BP; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+        if (!TWIN) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            uint32_t a0, a1, b0, b1;
+            l_decode2(A, dec, a0, a1);
+            l_decode2(B, dec, b0, b1);
+            const float2 va = make_float2(f16hi_plus(a0, -1024.f), f16hi_plus(a1, -1024.f));
+            const float2 vb = make_float2(f16hi_plus(b0, -1024.f), f16hi_plus(b1, -1024.f));
+#pragma unroll
+            for (int b = 0; b < BP; ++b) {
+              const float2 xv = lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m);
+              acc0[b] = __ffma2_rn(va, xv, acc0[b]);
+              acc1[b] = __ffma2_rn(vb, xv, acc1[b]);
+            }
+          }
+        } else {
+          // group gi of row 2l: codes 16 gi .. 16 gi + 15 at bits 96 gi ..; row 2l + 1
+          // starts at word 48 (bit 1536)
+          const uint32_t wa = la + 128u * (uint32_t)(3 * gi);
+          const uint32_t wbb = la + 128u * (uint32_t)(48 + 3 * gi);
+          const uint32_t a0w = lds_u32(wa), a1w = lds_u32(wa + 128u), a2w = lds_u32(wa + 256u);
+          const uint32_t b0w = lds_u32(wbb), b1w = lds_u32(wbb + 128u), b2w = lds_u32(wbb + 256u);
+          float va[16], vb[16];
+          va[0] = q6_twin_c<0>(a0w, a1w);   va[1] = q6_twin_c<6>(a0w, a1w);
+          va[2] = q6_twin_c<12>(a0w, a1w);  va[3] = q6_twin_c<18>(a0w, a1w);
+          va[4] = q6_twin_c<24>(a0w, a1w);  va[5] = q6_twin_c<30>(a0w, a1w);
+          va[6] = q6_twin_c<4>(a1w, a2w);   va[7] = q6_twin_c<10>(a1w, a2w);
+          va[8] = q6_twin_c<16>(a1w, a2w);  va[9] = q6_twin_c<22>(a1w, a2w);
+          va[10] = q6_twin_c<28>(a1w, a2w); va[11] = q6_twin_c<2>(a2w, 0u);
+          va[12] = q6_twin_c<8>(a2w, 0u);   va[13] = q6_twin_c<14>(a2w, 0u);
+          va[14] = q6_twin_c<20>(a2w, 0u);  va[15] = q6_twin_c<26>(a2w, 0u);
+          vb[0] = q6_twin_c<0>(b0w, b1w);   vb[1] = q6_twin_c<6>(b0w, b1w);
+          vb[2] = q6_twin_c<12>(b0w, b1w);  vb[3] = q6_twin_c<18>(b0w, b1w);
+          vb[4] = q6_twin_c<24>(b0w, b1w);  vb[5] = q6_twin_c<30>(b0w, b1w);
+          vb[6] = q6_twin_c<4>(b1w, b2w);   vb[7] = q6_twin_c<10>(b1w, b2w);
+          vb[8] = q6_twin_c<16>(b1w, b2w);  vb[9] = q6_twin_c<22>(b1w, b2w);
+          vb[10] = q6_twin_c<28>(b1w, b2w); vb[11] = q6_twin_c<2>(b2w, 0u);
+          vb[12] = q6_twin_c<8>(b2w, 0u);   vb[13] = q6_twin_c<14>(b2w, 0u);
+          vb[14] = q6_twin_c<20>(b2w, 0u);  vb[15] = q6_twin_c<26>(b2w, 0u);
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int b = 0; b < BP; ++b) {
+              const float2 xv = lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m);
+              acc0[b] = __ffma2_rn(make_float2(va[2 * m], va[2 * m + 1]), xv, acc0[b]);
+              acc1[b] = __ffma2_rn(make_float2(vb[2 * m], vb[2 * m + 1]), xv, acc1[b]);
+            }
+        }
+        // scales of group gi of rows 2l (chunk gi/8) and 2l + 1 (chunk 2 + gi/8)
+        const uint32_t sa = qp + (uint32_t)((((gi >> 3) * 32) + lane) * 16 + 2 * (gi & 7));
+        const float s0 = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
+        const float s1 = __half2float(__ushort_as_half((unsigned short)lds_u16(sa + 1024u)));
+#pragma unroll
+        for (int b = 0; b < BP; ++b) {
+          const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], gi);
+          p0[b] = fmaf(s0, (acc0[b].x + acc0[b].y) - 32.f * Xg, p0[b]);
+          p1[b] = fmaf(s1, (acc1[b].x + acc1[b].y) - 32.f * Xg, p1[b]);
+        }
+      }
+      if (!TWIN) {
+        const uint32_t end = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
+        if (A.consumed() != mid || B.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
+      }
+    }
+    // release the stage: this warp's reads of it are done (their values are in
+    // the partial sums), ordered before the producer's next bulk copy into it
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    // a tile too long for its stage commits zeros, so that its strip still
+    // completes; a tile behind an invalid strip-list entry commits nothing
+    if (!valid && lane == 0) report(a.status, LW_DEV_BAD_STRIPS);
+    if (ps2 >= 0) l_finish(a, ps2, lane, old2);
+    ps2 = ps1;
+    if (ps1 >= 0) old2 = l_count(a, ps1, lane);
+    if (valid) l_store<BP>(a, strip, kt, lane, p0, p1);
+    ps1 = valid ? strip : -1;
+  }
+  if (ps2 >= 0) l_finish(a, ps2, lane, old2);
+  if (ps1 >= 0) l_finish(a, ps1, lane, l_count(a, ps1, lane));
+  pdl_trigger();
+}
+
+}  // namespace dev
+}  // namespace lw

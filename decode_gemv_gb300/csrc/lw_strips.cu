@@ -1,6 +1,7 @@
 // lw_decode_gemm_strips: the fused 4-/6-bit product over a list of 64-row
-// strips (tile-skip launch list; the strip-list instantiations of
-// q_product_kernel live in this translation unit).
+// strips (tile-skip launch list): the table-driven kernel when the bundle's
+// table fits it, else the strip-list instantiations of q_product_kernel,
+// which live in this translation unit.
 #include "lw_qlaunch.h"
 
 using namespace lw;
@@ -33,7 +34,8 @@ extern "C" lw_status lw_decode_gemm_strips(const lw_dev_bundle* b, const int32_t
     const float* xp = xf + (size_t)b0 * b->cols;
     float* yp = Y + (size_t)b0 * b->rows;
     void* wp = ws;
-    s = q_products_impl<true>(&b, 1, &xp, nb, &yp, &wp, strips, n_strips, d_status, st);
+    s = lut_fits(b) ? launch_q_lut(&b, 1, &xp, nb, &yp, &wp, d_status, st, strips, n_strips)
+                    : q_products_impl<true>(&b, 1, &xp, nb, &yp, &wp, strips, n_strips, d_status, st);
     if (s != LW_OK) return s;
   }
   return LW_OK;

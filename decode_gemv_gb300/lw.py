@@ -36,7 +36,8 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_bundle_desc", "lw_bundle_serialized_bytes", "lw_bundle_serialize",
             "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load", "lw_transcode_twin",
             "lw_twin_tile_rows", "lw_decode_gemm_strips", "lw_graph_begin", "lw_graph_end",
-            "lw_graph_launch", "lw_graph_free", "lw_decode_gemm_group", "lw_twin_gemm_group"]
+            "lw_graph_launch", "lw_graph_free", "lw_decode_gemm_group", "lw_twin_gemm_group",
+            "lw_table_lut_entries"]
 
 
 class LwError(RuntimeError):
@@ -60,14 +61,15 @@ class LwSections(ctypes.Structure):
                 ("coded_bytes", ctypes.c_uint64), ("n_tiles", ctypes.c_uint64),
                 ("n_verbatim", ctypes.c_int64), ("max_tile_rows", ctypes.c_int32),
                 ("max_len", ctypes.c_int32), ("min_len", ctypes.c_int32),
-                ("palette_size", ctypes.c_int32), ("bits_per_weight", ctypes.c_double)]
+                ("palette_size", ctypes.c_int32), ("bits_per_weight", ctypes.c_double),
+                ("lut_entries", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class LwDevBundle(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("twin", ctypes.c_int32),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
                 ("max_tile_rows", ctypes.c_int32), ("lmin", ctypes.c_int32),
-                ("lmax", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("lmax", ctypes.c_int32), ("lut_entries", ctypes.c_int32),
                 ("words", ctypes.c_void_p), ("tile_off", ctypes.c_void_p),
                 ("lane_bits", ctypes.c_void_p), ("table", ctypes.c_void_p),
                 ("qparams", ctypes.c_void_p), ("signman", ctypes.c_void_p),
@@ -123,6 +125,7 @@ def load():
         "lw_graph_end": ([P, P], i32),
         "lw_graph_launch": ([P, P], i32),
         "lw_graph_free": ([P], None),
+        "lw_table_lut_entries": ([P], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -162,6 +165,7 @@ class BundleStats:
     min_len: int
     palette_size: int
     bits_per_weight: float
+    lut_entries: int = 0
 
 
 class HostBundle:
@@ -174,7 +178,8 @@ class HostBundle:
         _check(load().lw_bundle_sections(self._h, ctypes.byref(s)), "lw_bundle_sections")
         self.stats = BundleStats(int(s.coded_bytes), int(s.n_tiles), int(s.n_verbatim),
                                  int(s.max_tile_rows), int(s.max_len), int(s.min_len),
-                                 int(s.palette_size), float(s.bits_per_weight))
+                                 int(s.palette_size), float(s.bits_per_weight),
+                                 int(s.lut_entries))
         self.sections = {}
         for i, name in enumerate(SECTION_NAMES):
             n = int(s.bytes[i])
@@ -258,6 +263,15 @@ def lw_table_from_lengths(fmt: int, code_len, palette=None) -> np.ndarray:
     return out
 
 
+def lw_table_lut_entries(table: np.ndarray) -> int:
+    """Entries of the compact decode table the table-driven kernel builds from
+    this lw_table (the lut_entries hint of a device bundle)."""
+    t = np.ascontiguousarray(table, dtype=np.uint8)
+    if t.size != TABLE_BYTES:
+        raise LwError(1, "lw_table_lut_entries", f"a table is {TABLE_BYTES} bytes, got {t.size}")
+    return int(load().lw_table_lut_entries(_np_ptr(t)))
+
+
 def table_fields(table: np.ndarray) -> dict:
     """Decode the documented lw_table layout (for tests and reports)."""
     t = np.asarray(table, dtype=np.uint8)
@@ -295,7 +309,7 @@ class DeviceBundle:
     lw_dev_bundle view that the C calls take."""
 
     def __init__(self, fmt, twin, rows, cols, sections: dict, max_tile_rows, lmin, lmax,
-                 device="cuda", coded_bytes=None):
+                 device="cuda", coded_bytes=None, lut_entries=0):
         import torch
         self.fmt, self.twin, self.rows, self.cols = fmt, bool(twin), rows, cols
         self.tensors = {}
@@ -308,14 +322,15 @@ class DeviceBundle:
                                sum(t.numel() for t in self.tensors.values()))
         v = LwDevBundle()
         v.fmt, v.twin, v.rows, v.cols = fmt, int(twin), rows, cols
-        v.max_tile_rows, v.lmin, v.lmax = max_tile_rows, lmin, lmax
+        v.max_tile_rows, v.lmin, v.lmax, v.lut_entries = max_tile_rows, lmin, lmax, lut_entries
         for name in SECTION_NAMES:
             t = self.tensors.get(name)
             setattr(v, name, t.data_ptr() if t is not None else None)
         self.view = v
 
     @classmethod
-    def from_tensors(cls, fmt, twin, rows, cols, tensors: dict, max_tile_rows, lmin, lmax):
+    def from_tensors(cls, fmt, twin, rows, cols, tensors: dict, max_tile_rows, lmin, lmax,
+                     lut_entries=0):
         """A view over device tensors that already hold the sections."""
         self = cls.__new__(cls)
         self.fmt, self.twin, self.rows, self.cols = fmt, bool(twin), rows, cols
@@ -323,7 +338,7 @@ class DeviceBundle:
         self.coded_bytes = int(sum(t.numel() * t.element_size() for t in self.tensors.values()))
         v = LwDevBundle()
         v.fmt, v.twin, v.rows, v.cols = fmt, int(twin), rows, cols
-        v.max_tile_rows, v.lmin, v.lmax = max_tile_rows, lmin, lmax
+        v.max_tile_rows, v.lmin, v.lmax, v.lut_entries = max_tile_rows, lmin, lmax, lut_entries
         for name in SECTION_NAMES:
             t = self.tensors.get(name)
             setattr(v, name, t.data_ptr() if t is not None else None)
@@ -334,7 +349,7 @@ class DeviceBundle:
     def upload(cls, hb: HostBundle, device="cuda"):
         return cls(hb.desc.fmt, hb.desc.twin, hb.desc.rows, hb.desc.cols, hb.sections,
                    hb.stats.max_tile_rows, hb.stats.min_len, hb.stats.max_len, device,
-                   hb.stats.coded_bytes)
+                   hb.stats.coded_bytes, hb.stats.lut_entries)
 
     @property
     def ref(self):

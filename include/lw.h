@@ -187,13 +187,20 @@ typedef struct {
   int32_t min_len;          /* shortest code length (lmin) */
   int32_t palette_size;     /* BF16 */
   double bits_per_weight;   /* 8 * coded_bytes / (N*K) */
+  int32_t lut_entries;      /* 4-/6-bit coded bundles: entries of the compact
+                               decode table (index max(peek >> s, peek - C),
+                               s and C chosen per table, 128 bytes each in
+                               shared memory); 0 otherwise */
+  int32_t reserved;
 } lw_sections;
 
 /*
  * Device view of an uploaded bundle: raw device pointers into caller-owned
  * buffers holding byte-for-byte copies of the host sections (NULL where a
  * section is absent).  Filled by the caller; the library only reads it on the
- * host at call time.
+ * host at call time.  words, lane_bits, table, qparams, signman and lane_mid
+ * must be 16-byte aligned (the kernels copy them with the bulk-copy engine);
+ * calls refuse other addresses with LW_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t fmt;
@@ -203,7 +210,13 @@ typedef struct {
   int32_t max_tile_rows;    /* from lw_sections; bounds shared-memory staging */
   int32_t lmin, lmax;       /* from lw_sections: code-length span of the table
                                (selects the kernel variant; checked on device) */
-  int32_t reserved;
+  int32_t lut_entries;      /* from lw_sections: entries of the compact decode
+                               table of the table-driven 4-/6-bit product
+                               kernel.  1..512 selects that kernel (the device
+                               rebuilds the table from the bundle's lw_table
+                               and reports LW_DEV_BAD_TABLE if it needs more);
+                               0 selects the comparator kernel (any table).
+                               Ignored for twins and BF16. */
   const uint32_t* words;
   const uint32_t* tile_off;
   const uint16_t* lane_bits;
@@ -483,6 +496,12 @@ lw_status lw_decode_gemv_noalloc(const lw_dev_bundle* b, const void* x, float* y
                                  int32_t* d_status, void* stream);
 size_t lw_noalloc_scratch_bytes(void);
 
+/* Entries of the compact decode table that the table-driven 4-/6-bit
+   product kernel builds from this decoder table (the value lw_sections and
+   lw_dev_bundle carry as lut_entries); 0 for a NULL table or a BF16 table.
+   Host only; for tables built by lw_table_from_lengths. */
+int32_t lw_table_lut_entries(const lw_table* t);
+
 /* The status's name ("LW_OK", "LW_ERR_SHAPE", ...; "unknown lw_status" for
    other values): a static string, never NULL, not to be freed. */
 const char* lw_status_string(lw_status s);
@@ -511,9 +530,10 @@ lw_status lw_graph_end(void* stream, lw_graph** out);
 lw_status lw_graph_launch(const lw_graph* g, void* stream);
 void lw_graph_free(lw_graph* g);
 
-/* ABI revision of this header: 3 (2 + grouped launches, strip lists, the
-   load-time transcode, bundle files, step graphs, LW_ERR_IO,
-   LW_DEV_BAD_STRIPS).  The
+/* ABI revision of this header: 4 (3 + lw_sections.lut_entries and
+   lw_dev_bundle.lut_entries, which selects the table-driven 4-/6-bit
+   product kernel; 3 added grouped launches, strip lists, the load-time
+   transcode, bundle files, step graphs, LW_ERR_IO, LW_DEV_BAD_STRIPS).  The
    bundle file format carries its own version. */
 int32_t lw_version(void);
 

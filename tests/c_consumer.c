@@ -92,7 +92,7 @@ int main(void) {
   lw_desc odd = {LW_FMT_Q4_PAIR, 0, N + 1, K};
   if (lw_encode_bundle(&odd, codes, scales, mins, &bad) != LW_ERR_SHAPE) return failed("shape");
   if (lw_encode_bundle(&d, NULL, scales, mins, &bad) != LW_ERR_INVALID_ARG) return failed("NULL");
-  if (lw_version() != 3) return failed("version");
+  if (lw_version() != 4) return failed("version");
 
   free(buf);
   lw_bundle_free(c);

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lw.EXPORTED)
-    assert lw.load().lw_version() == 3
+    assert lw.load().lw_version() == 4
 
 
 def _q4(seed, rows, cols, sd=1.6):
