@@ -12,14 +12,18 @@ namespace {
 
 using LKernel = void (*)(const dev::LLaunch);
 
-template <int FMT, bool TWIN>
-LKernel pick_lut(int bp) {
+template <int FMT, bool TWIN, int R>
+LKernel pick_lut_r(int bp) {
   switch (bp) {
-    case 1: return dev::q_lut_kernel<FMT, TWIN, 1>;
-    case 2: return dev::q_lut_kernel<FMT, TWIN, 2>;
-    case 4: return dev::q_lut_kernel<FMT, TWIN, 4>;
-    default: return dev::q_lut_kernel<FMT, TWIN, 8>;
+    case 1: return dev::q_lut_kernel<FMT, TWIN, 1, R>;
+    case 2: return dev::q_lut_kernel<FMT, TWIN, 2, R>;
+    case 4: return dev::q_lut_kernel<FMT, TWIN, 4, R>;
+    default: return dev::q_lut_kernel<FMT, TWIN, 8, R>;
   }
+}
+template <int FMT, bool TWIN>
+LKernel pick_lut(int bp, int r) {
+  return r == 2 ? pick_lut_r<FMT, TWIN, 2>(bp) : pick_lut_r<FMT, TWIN, 1>(bp);
 }
 
 // Largest dynamic shared memory a CTA may use on the current device.
@@ -49,8 +53,6 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
   const int fmt = bs[0]->fmt;
   const bool twin = bs[0]->twin != 0;
   const int bp = batch <= 1 ? 1 : (batch <= 2 ? 2 : (batch <= 4 ? 4 : 8));
-  LKernel k = fmt == LW_FMT_Q4_PAIR ? (twin ? pick_lut<dev::kQ4, true>(bp) : pick_lut<dev::kQ4, false>(bp))
-                                    : (twin ? pick_lut<dev::kQ6, true>(bp) : pick_lut<dev::kQ6, false>(bp));
   int max_rows = 0;
   long long total = 0;
   // tiles of each matrix (with a strip list, a single matrix: its listed strips')
@@ -115,12 +117,25 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
     max_per_cta = per > max_per_cta ? per : max_per_cta;
   }
   const int grid = g.cfirst[n];
-  // consumer warps: at most 16 and four fewer than stages (copies in flight
-  // while every warp decodes), and no more than a CTA has tiles; warps take tiles as they free
-  // up, so the tiles of a CTA need not divide evenly among them
-  int nw = S - 4 < 16 ? S - 4 : 16;
-  if (nw > max_per_cta) nw = max_per_cta;
-  if (nw < 1) nw = 1;
+  // rows per unit: a whole tile per warp (R = 2: two interleaved streams per
+  // lane sharing the activation loads) when a CTA has tiles for more than a
+  // wave of 16 warps; half a tile per warp (R = 1: twice the warps, better
+  // latency hiding and balance) for CTAs with fewer tiles
+  const int R = max_per_cta > 16 ? 2 : 1;
+  LKernel k = fmt == LW_FMT_Q4_PAIR
+                  ? (twin ? pick_lut<dev::kQ4, true>(bp, R) : pick_lut<dev::kQ4, false>(bp, R))
+                  : (twin ? pick_lut<dev::kQ6, true>(bp, R) : pick_lut<dev::kQ6, false>(bp, R));
+  // consumer warps: at most 16 (R = 2) or kLMaxConsumers (R = 1), and
+  // (2 / R) x four fewer than stages (copies in flight while every warp
+  // decodes), spread so that a CTA's units come in whole waves, and at
+  // least 8 (they build the decode table)
+  int nw_max = (2 / R) * (S - 4);
+  const int cap = R == 2 ? 16 : dev::kLMaxConsumers;
+  if (nw_max > cap) nw_max = cap;
+  const int units = (2 / R) * max_per_cta;
+  const int waves = (units + nw_max - 1) / nw_max;
+  int nw = (units + waves - 1) / waves;
+  if (nw < 8) nw = 8 < nw_max ? 8 : nw_max;
   for (int i = 0; i < n; ++i) {
     const lw_dev_bundle* b = bs[i];
     dev::QArgs& a = g.m[i];

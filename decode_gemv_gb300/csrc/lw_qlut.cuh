@@ -20,28 +20,31 @@
 //    waits for the stage to be announced for that tile and then for its
 //    barrier, decodes it and releases the stage on its "empty" mbarrier.
 //    Every wait is bounded.
-//  * a consumer warp decodes a whole tile: lane l runs the lane's two rows
-//    (2l from the start of its stream, 2l + 1 from its mid offset) as two
-//    interleaved streams, so both rows share the activation loads;
+//  * a consumer warp decodes a unit of a tile: with R = 2, a whole tile,
+//    lane l running its two rows (2l from the start of its stream, 2l + 1
+//    from its mid offset) as two interleaved streams that share the
+//    activation loads; with R = 1, one row of every lane, so a tile's two
+//    units run on two warps -- the scheduler then hides one warp's lookup
+//    latency with another's work (a warp issues in order), and the
+//    half-tile units balance better over the warps; the launcher takes
+//    R = 1 for CTAs with few tiles;
 //  * decoding is a lookup: the peek indexes a compact table (lw_lut.h) in
 //    shared memory that is replicated once per lane -- lane l's copy of an
 //    entry sits in bank l, so a warp's 32 lookups are one conflict-free
 //    shared-memory wavefront whatever symbols the lanes decode.  An entry
-//    holds the code length (bits 0..7), and the symbol's weights in the form
-//    the product consumes: 4-bit pairs carry the even column's code as a
-//    byte (bits 8..15, turned into the fp32 128 + c by one byte permute) and
-//    the odd column's code as the fp16 1024 + c (bits 16..31, turned into
-//    the exact fp32 c by one mixed-precision add, which runs on the FMA
-//    pipes and keeps the integer ALU pipe -- the decoder's bottleneck -- for
-//    the bit work); 6-bit codes carry only the fp16 form;
+//    holds the code length (bits 0..4) and the symbol's weights in a form
+//    that only FMA-pipe instructions turn into fp32 (the integer ALU pipe,
+//    the decoder's bottleneck, keeps the bit work): 4-bit pairs as two fp16
+//    codes (the length sits in the low mantissa bits of one, where a
+//    rounding fp16 add of 1024 drops it), 6-bit codes as the fp16 1024 + c;
 //  * one 32-bit window serves two symbols (an 11-bit code leaves at least 21
 //    valid bits): window = funnel shift of two stream words by the bit
 //    position; the second peek comes from the window shifted by the first
 //    length; the position advances by both lengths and the words by at most
 //    one per step, branch-free (the next word is reloaded every step);
-//  * products in packed fp32 FMA (FFMA2): even and odd columns in the two
-//    halves, then per row and tile part = scale * ((acc.x - 128 X_even) +
-//    acc.y) + min * X (4-bit) or, per 16-weight group, scale * (acc.x +
+//  * products in packed fp32 FMA (FFMA2) on the exact codes: even and odd
+//    columns in the two halves, then per row and tile part = scale * (acc.x
+//    + acc.y) + min * X (4-bit) or, per 16-weight group, scale * (acc.x +
 //    acc.y - 32 X_group) (6-bit), in a fixed order; the twin executes the
 //    same floating-point operations on the same values, so the twin's y is
 //    bitwise equal to the coded y;
@@ -92,7 +95,15 @@ constexpr int kLHdrTiles = kLRawTab + (int)sizeof(lw_table);   // int[S]: tile e
 constexpr int kLHdrBytes = kLHdrTiles + 4 * kLMaxStages;
 constexpr int kLGuardRows = 132;  // rows a corrupt 6-bit stream may read past its stage
 constexpr int kLProducers = 4;    // producer warps (each issues its own stages' copies)
+constexpr int kLMaxConsumers = 24;  // consumer warps at most (two per tile being decoded)
 
+// a * b + c as one integer multiply-add (FMA pipe; the compiler would
+// otherwise often use shift-and-add forms on the integer ALU pipe)
+__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 __device__ __forceinline__ uint32_t shf_l_wrap(uint32_t lo, uint32_t hi, uint32_t n) {
   uint32_t d;
   asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(lo), "r"(hi), "r"(n));
@@ -101,11 +112,6 @@ __device__ __forceinline__ uint32_t shf_l_wrap(uint32_t lo, uint32_t hi, uint32_
 __device__ __forceinline__ uint32_t shf_r_clamp(uint32_t lo, uint32_t hi, uint32_t n) {
   uint32_t d;
   asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(lo), "r"(hi), "r"(n));
-  return d;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
 // exact fp32 value of the fp16 in the high half of e, plus c
@@ -131,11 +137,34 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// fp16 bit pattern of a small integer c (0..15), exactly.
+__device__ __forceinline__ uint32_t f16_bits(uint32_t c) {
+  return (uint32_t)__half_as_ushort(__uint2half_rn(c));
+}
+
 // Table entry of a 4-bit pair symbol / a 6-bit code of length L.
+//  4-bit: low half = fp16(c_even) with L in its bits 0..4 (an fp16 of an
+//  integer below 16 has its lowest 7 mantissa bits zero, so the junk is below
+//  half an ulp of 1024 and the rounding add of 1024 in q4_vals removes it);
+//  high half = fp16(c_odd).  Bits 0..4 of the entry are L and bit 5 is zero,
+//  as the stream advance needs.
+//  6-bit: high half = fp16(1024 + c), low half = L.
 __device__ __forceinline__ uint32_t lut_entry(int fmt, uint32_t sym, int L) {
   if (fmt == LW_FMT_Q4_PAIR)
-    return ((0x6400u | ((sym >> 4) & 15u)) << 16) | ((sym & 15u) << 8) | (uint32_t)L;
+    return (f16_bits((sym >> 4) & 15u) << 16) | f16_bits(sym & 15u) | (uint32_t)L;
   return ((0x6400u | (sym & 63u)) << 16) | (uint32_t)L;
+}
+
+// The exact fp32 codes (c_even, c_odd) of a 4-bit entry: one fp16x2 add of
+// 1024 (rounding to the integer grid of [1024, 2048) drops the length bits),
+// then two mixed-precision adds of -1024 -- all on the FMA pipes.
+__device__ __forceinline__ float2 q4_vals(uint32_t e) {
+  uint32_t h;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(e), "r"(0x64006400u));
+  float lo, hi;
+  asm("{.reg .b16 a, b; mov.b32 {a, b}, %2; add.rn.f32.f16 %0, a, %3; add.rn.f32.f16 %1, b, %3;}"
+      : "=f"(lo), "=f"(hi) : "r"(h), "f"(-1024.f));
+  return make_float2(lo, hi);
 }
 
 // Build the replicated table of a checked, staged lw_table: consumer warp w
@@ -199,53 +228,36 @@ struct LDec {
 __device__ __forceinline__ void l_decode2(LStream& st, const LDec& d, uint32_t& e0, uint32_t& e1) {
   const uint32_t w = shf_l_wrap(st.nxt, st.cur, st.pos);
   const int i0 = __viaddmax_s32((int)(w >> 21), d.negC, (int)(w >> d.sh));
-  e0 = lds_u32(d.lutl + (uint32_t)i0 * 128u);
+  e0 = lds_u32(imad((uint32_t)i0, 128u, d.lutl));
   const uint32_t w1 = shf_l_wrap(0u, w, e0);
   const int i1 = __viaddmax_s32((int)(w1 >> 21), d.negC, (int)(w1 >> d.sh));
-  e1 = lds_u32(d.lutl + (uint32_t)i1 * 128u);
-  const uint32_t p2 = st.pos + e0 + e1;
+  e1 = lds_u32(imad((uint32_t)i1, 128u, d.lutl));
+  const uint32_t p2 = imad(e1, 1u, imad(e0, 1u, st.pos));
   const uint32_t hb = p2 & 32u;   // 32 when the window moves on by a word
-  st.pos = p2 ^ hb;
+  st.pos = imad(hb, 0xFFFFFFFFu, p2);   // p2 - hb
   st.cur = shf_r_clamp(st.cur, st.nxt, hb);
   st.nxt = shf_r_clamp(st.nxt, st.nx2, hb);
-  st.wp += hb * 4u;
+  st.wp = imad(hb, 4u, st.wp);
   st.nx2 = lds_u32(st.wp);
 }
 
-// fp32 128 + c of the byte-sized code in byte 1 of e (the even column of a
-// 4-bit pair entry)
-__device__ __forceinline__ float even_val(uint32_t e) {
-  return __uint_as_float(prmt(e, 0x43u, 0x4155u));
-}
 
-// Sums of the tile's 256 activations of one row: over the even columns and
-// over all columns (fixed order: per lane 4 + 4 sequential, then a
-// butterfly; every lane gets the same values).
-__device__ __forceinline__ void tile_sums(uint32_t sx, int lane, float& xe, float& xall) {
-  const float4 u = lds_f4(sx + 32u * (uint32_t)lane);
-  const float4 v = lds_f4(sx + 32u * (uint32_t)lane + 16u);
-  float e = ((u.x + u.z) + v.x) + v.z;
-  float o = ((u.y + u.w) + v.y) + v.w;
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) {
-    e += __shfl_xor_sync(0xFFFFFFFFu, e, m);
-    o += __shfl_xor_sync(0xFFFFFFFFu, o, m);
-  }
-  xe = e;
-  xall = e + o;
-}
 
-// Values of the four pairs of a 4-bit twin word (codes MSB-first in stream
-// order: code k at bits 28 - 4k .. 31 - 4k; even columns are codes 0, 2, 4,
-// 6), in the coded entries' forms: even 128 + c, odd c.
+
+// The exact fp32 codes of the four pairs of a 4-bit twin word (codes
+// MSB-first in stream order: code k at bits 28 - 4k .. 31 - 4k; even columns
+// are codes 0, 2, 4, 6): each logic op builds two fp16 1024 + c, each mixed-
+// precision add subtracts 1024 -- the coded entries' values, so the twin's
+// products are the coded kernel's.
 __device__ __forceinline__ void q4_twin_word(uint32_t w, float2 (&v)[4]) {
-  const uint32_t E = (w >> 4) & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6 as bytes 3..0
-  const uint32_t O1 = (w & 0x000F000Fu) | 0x64006400u;  // fp16 1024 + code 3 | 1024 + code 7
-  const uint32_t O2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;   // 1024 + code 1 | 1024 + code 5
-  v[0] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4355u)), f16hi_plus(O2, -1024.f));
-  v[1] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4255u)), f16hi_plus(O1, -1024.f));
-  v[2] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4155u)), f16lo_plus(O2, -1024.f));
-  v[3] = make_float2(__uint_as_float(prmt(E, 0x43u, 0x4055u)), f16lo_plus(O1, -1024.f));
+  const uint32_t A = (w & 0x000F000Fu) | 0x64006400u;           // codes 3 | 7
+  const uint32_t B = ((w >> 4) & 0x000F000Fu) | 0x64006400u;    // codes 2 | 6
+  const uint32_t C = ((w >> 8) & 0x000F000Fu) | 0x64006400u;    // codes 1 | 5
+  const uint32_t D = ((w >> 12) & 0x000F000Fu) | 0x64006400u;   // codes 0 | 4
+  v[0] = make_float2(f16hi_plus(D, -1024.f), f16hi_plus(C, -1024.f));
+  v[1] = make_float2(f16hi_plus(B, -1024.f), f16hi_plus(A, -1024.f));
+  v[2] = make_float2(f16lo_plus(D, -1024.f), f16lo_plus(C, -1024.f));
+  v[3] = make_float2(f16lo_plus(B, -1024.f), f16lo_plus(A, -1024.f));
 }
 
 // fp32 value c of the 6-bit code at stream bit B of the lane's twin words
@@ -259,30 +271,35 @@ __device__ __forceinline__ float q6_twin_c(uint32_t w0, uint32_t w1) {
   return f16lo_plus((t & 63u) | 0x6400u, -1024.f);
 }
 
-// Split-K commit of a warp's tile, in three parts that the consumer loop
-// spreads over three tiles so that no warp waits for a round trip to L2:
-// l_store writes the partial sums of rows (2l, 2l + 1) of tile (strip, kt);
-// a tile later, l_count counts it in (lane 0: an acq_rel atomicInc that
-// wraps to zero -- its release covers every lane's stores, ordered by the
-// warp barrier, which by then have long landed); another tile later,
-// l_finish reads the count, and the warp that brought it to TK adds the
-// strip's partials in ascending tile order and writes y.
-template <int BP>
-__device__ __forceinline__ void l_store(const QArgs& a, int strip, int kt, int lane,
-                                        const float (&p0)[BP], const float (&p1)[BP]) {
-  const int row0 = strip * 64 + 2 * lane;
+// Split-K commit of a warp's unit (one row of every lane of a tile), in
+// three parts that the consumer loop spreads over three units so that no
+// warp waits for a round trip to L2: l_store writes the partial sum of each
+// lane's row of tile (strip, kt); a unit later, l_count counts it in (lane
+// 0: an acq_rel atomicInc that wraps to zero -- its release covers every
+// lane's stores, ordered by the warp barrier, which by then have long
+// landed); another unit later, l_finish reads the count, and the warp that
+// brought it to 2 TK adds the strip's partials in ascending tile order and
+// writes y.
+template <int R, int BP>
+__device__ __forceinline__ void l_store(const QArgs& a, int strip, int kt, int row,
+                                        const float (&p)[R][BP]) {
 #pragma unroll
   for (int b = 0; b < BP; ++b)
-    if (b < a.batch)
-      *reinterpret_cast<float2*>(a.ws + ((size_t)kt * a.batch + b) * a.N + row0) =
-          make_float2(p0[b], p1[b]);
+    if (b < a.batch) {
+      float* q = a.ws + ((size_t)kt * a.batch + b) * a.N + strip * 64 + row;
+      if (R == 2) *reinterpret_cast<float2*>(q) = make_float2(p[0][b], p[R - 1][b]);
+      else *q = p[0][b];
+    }
 }
+// UPT units per tile: the strip completes after UPT * TK of them
+template <int UPT>
 __device__ __forceinline__ uint32_t l_count(const QArgs& a, int strip, int lane) {
   __syncwarp();
-  return lane == 0 ? atom_inc_acq_rel(a.counters + strip, (unsigned)(a.TK - 1)) : 0u;
+  return lane == 0 ? atom_inc_acq_rel(a.counters + strip, (unsigned)(UPT * a.TK - 1)) : 0u;
 }
+template <int UPT>
 __device__ __forceinline__ void l_finish(const QArgs& a, int strip, int lane, uint32_t old) {
-  if (__shfl_sync(0xFFFFFFFFu, old, 0) != (uint32_t)(a.TK - 1)) return;
+  if (__shfl_sync(0xFFFFFFFFu, old, 0) != (uint32_t)(UPT * a.TK - 1)) return;
   __syncwarp();   // the last arriver's acquire (lane 0) orders the reads below
   const int row0 = strip * 64 + 2 * lane;
   const size_t step = (size_t)a.batch * a.N;
@@ -302,8 +319,8 @@ __device__ __forceinline__ void l_finish(const QArgs& a, int strip, int lane, ui
   }
 }
 
-template <int FMT, bool TWIN, int BP>
-__global__ void __launch_bounds__((16 + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
+template <int FMT, bool TWIN, int BP, int R>
+__global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int nthreads = blockDim.x;
   const int nw = nthreads / 32 - kLProducers;   // consumer warps; warps nw.. produce
@@ -336,7 +353,7 @@ __global__ void __launch_bounds__((16 + kLProducers) * 32, 1) q_lut_kernel(const
     mbar_init(tbar, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2 / R);   // every unit of the tile releases it
       stage_tile[s] = -1;
     }
     fence_barrier_init();
@@ -456,15 +473,18 @@ __global__ void __launch_bounds__((16 + kLProducers) * 32, 1) q_lut_kernel(const
   }
   pdl_wait();
   int* next = reinterpret_cast<int*>(smem + kLHdrNext);
-  // commit pipeline: strip of the tile stored last (not yet counted), and
+  // commit pipeline: strip of the unit stored last (not yet counted), and
   // the strip counted last with its pending count (-1: none)
   int ps1 = -1, ps2 = -1;
   uint32_t old2 = 0u;
+  constexpr int UPT = 2 / R;            // units per tile
+  const int n_units = UPT * n_local;    // unit u: rows 2l + h0 .. 2l + h0 + R - 1 of tile u / UPT
   while (true) {
-    int i = 0;
-    if (lane == 0) i = *err ? n_local : atomicAdd(next, 1);
-    i = __shfl_sync(0xFFFFFFFFu, i, 0);
-    if (i >= n_local) break;
+    int u = 0;
+    if (lane == 0) u = *err ? n_units : atomicAdd(next, 1);
+    u = __shfl_sync(0xFFFFFFFFu, u, 0);
+    if (u >= n_units) break;
+    const int i = u / UPT, h0 = R == 1 ? (u & 1) : 0;
     const int s = i % S;
     // first the producer's announcement that stage s carries tile i (then the
     // barrier's phase i / S is the one in progress), then the barrier
@@ -472,8 +492,10 @@ __global__ void __launch_bounds__((16 + kLProducers) * 32, 1) q_lut_kernel(const
     if (!got) {
       const long long t0 = clock64();
       bool announced;
-      while (!(announced = ld_acquire(&stage_tile[s]) == i))
+      while (!(announced = ld_acquire(&stage_tile[s]) == i)) {
         if (*err || clock64() - t0 > kWaitCycles) break;
+        __nanosleep(64);   // leave the issue slots to the warps that decode
+      }
       if (announced)
         while (!(got = mbar_try_wait(&full[s], (i / S) & 1)))
           if (*err || clock64() - t0 > kWaitCycles) break;
@@ -491,173 +513,185 @@ __global__ void __launch_bounds__((16 + kLProducers) * 32, 1) q_lut_kernel(const
     const uint32_t qp = wb + (uint32_t)g.qp_off;
     const uint32_t sx = wb + (uint32_t)g.x_off;
     const bool fits = lds_s32(sx + BP * 1024) != 0;
-    float p0[BP], p1[BP];
+    // the unit's row streams: row 2l from the lane's start, row 2l + 1 from its mid offset
+    uint32_t start[R], end[R];
+    if (!TWIN) {
+      const uint32_t mid = lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
+      const uint32_t last = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
 #pragma unroll
-    for (int b = 0; b < BP; ++b) p0[b] = p1[b] = 0.f;
+      for (int r = 0; r < R; ++r) {
+        const int h = h0 + r;
+        start[r] = h ? mid : 0u;
+        end[r] = h ? last : mid;
+      }
+    }
+    float p[R][BP];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < BP; ++b) p[r][b] = 0.f;
     if (!fits) {
       if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
     } else if (FMT == kQ4) {
-      float xe[BP], xa[BP];
+      float xa[BP];
 #pragma unroll
-      for (int b = 0; b < BP; ++b) tile_sums(sx + 1024u * b, lane, xe[b], xa[b]);
-      float2 acc0[BP], acc1[BP];
+      for (int b = 0; b < BP; ++b) xa[b] = tile_sum256(sx + 1024u * b, lane);
+      float2 acc[R][BP];
 #pragma unroll
-      for (int b = 0; b < BP; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < BP; ++b) acc[r][b] = make_float2(0.f, 0.f);
       if (!TWIN) {
-        const uint32_t mid = lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
-        LStream A, B;
-        A.init(wb, lane, g.stage_rows, 0u);
-        B.init(wb, lane, g.stage_rows, mid);
-#pragma unroll 4
+        LStream st[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
+#pragma unroll 8 / R
         for (int j = 0; j < 64; ++j) {
-          uint32_t a0, a1, b0, b1;
-          l_decode2(A, dec, a0, a1);
-          l_decode2(B, dec, b0, b1);
-          const float2 va0 = make_float2(even_val(a0), f16hi_plus(a0, -1024.f));
-          const float2 va1 = make_float2(even_val(a1), f16hi_plus(a1, -1024.f));
-          const float2 vb0 = make_float2(even_val(b0), f16hi_plus(b0, -1024.f));
-          const float2 vb1 = make_float2(even_val(b1), f16hi_plus(b1, -1024.f));
+          float2 v[R][2];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            uint32_t e0, e1;
+            l_decode2(st[r], dec, e0, e1);
+            v[r][0] = q4_vals(e0);
+            v[r][1] = q4_vals(e1);
+          }
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float4 xv = lds_f4(sx + 1024u * b + 16u * (uint32_t)j);
-            acc0[b] = __ffma2_rn(va0, make_float2(xv.x, xv.y), acc0[b]);
-            acc0[b] = __ffma2_rn(va1, make_float2(xv.z, xv.w), acc0[b]);
-            acc1[b] = __ffma2_rn(vb0, make_float2(xv.x, xv.y), acc1[b]);
-            acc1[b] = __ffma2_rn(vb1, make_float2(xv.z, xv.w), acc1[b]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              acc[r][b] = __ffma2_rn(v[r][0], make_float2(xv.x, xv.y), acc[r][b]);
+              acc[r][b] = __ffma2_rn(v[r][1], make_float2(xv.z, xv.w), acc[r][b]);
+            }
           }
         }
-        const uint32_t end = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
-        if (A.consumed() != mid || B.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
       } else {
         // twin: row 2l in words 0..31 of lane l, row 2l + 1 in words 32..63
-        const uint32_t la = wb + 4u * (uint32_t)lane;
-#pragma unroll 2
+        const uint32_t la = wb + 4u * (uint32_t)lane + 4096u * (uint32_t)h0;
+#pragma unroll 4 / R
         for (int jj = 0; jj < 32; ++jj) {
-          float2 va[4], vb[4];
-          q4_twin_word(lds_u32(la + 128u * (uint32_t)jj), va);
-          q4_twin_word(lds_u32(la + 128u * (uint32_t)(32 + jj)), vb);
+          float2 v[R][4];
+#pragma unroll
+          for (int r = 0; r < R; ++r) q4_twin_word(lds_u32(la + 4096u * r + 128u * (uint32_t)jj), v[r]);
 #pragma unroll
           for (int b = 0; b < BP; ++b) {
             const float4 xa4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj);
             const float4 xb4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj + 16u);
-            acc0[b] = __ffma2_rn(va[0], make_float2(xa4.x, xa4.y), acc0[b]);
-            acc0[b] = __ffma2_rn(va[1], make_float2(xa4.z, xa4.w), acc0[b]);
-            acc0[b] = __ffma2_rn(va[2], make_float2(xb4.x, xb4.y), acc0[b]);
-            acc0[b] = __ffma2_rn(va[3], make_float2(xb4.z, xb4.w), acc0[b]);
-            acc1[b] = __ffma2_rn(vb[0], make_float2(xa4.x, xa4.y), acc1[b]);
-            acc1[b] = __ffma2_rn(vb[1], make_float2(xa4.z, xa4.w), acc1[b]);
-            acc1[b] = __ffma2_rn(vb[2], make_float2(xb4.x, xb4.y), acc1[b]);
-            acc1[b] = __ffma2_rn(vb[3], make_float2(xb4.z, xb4.w), acc1[b]);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              acc[r][b] = __ffma2_rn(v[r][0], make_float2(xa4.x, xa4.y), acc[r][b]);
+              acc[r][b] = __ffma2_rn(v[r][1], make_float2(xa4.z, xa4.w), acc[r][b]);
+              acc[r][b] = __ffma2_rn(v[r][2], make_float2(xb4.x, xb4.y), acc[r][b]);
+              acc[r][b] = __ffma2_rn(v[r][3], make_float2(xb4.z, xb4.w), acc[r][b]);
+            }
           }
         }
       }
-      // scale | min << 16 of rows 2l and 2l + 1
-      const uint2 q = lds_u2(qp + 8u * (uint32_t)lane);
-      const float sc0 = __half2float(__ushort_as_half((unsigned short)(q.x & 0xFFFFu)));
-      const float mn0 = __half2float(__ushort_as_half((unsigned short)(q.x >> 16)));
-      const float sc1 = __half2float(__ushort_as_half((unsigned short)(q.y & 0xFFFFu)));
-      const float mn1 = __half2float(__ushort_as_half((unsigned short)(q.y >> 16)));
 #pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        p0[b] = fmaf(sc0, (acc0[b].x - 128.f * xe[b]) + acc0[b].y, mn0 * xa[b]);
-        p1[b] = fmaf(sc1, (acc1[b].x - 128.f * xe[b]) + acc1[b].y, mn1 * xa[b]);
+      for (int r = 0; r < R; ++r) {
+        // scale | min << 16 of row 2l + h0 + r
+        const uint32_t q = lds_u32(qp + 4u * (uint32_t)(2 * lane + h0 + r));
+        const float sc = __half2float(__ushort_as_half((unsigned short)(q & 0xFFFFu)));
+        const float mn = __half2float(__ushort_as_half((unsigned short)(q >> 16)));
+#pragma unroll
+        for (int b = 0; b < BP; ++b) p[r][b] = fmaf(sc, acc[r][b].x + acc[r][b].y, mn * xa[b]);
       }
     } else {  // 6-bit: 16 groups of 16 weights per row
       float X[BP];
 #pragma unroll
       for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
-      const uint32_t mid = TWIN ? 0u : lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
-      LStream A, B;
-      if (!TWIN) {
-        A.init(wb, lane, g.stage_rows, 0u);
-        B.init(wb, lane, g.stage_rows, mid);
-      }
-      const uint32_t la = wb + 4u * (uint32_t)lane;
+      LStream st[R];
+      if (!TWIN)
+#pragma unroll
+        for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
+      // twin: row 2l in words 0..47, row 2l + 1 in words 48..95
+      const uint32_t la = wb + 4u * (uint32_t)lane + 6144u * (uint32_t)h0;
 #pragma unroll 1
       for (int gi = 0; gi < 16; ++gi) {
-        float2 acc0[BP], acc1[BP];
+        float2 acc[R][BP];
 #pragma unroll
-        for (int b = 0; b < BP; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int b = 0; b < BP; ++b) acc[r][b] = make_float2(0.f, 0.f);
         if (!TWIN) {
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
-            uint32_t a0, a1, b0, b1;
-            l_decode2(A, dec, a0, a1);
-            l_decode2(B, dec, b0, b1);
-            const float2 va = make_float2(f16hi_plus(a0, -1024.f), f16hi_plus(a1, -1024.f));
-            const float2 vb = make_float2(f16hi_plus(b0, -1024.f), f16hi_plus(b1, -1024.f));
+            float2 v[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              uint32_t e0, e1;
+              l_decode2(st[r], dec, e0, e1);
+              v[r] = make_float2(f16hi_plus(e0, -1024.f), f16hi_plus(e1, -1024.f));
+            }
 #pragma unroll
             for (int b = 0; b < BP; ++b) {
               const float2 xv = lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m);
-              acc0[b] = __ffma2_rn(va, xv, acc0[b]);
-              acc1[b] = __ffma2_rn(vb, xv, acc1[b]);
+#pragma unroll
+              for (int r = 0; r < R; ++r) acc[r][b] = __ffma2_rn(v[r], xv, acc[r][b]);
             }
           }
         } else {
-          // group gi of row 2l: codes 16 gi .. 16 gi + 15 at bits 96 gi ..; row 2l + 1
-          // starts at word 48 (bit 1536)
-          const uint32_t wa = la + 128u * (uint32_t)(3 * gi);
-          const uint32_t wbb = la + 128u * (uint32_t)(48 + 3 * gi);
-          const uint32_t a0w = lds_u32(wa), a1w = lds_u32(wa + 128u), a2w = lds_u32(wa + 256u);
-          const uint32_t b0w = lds_u32(wbb), b1w = lds_u32(wbb + 128u), b2w = lds_u32(wbb + 256u);
-          float va[16], vb[16];
-          va[0] = q6_twin_c<0>(a0w, a1w);   va[1] = q6_twin_c<6>(a0w, a1w);
-          va[2] = q6_twin_c<12>(a0w, a1w);  va[3] = q6_twin_c<18>(a0w, a1w);
-          va[4] = q6_twin_c<24>(a0w, a1w);  va[5] = q6_twin_c<30>(a0w, a1w);
-          va[6] = q6_twin_c<4>(a1w, a2w);   va[7] = q6_twin_c<10>(a1w, a2w);
-          va[8] = q6_twin_c<16>(a1w, a2w);  va[9] = q6_twin_c<22>(a1w, a2w);
-          va[10] = q6_twin_c<28>(a1w, a2w); va[11] = q6_twin_c<2>(a2w, 0u);
-          va[12] = q6_twin_c<8>(a2w, 0u);   va[13] = q6_twin_c<14>(a2w, 0u);
-          va[14] = q6_twin_c<20>(a2w, 0u);  va[15] = q6_twin_c<26>(a2w, 0u);
-          vb[0] = q6_twin_c<0>(b0w, b1w);   vb[1] = q6_twin_c<6>(b0w, b1w);
-          vb[2] = q6_twin_c<12>(b0w, b1w);  vb[3] = q6_twin_c<18>(b0w, b1w);
-          vb[4] = q6_twin_c<24>(b0w, b1w);  vb[5] = q6_twin_c<30>(b0w, b1w);
-          vb[6] = q6_twin_c<4>(b1w, b2w);   vb[7] = q6_twin_c<10>(b1w, b2w);
-          vb[8] = q6_twin_c<16>(b1w, b2w);  vb[9] = q6_twin_c<22>(b1w, b2w);
-          vb[10] = q6_twin_c<28>(b1w, b2w); vb[11] = q6_twin_c<2>(b2w, 0u);
-          vb[12] = q6_twin_c<8>(b2w, 0u);   vb[13] = q6_twin_c<14>(b2w, 0u);
-          vb[14] = q6_twin_c<20>(b2w, 0u);  vb[15] = q6_twin_c<26>(b2w, 0u);
 #pragma unroll
-          for (int m = 0; m < 8; ++m)
+          for (int r = 0; r < R; ++r) {
+            // group gi: codes 16 gi .. 16 gi + 15 at bits 96 gi .. of the row's words
+            const uint32_t wa = la + 6144u * r + 128u * (uint32_t)(3 * gi);
+            const uint32_t w0 = lds_u32(wa), w1 = lds_u32(wa + 128u), w2 = lds_u32(wa + 256u);
+            float v[16];
+            v[0] = q6_twin_c<0>(w0, w1);   v[1] = q6_twin_c<6>(w0, w1);
+            v[2] = q6_twin_c<12>(w0, w1);  v[3] = q6_twin_c<18>(w0, w1);
+            v[4] = q6_twin_c<24>(w0, w1);  v[5] = q6_twin_c<30>(w0, w1);
+            v[6] = q6_twin_c<4>(w1, w2);   v[7] = q6_twin_c<10>(w1, w2);
+            v[8] = q6_twin_c<16>(w1, w2);  v[9] = q6_twin_c<22>(w1, w2);
+            v[10] = q6_twin_c<28>(w1, w2); v[11] = q6_twin_c<2>(w2, 0u);
+            v[12] = q6_twin_c<8>(w2, 0u);  v[13] = q6_twin_c<14>(w2, 0u);
+            v[14] = q6_twin_c<20>(w2, 0u); v[15] = q6_twin_c<26>(w2, 0u);
 #pragma unroll
-            for (int b = 0; b < BP; ++b) {
-              const float2 xv = lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m);
-              acc0[b] = __ffma2_rn(make_float2(va[2 * m], va[2 * m + 1]), xv, acc0[b]);
-              acc1[b] = __ffma2_rn(make_float2(vb[2 * m], vb[2 * m + 1]), xv, acc1[b]);
-            }
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+              for (int b = 0; b < BP; ++b)
+                acc[r][b] = __ffma2_rn(make_float2(v[2 * m], v[2 * m + 1]),
+                                       lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m),
+                                       acc[r][b]);
+          }
         }
-        // scales of group gi of rows 2l (chunk gi/8) and 2l + 1 (chunk 2 + gi/8)
-        const uint32_t sa = qp + (uint32_t)((((gi >> 3) * 32) + lane) * 16 + 2 * (gi & 7));
-        const float s0 = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
-        const float s1 = __half2float(__ushort_as_half((unsigned short)lds_u16(sa + 1024u)));
 #pragma unroll
-        for (int b = 0; b < BP; ++b) {
-          const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], gi);
-          p0[b] = fmaf(s0, (acc0[b].x + acc0[b].y) - 32.f * Xg, p0[b]);
-          p1[b] = fmaf(s1, (acc1[b].x + acc1[b].y) - 32.f * Xg, p1[b]);
+        for (int r = 0; r < R; ++r) {
+          // scale of group gi of row 2l + h: chunk 2h + gi/8, position gi % 8
+          const int h = h0 + r;
+          const uint32_t sa = qp + (uint32_t)((((2 * h + (gi >> 3)) * 32) + lane) * 16 + 2 * (gi & 7));
+          const float sc = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
+#pragma unroll
+          for (int b = 0; b < BP; ++b) {
+            const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], gi);
+            p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 32.f * Xg, p[r][b]);
+          }
         }
       }
-      if (!TWIN) {
-        const uint32_t end = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
-        if (A.consumed() != mid || B.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
-      }
+      if (!TWIN)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
     }
-    // release the stage: this warp's reads of it are done (their values are in
-    // the partial sums), ordered before the producer's next bulk copy into it
+    // release the stage (UPT units per stage): this warp's reads of it are
+    // done (their values are in the partial sums), ordered before the
+    // producer's next bulk copy into it
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     // a tile too long for its stage commits zeros, so that its strip still
     // completes; a tile behind an invalid strip-list entry commits nothing
-    if (!valid && lane == 0) report(a.status, LW_DEV_BAD_STRIPS);
-    if (ps2 >= 0) l_finish(a, ps2, lane, old2);
+    if (!valid && lane == 0 && h0 == 0) report(a.status, LW_DEV_BAD_STRIPS);
+    if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
     ps2 = ps1;
-    if (ps1 >= 0) old2 = l_count(a, ps1, lane);
-    if (valid) l_store<BP>(a, strip, kt, lane, p0, p1);
+    if (ps1 >= 0) old2 = l_count<UPT>(a, ps1, lane);
+    if (valid) l_store<R, BP>(a, strip, kt, 2 * lane + h0, p);
     ps1 = valid ? strip : -1;
   }
-  if (ps2 >= 0) l_finish(a, ps2, lane, old2);
-  if (ps1 >= 0) l_finish(a, ps1, lane, l_count(a, ps1, lane));
+  if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
+  if (ps1 >= 0) l_finish<UPT>(a, ps1, lane, l_count<UPT>(a, ps1, lane));
   pdl_trigger();
 }
 
