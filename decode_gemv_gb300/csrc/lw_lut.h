@@ -50,27 +50,40 @@ LW_HD int lut_limit(const uint32_t* lim_m1, int lmin, int lmax, int L) {
   return (int)((lim_m1[L - lmin] + 1u) >> 21);
 }
 
+// The shape for one choice of s (1 <= s <= 10).
+LW_HD LutShape lut_shape_at(const uint32_t* lim_m1, int lmin, int lmax, int s) {
+  const int T = lut_limit(lim_m1, lmin, lmax, 11 - s);
+  if (T >= 2048) return LutShape{s, 2048, T, 2048 >> s};
+  int L1 = 12 - s;   // length of the code starting at peek T
+  while (L1 < 11 && lut_limit(lim_m1, lmin, lmax, L1) <= T) ++L1;
+  const int B = 1 << (11 - L1);
+  return LutShape{s, T + B - (T >> s) - 1, T, (T >> s) + 1 + (2048 - T - B)};
+}
+// The smallest shape; among equally small ones, the one of smallest s.
 LW_HD LutShape lut_shape(const uint32_t* lim_m1, int lmin, int lmax) {
   LutShape best{0, 0, 2048, 2048};
   if (lmin < 1 || lmax > 11 || lmin > lmax) return best;   // not a valid table
   for (int s = 1; s <= 10; ++s) {
-    const int T = lut_limit(lim_m1, lmin, lmax, 11 - s);
-    int n, C;
-    if (T >= 2048) {
-      n = 2048 >> s;
-      C = 2048;
-    } else {
-      int L1 = 12 - s;   // length of the code starting at peek T
-      while (L1 < 11 && lut_limit(lim_m1, lmin, lmax, L1) <= T) ++L1;
-      const int B = 1 << (11 - L1);
-      n = (T >> s) + 1 + (2048 - T - B);
-      C = T + B - (T >> s) - 1;
-    }
-    if (n < best.n) best = LutShape{s, C, T, n};
+    const LutShape c = lut_shape_at(lim_m1, lmin, lmax, s);
+    if (c.n < best.n) best = c;
   }
   return best;
 }
-
+#if defined(__CUDACC__)
+// lut_shape by one warp, lane s - 1 trying s (every lane gets the result).
+__device__ __forceinline__ LutShape lut_shape_warp(const uint32_t* lim_m1, int lmin, int lmax,
+                                                   int lane) {
+  if (lmin < 1 || lmax > 11 || lmin > lmax) return LutShape{0, 0, 2048, 2048};
+  LutShape c{0, 0, 2048, 2048};
+  if (lane < 10) c = lut_shape_at(lim_m1, lmin, lmax, lane + 1);
+  // smallest n, then smallest s (n <= 2048 < 2^12, s <= 10 < 2^4)
+  const unsigned key = __reduce_min_sync(0xFFFFFFFFu, ((unsigned)c.n << 4) | (unsigned)c.s);
+  const int src = (int)(key & 15u) - 1;   // the lane that tried the winning s (>= 0: n < 2048)
+  if (src < 0) return LutShape{0, 0, 2048, 2048};
+  return LutShape{__shfl_sync(0xFFFFFFFFu, c.s, src), __shfl_sync(0xFFFFFFFFu, c.C, src),
+                  __shfl_sync(0xFFFFFFFFu, c.T, src), __shfl_sync(0xFFFFFFFFu, c.n, src)};
+}
+#endif
 // The peek that table index i stands for (any peek mapping to i decodes the
 // same codeword).
 LW_HD int lut_peek(const LutShape& sh, int i) {

@@ -169,28 +169,34 @@ __device__ __forceinline__ float2 q4_vals(uint32_t e) {
 
 // Build the replicated table of a checked, staged lw_table: consumer warp w
 // takes entries 32 w .. 32 w + 31, then 32 (w + NW) .., ...; lane j decodes
-// entry i0 + j, then every entry of the group is broadcast and each lane
-// stores its own copy (lane l's copy of entry i at table + 128 i + 4 l).
+// entry i0 + j and stores its 32 copies (lane l's copy of entry i at
+// table + 128 i + 4 l).
 __device__ __forceinline__ void lut_build(const lw_table* tb, const LutShape& sh, uint32_t lut,
                                           int warp, int nw, int lane) {
   const int lmin = tb->lmin, lmax = tb->lmax;
+  // the limits in registers (lim_m1[j] = all ones from lmax - lmin on)
+  uint32_t lim[10];
+#pragma unroll
+  for (int j = 0; j < 10; ++j) lim[j] = tb->lim_m1[j];
   for (int i0 = warp * 32; i0 < sh.n; i0 += nw * 32) {
     // lane j decodes entry i0 + j
     uint32_t e = 0;
     const int i = i0 + lane;
     if (i < sh.n) {
       const uint32_t win = (uint32_t)lut_peek(sh, i) << 21;
+      // the code's length: lmin plus the limits below the window
       int L = lmin;
-      while (L < lmax && win > tb->lim_m1[L - lmin]) ++L;
+#pragma unroll
+      for (int j = 0; j < 10; ++j) L += (j < lmax - lmin && win > lim[j]) ? 1 : 0;
       const int idx = (int)(win >> (32 - L)) + tb->off[L - lmin];
       e = lut_entry(tb->fmt, tb->sym[idx], L);
-    }
-    const int cnt = sh.n - i0 < 32 ? sh.n - i0 : 32;
-    for (int j = 0; j < cnt; ++j) {
-      const uint32_t v = __shfl_sync(0xFFFFFFFFu, e, j);
-      asm volatile("st.shared.u32 [%0], %1;" ::"r"(lut + (uint32_t)(i0 + j) * 128u + 4u * lane),
-                   "r"(v)
-                   : "memory");
+      // the lane writes its entry's 32 copies, copy (lane + r) mod 32 at
+      // step r: the warp's 32 stores of a step hit 32 different banks
+      const uint32_t row = lut + (uint32_t)i * 128u;
+#pragma unroll 8
+      for (int r = 0; r < 32; ++r)
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(row + 4u * (uint32_t)((lane + r) & 31)), "r"(e)
+                     : "memory");
     }
   }
 }
@@ -319,6 +325,20 @@ __device__ __forceinline__ void l_finish(const QArgs& a, int strip, int lane, ui
   }
 }
 
+// Row range [r0, r1) and bundle tile t of local tile i of a CTA (zeros past
+// its last tile).
+__device__ __forceinline__ void l_rows(const QArgs& a, int c0, int cnt, int n_local, int i,
+                                       uint32_t& r0, uint32_t& r1, int& t) {
+  r0 = r1 = 0u;
+  t = 0;
+  if (i < n_local) {
+    bool v;
+    t = list_tile<true>(a, c0 + i * cnt, v);
+    r0 = __ldg(a.tile_off + t);
+    r1 = __ldg(a.tile_off + t + 1);
+  }
+}
+
 template <int FMT, bool TWIN, int BP, int R>
 __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -339,6 +359,15 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
   volatile int* err = reinterpret_cast<volatile int*>(smem + kLHdrErr);
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kLRawTab);
   const uint32_t sbase = smem_addr(smem);
+  // Let the stream's next kernel be scheduled at once: its CTAs take each SM
+  // as this kernel's CTA there exits, and run their prologue (barriers,
+  // decode table, first weight copies) while the other SMs still drain.
+  pdl_trigger();
+  // a producer's first loads (the row ranges of its first 32 tiles) go out
+  // before anything else
+  uint32_t cr0 = 0u, cr1 = 0u;
+  int ct = 0;
+  if (producer) l_rows(a, c0, cnt, n_local, (warp - nw) + lane * kLProducers, cr0, cr1, ct);
 
   // activation rows beyond `batch` stay zero in every stage
   if (BP > 1) {
@@ -369,27 +398,37 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
   // 32 c + j of the current chunk c and the next (in flight a chunk ahead);
   // lane 0 issues each tile's copies once its stage is free.
   if (producer) {
-    pdl_wait();
     constexpr uint32_t qpb = QFmt<FMT>::qp_bytes;
     const int pw = warp - nw;                  // producer index
     auto rows_of = [&](int k, uint32_t& r0, uint32_t& r1, int& t) {
-      const int i = pw + k * kLProducers;
-      r0 = r1 = 0u;
-      t = 0;
-      if (i < n_local) {
-        bool v;
-        t = list_tile<true>(a, c0 + i * cnt, v);
-        r0 = __ldg(a.tile_off + t);
-        r1 = __ldg(a.tile_off + t + 1);
-      }
+      l_rows(a, c0, cnt, n_local, pw + k * kLProducers, r0, r1, t);
     };
-    uint32_t cr0, cr1, nr0, nr1;
-    int ct, nt, cb = 0;
-    rows_of(lane, cr0, cr1, ct);
+    uint32_t nr0, nr1;
+    int nt, cb = 0;
     rows_of(32 + lane, nr0, nr1, nt);
     int issued = -1;   // last local tile this warp issued
+    // The first pass over the ring (tiles i < S, chunk 0) needs no free stage
+    // and its weight copies read the bundle only: they go out before the
+    // wait for the previous kernel, their activation copies after it.
+    const uint32_t xbytes = (uint32_t)a.batch * 1024u;
+    auto copy_x = [&](int k) {
+      const int t = __shfl_sync(0xFFFFFFFFu, ct, k);
+      if (lane == 0) {
+        const int i = pw + k * kLProducers, s = i % S, kt = t % a.TK;
+        uint8_t* st = smem + g.ring_off + s * g.stage_bytes;
+        for (int b = 0; b < a.batch; ++b)
+          bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
+                   &full[s]);
+      }
+    };
+    bool waited = false;
     for (int k = 0; pw + k * kLProducers < n_local; ++k) {
       const int i = pw + k * kLProducers;
+      if (!waited && i >= S) {
+        pdl_wait();
+        waited = true;
+        for (int kk = 0; kk < k; ++kk) copy_x(kk);
+      }
       if (k == cb + 32) {   // move to the next chunk; start loading the one after
         cr0 = nr0; cr1 = nr1; ct = nt;
         cb += 32;
@@ -419,7 +458,6 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
         const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(g.stage_rows - 2);
         const uint32_t wbytes = fits ? (r1 - r0) * 128u : 0u;
         const uint32_t mbytes = TWIN ? 0u : 128u;   // mid offsets + lane bit counts
-        const uint32_t xbytes = (uint32_t)a.batch * 1024u;
         // the stage records whether the tile fits (read by the consumer after
         // the barrier completes, which orders this store before it)
         *reinterpret_cast<volatile int*>(st + g.x_off + BP * 1024) = fits ? 1 : 0;
@@ -434,18 +472,23 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
           bulk_g2s(st + g.mid_off, a.lane_mid + (size_t)t * 32, 64, &full[s]);
           bulk_g2s(st + g.lb_off, a.lane_bits + (size_t)t * 32, 64, &full[s]);
         }
-        const int kt = t % a.TK;
-        for (int b = 0; b < a.batch; ++b)
-          bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
-                   &full[s]);
+        if (waited) {
+          const int kt = t % a.TK;
+          for (int b = 0; b < a.batch; ++b)
+            bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
+                     &full[s]);
+        }
       }
       issued = i;
+    }
+    if (!waited) {   // every tile of this warp was in the first pass
+      pdl_wait();
+      for (int kk = 0; pw + kk * kLProducers <= issued; ++kk) copy_x(kk);
     }
     // after an error: let this warp's copies still in flight land before leaving
     if (lane == 0 && *err)
       for (int i = issued; i >= 0 && i > issued - S; i -= kLProducers)
         mbar_wait(&full[i % S], (i / S) & 1);
-    pdl_trigger();
     return;
   }
 
@@ -456,7 +499,7 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
     bool ok = got && table_ok_warp(tb, FMT, QFmt<FMT>::alpha, 10, lane);
     LutShape sh{0, 0, 2048, 2048};
     if (ok) {
-      sh = lut_shape(tb->lim_m1, tb->lmin, tb->lmax);
+      sh = lut_shape_warp(tb->lim_m1, tb->lmin, tb->lmax, lane);
       ok = sh.n <= g.lut_cap;
     }
     if (!ok) {
@@ -692,7 +735,6 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
   }
   if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
   if (ps1 >= 0) l_finish<UPT>(a, ps1, lane, l_count<UPT>(a, ps1, lane));
-  pdl_trigger();
 }
 
 }  // namespace dev

@@ -1,6 +1,6 @@
 """Huffman lanes against rANS lanes on the workloads' weight distributions
-(analysis, test infrastructure: uses the oracle only).  Prints a markdown
-table; `python oracle/compare_rans.py > profiles/rans_vs_huffman.md`."""
+(analysis, test infrastructure: uses the oracle only).  Prints the
+comparison as a markdown table on standard output."""
 import os
 import sys
 
