@@ -130,7 +130,7 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
   // decodes), spread so that a CTA's units come in whole waves, and at
   // least 8 (they build the decode table)
   int nw_max = (2 / R) * (S - 4);
-  const int cap = R == 2 ? 16 : dev::kLMaxConsumers;
+  const int cap = R == 2 ? dev::kLMaxConsumersR<2> : dev::kLMaxConsumersR<1>;
   if (nw_max > cap) nw_max = cap;
   const int units = (2 / R) * max_per_cta;
   const int waves = (units + nw_max - 1) / nw_max;

@@ -95,7 +95,11 @@ constexpr int kLHdrTiles = kLRawTab + (int)sizeof(lw_table);   // int[S]: tile e
 constexpr int kLHdrBytes = kLHdrTiles + 4 * kLMaxStages;
 constexpr int kLGuardRows = 132;  // rows a corrupt 6-bit stream may read past its stage
 constexpr int kLProducers = 4;    // producer warps (each issues its own stages' copies)
-constexpr int kLMaxConsumers = 24;  // consumer warps at most (two per tile being decoded)
+constexpr int kLMaxConsumers = 24;
+// consumer warps a launch of R rows per unit may use (R = 2: 16, so that
+// the kernel may keep more registers per thread)
+template <int R>
+constexpr int kLMaxConsumersR = R == 2 ? 16 : kLMaxConsumers;  // consumer warps at most (two per tile being decoded)
 
 // a * b + c as one integer multiply-add (FMA pipe; the compiler would
 // otherwise often use shift-and-add forms on the integer ALU pipe)
@@ -303,26 +307,43 @@ __device__ __forceinline__ uint32_t l_count(const QArgs& a, int strip, int lane)
   __syncwarp();
   return lane == 0 ? atom_inc_acq_rel(a.counters + strip, (unsigned)(UPT * a.TK - 1)) : 0u;
 }
+// The strip's reduction (the last arriver's warp), G partials per round
+// trip to L2 (G = 16: two groups of 8 loaded before either is added).
+template <int G>
+__device__ __forceinline__ void l_reduce(const QArgs& a, int strip, int lane) {
+  const int row0 = strip * 64 + 2 * lane;
+  const size_t step = (size_t)a.batch * a.N;
+  for (int b = 0; b < a.batch; ++b) {
+    const float2* base = reinterpret_cast<const float2*>(a.ws + (size_t)b * a.N + row0);
+    const size_t st2 = step / 2;   // float2 stride between tiles of the strip
+    // the sum runs in ascending tile order
+    float2 s = make_float2(0.f, 0.f);
+    for (int k0 = 0; k0 < a.TK; k0 += G) {
+      float2 v[8], w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.TK) v[i] = __ldcg(base + (size_t)(k0 + i) * st2);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (G == 16 && k0 + 8 + i < a.TK) w[i] = __ldcg(base + (size_t)(k0 + 8 + i) * st2);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (k0 + i < a.TK) {
+          if (k0 + i == 0) s = v[0];
+          else { s.x += v[i].x; s.y += v[i].y; }
+        }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (G == 16 && k0 + 8 + i < a.TK) { s.x += w[i].x; s.y += w[i].y; }
+    }
+    *reinterpret_cast<float2*>(a.y + (size_t)b * a.N + row0) = s;
+  }
+}
 template <int UPT>
 __device__ __forceinline__ void l_finish(const QArgs& a, int strip, int lane, uint32_t old) {
   if (__shfl_sync(0xFFFFFFFFu, old, 0) != (uint32_t)(UPT * a.TK - 1)) return;
   __syncwarp();   // the last arriver's acquire (lane 0) orders the reads below
-  const int row0 = strip * 64 + 2 * lane;
-  const size_t step = (size_t)a.batch * a.N;
-  for (int b = 0; b < a.batch; ++b) {
-    const float* base = a.ws + (size_t)b * a.N + row0;
-    float2 s = __ldcg(reinterpret_cast<const float2*>(base));
-    for (int k0 = 1; k0 < a.TK; k0 += 8) {
-      float2 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (k0 + i < a.TK) v[i] = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(k0 + i) * step));
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (k0 + i < a.TK) { s.x += v[i].x; s.y += v[i].y; }
-    }
-    *reinterpret_cast<float2*>(a.y + (size_t)b * a.N + row0) = s;
-  }
+  l_reduce<UPT == 1 ? 16 : 8>(a, strip, lane);
 }
 
 // Row range [r0, r1) and bundle tile t of local tile i of a CTA (zeros past
@@ -340,7 +361,7 @@ __device__ __forceinline__ void l_rows(const QArgs& a, int c0, int cnt, int n_lo
 }
 
 template <int FMT, bool TWIN, int BP, int R>
-__global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
+__global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int nthreads = blockDim.x;
   const int nw = nthreads / 32 - kLProducers;   // consumer warps; warps nw.. produce
@@ -733,8 +754,10 @@ __global__ void __launch_bounds__((kLMaxConsumers + kLProducers) * 32, 1) q_lut_
     if (valid) l_store<R, BP>(a, strip, kt, 2 * lane + h0, p);
     ps1 = valid ? strip : -1;
   }
+  // drain: the last count's round trip overlaps the pending finish
+  const uint32_t old1 = ps1 >= 0 ? l_count<UPT>(a, ps1, lane) : 0u;
   if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
-  if (ps1 >= 0) l_finish<UPT>(a, ps1, lane, l_count<UPT>(a, ps1, lane));
+  if (ps1 >= 0) l_finish<UPT>(a, ps1, lane, old1);
 }
 
 }  // namespace dev
