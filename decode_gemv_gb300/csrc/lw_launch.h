@@ -104,6 +104,9 @@ inline float* workspace_partials(const lw_dev_bundle* b, void* ws) {
 
 // Table-driven 4-/6-bit product kernel (and the fixed-width twins on the same
 // skeleton): usable for a coded bundle whose lut_entries hint is 1..kLutCap.
+// The pending one-shot request of lw_test_stall_next (microseconds; 0:
+// none), cleared by the call.
+int take_test_stall();
 bool lut_fits(const lw_dev_bundle* b);
 // With a strip list (device array of n_strips 64-row strips), n must be 1.
 lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,

@@ -3,6 +3,8 @@
 #include <mutex>
 
 #include "lw_internal.h"
+#include <atomic>
+
 #include "lw_launch.h"
 #include "lw_qlut.cuh"
 
@@ -93,6 +95,16 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
     return fail(LW_ERR_UNSUPPORTED, "tiles of %d rows do not fit the table-driven kernel", max_rows);
   g.nstage = S;
   g.lut_off = g.ring_off + S * g.stage_bytes;
+  g.wait_cycles = dev::kWaitCycles;
+  g.stall_tile = -1;
+  // testing (lw_test_stall_next): one launch whose first stage of CTA 0 is
+  // never filled, and every wait of it limited to the requested time (SM
+  // cycles at most 2.1 GHz)
+  const int stall_us = take_test_stall();
+  if (stall_us > 0) {
+    g.wait_cycles = 2100LL * stall_us;
+    g.stall_tile = 0;
+  }
   const size_t smem = (size_t)g.lut_off + (size_t)lut_bytes;
   // CTAs: one per SM, shared among the matrices in proportion to their tiles
   const int G = device_sm_count();
@@ -164,4 +176,14 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
   return check_launch("table-driven product kernel");
 }
 
+std::atomic<int> g_test_stall_us{0};
+int take_test_stall() { return g_test_stall_us.exchange(0); }
+
 }  // namespace lw
+
+extern "C" lw_status lw_test_stall_next(int32_t wait_us) {
+  if (wait_us < 0 || wait_us > 1000000)
+    return lw::fail(LW_ERR_INVALID_ARG, "wait_us %d outside 0..1000000", (int)wait_us);
+  lw::g_test_stall_us.store(wait_us);
+  return LW_OK;
+}

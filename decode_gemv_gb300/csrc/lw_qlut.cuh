@@ -80,6 +80,8 @@ struct LLaunch {
   int lb_off;       // lane bit counts (coded bundles)
   int x_off;
   int ring_off;     // shared-memory offset of stage 0
+  long long wait_cycles;   // limit of every wait on a stage (SM clock cycles)
+  int stall_tile;   // testing: local tile of CTA 0 whose stage is armed without copies (-1: none)
   int lut_off;      // shared-memory offset of the decode table (coded bundles)
   int lut_cap;      // entries it holds (>= every member's table)
 };
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
     const uint32_t xbytes = (uint32_t)a.batch * 1024u;
     auto copy_x = [&](int k) {
       const int t = __shfl_sync(0xFFFFFFFFu, ct, k);
-      if (lane == 0) {
+      if (lane == 0 && !(blockIdx.x == 0 && pw + k * kLProducers == g.stall_tile)) {
         const int i = pw + k * kLProducers, s = i % S, kt = t % a.TK;
         uint8_t* st = smem + g.ring_off + s * g.stage_bytes;
         for (int b = 0; b < a.batch; ++b)
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
         if (!got) {
           const long long t0 = clock64();
           while (!(got = mbar_try_wait(&empty[s], ((i / S) - 1) & 1)))
-            if (*err || clock64() - t0 > kWaitCycles) break;
+            if (*err || clock64() - t0 > g.wait_cycles) break;
         }
         if (!got && !*err) report(a.status, LW_DEV_TIMEOUT);
         ok = got && !*err;
@@ -487,17 +489,22 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
         // previous phase (same parity, two phases back) for its own
         st_release(&stage_tile[s], i);
         mbar_arrive_expect_tx(&full[s], wbytes + qpb + mbytes + xbytes);
-        if (wbytes) bulk_g2s(st, a.words + (size_t)r0 * 32, wbytes, &full[s]);
-        bulk_g2s(st + g.qp_off, a.qparams + (size_t)t * qpb, qpb, &full[s]);
-        if (!TWIN) {
-          bulk_g2s(st + g.mid_off, a.lane_mid + (size_t)t * 32, 64, &full[s]);
-          bulk_g2s(st + g.lb_off, a.lane_bits + (size_t)t * 32, 64, &full[s]);
-        }
-        if (waited) {
-          const int kt = t % a.TK;
-          for (int b = 0; b < a.batch; ++b)
-            bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
-                     &full[s]);
+        // testing: a stage armed for copies that are never issued (nothing in
+        // flight; its consumer's wait runs out)
+        const bool stall = blockIdx.x == 0 && i == g.stall_tile;
+        if (!stall) {
+          if (wbytes) bulk_g2s(st, a.words + (size_t)r0 * 32, wbytes, &full[s]);
+          bulk_g2s(st + g.qp_off, a.qparams + (size_t)t * qpb, qpb, &full[s]);
+          if (!TWIN) {
+            bulk_g2s(st + g.mid_off, a.lane_mid + (size_t)t * 32, 64, &full[s]);
+            bulk_g2s(st + g.lb_off, a.lane_bits + (size_t)t * 32, 64, &full[s]);
+          }
+          if (waited) {
+            const int kt = t % a.TK;
+            for (int b = 0; b < a.batch; ++b)
+              bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
+                       &full[s]);
+          }
         }
       }
       issued = i;
@@ -508,8 +515,11 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
     }
     // after an error: let this warp's copies still in flight land before leaving
     if (lane == 0 && *err)
-      for (int i = issued; i >= 0 && i > issued - S; i -= kLProducers)
-        mbar_wait(&full[i % S], (i / S) & 1);
+      for (int i = issued; i >= 0 && i > issued - S; i -= kLProducers) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&full[i % S], (i / S) & 1) && clock64() - t0 <= g.wait_cycles) {
+        }
+      }
     return;
   }
 
@@ -544,35 +554,54 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
   constexpr int UPT = 2 / R;            // units per tile
   const int n_units = UPT * n_local;    // unit u: rows 2l + h0 .. 2l + h0 + R - 1 of tile u / UPT
   while (true) {
-    int u = 0;
-    if (lane == 0) u = *err ? n_units : atomicAdd(next, 1);
+    int u = 0, e = 0;
+    if (lane == 0) {
+      u = atomicAdd(next, 1);
+      e = *err;
+    }
     u = __shfl_sync(0xFFFFFFFFu, u, 0);
     if (u >= n_units) break;
+    // after an error in this CTA the remaining units are only counted (see
+    // below): no wait, no decode
+    bool ghost = __shfl_sync(0xFFFFFFFFu, e, 0) != 0;
     const int i = u / UPT, h0 = R == 1 ? (u & 1) : 0;
     const int s = i % S;
-    // first the producer's announcement that stage s carries tile i (then the
-    // barrier's phase i / S is the one in progress), then the barrier
-    bool got = ld_acquire(&stage_tile[s]) == i && mbar_try_wait(&full[s], (i / S) & 1);
-    if (!got) {
-      const long long t0 = clock64();
-      bool announced;
-      while (!(announced = ld_acquire(&stage_tile[s]) == i)) {
-        if (*err || clock64() - t0 > kWaitCycles) break;
-        __nanosleep(64);   // leave the issue slots to the warps that decode
+    if (!ghost) {
+      // first the producer's announcement that stage s carries tile i (then
+      // the barrier's phase i / S is the one in progress), then the barrier
+      bool got = ld_acquire(&stage_tile[s]) == i && mbar_try_wait(&full[s], (i / S) & 1);
+      if (!got) {
+        const long long t0 = clock64();
+        bool announced;
+        while (!(announced = ld_acquire(&stage_tile[s]) == i)) {
+          if (*err || clock64() - t0 > g.wait_cycles) break;
+          __nanosleep(64);   // leave the issue slots to the warps that decode
+        }
+        if (announced)
+          while (!(got = mbar_try_wait(&full[s], (i / S) & 1)))
+            if (*err || clock64() - t0 > g.wait_cycles) break;
       }
-      if (announced)
-        while (!(got = mbar_try_wait(&full[s], (i / S) & 1)))
-          if (*err || clock64() - t0 > kWaitCycles) break;
-    }
-    got = __all_sync(0xFFFFFFFFu, got);
-    if (!got) {
-      if (lane == 0 && !*err) report(a.status, LW_DEV_TIMEOUT);
-      *err = 1;
-      break;
+      got = __all_sync(0xFFFFFFFFu, got);
+      if (!got) {
+        if (lane == 0 && !*err) report(a.status, LW_DEV_TIMEOUT);
+        *err = 1;
+        ghost = true;
+      }
     }
     bool valid;
     const int t = list_tile<true>(a, c0 + i * cnt, valid);   // a tile of the bundle
     const int strip = t / a.TK, kt = t % a.TK;
+    if (ghost) {
+      // Counted without a partial sum: every unit of the launch is counted
+      // exactly once whatever happens, so each strip counter wraps back to
+      // zero and the workspace serves the next call (this launch's outputs
+      // are void: *d_status holds the error).
+      if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
+      ps2 = ps1;
+      if (ps1 >= 0) old2 = l_count<UPT>(a, ps1, lane);
+      ps1 = valid ? strip : -1;
+      continue;
+    }
     const uint32_t wb = sbase + (uint32_t)(g.ring_off + s * g.stage_bytes);
     const uint32_t qp = wb + (uint32_t)g.qp_off;
     const uint32_t sx = wb + (uint32_t)g.x_off;
@@ -609,7 +638,7 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
         LStream st[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
-#pragma unroll 8 / R
+#pragma unroll 8
         for (int j = 0; j < 64; ++j) {
           float2 v[R][2];
 #pragma unroll

@@ -19,6 +19,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "liblw.so")
 
 LW_FMT_Q4_PAIR, LW_FMT_Q6, LW_FMT_BF16_EXP = 1, 2, 3
+# device status codes (*d_status), as in include/lw.h
+(LW_DEV_OK, LW_DEV_LANE_LENGTH, LW_DEV_BAD_CODE, LW_DEV_TILE_SIZE, LW_DEV_TIMEOUT,
+ LW_DEV_BAD_TABLE, LW_DEV_BAD_STRIPS) = range(7)
 (LW_OK, LW_ERR_INVALID_ARG, LW_ERR_SHAPE, LW_ERR_UNSUPPORTED, LW_ERR_ALLOC, LW_ERR_CORRUPT,
  LW_ERR_CUDA, LW_ERR_IO) = range(8)
 SECTION_NAMES = ["words", "tile_off", "lane_bits", "table", "qparams", "signman",
@@ -37,7 +40,7 @@ EXPORTED = ["lw_encode_bundle", "lw_bundle_sections", "lw_bundle_free", "lw_tabl
             "lw_bundle_deserialize", "lw_bundle_save", "lw_bundle_load", "lw_transcode_twin",
             "lw_twin_tile_rows", "lw_decode_gemm_strips", "lw_graph_begin", "lw_graph_end",
             "lw_graph_launch", "lw_graph_free", "lw_decode_gemm_group", "lw_twin_gemm_group",
-            "lw_table_lut_entries"]
+            "lw_table_lut_entries", "lw_test_stall_next"]
 
 
 class LwError(RuntimeError):
@@ -126,6 +129,7 @@ def load():
         "lw_graph_launch": ([P, P], i32),
         "lw_graph_free": ([P], None),
         "lw_table_lut_entries": ([P], i32),
+        "lw_test_stall_next": ([i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -270,6 +274,13 @@ def lw_table_lut_entries(table: np.ndarray) -> int:
     if t.size != TABLE_BYTES:
         raise LwError(1, "lw_table_lut_entries", f"a table is {TABLE_BYTES} bytes, got {t.size}")
     return int(load().lw_table_lut_entries(_np_ptr(t)))
+
+
+def lw_test_stall_next(wait_us: int) -> None:
+    """Testing hook: the next table-driven product launch leaves one stage
+    unfilled and limits its waits to `wait_us` microseconds (it reports
+    LW_DEV_TIMEOUT and finishes)."""
+    _check(load().lw_test_stall_next(int(wait_us)), "lw_test_stall_next")
 
 
 def table_fields(table: np.ndarray) -> dict:

@@ -496,6 +496,22 @@ lw_status lw_decode_gemv_noalloc(const lw_dev_bundle* b, const void* x, float* y
                                  int32_t* d_status, void* stream);
 size_t lw_noalloc_scratch_bytes(void);
 
+/*
+ * Testing hook for the bounded waits (not for production use): the next
+ * launch of the table-driven 4-/6-bit product kernel in this process (the
+ * CUDA-core path of lw_decode_gemv, lw_decode_gemm, lw_twin_gemv,
+ * lw_twin_gemm and their group and strip forms, whichever runs first)
+ * arms the first stage of its first CTA for copies it never issues, and
+ * limits every wait of that launch to `wait_us` microseconds instead of
+ * about a second.  The consumer of that stage gives up, writes
+ * LW_DEV_TIMEOUT into *d_status, and the launch finishes with no copy in
+ * flight; its outputs are void, and every workspace counter still ends at
+ * zero, so the workspace serves the next call.  One launch only; a later
+ * request replaces a pending one, and wait_us = 0 withdraws it.  Errors:
+ * LW_ERR_INVALID_ARG (wait_us outside 0..1000000).
+ */
+lw_status lw_test_stall_next(int32_t wait_us);
+
 /* Entries of the compact decode table that the table-driven 4-/6-bit
    product kernel builds from this decoder table (the value lw_sections and
    lw_dev_bundle carry as lut_entries); 0 for a NULL table or a BF16 table.

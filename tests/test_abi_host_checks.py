@@ -169,3 +169,13 @@ def test_gemm_group_batch_checks(lib):
         for batch in (0, 9, -1):
             st, msg = status(lib, fn, arr, 2, xs, batch, ys, ws, 1 << 40, None, None)
             assert st == lw.LW_ERR_INVALID_ARG and msg, (fn, batch, st)
+
+
+def test_stall_hook_arguments(lib):
+    """The testing hook checks its range; 0 withdraws a pending request (so
+    this test leaves none behind)."""
+    for bad in (-1, 1000001):
+        st, msg = status(lib, "lw_test_stall_next", bad)
+        assert st == 1 and "wait_us" in msg
+    assert lib.lw_test_stall_next(5) == 0
+    assert lib.lw_test_stall_next(0) == 0

@@ -1,0 +1,76 @@
+"""The bounded waits of the table-driven product kernel, driven to expiry
+without a fault: lw_test_stall_next makes the next launch arm one stage for
+copies it never issues (nothing in flight) and limits its waits to 1 ms.
+The launch must report LW_DEV_TIMEOUT, return within the short limit, leave
+every workspace counter at zero, and the same workspace must then serve a
+normal call that is bitwise equal to one on a fresh workspace."""
+import time
+
+import numpy as np
+import pytest
+
+from decode_gemv_gb300 import inputs
+from decode_gemv_gb300 import lw
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lw.load()
+
+
+def call(db, X, Y, ws, st, batch, twin):
+    if twin:
+        if batch == 1:
+            lw.lw_twin_gemv(db, X, Y, ws, st)
+        else:
+            lw.lw_twin_gemm(db, X, batch, Y, ws, st)
+    elif batch == 1:
+        lw.lw_decode_gemv(db, X, Y, ws, st)
+    else:
+        lw.lw_decode_gemm(db, X, batch, Y, ws, st)
+
+
+@pytest.mark.parametrize("twin", [False, True])
+@pytest.mark.parametrize("batch", [1, 3])
+def test_stalled_stage_times_out_and_workspace_survives(twin, batch):
+    rows, cols = 2048, 4096    # 512 tiles: CTA 0 holds several
+    m = inputs.small_q4(907 + batch, rows, cols, batch=batch)
+    hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"], twin=twin)
+    db = lw.DeviceBundle.upload(hb, DEV)
+    X = torch.from_numpy(m["x"]).to(DEV)
+    nbytes = lw.lw_workspace_bytes(db, batch)
+
+    def fresh():
+        return (torch.zeros(nbytes // 4, dtype=torch.int32, device=DEV),
+                torch.zeros(1, dtype=torch.int32, device=DEV),
+                torch.full((batch, rows), float("nan"), dtype=torch.float32, device=DEV))
+
+    ws0, st0, Y0 = fresh()
+    call(db, X, Y0, ws0, st0, batch, twin)
+    torch.cuda.synchronize()
+    assert int(st0.item()) == 0
+
+    ws, st, Y = fresh()
+    lw.lw_test_stall_next(1000)
+    t0 = time.perf_counter()
+    call(db, X, Y, ws, st, batch, twin)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(st.item()) == lw.LW_DEV_TIMEOUT
+    assert elapsed < 0.5          # the 1 ms limit governed, not the ~1 s default
+    counters = ws[: rows // 64].cpu().numpy()
+    assert not counters.any()     # every unit was counted: the workspace is clean
+
+    st.zero_()
+    Y.fill_(float("nan"))
+    call(db, X, Y, ws, st, batch, twin)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(Y.cpu().numpy().view(np.uint32), Y0.cpu().numpy().view(np.uint32))
