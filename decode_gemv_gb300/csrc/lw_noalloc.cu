@@ -26,10 +26,13 @@
 namespace {
 
 // Maximum scratch: 16 MiB per GPU.  A matrix fits if lw_workspace_bytes(b, 1)
-// <= 16 MiB: partial sums for up to 8 activation rows, (K/256) * 8 * N * 4
-// bytes, plus N/64 counters -- about (K/256) * N <= 512 Ki.  Every matrix of
-// the 7-8B layers used here fits (e.g. 14336 x 4096 and 4096 x 14336 need
-// 7.3 MB); larger ones are rejected with LW_ERR_UNSUPPORTED.
+// <= 16 MiB.  That figure counts the partial sums reserved for a pass of 8
+// activation rows, (K/256) * 8 * N * 4 bytes, plus N/64 counters -- about
+// (K/256) * N <= 512 Ki -- although a batch-1 call writes an eighth of the
+// partials: the limit is the workspace lw_decode_gemv would demand, so that
+// the two entry points accept the same matrices.  Every matrix of the 7-8B
+// layers used here fits (e.g. 14336 x 4096 and 4096 x 14336 need 7.3 MB);
+// larger ones are rejected with LW_ERR_UNSUPPORTED.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -38,16 +41,24 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
-// Device address of the array on the current device (set up on first use on
-// that device, which must therefore happen before any stream capture).
-lw_status scratch_on_current_device(void** out) {
+// Device address of the array on the current device.  Outside stream capture
+// it is looked up on every call (after a device reset the module may load at
+// another address); under capture, where the lookup is not made, the address
+// the last call outside capture found on this device is used, so a first
+// call must come before any capture.
+lw_status scratch_on_current_device(cudaStream_t st, void** out) {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
     cudaGetLastError();
     return lw::fail(LW_ERR_CUDA, "lw_decode_gemv_noalloc: no current device");
   }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    const cudaError_t e = cudaGetLastError();
+    return lw::fail(LW_ERR_CUDA, "lw_decode_gemv_noalloc: stream: %s", cudaGetErrorString(e));
+  }
   std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_ptr[d]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
@@ -56,6 +67,10 @@ lw_status scratch_on_current_device(void** out) {
                       cudaGetErrorString(e));
     }
     g_scratch_ptr[d] = p;
+  } else if (!g_scratch_ptr[d]) {
+    return lw::fail(LW_ERR_CUDA,
+                    "lw_decode_gemv_noalloc: first call on device %d made under stream capture; "
+                    "make one call outside capture first", d);
   }
   *out = g_scratch_ptr[d];
   return LW_OK;
@@ -70,16 +85,21 @@ extern "C" lw_status lw_decode_gemv_noalloc(const lw_dev_bundle* b, const void* 
   lw::clear_error();
   lw_status s = lw::check_dev_bundle(b, false, true);
   if (s != LW_OK) return s;
+  // the argument checks of lw_decode_gemv, before anything is queued
+  if (!x || !y) return lw::fail(LW_ERR_INVALID_ARG, "lw_decode_gemv_noalloc: NULL x/y");
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(y) & 7u))
+    return lw::fail(LW_ERR_INVALID_ARG,
+                    "lw_decode_gemv_noalloc: x must be 16-byte aligned, y 8-byte aligned");
   const size_t need = lw_workspace_bytes(b, 1);
   if (need > kNoAllocScratchBytes)
     return lw::fail(LW_ERR_UNSUPPORTED,
                     "lw_decode_gemv_noalloc: a %lldx%lld matrix needs %zu bytes of scratch, more "
                     "than the fixed %zu; use lw_decode_gemv with a caller workspace",
                     (long long)b->rows, (long long)b->cols, need, kNoAllocScratchBytes);
-  void* ws = nullptr;
-  s = scratch_on_current_device(&ws);
-  if (s != LW_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  s = scratch_on_current_device(st, &ws);
+  if (s != LW_OK) return s;
   // the strip counters must start at zero; nothing else needs clearing
   uint32_t* counters = lw::workspace_counters(b, ws);
   if (cudaMemsetAsync(counters, 0, (size_t)(b->rows / 64) * sizeof(uint32_t), st) != cudaSuccess)

@@ -97,11 +97,11 @@ constexpr int kLHdrTiles = kLRawTab + (int)sizeof(lw_table);   // int[S]: tile e
 constexpr int kLHdrBytes = kLHdrTiles + 4 * kLMaxStages;
 constexpr int kLGuardRows = 132;  // rows a corrupt 6-bit stream may read past its stage
 constexpr int kLProducers = 4;    // producer warps (each issues its own stages' copies)
-constexpr int kLMaxConsumers = 24;
+constexpr int kLMaxConsumers = 24;  // consumer warps at most
 // consumer warps a launch of R rows per unit may use (R = 2: 16, so that
 // the kernel may keep more registers per thread)
 template <int R>
-constexpr int kLMaxConsumersR = R == 2 ? 16 : kLMaxConsumers;  // consumer warps at most (two per tile being decoded)
+constexpr int kLMaxConsumersR = R == 2 ? 16 : kLMaxConsumers;
 
 // a * b + c as one integer multiply-add (FMA pipe; the compiler would
 // otherwise often use shift-and-add forms on the integer ALU pipe)
@@ -591,196 +591,191 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
     bool valid;
     const int t = list_tile<true>(a, c0 + i * cnt, valid);   // a tile of the bundle
     const int strip = t / a.TK, kt = t % a.TK;
-    if (ghost) {
-      // Counted without a partial sum: every unit of the launch is counted
-      // exactly once whatever happens, so each strip counter wraps back to
-      // zero and the workspace serves the next call (this launch's outputs
-      // are void: *d_status holds the error).
-      if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
-      ps2 = ps1;
-      if (ps1 >= 0) old2 = l_count<UPT>(a, ps1, lane);
-      ps1 = valid ? strip : -1;
-      continue;
-    }
-    const uint32_t wb = sbase + (uint32_t)(g.ring_off + s * g.stage_bytes);
-    const uint32_t qp = wb + (uint32_t)g.qp_off;
-    const uint32_t sx = wb + (uint32_t)g.x_off;
-    const bool fits = lds_s32(sx + BP * 1024) != 0;
-    // the unit's row streams: row 2l from the lane's start, row 2l + 1 from its mid offset
-    uint32_t start[R], end[R];
-    if (!TWIN) {
-      const uint32_t mid = lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
-      const uint32_t last = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int h = h0 + r;
-        start[r] = h ? mid : 0u;
-        end[r] = h ? last : mid;
-      }
-    }
     float p[R][BP];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < BP; ++b) p[r][b] = 0.f;
-    if (!fits) {
-      if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
-    } else if (FMT == kQ4) {
-      float xa[BP];
-#pragma unroll
-      for (int b = 0; b < BP; ++b) xa[b] = tile_sum256(sx + 1024u * b, lane);
-      float2 acc[R][BP];
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int b = 0; b < BP; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    // A ghost unit is counted without a partial sum: every unit of the launch
+    // is counted exactly once whatever happens, so each strip counter wraps
+    // back to zero and the workspace serves the next call (this launch's
+    // outputs are void: *d_status holds the error).
+    if (!ghost) {
+      const uint32_t wb = sbase + (uint32_t)(g.ring_off + s * g.stage_bytes);
+      const uint32_t qp = wb + (uint32_t)g.qp_off;
+      const uint32_t sx = wb + (uint32_t)g.x_off;
+      const bool fits = lds_s32(sx + BP * 1024) != 0;
+      // the unit's row streams: row 2l from the lane's start, row 2l + 1 from its mid offset
+      uint32_t start[R], end[R];
       if (!TWIN) {
-        LStream st[R];
+        const uint32_t mid = lds_u16(wb + (uint32_t)g.mid_off + 2u * (uint32_t)lane);
+        const uint32_t last = lds_u16(wb + (uint32_t)g.lb_off + 2u * (uint32_t)lane);
 #pragma unroll
-        for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
-#pragma unroll 8
-        for (int j = 0; j < 64; ++j) {
-          float2 v[R][2];
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            uint32_t e0, e1;
-            l_decode2(st[r], dec, e0, e1);
-            v[r][0] = q4_vals(e0);
-            v[r][1] = q4_vals(e1);
-          }
-#pragma unroll
-          for (int b = 0; b < BP; ++b) {
-            const float4 xv = lds_f4(sx + 1024u * b + 16u * (uint32_t)j);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              acc[r][b] = __ffma2_rn(v[r][0], make_float2(xv.x, xv.y), acc[r][b]);
-              acc[r][b] = __ffma2_rn(v[r][1], make_float2(xv.z, xv.w), acc[r][b]);
-            }
-          }
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-          if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
-      } else {
-        // twin: row 2l in words 0..31 of lane l, row 2l + 1 in words 32..63
-        const uint32_t la = wb + 4u * (uint32_t)lane + 4096u * (uint32_t)h0;
-#pragma unroll 4 / R
-        for (int jj = 0; jj < 32; ++jj) {
-          float2 v[R][4];
-#pragma unroll
-          for (int r = 0; r < R; ++r) q4_twin_word(lds_u32(la + 4096u * r + 128u * (uint32_t)jj), v[r]);
-#pragma unroll
-          for (int b = 0; b < BP; ++b) {
-            const float4 xa4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj);
-            const float4 xb4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj + 16u);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              acc[r][b] = __ffma2_rn(v[r][0], make_float2(xa4.x, xa4.y), acc[r][b]);
-              acc[r][b] = __ffma2_rn(v[r][1], make_float2(xa4.z, xa4.w), acc[r][b]);
-              acc[r][b] = __ffma2_rn(v[r][2], make_float2(xb4.x, xb4.y), acc[r][b]);
-              acc[r][b] = __ffma2_rn(v[r][3], make_float2(xb4.z, xb4.w), acc[r][b]);
-            }
-          }
+        for (int r = 0; r < R; ++r) {
+          const int h = h0 + r;
+          start[r] = h ? mid : 0u;
+          end[r] = h ? last : mid;
         }
       }
+      if (!fits) {
+        if (lane == 0) report(a.status, LW_DEV_TILE_SIZE);
+      } else if (FMT == kQ4) {
+        float xa[BP];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        // scale | min << 16 of row 2l + h0 + r
-        const uint32_t q = lds_u32(qp + 4u * (uint32_t)(2 * lane + h0 + r));
-        const float sc = __half2float(__ushort_as_half((unsigned short)(q & 0xFFFFu)));
-        const float mn = __half2float(__ushort_as_half((unsigned short)(q >> 16)));
-#pragma unroll
-        for (int b = 0; b < BP; ++b) p[r][b] = fmaf(sc, acc[r][b].x + acc[r][b].y, mn * xa[b]);
-      }
-    } else {  // 6-bit: 16 groups of 16 weights per row
-      float X[BP];
-#pragma unroll
-      for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
-      LStream st[R];
-      if (!TWIN)
-#pragma unroll
-        for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
-      // twin: row 2l in words 0..47, row 2l + 1 in words 48..95
-      const uint32_t la = wb + 4u * (uint32_t)lane + 6144u * (uint32_t)h0;
-#pragma unroll 1
-      for (int gi = 0; gi < 16; ++gi) {
+        for (int b = 0; b < BP; ++b) xa[b] = tile_sum256(sx + 1024u * b, lane);
         float2 acc[R][BP];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
           for (int b = 0; b < BP; ++b) acc[r][b] = make_float2(0.f, 0.f);
         if (!TWIN) {
+          LStream st[R];
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            float2 v[R];
+          for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
+#pragma unroll 8
+          for (int j = 0; j < 64; ++j) {
+            float2 v[R][2];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
               uint32_t e0, e1;
               l_decode2(st[r], dec, e0, e1);
-              v[r] = make_float2(f16hi_plus(e0, -1024.f), f16hi_plus(e1, -1024.f));
+              v[r][0] = q4_vals(e0);
+              v[r][1] = q4_vals(e1);
             }
 #pragma unroll
             for (int b = 0; b < BP; ++b) {
-              const float2 xv = lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m);
+              const float4 xv = lds_f4(sx + 1024u * b + 16u * (uint32_t)j);
 #pragma unroll
-              for (int r = 0; r < R; ++r) acc[r][b] = __ffma2_rn(v[r], xv, acc[r][b]);
+              for (int r = 0; r < R; ++r) {
+                acc[r][b] = __ffma2_rn(v[r][0], make_float2(xv.x, xv.y), acc[r][b]);
+                acc[r][b] = __ffma2_rn(v[r][1], make_float2(xv.z, xv.w), acc[r][b]);
+              }
             }
           }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
         } else {
+          // twin: row 2l in words 0..31 of lane l, row 2l + 1 in words 32..63
+          const uint32_t la = wb + 4u * (uint32_t)lane + 4096u * (uint32_t)h0;
+#pragma unroll 4 / R
+          for (int jj = 0; jj < 32; ++jj) {
+            float2 v[R][4];
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            // group gi: codes 16 gi .. 16 gi + 15 at bits 96 gi .. of the row's words
-            const uint32_t wa = la + 6144u * r + 128u * (uint32_t)(3 * gi);
-            const uint32_t w0 = lds_u32(wa), w1 = lds_u32(wa + 128u), w2 = lds_u32(wa + 256u);
-            float v[16];
-            v[0] = q6_twin_c<0>(w0, w1);   v[1] = q6_twin_c<6>(w0, w1);
-            v[2] = q6_twin_c<12>(w0, w1);  v[3] = q6_twin_c<18>(w0, w1);
-            v[4] = q6_twin_c<24>(w0, w1);  v[5] = q6_twin_c<30>(w0, w1);
-            v[6] = q6_twin_c<4>(w1, w2);   v[7] = q6_twin_c<10>(w1, w2);
-            v[8] = q6_twin_c<16>(w1, w2);  v[9] = q6_twin_c<22>(w1, w2);
-            v[10] = q6_twin_c<28>(w1, w2); v[11] = q6_twin_c<2>(w2, 0u);
-            v[12] = q6_twin_c<8>(w2, 0u);  v[13] = q6_twin_c<14>(w2, 0u);
-            v[14] = q6_twin_c<20>(w2, 0u); v[15] = q6_twin_c<26>(w2, 0u);
+            for (int r = 0; r < R; ++r) q4_twin_word(lds_u32(la + 4096u * r + 128u * (uint32_t)jj), v[r]);
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
+            for (int b = 0; b < BP; ++b) {
+              const float4 xa4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj);
+              const float4 xb4 = lds_f4(sx + 1024u * b + 32u * (uint32_t)jj + 16u);
 #pragma unroll
-              for (int b = 0; b < BP; ++b)
-                acc[r][b] = __ffma2_rn(make_float2(v[2 * m], v[2 * m + 1]),
-                                       lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m),
-                                       acc[r][b]);
+              for (int r = 0; r < R; ++r) {
+                acc[r][b] = __ffma2_rn(v[r][0], make_float2(xa4.x, xa4.y), acc[r][b]);
+                acc[r][b] = __ffma2_rn(v[r][1], make_float2(xa4.z, xa4.w), acc[r][b]);
+                acc[r][b] = __ffma2_rn(v[r][2], make_float2(xb4.x, xb4.y), acc[r][b]);
+                acc[r][b] = __ffma2_rn(v[r][3], make_float2(xb4.z, xb4.w), acc[r][b]);
+              }
+            }
           }
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          // scale of group gi of row 2l + h: chunk 2h + gi/8, position gi % 8
-          const int h = h0 + r;
-          const uint32_t sa = qp + (uint32_t)((((2 * h + (gi >> 3)) * 32) + lane) * 16 + 2 * (gi & 7));
-          const float sc = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
+          // scale | min << 16 of row 2l + h0 + r
+          const uint32_t q = lds_u32(qp + 4u * (uint32_t)(2 * lane + h0 + r));
+          const float sc = __half2float(__ushort_as_half((unsigned short)(q & 0xFFFFu)));
+          const float mn = __half2float(__ushort_as_half((unsigned short)(q >> 16)));
 #pragma unroll
-          for (int b = 0; b < BP; ++b) {
-            const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], gi);
-            p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 32.f * Xg, p[r][b]);
+          for (int b = 0; b < BP; ++b) p[r][b] = fmaf(sc, acc[r][b].x + acc[r][b].y, mn * xa[b]);
+        }
+      } else {  // 6-bit: 16 groups of 16 weights per row
+        float X[BP];
+#pragma unroll
+        for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
+        LStream st[R];
+        if (!TWIN)
+#pragma unroll
+          for (int r = 0; r < R; ++r) st[r].init(wb, lane, g.stage_rows, start[r]);
+        // twin: row 2l in words 0..47, row 2l + 1 in words 48..95
+        const uint32_t la = wb + 4u * (uint32_t)lane + 6144u * (uint32_t)h0;
+#pragma unroll 1
+        for (int gi = 0; gi < 16; ++gi) {
+          float2 acc[R][BP];
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < BP; ++b) acc[r][b] = make_float2(0.f, 0.f);
+          if (!TWIN) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              float2 v[R];
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                uint32_t e0, e1;
+                l_decode2(st[r], dec, e0, e1);
+                v[r] = make_float2(f16hi_plus(e0, -1024.f), f16hi_plus(e1, -1024.f));
+              }
+#pragma unroll
+              for (int b = 0; b < BP; ++b) {
+                const float2 xv = lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m);
+#pragma unroll
+                for (int r = 0; r < R; ++r) acc[r][b] = __ffma2_rn(v[r], xv, acc[r][b]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              // group gi: codes 16 gi .. 16 gi + 15 at bits 96 gi .. of the row's words
+              const uint32_t wa = la + 6144u * r + 128u * (uint32_t)(3 * gi);
+              const uint32_t w0 = lds_u32(wa), w1 = lds_u32(wa + 128u), w2 = lds_u32(wa + 256u);
+              float v[16];
+              v[0] = q6_twin_c<0>(w0, w1);   v[1] = q6_twin_c<6>(w0, w1);
+              v[2] = q6_twin_c<12>(w0, w1);  v[3] = q6_twin_c<18>(w0, w1);
+              v[4] = q6_twin_c<24>(w0, w1);  v[5] = q6_twin_c<30>(w0, w1);
+              v[6] = q6_twin_c<4>(w1, w2);   v[7] = q6_twin_c<10>(w1, w2);
+              v[8] = q6_twin_c<16>(w1, w2);  v[9] = q6_twin_c<22>(w1, w2);
+              v[10] = q6_twin_c<28>(w1, w2); v[11] = q6_twin_c<2>(w2, 0u);
+              v[12] = q6_twin_c<8>(w2, 0u);  v[13] = q6_twin_c<14>(w2, 0u);
+              v[14] = q6_twin_c<20>(w2, 0u); v[15] = q6_twin_c<26>(w2, 0u);
+#pragma unroll
+              for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int b = 0; b < BP; ++b)
+                  acc[r][b] = __ffma2_rn(make_float2(v[2 * m], v[2 * m + 1]),
+                                         lds_f2(sx + 1024u * b + 64u * (uint32_t)gi + 8u * (uint32_t)m),
+                                         acc[r][b]);
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            // scale of group gi of row 2l + h: chunk 2h + gi/8, position gi % 8
+            const int h = h0 + r;
+            const uint32_t sa = qp + (uint32_t)((((2 * h + (gi >> 3)) * 32) + lane) * 16 + 2 * (gi & 7));
+            const float sc = __half2float(__ushort_as_half((unsigned short)lds_u16(sa)));
+#pragma unroll
+            for (int b = 0; b < BP; ++b) {
+              const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], gi);
+              p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 32.f * Xg, p[r][b]);
+            }
           }
         }
-      }
-      if (!TWIN)
+        if (!TWIN)
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-          if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
+          for (int r = 0; r < R; ++r)
+            if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
+      }
+      // release the stage (UPT units per stage): this warp's reads of it are
+      // done (their values are in the partial sums), ordered before the
+      // producer's next bulk copy into it
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      // a tile too long for its stage commits zeros, so that its strip still
+      // completes; a tile behind an invalid strip-list entry commits nothing
+      if (!valid && lane == 0 && h0 == 0) report(a.status, LW_DEV_BAD_STRIPS);
     }
-    // release the stage (UPT units per stage): this warp's reads of it are
-    // done (their values are in the partial sums), ordered before the
-    // producer's next bulk copy into it
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    // a tile too long for its stage commits zeros, so that its strip still
-    // completes; a tile behind an invalid strip-list entry commits nothing
-    if (!valid && lane == 0 && h0 == 0) report(a.status, LW_DEV_BAD_STRIPS);
     if (ps2 >= 0) l_finish<UPT>(a, ps2, lane, old2);
     ps2 = ps1;
     if (ps1 >= 0) old2 = l_count<UPT>(a, ps1, lane);
-    if (valid) l_store<R, BP>(a, strip, kt, 2 * lane + h0, p);
+    if (valid && !ghost) l_store<R, BP>(a, strip, kt, 2 * lane + h0, p);
     ps1 = valid ? strip : -1;
   }
   // drain: the last count's round trip overlaps the pending finish

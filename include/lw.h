@@ -486,10 +486,16 @@ int32_t lw_twin_tile_rows(int32_t fmt);
  * `ws`/`ws_bytes`.  Scratch comes from a fixed array in device memory of
  * lw_noalloc_scratch_bytes() bytes (16 MiB), held on every GPU that loads
  * the library until the process exits; a matrix whose
- * lw_workspace_bytes(b, 1) exceeds it is rejected with LW_ERR_UNSUPPORTED.
- * The first call on a device looks up the array's device address (do it
- * before any stream capture).  Every call clears the array's counters on
- * `stream` first.  All calls share the array: calls that overlap on the GPU
+ * lw_workspace_bytes(b, 1) exceeds it is rejected with LW_ERR_UNSUPPORTED
+ * (that figure counts partial sums for a pass of 8 activation rows,
+ * (K/256)*8*N*4 bytes, of which a batch-1 call writes an eighth: both
+ * entry points accept the same matrices).  Outside stream capture every
+ * call looks up the array's device address; under capture the address the
+ * last call outside capture found on the device is used, so make one call
+ * on the device before capturing.  After its argument checks every call
+ * clears the array's counters on `stream` (they protect against an earlier
+ * call that ended early, e.g. a refused or aborted launch); then it runs
+ * lw_decode_gemv.  All calls share the array: calls that overlap on the GPU
  * race and must be serialised by the caller.  Allocates nothing.
  */
 lw_status lw_decode_gemv_noalloc(const lw_dev_bundle* b, const void* x, float* y,

@@ -179,3 +179,28 @@ def test_stall_hook_arguments(lib):
         assert st == 1 and "wait_us" in msg
     assert lib.lw_test_stall_next(5) == 0
     assert lib.lw_test_stall_next(0) == 0
+
+
+def test_no_alloc_argument_errors(lib):
+    """lw_decode_gemv_noalloc checks its arguments before it queues anything:
+    on a machine without a GPU the refusals name the argument (a queued clear
+    of the shared counters would fail first with LW_ERR_CUDA)."""
+    v = view()
+    x, y = P(FAKE + 0xA000000), P(FAKE + 0xB000000)
+    cases = [
+        (ctypes.byref(view(fmt=9)), x, y, lw.LW_ERR_UNSUPPORTED),
+        (ctypes.byref(view(rows=100)), x, y, lw.LW_ERR_SHAPE),
+        (ctypes.byref(v), None, y, lw.LW_ERR_INVALID_ARG),
+        (ctypes.byref(v), x, None, lw.LW_ERR_INVALID_ARG),
+        (ctypes.byref(v), P(FAKE + 0xA000008), y, lw.LW_ERR_INVALID_ARG),   # x misaligned
+        (ctypes.byref(v), x, P(FAKE + 0xB000004), lw.LW_ERR_INVALID_ARG),   # y misaligned
+        (ctypes.byref(view(twin=1)), x, y, lw.LW_ERR_INVALID_ARG),
+    ]
+    for vb, xx, yy, want in cases:
+        st, msg = status(lib, "lw_decode_gemv_noalloc", vb, xx, yy, None, None)
+        assert st == want, (st, want, msg)
+        assert "clearing" not in msg
+    # a matrix beyond the scratch is refused before any device work
+    big = view(rows=64 * 1024, cols=256 * 64)
+    st, msg = status(lib, "lw_decode_gemv_noalloc", ctypes.byref(big), x, y, None, None)
+    assert st == lw.LW_ERR_UNSUPPORTED and "scratch" in msg

@@ -2,7 +2,9 @@
 GEMV (scratch in a fixed device array inside the library) for callers that
 cannot allocate device memory -- e.g. code under CUDA-graph capture or an
 engine whose own pool owns all device memory.  Checked through the C ABI
-against lw_decode_gemv with a caller workspace, on two calls in a row.  This
+against lw_decode_gemv with a caller workspace, on two calls in a row, for
+the 4-bit, 6-bit and BF16-exponent formats (the argument checks that run
+before the shared counters are cleared are covered on the CPU).  This
 file is collected last so that a run stopping at the first failure has run
 everything else; it also passes alone in a fresh process (the first call then
 sets the scratch up)."""
@@ -25,7 +27,8 @@ def need_gpu():
 
 
 def _bundle(m, fmt):
-    hb = lw.lw_encode_bundle(fmt, m["codes"], m["scales"], m.get("mins"))
+    payload = m["bits"] if fmt == lw.LW_FMT_BF16_EXP else m["codes"]
+    hb = lw.lw_encode_bundle(fmt, payload, m.get("scales"), m.get("mins"))
     return lw.DeviceBundle.upload(hb, "cuda")
 
 
@@ -50,17 +53,22 @@ def _no_alloc(db, x):
 
 @pytest.mark.parametrize("fmt,shape", [(lw.LW_FMT_Q4_PAIR, (256, 1024)),
                                        (lw.LW_FMT_Q6, (192, 768)),
-                                       (lw.LW_FMT_Q4_PAIR, (4096, 14336))])
+                                       (lw.LW_FMT_Q4_PAIR, (4096, 14336)),
+                                       (lw.LW_FMT_BF16_EXP, (256, 1024))])
 def test_no_alloc_matches_workspace_entry_point(fmt, shape):
     n, k = shape
-    m = inputs.small_q4(101, n, k, batch=2) if fmt == lw.LW_FMT_Q4_PAIR \
-        else inputs.small_q6(101, n, k, batch=2)
+    make = {lw.LW_FMT_Q4_PAIR: inputs.small_q4, lw.LW_FMT_Q6: inputs.small_q6,
+            lw.LW_FMT_BF16_EXP: inputs.small_bf16}[fmt]
+    m = make(101, n, k, batch=2)
     db = _bundle(m, fmt)
     assert lw.lw_workspace_bytes(db, 1) <= lw.lw_noalloc_scratch_bytes()
     # two calls in a row, with different activations: the second must not see
     # anything the first left in the shared scratch
     for b in (0, 1):
-        x = torch.from_numpy(np.ascontiguousarray(m["x"][b])).to("cuda")
+        xb = np.ascontiguousarray(m["x"][b])
+        if fmt == lw.LW_FMT_BF16_EXP:
+            xb = xb.view(np.int16)    # bf16 bits
+        x = torch.from_numpy(xb).to("cuda")
         want = _with_workspace(db, x)
         got = _no_alloc(db, x)
         nw = rel_errors(got, want, np.abs(want) + 1e-30)[0]
