@@ -474,28 +474,58 @@ def per_call_ms(torch, stream, calls_by_copy, reps=8):
     return out / reps
 
 
+KERNEL_SOURCES = ("lw_qlut.cuh", "lw_lut.h", "lw_qkern.cuh", "lw_dev.cuh", "lw_qlut.cu")
+
+
 def kernel_source_digest():
+    """sha256 over the sources of the table-driven product kernel and its launcher."""
     h = hashlib.sha256()
-    for f in ("lw_qkern.cuh", "lw_dev.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "decode_gemv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def measured_traffic(names, launches):
-    """DRAM bytes (read + write) per launch of the fused kernel on this
-    workload, from the committed ncu capture -- only while the kernel source
-    and the step's launches are the ones that were profiled, else None."""
+def kernel_counters():
+    """The committed ncu counters of the table-driven kernel (per-launch DRAM
+    bytes of this step, instruction and issue counts of the gate matrix) --
+    only while the kernel's sources are the ones that were profiled, else
+    None."""
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic_q_product_kernel.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "q_lut_kernel_counters.json")) as f:
             d = json.load(f)
     except Exception:  # noqa: BLE001
         return None
-    if d.get("source_sha256") != kernel_source_digest() or names:
+    return d if d.get("source_sha256") == kernel_source_digest() else None
+
+
+def measured_traffic(names, launches):
+    """DRAM bytes (read + write) per launch of the fused kernel on this step
+    (mean over the step's launches, and each launch's), from the committed
+    capture, or (None, None) when the kernel or the launches differ."""
+    d = kernel_counters()
+    if d is None or names or d.get("launches") != launches:
+        return None, None
+    per = d["traffic_per_launch_bytes"]
+    return sum(per.values()) / len(per), per
+
+
+def issue_roofline(achieved_gbs, bytes_per_pair, sm_mhz, sms):
+    """The instruction-issue roof of the decode: warp-instructions per pair
+    symbol (per lane) from the committed capture of the gate matrix, the
+    coded GB/s that count allows at one instruction per cycle on each of the
+    SM's four schedulers, and the fraction of it achieved."""
+    d = kernel_counters()
+    if d is None or not sm_mhz:
         return None
-    if d.get("launches") != launches:
-        return None
-    return d["bytes_per_launch"]
+    ipp = d["gate"]["warp_inst_per_pair"]
+    ceiling = sms * 4 * sm_mhz * 1e6 * 32 / ipp * bytes_per_pair / 1e9
+    return {"warp_inst_per_pair": ipp, "issue_active_pct": d["gate"]["issue_active_pct"],
+            "ceiling_gbs": ceiling, "achieved_gbs": achieved_gbs, "frac": achieved_gbs / ceiling,
+            "hbm_frac_at_ceiling": None,
+            "basis": "ceiling = SMs x 4 schedulers x SM clock (median sampled in the timed region) "
+                     "x 32 lanes / warp-instructions per pair x coded bytes per pair of the step; "
+                     "counts from the committed one-kernel capture of the gate matrix"}
 
 
 def dequant_bf16(m):
@@ -692,6 +722,12 @@ def run_ours(args):
     mean_call_ms = t_max / launches_per_step
     mean_call_bytes = coded_step / launches_per_step
     achieved = mean_call_bytes / (mean_call_ms * 1e-3) / 1e9
+    traffic_mean, traffic_per = measured_traffic(
+        names, [[mats[j]["spec"].name for j in g] for g in groups])
+    issue = issue_roofline(achieved, coded_step / (weights / 2), clocks.get("sm_mhz"),
+                           torch.cuda.get_device_properties(dev).multi_processor_count)
+    if issue is not None:
+        issue["hbm_frac_at_ceiling"] = issue["ceiling_gbs"] / peak
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -708,17 +744,20 @@ def run_ours(args):
             "step_ms_spread": dict(spread, note="each step timed alone with its own event pair, "
                                                 "after the timed region (not part of value)"),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": measured_traffic(names, [[mats[j]["spec"].name for j in g] for g in groups]),
+                         "frac": achieved / peak, "traffic": traffic_mean,
+                         "traffic_per_launch": traffic_per,
                          "peak_kind": peak_kind,
-                         "kernel": "q_product_kernel (fused decode + GEMV + ordered split-K reduction), "
+                         "kernel": "q_lut_kernel (table-driven fused decode + GEMV + ordered split-K "
+                                   "reduction), "
                                    + ("one launch per matrix" if len(groups) == n_mat else
                                       "one launch per group " + "/".join(
                                           "+".join(mats[j]["spec"].name for j in g) for g in groups)),
+                         "issue": issue,
                          "per_matrix_ms": {x["spec"].name: float(v) for x, v in zip(mats, per_mat)},
                          "per_matrix_note": "each call alone, one graph per call (diagnostic)",
-                         "note": "bound in practice by instruction issue, not HBM: ~29 warp-instructions "
-                                 "per decoded pair symbol put the issue-rate ceiling near 1.05 TB/s of "
-                                 "coded bytes (profiles/q_product_kernel_gate_q4.md)"},
+                         "note": "bound in practice by instruction issue, not HBM: the decode's "
+                                 "warp-instructions per pair symbol (roofline.issue) cap the coded "
+                                 "bytes per second far below the HBM peak"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks, "device_status": status}
     if keep:
