@@ -107,6 +107,16 @@ inline float* workspace_partials(const lw_dev_bundle* b, void* ws) {
 // The pending one-shot request of lw_test_stall_next (microseconds; 0:
 // none), cleared by the call.
 int take_test_stall();
+// The table-driven kernel takes a launch when every matrix's table fits it
+// and the pass has at most kLutMaxRowsQ4 (4-bit) or kLutMaxRowsQ6 (6-bit)
+// activation rows.  Beyond those the staged activation slices leave the ring
+// 8 stages or fewer next to the table, too few for the decoding warps, and
+// the comparator kernel is faster (measured: 6-bit at 4 and 8 rows, 4-bit at
+// 8).  Both kernels execute the same floating-point operations in the same
+// order, so the choice never changes a result bit.
+constexpr int kLutMaxRowsQ4 = 4;
+constexpr int kLutMaxRowsQ6 = 2;
+bool lut_takes(const lw_dev_bundle* const* bs, int n, int batch);
 bool lut_fits(const lw_dev_bundle* b);
 // With a strip list (device array of n_strips 64-row strips), n must be 1.
 lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,

@@ -95,13 +95,11 @@ lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch,
 
 // Fused products of n matrices of one format (one launch): matrix i reads
 // x[i] (`batch` rows), writes y[i] and uses workspace ws[i].
-// The table-driven kernel when every matrix's table fits it, else the
-// comparator kernel (any table).
+// The table-driven kernel when it takes the launch (lut_takes), else the
+// comparator kernel (any table, any batch).
 lw_status launch_q_products(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,
                             float* const* y, void* const* ws, int32_t* status, cudaStream_t st) {
-  bool lut = true;
-  for (int i = 0; i < n; ++i) lut = lut && lut_fits(bs[i]);
-  if (lut) return launch_q_lut(bs, n, x, batch, y, ws, status, st);
+  if (lut_takes(bs, n, batch)) return launch_q_lut(bs, n, x, batch, y, ws, status, st);
   return q_products_impl<false>(bs, n, x, batch, y, ws, nullptr, 0, status, st);
 }
 

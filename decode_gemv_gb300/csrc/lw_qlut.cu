@@ -43,10 +43,56 @@ int max_dyn_smem() {
   return cache[d];
 }
 
+// The ring of a launch of n matrices of one format at `batch` activation
+// rows: stage layout, table capacity and stage count S (capped at
+// kLMaxStages, a multiple of the producer count).
+struct LRing {
+  int bp, stage_rows, qp_off, mid_off, lb_off, x_off, stage_bytes, ring_off, lut_cap, lut_bytes, S;
+};
+LRing lut_ring(const lw_dev_bundle* const* bs, int n, int batch) {
+  LRing r{};
+  const int fmt = bs[0]->fmt;
+  const bool twin = bs[0]->twin != 0;
+  r.bp = batch <= 1 ? 1 : (batch <= 2 ? 2 : (batch <= 4 ? 4 : 8));
+  int max_rows = 0;
+  for (int i = 0; i < n; ++i) max_rows = bs[i]->max_tile_rows > max_rows ? bs[i]->max_tile_rows : max_rows;
+  // stage: coded rows (a stream reads up to two rows past its last word) |
+  // scales/mins | mid offsets | lane bit counts | activation slices | "fits"
+  // flag
+  r.stage_rows = max_rows + 2;
+  r.qp_off = r.stage_rows * 128;
+  r.mid_off = r.qp_off + qparam_tile_bytes(fmt);
+  r.lb_off = r.mid_off + 64;
+  r.x_off = r.mid_off + (twin ? 0 : 128);
+  r.stage_bytes = (r.x_off + r.bp * 1024 + 16 + 127) / 128 * 128;
+  r.ring_off = (dev::kLHdrBytes + 127) / 128 * 128;
+  // the decode table: the largest member's entries (the device checks each
+  // table against it), and at least the rows a corrupt stream of the last
+  // stage could read past it
+  int lut_cap = 0;
+  for (int i = 0; i < n; ++i) lut_cap = bs[i]->lut_entries > lut_cap ? bs[i]->lut_entries : lut_cap;
+  if (lut_cap < dev::kLGuardRows) lut_cap = dev::kLGuardRows;
+  r.lut_cap = lut_cap;
+  r.lut_bytes = twin ? 0 : lut_cap * 128;
+  int S = (max_dyn_smem() - r.ring_off - r.lut_bytes) / r.stage_bytes;
+  if (S > dev::kLMaxStages) S = dev::kLMaxStages;
+  S -= S % dev::kLProducers;   // every stage has one producer: stage s, producer s mod 4
+  r.S = S;
+  return r;
+}
+
 }  // namespace
 
 bool lut_fits(const lw_dev_bundle* b) {
   return b->twin || (b->lut_entries >= 1 && b->lut_entries <= kLutCap);
+}
+
+bool lut_takes(const lw_dev_bundle* const* bs, int n, int batch) {
+  const int max_rows = bs[0]->fmt == LW_FMT_Q6 ? kLutMaxRowsQ6 : kLutMaxRowsQ4;
+  if (batch > max_rows) return false;
+  for (int i = 0; i < n; ++i)
+    if (!lut_fits(bs[i])) return false;
+  return true;
 }
 
 lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const* x, int batch,
@@ -54,45 +100,31 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
                        const int32_t* strips, int n_strips) {
   const int fmt = bs[0]->fmt;
   const bool twin = bs[0]->twin != 0;
-  const int bp = batch <= 1 ? 1 : (batch <= 2 ? 2 : (batch <= 4 ? 4 : 8));
-  int max_rows = 0;
+  const LRing ring = lut_ring(bs, n, batch);
+  const int bp = ring.bp;
   long long total = 0;
   // tiles of each matrix (with a strip list, a single matrix: its listed strips')
   auto n_tiles = [&](int i) -> long long {
     return strips ? (long long)n_strips * (bs[i]->cols / 256) : tiles_of(bs[i]->rows, bs[i]->cols);
   };
-  for (int i = 0; i < n; ++i) {
-    max_rows = bs[i]->max_tile_rows > max_rows ? bs[i]->max_tile_rows : max_rows;
-    total += n_tiles(i);
-  }
+  for (int i = 0; i < n; ++i) total += n_tiles(i);
   if (total < 1) return LW_OK;
   if (total > (1ll << 30)) return fail(LW_ERR_SHAPE, "group too large");
   dev::LLaunch g{};
   g.n = n;
-  // stage: coded rows (a stream reads up to two rows past its last word) |
-  // scales/mins | mid offsets | lane bit counts | activation slices | "fits"
-  // flag
-  g.stage_rows = max_rows + 2;
-  g.qp_off = g.stage_rows * 128;
-  g.mid_off = g.qp_off + qparam_tile_bytes(fmt);
-  g.lb_off = g.mid_off + 64;
-  g.x_off = g.mid_off + (twin ? 0 : 128);
-  g.stage_bytes = (g.x_off + bp * 1024 + 16 + 127) / 128 * 128;
-  g.ring_off = (dev::kLHdrBytes + 127) / 128 * 128;
-  // the decode table: the largest member's entries (the device checks each
-  // table against it), and at least the rows a corrupt stream of the last
-  // stage could read past it
-  int lut_cap = 0;
-  for (int i = 0; i < n; ++i) lut_cap = bs[i]->lut_entries > lut_cap ? bs[i]->lut_entries : lut_cap;
-  if (lut_cap < dev::kLGuardRows) lut_cap = dev::kLGuardRows;
-  g.lut_cap = lut_cap;
-  const int lut_bytes = twin ? 0 : lut_cap * 128;
-  const int budget = max_dyn_smem();
-  int S = (budget - g.ring_off - lut_bytes) / g.stage_bytes;
-  if (S > dev::kLMaxStages) S = dev::kLMaxStages;
-  S -= S % dev::kLProducers;   // every stage has one producer: stage s, producer s mod 4
+  g.stage_rows = ring.stage_rows;
+  g.qp_off = ring.qp_off;
+  g.mid_off = ring.mid_off;
+  g.lb_off = ring.lb_off;
+  g.x_off = ring.x_off;
+  g.stage_bytes = ring.stage_bytes;
+  g.ring_off = ring.ring_off;
+  g.lut_cap = ring.lut_cap;
+  const int lut_bytes = ring.lut_bytes;
+  const int S = ring.S;
   if (S < 2 * dev::kLProducers)
-    return fail(LW_ERR_UNSUPPORTED, "tiles of %d rows do not fit the table-driven kernel", max_rows);
+    return fail(LW_ERR_UNSUPPORTED, "tiles of %d rows do not fit the table-driven kernel",
+                ring.stage_rows - 2);
   g.nstage = S;
   g.lut_off = g.ring_off + S * g.stage_bytes;
   g.wait_cycles = dev::kWaitCycles;

@@ -161,15 +161,24 @@ __device__ __forceinline__ uint32_t lut_entry(int fmt, uint32_t sym, int L) {
   return ((0x6400u | (sym & 63u)) << 16) | (uint32_t)L;
 }
 
-// The exact fp32 codes (c_even, c_odd) of a 4-bit entry: one fp16x2 add of
-// 1024 (rounding to the integer grid of [1024, 2048) drops the length bits),
-// then two mixed-precision adds of -1024 -- all on the FMA pipes.
+// The codes enter the products as the exact fp32 values 16 + c (4-bit) and
+// 64 + c (6-bit), the bias removed once per tile row (4-bit: 16 * sum x) or
+// per 16-weight group (6-bit: 96 * sum x, folding in the code offset 32):
+// the comparator kernel's operands and epilogue, so both kernels execute
+// the same floating-point operations and give bitwise-equal results.
+constexpr float kQ4Unbias = -1008.f;   // 1024 + c -> 16 + c
+constexpr float kQ6Unbias = -960.f;    // 1024 + c -> 64 + c
+
+// The exact fp32 values (16 + c_even, 16 + c_odd) of a 4-bit entry: one
+// fp16x2 add of 1024 (rounding to the integer grid of [1024, 2048) drops the
+// length bits), then two mixed-precision adds of -1008 -- all on the FMA
+// pipes.
 __device__ __forceinline__ float2 q4_vals(uint32_t e) {
   uint32_t h;
   asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(e), "r"(0x64006400u));
   float lo, hi;
   asm("{.reg .b16 a, b; mov.b32 {a, b}, %2; add.rn.f32.f16 %0, a, %3; add.rn.f32.f16 %1, b, %3;}"
-      : "=f"(lo), "=f"(hi) : "r"(h), "f"(-1024.f));
+      : "=f"(lo), "=f"(hi) : "r"(h), "f"(kQ4Unbias));
   return make_float2(lo, hi);
 }
 
@@ -256,31 +265,31 @@ __device__ __forceinline__ void l_decode2(LStream& st, const LDec& d, uint32_t& 
 
 
 
-// The exact fp32 codes of the four pairs of a 4-bit twin word (codes
+// The exact fp32 values 16 + c of the four pairs of a 4-bit twin word (codes
 // MSB-first in stream order: code k at bits 28 - 4k .. 31 - 4k; even columns
 // are codes 0, 2, 4, 6): each logic op builds two fp16 1024 + c, each mixed-
-// precision add subtracts 1024 -- the coded entries' values, so the twin's
+// precision add subtracts 1008 -- the coded entries' values, so the twin's
 // products are the coded kernel's.
 __device__ __forceinline__ void q4_twin_word(uint32_t w, float2 (&v)[4]) {
   const uint32_t A = (w & 0x000F000Fu) | 0x64006400u;           // codes 3 | 7
   const uint32_t B = ((w >> 4) & 0x000F000Fu) | 0x64006400u;    // codes 2 | 6
   const uint32_t C = ((w >> 8) & 0x000F000Fu) | 0x64006400u;    // codes 1 | 5
   const uint32_t D = ((w >> 12) & 0x000F000Fu) | 0x64006400u;   // codes 0 | 4
-  v[0] = make_float2(f16hi_plus(D, -1024.f), f16hi_plus(C, -1024.f));
-  v[1] = make_float2(f16hi_plus(B, -1024.f), f16hi_plus(A, -1024.f));
-  v[2] = make_float2(f16lo_plus(D, -1024.f), f16lo_plus(C, -1024.f));
-  v[3] = make_float2(f16lo_plus(B, -1024.f), f16lo_plus(A, -1024.f));
+  v[0] = make_float2(f16hi_plus(D, kQ4Unbias), f16hi_plus(C, kQ4Unbias));
+  v[1] = make_float2(f16hi_plus(B, kQ4Unbias), f16hi_plus(A, kQ4Unbias));
+  v[2] = make_float2(f16lo_plus(D, kQ4Unbias), f16lo_plus(C, kQ4Unbias));
+  v[3] = make_float2(f16lo_plus(B, kQ4Unbias), f16lo_plus(A, kQ4Unbias));
 }
 
-// fp32 value c of the 6-bit code at stream bit B of the lane's twin words
-// (row base address rb = stage + 4 lane; word j at rb + 128 j).
+// fp32 value 64 + c of the 6-bit code at stream bit B of the lane's twin
+// words (row base address rb = stage + 4 lane; word j at rb + 128 j).
 template <int B>
 __device__ __forceinline__ float q6_twin_c(uint32_t w0, uint32_t w1) {
   constexpr int o = B % 32;
   uint32_t t;
   if constexpr (o <= 26) t = w0 >> (26 - o);   // the code is bits 31-o..26-o of w0
   else t = __funnelshift_l(w1, w0, o - 26);     // it continues into w1
-  return f16lo_plus((t & 63u) | 0x6400u, -1024.f);
+  return f16lo_plus((t & 63u) | 0x6400u, kQ6Unbias);
 }
 
 // Split-K commit of a warp's unit (one row of every lane of a tile), in
@@ -684,7 +693,8 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
           const float sc = __half2float(__ushort_as_half((unsigned short)(q & 0xFFFFu)));
           const float mn = __half2float(__ushort_as_half((unsigned short)(q >> 16)));
 #pragma unroll
-          for (int b = 0; b < BP; ++b) p[r][b] = fmaf(sc, acc[r][b].x + acc[r][b].y, mn * xa[b]);
+          for (int b = 0; b < BP; ++b)
+            p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 16.f * xa[b], mn * xa[b]);
         }
       } else {  // 6-bit: 16 groups of 16 weights per row
         float X[BP];
@@ -711,7 +721,7 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
               for (int r = 0; r < R; ++r) {
                 uint32_t e0, e1;
                 l_decode2(st[r], dec, e0, e1);
-                v[r] = make_float2(f16hi_plus(e0, -1024.f), f16hi_plus(e1, -1024.f));
+                v[r] = make_float2(f16hi_plus(e0, kQ6Unbias), f16hi_plus(e1, kQ6Unbias));
               }
 #pragma unroll
               for (int b = 0; b < BP; ++b) {
@@ -753,7 +763,7 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
 #pragma unroll
             for (int b = 0; b < BP; ++b) {
               const float Xg = __shfl_sync(0xFFFFFFFFu, X[b], gi);
-              p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 32.f * Xg, p[r][b]);
+              p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 96.f * Xg, p[r][b]);
             }
           }
         }

@@ -34,7 +34,7 @@ extern "C" lw_status lw_decode_gemm_strips(const lw_dev_bundle* b, const int32_t
     const float* xp = xf + (size_t)b0 * b->cols;
     float* yp = Y + (size_t)b0 * b->rows;
     void* wp = ws;
-    s = lut_fits(b) ? launch_q_lut(&b, 1, &xp, nb, &yp, &wp, d_status, st, strips, n_strips)
+    s = lut_takes(&b, 1, nb) ? launch_q_lut(&b, 1, &xp, nb, &yp, &wp, d_status, st, strips, n_strips)
                     : q_products_impl<true>(&b, 1, &xp, nb, &yp, &wp, strips, n_strips, d_status, st);
     if (s != LW_OK) return s;
   }

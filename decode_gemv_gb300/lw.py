@@ -320,8 +320,14 @@ class DeviceBundle:
     lw_dev_bundle view that the C calls take."""
 
     def __init__(self, fmt, twin, rows, cols, sections: dict, max_tile_rows, lmin, lmax,
-                 device="cuda", coded_bytes=None, lut_entries=0):
+                 device="cuda", coded_bytes=None, lut_entries=None):
+        """lut_entries: the compact decode table's size (lw_sections); None
+        computes it from the host table section (lw_table_lut_entries)."""
         import torch
+        if lut_entries is None:
+            tab = sections.get("table")
+            lut_entries = (lw_table_lut_entries(np.ascontiguousarray(tab).view(np.uint8).reshape(-1))
+                           if tab is not None and not twin and fmt != LW_FMT_BF16_EXP else 0)
         self.fmt, self.twin, self.rows, self.cols = fmt, bool(twin), rows, cols
         self.tensors = {}
         for name in SECTION_NAMES:

@@ -107,3 +107,20 @@ def test_bundle_stats_carry_the_hint():
     b = inputs.small_bf16(6, 64, 512)
     hbb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, b["bits"])
     assert hbb.stats.lut_entries == 0
+
+
+def test_device_view_computes_the_hint_when_not_given():
+    """A device view built from host sections without the bundle's stats (as
+    a bundle rebuilt in another process is) still carries the compact-table
+    size, so its products take the table-driven kernel (views on the CPU)."""
+    pytest.importorskip("torch")
+    m = inputs.small_q4(11, 256, 1024)
+    hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"])
+    args = (hb.desc.fmt, hb.desc.twin, hb.desc.rows, hb.desc.cols, hb.sections,
+            hb.stats.max_tile_rows, hb.stats.min_len, hb.stats.max_len)
+    db = lw.DeviceBundle(*args, device="cpu")
+    assert hb.stats.lut_entries > 0 and db.view.lut_entries == hb.stats.lut_entries
+    tw = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"], twin=True)
+    dt = lw.DeviceBundle(tw.desc.fmt, tw.desc.twin, tw.desc.rows, tw.desc.cols, tw.sections,
+                         tw.stats.max_tile_rows, tw.stats.min_len, tw.stats.max_len, device="cpu")
+    assert dt.view.lut_entries == 0
