@@ -111,6 +111,14 @@ lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int bat
   const int ncmp = twin ? 0 : ncmp_bucket_b(b->lmax - b->lmin);
   for (int b0 = 0; b0 < batch; b0 += 8) {
     const int nb = batch - b0 < 8 ? batch - b0 : 8;
+    if (lut_takes(&b, 1, nb)) {   // the table-driven kernel (same result bits)
+      const float* xp = reinterpret_cast<const float*>(x + (size_t)b0 * b->cols);
+      float* yp = y + (size_t)b0 * b->rows;
+      void* wp = ws;
+      const lw_status s = launch_q_lut(&b, 1, &xp, nb, &yp, &wp, status, st);
+      if (s != LW_OK) return s;
+      continue;
+    }
     const int bp = nb <= 1 ? 1 : (nb <= 2 ? 2 : (nb <= 4 ? 4 : 8));
     BKernel k = twin ? pick_b_product_bp<true>(bp, ncmp) : pick_b_product_bp<false>(bp, ncmp);
     dev::BArgs a = common_args(b);

@@ -555,7 +555,7 @@ extern "C" lw_status lw_bundle_sections(const lw_bundle* B, lw_sections* s) {
   s->min_len = B->table.lmin;
   s->palette_size = B->table.n_palette;
   s->bits_per_weight = 8.0 * (double)tot / ((double)B->desc.rows * (double)B->desc.cols);
-  if (!B->desc.twin && B->desc.fmt != LW_FMT_BF16_EXP)
+  if (!B->desc.twin)
     s->lut_entries = lw::lut_shape(B->table.lim_m1, B->table.lmin, B->table.lmax).n;
   return LW_OK;
 }
@@ -651,9 +651,7 @@ extern "C" const char* lw_status_string(lw_status s) {
 extern "C" const char* lw_last_error(void) { return g_err.c_str(); }
 
 extern "C" int32_t lw_table_lut_entries(const lw_table* t) {
-  if (!t || t->fmt == LW_FMT_BF16_EXP || t->lmin < 1 || t->lmax > LW_MAX_CODE_LEN ||
-      t->lmin > t->lmax)
-    return 0;
+  if (!t || t->lmin < 1 || t->lmax > LW_MAX_CODE_LEN || t->lmin > t->lmax) return 0;
   return lw::lut_shape(t->lim_m1, t->lmin, t->lmax).n;
 }
 

@@ -116,6 +116,7 @@ int take_test_stall();
 // order, so the choice never changes a result bit.
 constexpr int kLutMaxRowsQ4 = 4;
 constexpr int kLutMaxRowsQ6 = 2;
+constexpr int kLutMaxRowsB16 = 4;   // BF16 exponent: coded single matrices
 bool lut_takes(const lw_dev_bundle* const* bs, int n, int batch);
 bool lut_fits(const lw_dev_bundle* b);
 // With a strip list (device array of n_strips 64-row strips), n must be 1.

@@ -71,6 +71,12 @@ struct QArgs {
   int mid_offset;        // byte offset of the tile's lane_mid copy in a stage
   // tensor-core product only
   int nsplit, bpad, tmem_cols, xs_off, wstage_off;
+  // BF16 exponent bundles in the table-driven kernel (x then holds bf16)
+  const uint8_t* signman;   // [n_tiles][32 chunks][32 lanes][16 B]
+  const uint32_t* vflags;   // [N][GW]
+  const uint32_t* vrow_off; // [N + 1]
+  const uint8_t* vexp;      // [n_verbatim][64]
+  int GW;
 };
 
 // The product kernel's launch: one matrix, or a group of independent
@@ -109,7 +115,7 @@ __device__ __forceinline__ int group_seek(const QLaunch& g, int t, int m) {
   return m;
 }
 
-constexpr int kQ4 = LW_FMT_Q4_PAIR, kQ6 = LW_FMT_Q6;
+constexpr int kQ4 = LW_FMT_Q4_PAIR, kQ6 = LW_FMT_Q6, kB16 = LW_FMT_BF16_EXP;
 
 template <int FMT> struct QFmt;
 template <> struct QFmt<LW_FMT_Q4_PAIR> {
@@ -117,6 +123,9 @@ template <> struct QFmt<LW_FMT_Q4_PAIR> {
 };
 template <> struct QFmt<LW_FMT_Q6> {
   static constexpr int alpha = 64, qp_bytes = 2048;
+};
+template <> struct QFmt<LW_FMT_BF16_EXP> {
+  static constexpr int alpha = 16, qp_bytes = 0;
 };
 
 // shared-memory map (bytes)

@@ -27,6 +27,14 @@ template <int FMT, bool TWIN>
 LKernel pick_lut(int bp, int r) {
   return r == 2 ? pick_lut_r<FMT, TWIN, 2>(bp) : pick_lut_r<FMT, TWIN, 1>(bp);
 }
+// BF16 exponent bundles: coded, whole-tile units, up to 4 rows per pass
+LKernel pick_lut_b16(int bp) {
+  switch (bp) {
+    case 1: return dev::q_lut_kernel<dev::kB16, false, 1, 2>;
+    case 2: return dev::q_lut_kernel<dev::kB16, false, 2, 2>;
+    default: return dev::q_lut_kernel<dev::kB16, false, 4, 2>;
+  }
+}
 
 // Largest dynamic shared memory a CTA may use on the current device.
 int max_dyn_smem() {
@@ -47,7 +55,8 @@ int max_dyn_smem() {
 // rows: stage layout, table capacity and stage count S (capped at
 // kLMaxStages, a multiple of the producer count).
 struct LRing {
-  int bp, stage_rows, qp_off, mid_off, lb_off, x_off, stage_bytes, ring_off, lut_cap, lut_bytes, S;
+  int bp, stage_rows, qp_off, mid_off, lb_off, vi_off, xb_off, x_off, stage_bytes, ring_off, lut_cap,
+      lut_bytes, S;
 };
 LRing lut_ring(const lw_dev_bundle* const* bs, int n, int batch) {
   LRing r{};
@@ -57,13 +66,21 @@ LRing lut_ring(const lw_dev_bundle* const* bs, int n, int batch) {
   int max_rows = 0;
   for (int i = 0; i < n; ++i) max_rows = bs[i]->max_tile_rows > max_rows ? bs[i]->max_tile_rows : max_rows;
   // stage: coded rows (a stream reads up to two rows past its last word) |
-  // scales/mins | mid offsets | lane bit counts | activation slices | "fits"
-  // flag
+  // scales/mins | mid offsets | lane bit counts | [BF16: verbatim
+  // information (4 B per row), bf16 activation rows] | fp32 activation rows
+  // | "fits" flag
   r.stage_rows = max_rows + 2;
   r.qp_off = r.stage_rows * 128;
   r.mid_off = r.qp_off + qparam_tile_bytes(fmt);
   r.lb_off = r.mid_off + 64;
-  r.x_off = r.mid_off + (twin ? 0 : 128);
+  if (fmt == LW_FMT_BF16_EXP) {
+    r.vi_off = r.mid_off + 128;
+    r.xb_off = r.vi_off + 256;
+    r.x_off = r.xb_off + r.bp * 512;
+  } else {
+    r.vi_off = 0;
+    r.x_off = r.xb_off = r.mid_off + (twin ? 0 : 128);
+  }
   r.stage_bytes = (r.x_off + r.bp * 1024 + 16 + 127) / 128 * 128;
   r.ring_off = (dev::kLHdrBytes + 127) / 128 * 128;
   // the decode table: the largest member's entries (the device checks each
@@ -88,7 +105,10 @@ bool lut_fits(const lw_dev_bundle* b) {
 }
 
 bool lut_takes(const lw_dev_bundle* const* bs, int n, int batch) {
-  const int max_rows = bs[0]->fmt == LW_FMT_Q6 ? kLutMaxRowsQ6 : kLutMaxRowsQ4;
+  const int fmt = bs[0]->fmt;
+  if (fmt == LW_FMT_BF16_EXP && (n != 1 || bs[0]->twin)) return false;
+  const int max_rows = fmt == LW_FMT_Q6 ? kLutMaxRowsQ6 : (fmt == LW_FMT_Q4_PAIR ? kLutMaxRowsQ4
+                                                                               : kLutMaxRowsB16);
   if (batch > max_rows) return false;
   for (int i = 0; i < n; ++i)
     if (!lut_fits(bs[i])) return false;
@@ -117,6 +137,8 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
   g.mid_off = ring.mid_off;
   g.lb_off = ring.lb_off;
   g.x_off = ring.x_off;
+  g.xb_off = ring.xb_off;
+  g.vi_off = ring.vi_off;
   g.stage_bytes = ring.stage_bytes;
   g.ring_off = ring.ring_off;
   g.lut_cap = ring.lut_cap;
@@ -165,8 +187,9 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
   // lane sharing the activation loads) when a CTA has tiles for more than a
   // wave of 16 warps; half a tile per warp (R = 1: twice the warps, better
   // latency hiding and balance) for CTAs with fewer tiles
-  const int R = max_per_cta > 16 ? 2 : 1;
-  LKernel k = fmt == LW_FMT_Q4_PAIR
+  const int R = max_per_cta > 16 || fmt == LW_FMT_BF16_EXP ? 2 : 1;
+  LKernel k = fmt == LW_FMT_BF16_EXP ? pick_lut_b16(bp)
+              : fmt == LW_FMT_Q4_PAIR
                   ? (twin ? pick_lut<dev::kQ4, true>(bp, R) : pick_lut<dev::kQ4, false>(bp, R))
                   : (twin ? pick_lut<dev::kQ6, true>(bp, R) : pick_lut<dev::kQ6, false>(bp, R));
   // consumer warps: at most 16 (R = 2) or kLMaxConsumers (R = 1), and
@@ -174,7 +197,8 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
   // decodes), spread so that a CTA's units come in whole waves, and at
   // least 8 (they build the decode table)
   int nw_max = (2 / R) * (S - 4);
-  const int cap = R == 2 ? dev::kLMaxConsumersR<2> : dev::kLMaxConsumersR<1>;
+  const int cap = fmt == LW_FMT_BF16_EXP ? dev::kLMaxConsumersB16
+                  : (R == 2 ? dev::kLMaxConsumersR<2> : dev::kLMaxConsumersR<1>);
   if (nw_max > cap) nw_max = cap;
   const int units = (2 / R) * max_per_cta;
   const int waves = (units + nw_max - 1) / nw_max;
@@ -200,6 +224,13 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
     a.K = (int)b->cols;
     a.n_tiles = (int)n_tiles(i);
     a.batch = batch;
+    if (fmt == LW_FMT_BF16_EXP) {
+      a.signman = b->signman;
+      a.vflags = b->vflags;
+      a.vrow_off = b->vrow_off;
+      a.vexp = b->vexp;
+      a.GW = (int)((b->cols / 64 + 31) / 32);
+    }
   }
   const int threads = (nw + dev::kLProducers) * 32;
   if (resident_blocks((const void*)k, threads, smem) < 1)

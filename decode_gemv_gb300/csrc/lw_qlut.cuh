@@ -1,6 +1,8 @@
 // Table-driven fused decode + GEMV / small-batch GEMM for 4-bit (pair-coded)
-// and 6-bit Huffman-coded weights, and the same skeleton for their
-// fixed-width twins.
+// and 6-bit Huffman-coded weights and for BF16 weights whose exponents are
+// Huffman-coded ("Unweight: Compressing LLM Weights for Faster Inference",
+// "The exponent's exploitable redundancy"), and the same skeleton for the
+// 4-/6-bit fixed-width twins.
 //
 // Method: "LazyWeights: Decode-on-Demand Edge LLMs" -- "2 . Code them" and
 // Fig. 3(a) (64x256 tiles of 32 interleaved lanes of two rows), "3 . Decode on
@@ -36,18 +38,25 @@
 //    that only FMA-pipe instructions turn into fp32 (the integer ALU pipe,
 //    the decoder's bottleneck, keeps the bit work): 4-bit pairs as two fp16
 //    codes (the length sits in the low mantissa bits of one, where a
-//    rounding fp16 add of 1024 drops it), 6-bit codes as the fp16 1024 + c;
+//    rounding fp16 add of 1024 drops it), 6-bit codes as the fp16 1024 + c,
+//    BF16 exponent symbols as the palette's exponent at its fp32 position;
 //  * one 32-bit window serves two symbols (an 11-bit code leaves at least 21
 //    valid bits): window = funnel shift of two stream words by the bit
 //    position; the second peek comes from the window shifted by the first
 //    length; the position advances by both lengths and the words by at most
 //    one per step, branch-free (the next word is reloaded every step);
-//  * products in packed fp32 FMA (FFMA2) on the exact codes: even and odd
-//    columns in the two halves, then per row and tile part = scale * (acc.x
-//    + acc.y) + min * X (4-bit) or, per 16-weight group, scale * (acc.x +
-//    acc.y - 32 X_group) (6-bit), in a fixed order; the twin executes the
-//    same floating-point operations on the same values, so the twin's y is
-//    bitwise equal to the coded y;
+//  * products in packed fp32 FMA (FFMA2) on the exact values 16 + c (4-bit)
+//    and 64 + c (6-bit): even and odd columns in the two halves, then per
+//    row and tile part = scale * (acc.x + acc.y - 16 X) + min * X (4-bit)
+//    or, per 16-weight group, scale * (acc.x + acc.y - 96 X_group) (6-bit),
+//    in a fixed order -- the operations of the comparator kernel, whose
+//    results this kernel's equal bit for bit, as do the twin's;
+//  * BF16: each weight's fp32 value is its sign+mantissa byte (read from
+//    global memory a 16-weight chunk ahead) joined with the decoded exponent
+//    by a byte permute and one logic op; a verbatim 64-column group holds
+//    the stream (its lengths masked to zero) and takes its raw exponent
+//    bytes; the activations are widened from bf16 once per tile; the
+//    per-row sum is the comparator BF16 kernel's (bit for bit);
 //  * split-K: each tile's partial sums go to the workspace; the last tile of
 //    a 64-row strip to finish (an atomicInc counter that wraps back to zero)
 //    adds them in ascending tile order -- one launch, deterministic;
@@ -80,6 +89,9 @@ struct LLaunch {
   int lb_off;       // lane bit counts (coded bundles)
   int x_off;
   int ring_off;     // shared-memory offset of stage 0
+  int xb_off;       // where a stage's activation copies land (BF16: bf16
+                    // rows, widened into x_off by the consumer; else x_off)
+  int vi_off;       // BF16: per row of the tile, first verbatim group << 4 | 4 flags
   long long wait_cycles;   // limit of every wait on a stage (SM clock cycles)
   int stall_tile;   // testing: local tile of CTA 0 whose stage is armed without copies (-1: none)
   int lut_off;      // shared-memory offset of the decode table (coded bundles)
@@ -102,6 +114,11 @@ constexpr int kLMaxConsumers = 24;  // consumer warps at most
 // the kernel may keep more registers per thread)
 template <int R>
 constexpr int kLMaxConsumersR = R == 2 ? 16 : kLMaxConsumers;
+// BF16 exponent bundles: 12 (more registers for the sign+mantissa and
+// verbatim bytes in flight)
+constexpr int kLMaxConsumersB16 = 12;
+template <int FMT, int R>
+constexpr int kLMaxConsumersOf = FMT == LW_FMT_BF16_EXP ? kLMaxConsumersB16 : kLMaxConsumersR<R>;
 
 // a * b + c as one integer multiply-add (FMA pipe; the compiler would
 // otherwise often use shift-and-add forms on the integer ALU pipe)
@@ -155,9 +172,12 @@ __device__ __forceinline__ uint32_t f16_bits(uint32_t c) {
 //  high half = fp16(c_odd).  Bits 0..4 of the entry are L and bit 5 is zero,
 //  as the stream advance needs.
 //  6-bit: high half = fp16(1024 + c), low half = L.
-__device__ __forceinline__ uint32_t lut_entry(int fmt, uint32_t sym, int L) {
-  if (fmt == LW_FMT_Q4_PAIR)
+//  BF16 exponent: the palette's exponent byte at bits 23..30 (its place in
+//  an fp32), L at bits 0..4.
+__device__ __forceinline__ uint32_t lut_entry(const lw_table* tb, uint32_t sym, int L) {
+  if (tb->fmt == LW_FMT_Q4_PAIR)
     return (f16_bits((sym >> 4) & 15u) << 16) | f16_bits(sym & 15u) | (uint32_t)L;
+  if (tb->fmt == LW_FMT_BF16_EXP) return ((uint32_t)tb->palette[sym & 15u] << 23) | (uint32_t)L;
   return ((0x6400u | (sym & 63u)) << 16) | (uint32_t)L;
 }
 
@@ -204,7 +224,7 @@ __device__ __forceinline__ void lut_build(const lw_table* tb, const LutShape& sh
 #pragma unroll
       for (int j = 0; j < 10; ++j) L += (j < lmax - lmin && win > lim[j]) ? 1 : 0;
       const int idx = (int)(win >> (32 - L)) + tb->off[L - lmin];
-      e = lut_entry(tb->fmt, tb->sym[idx], L);
+      e = lut_entry(tb, tb->sym[idx], L);
       // the lane writes its entry's 32 copies, copy (lane + r) mod 32 at
       // step r: the warp's 32 stores of a step hit 32 different banks
       const uint32_t row = lut + (uint32_t)i * 128u;
@@ -239,21 +259,42 @@ struct LStream {
 };
 
 // Per-table decode constants (registers).
+// Word q (compile-time after unrolling) of a 16-byte value.
+__device__ __forceinline__ uint32_t l_word(const uint4& v, int q) {
+  return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+}
+
+// fp32 bits of a BF16 weight from its sign+mantissa byte K of word w and
+// its exponent field E (exp << 23 in bits 23..30; other bits of E are
+// ignored): the byte permute puts the byte's mantissa at bits 16..22 and its
+// sign at bit 31; one logic op takes bits 23..30 from E.
+template <int K>
+__device__ __forceinline__ float b16_value(uint32_t w, uint32_t E) {
+  constexpr uint32_t sel = 0x44u | ((uint32_t)K << 8) | (((uint32_t)K | 8u) << 12);
+  uint32_t t;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(w), "r"(0u), "r"(sel));
+  return __uint_as_float((t & 0x807FFFFFu) | (E & 0x7F800000u));
+}
+
 struct LDec {
   uint32_t lutl;   // shared address of entry 0, lane's copy
   int negC;
   uint32_t sh;     // 21 + s
 };
 
-// Decode the next two symbols of a stream: their table entries.
-__device__ __forceinline__ void l_decode2(LStream& st, const LDec& d, uint32_t& e0, uint32_t& e1) {
+// Decode the next two symbols of a stream: their table entries.  keep =
+// 0xFFFFFFE0 holds the stream where it is (the entries' lengths do not
+// count: a BF16 verbatim group has no symbols); the default all ones
+// folds away.
+__device__ __forceinline__ void l_decode2(LStream& st, const LDec& d, uint32_t& e0, uint32_t& e1,
+                                          uint32_t keep = 0xFFFFFFFFu) {
   const uint32_t w = shf_l_wrap(st.nxt, st.cur, st.pos);
   const int i0 = __viaddmax_s32((int)(w >> 21), d.negC, (int)(w >> d.sh));
   e0 = lds_u32(imad((uint32_t)i0, 128u, d.lutl));
   const uint32_t w1 = shf_l_wrap(0u, w, e0);
   const int i1 = __viaddmax_s32((int)(w1 >> 21), d.negC, (int)(w1 >> d.sh));
   e1 = lds_u32(imad((uint32_t)i1, 128u, d.lutl));
-  const uint32_t p2 = imad(e1, 1u, imad(e0, 1u, st.pos));
+  const uint32_t p2 = imad(e1 & keep, 1u, imad(e0 & keep, 1u, st.pos));
   const uint32_t hb = p2 & 32u;   // 32 when the window moves on by a word
   st.pos = imad(hb, 0xFFFFFFFFu, p2);   // p2 - hb
   st.cur = shf_r_clamp(st.cur, st.nxt, hb);
@@ -372,7 +413,7 @@ __device__ __forceinline__ void l_rows(const QArgs& a, int c0, int cnt, int n_lo
 }
 
 template <int FMT, bool TWIN, int BP, int R>
-__global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
+__global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32, 1) q_lut_kernel(const __grid_constant__ LLaunch g) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int nthreads = blockDim.x;
   const int nw = nthreads / 32 - kLProducers;   // consumer warps; warps nw.. produce
@@ -442,15 +483,19 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
     // The first pass over the ring (tiles i < S, chunk 0) needs no free stage
     // and its weight copies read the bundle only: they go out before the
     // wait for the previous kernel, their activation copies after it.
-    const uint32_t xbytes = (uint32_t)a.batch * 1024u;
+    // an activation row of a tile: 256 fp32 (4-/6-bit) or bf16 (BF16)
+    constexpr uint32_t XROW = FMT == kB16 ? 512u : 1024u;
+    const uint32_t xbytes = (uint32_t)a.batch * XROW;
+    auto copy_xrows = [&](uint8_t* st, int kt, uint64_t* bar) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(a.x) + (size_t)kt * XROW;
+      for (int b = 0; b < a.batch; ++b)
+        bulk_g2s(st + g.xb_off + b * XROW, src + (size_t)b * a.K * (XROW / 256), XROW, bar);
+    };
     auto copy_x = [&](int k) {
       const int t = __shfl_sync(0xFFFFFFFFu, ct, k);
       if (lane == 0 && !(blockIdx.x == 0 && pw + k * kLProducers == g.stall_tile)) {
-        const int i = pw + k * kLProducers, s = i % S, kt = t % a.TK;
-        uint8_t* st = smem + g.ring_off + s * g.stage_bytes;
-        for (int b = 0; b < a.batch; ++b)
-          bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
-                   &full[s]);
+        const int i = pw + k * kLProducers, s = i % S;
+        copy_xrows(smem + g.ring_off + s * g.stage_bytes, t % a.TK, &full[s]);
       }
     };
     bool waited = false;
@@ -485,6 +530,26 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
       const int j = k - cb;   // 0..31: lane j of the current chunk
       const uint32_t r0 = __shfl_sync(0xFFFFFFFFu, cr0, j), r1 = __shfl_sync(0xFFFFFFFFu, cr1, j);
       const int t = __shfl_sync(0xFFFFFFFFu, ct, j);
+      if (FMT == kB16) {
+        // the verbatim information of the tile's rows (lane l: rows 2l and
+        // 2l + 1): the 4 flags of the tile's 64-column groups and the index
+        // of the row's first verbatim group from there (bundle data only)
+        const int strip = t / a.TK, g0 = 4 * (t % a.TK);
+        uint8_t* st = smem + g.ring_off + s * g.stage_bytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const size_t r = (size_t)strip * 64 + 2 * lane + h;
+          const uint32_t* f = a.vflags + r * (size_t)a.GW;
+          uint32_t before = 0;
+          for (int w = 0; w < g0 / 32; ++w) before += __popc(__ldg(f + w));
+          const uint32_t cur = __ldg(f + g0 / 32);
+          before += __popc(cur & ((1u << (g0 % 32)) - 1u));
+          const uint32_t vb = __ldg(a.vrow_off + r) + before;   // < 2^28 (at most N K / 64)
+          *reinterpret_cast<uint32_t*>(st + g.vi_off + 4 * (2 * lane + h)) =
+              (vb << 4) | ((cur >> (g0 % 32)) & 15u);
+        }
+        __syncwarp();   // every lane's stores before lane 0's arrival (a release)
+      }
       if (lane == 0) {
         uint8_t* st = smem + g.ring_off + s * g.stage_bytes;
         const bool fits = r1 >= r0 && r1 - r0 <= (uint32_t)(g.stage_rows - 2);
@@ -503,17 +568,12 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
         const bool stall = blockIdx.x == 0 && i == g.stall_tile;
         if (!stall) {
           if (wbytes) bulk_g2s(st, a.words + (size_t)r0 * 32, wbytes, &full[s]);
-          bulk_g2s(st + g.qp_off, a.qparams + (size_t)t * qpb, qpb, &full[s]);
+          if (qpb) bulk_g2s(st + g.qp_off, a.qparams + (size_t)t * qpb, qpb, &full[s]);
           if (!TWIN) {
             bulk_g2s(st + g.mid_off, a.lane_mid + (size_t)t * 32, 64, &full[s]);
             bulk_g2s(st + g.lb_off, a.lane_bits + (size_t)t * 32, 64, &full[s]);
           }
-          if (waited) {
-            const int kt = t % a.TK;
-            for (int b = 0; b < a.batch; ++b)
-              bulk_g2s(st + g.x_off + b * 1024, a.x + (size_t)b * a.K + (size_t)kt * 256, 1024,
-                       &full[s]);
-          }
+          if (waited) copy_xrows(st, t % a.TK, &full[s]);
         }
       }
       issued = i;
@@ -696,7 +756,7 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
           for (int b = 0; b < BP; ++b)
             p[r][b] = fmaf(sc, (acc[r][b].x + acc[r][b].y) - 16.f * xa[b], mn * xa[b]);
         }
-      } else {  // 6-bit: 16 groups of 16 weights per row
+      } else if (FMT == kQ6) {  // 6-bit: 16 groups of 16 weights per row
         float X[BP];
 #pragma unroll
         for (int b = 0; b < BP; ++b) X[b] = group_sum16(sx + 1024u * b, lane);
@@ -771,6 +831,103 @@ __global__ void __launch_bounds__((kLMaxConsumersR<R> + kLProducers) * 32, 1) q_
 #pragma unroll
           for (int r = 0; r < R; ++r)
             if (st[r].consumed() != end[r]) report(a.status, LW_DEV_LANE_LENGTH);
+      } else {  // BF16 exponent (coded, R = 2): both rows of every lane
+        static_assert(FMT != kB16 || (R == 2 && !TWIN), "BF16: coded, whole-tile units");
+        // the tile's activations bf16 -> fp32, once, by this warp (rows
+        // beyond the batch stay zero)
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
+          if (b < a.batch) {
+            const uint4 w8 = lds_u4(wb + (uint32_t)g.xb_off + 512u * b + 16u * (uint32_t)lane);
+            float4 lo, hi;
+            lo.x = __uint_as_float(w8.x << 16); lo.y = __uint_as_float(w8.x & 0xFFFF0000u);
+            lo.z = __uint_as_float(w8.y << 16); lo.w = __uint_as_float(w8.y & 0xFFFF0000u);
+            hi.x = __uint_as_float(w8.z << 16); hi.y = __uint_as_float(w8.z & 0xFFFF0000u);
+            hi.z = __uint_as_float(w8.w << 16); hi.w = __uint_as_float(w8.w & 0xFFFF0000u);
+            float4* xf = reinterpret_cast<float4*>(smem + g.ring_off + s * g.stage_bytes + g.x_off +
+                                                   1024 * b + 32 * lane);
+            xf[0] = lo;
+            xf[1] = hi;
+          }
+        __syncwarp();
+        // per row: the flags of its 4 groups, its first verbatim group from here
+        uint32_t fw[2], vb[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t vi = lds_u32(wb + (uint32_t)g.vi_off + 4u * (uint32_t)(2 * lane + h));
+          fw[h] = vi & 15u;
+          vb[h] = vi >> 4;
+        }
+        LStream st[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) st[h].init(wb, lane, g.stage_rows, start[h]);
+        // sign+mantissa bytes of row h's 16-weight chunk k: one 16-byte load
+        // per lane, a chunk ahead; a verbatim group's raw exponents likewise
+        const uint4* smb = reinterpret_cast<const uint4*>(a.signman + (size_t)t * 16384) + lane;
+        const uint4* veb = reinterpret_cast<const uint4*>(a.vexp);
+        uint4 nsm[2], nve[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          nsm[h] = __ldg(smb + (16 * h) * 32);
+          nve[h] = (fw[h] & 1u) ? __ldg(veb + (size_t)vb[h] * 4) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float2 acc[2][BP];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int b = 0; b < BP; ++b) acc[h][b] = make_float2(0.f, 0.f);
+#pragma unroll 1
+        for (int k = 0; k < 16; ++k) {
+          uint4 sm[2], ve[2];
+          uint32_t keep[2], vm[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            sm[h] = nsm[h];
+            ve[h] = nve[h];
+            const bool v = (fw[h] >> (k >> 2)) & 1u;
+            keep[h] = v ? 0xFFFFFFE0u : 0xFFFFFFFFu;   // a verbatim group holds the stream
+            vm[h] = v ? 0xFFFFFFFFu : 0u;
+            if (k < 15) {
+              const int g1 = (k + 1) >> 2;
+              nsm[h] = __ldg(smb + (16 * h + k + 1) * 32);
+              nve[h] = ((fw[h] >> g1) & 1u)
+                           ? __ldg(veb + (size_t)(vb[h] + __popc(fw[h] & ((1u << g1) - 1u))) * 4 +
+                                   ((k + 1) & 3))
+                           : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {   // weights 2q, 2q + 1 of the chunk
+            float2 f[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t e0, e1;
+              l_decode2(st[h], dec, e0, e1, keep[h]);
+              const uint32_t sw = l_word(sm[h], q >> 1), vw = l_word(ve[h], q >> 1);
+              // exponent fields: the entry's, or the verbatim byte j (2 (q & 1) and
+              // 2 (q & 1) + 1 of word vw) moved to bits 23..30 by one shift
+              // (b16_value reads nothing else of it)
+              const uint32_t ve0 = (q & 1) ? vw << 7 : vw << 23;
+              const uint32_t ve1 = (q & 1) ? vw >> 1 : vw << 15;
+              const uint32_t E0 = (e0 & ~vm[h]) | (ve0 & vm[h]);
+              const uint32_t E1 = (e1 & ~vm[h]) | (ve1 & vm[h]);
+              f[h] = (q & 1) ? make_float2(b16_value<2>(sw, E0), b16_value<3>(sw, E1))
+                             : make_float2(b16_value<0>(sw, E0), b16_value<1>(sw, E1));
+            }
+#pragma unroll
+            for (int b = 0; b < BP; ++b) {
+              const float2 xv = lds_f2(sx + 1024u * b + 4u * (uint32_t)(16 * k + 2 * q));
+#pragma unroll
+              for (int h = 0; h < 2; ++h) acc[h][b] = __ffma2_rn(f[h], xv, acc[h][b]);
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int b = 0; b < BP; ++b) p[h][b] = acc[h][b].x + acc[h][b].y;
+          if (st[h].consumed() != end[h]) report(a.status, LW_DEV_LANE_LENGTH);
+        }
       }
       // release the stage (UPT units per stage): this warp's reads of it are
       // done (their values are in the partial sums), ordered before the

@@ -327,7 +327,7 @@ class DeviceBundle:
         if lut_entries is None:
             tab = sections.get("table")
             lut_entries = (lw_table_lut_entries(np.ascontiguousarray(tab).view(np.uint8).reshape(-1))
-                           if tab is not None and not twin and fmt != LW_FMT_BF16_EXP else 0)
+                           if tab is not None and not twin else 0)
         self.fmt, self.twin, self.rows, self.cols = fmt, bool(twin), rows, cols
         self.tensors = {}
         for name in SECTION_NAMES:

@@ -187,10 +187,10 @@ typedef struct {
   int32_t min_len;          /* shortest code length (lmin) */
   int32_t palette_size;     /* BF16 */
   double bits_per_weight;   /* 8 * coded_bytes / (N*K) */
-  int32_t lut_entries;      /* 4-/6-bit coded bundles: entries of the compact
-                               decode table (index max(peek >> s, peek - C),
-                               s and C chosen per table, 128 bytes each in
-                               shared memory); 0 otherwise */
+  int32_t lut_entries;      /* coded bundles: entries of the compact decode
+                               table (index max(peek >> s, peek - C), s and
+                               C chosen per table, 128 bytes each in shared
+                               memory); 0 for twins */
   int32_t reserved;
 } lw_sections;
 
@@ -211,8 +211,9 @@ typedef struct {
   int32_t lmin, lmax;       /* from lw_sections: code-length span of the table
                                (selects the kernel variant; checked on device) */
   int32_t lut_entries;      /* from lw_sections: entries of the compact decode
-                               table of the table-driven 4-/6-bit product
-                               kernel.  1..512 selects that kernel (the device
+                               table of the table-driven product kernel
+                               (4-/6-bit, and BF16 up to 4 activation rows
+                               per pass).  1..512 selects that kernel (the device
                                rebuilds the table from the bundle's lw_table
                                and reports LW_DEV_BAD_TABLE if it needs more);
                                0 selects the comparator kernel (any table).
@@ -518,10 +519,10 @@ size_t lw_noalloc_scratch_bytes(void);
  */
 lw_status lw_test_stall_next(int32_t wait_us);
 
-/* Entries of the compact decode table that the table-driven 4-/6-bit
-   product kernel builds from this decoder table (the value lw_sections and
-   lw_dev_bundle carry as lut_entries); 0 for a NULL table or a BF16 table.
-   Host only; for tables built by lw_table_from_lengths. */
+/* Entries of the compact decode table that the table-driven product
+   kernel builds from this decoder table (the value lw_sections and
+   lw_dev_bundle carry as lut_entries); 0 for a NULL table.  Host only; for
+   tables built by lw_table_from_lengths. */
 int32_t lw_table_lut_entries(const lw_table* t);
 
 /* The status's name ("LW_OK", "LW_ERR_SHAPE", ...; "unknown lw_status" for
@@ -553,8 +554,8 @@ lw_status lw_graph_launch(const lw_graph* g, void* stream);
 void lw_graph_free(lw_graph* g);
 
 /* ABI revision of this header: 4 (3 + lw_sections.lut_entries and
-   lw_dev_bundle.lut_entries, which selects the table-driven 4-/6-bit
-   product kernel; 3 added grouped launches, strip lists, the load-time
+   lw_dev_bundle.lut_entries, which selects the table-driven product
+   kernel; 3 added grouped launches, strip lists, the load-time
    transcode, bundle files, step graphs, LW_ERR_IO, LW_DEV_BAD_STRIPS).  The
    bundle file format carries its own version. */
 int32_t lw_version(void);

@@ -106,7 +106,22 @@ def test_bundle_stats_carry_the_hint():
     assert tw.stats.lut_entries == 0
     b = inputs.small_bf16(6, 64, 512)
     hbb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, b["bits"])
-    assert hbb.stats.lut_entries == 0
+    n = lw.lw_table_lut_entries(hbb.sections["table"])
+    assert hbb.stats.lut_entries == n and 1 <= n <= 512
+    bt = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, b["bits"], twin=True)
+    assert bt.stats.lut_entries == 0
+
+
+def test_workload_bf16_tables_fit():
+    """The Llama MLP's exponent tables (16-symbol palettes): their compact
+    tables are those of brute force and fit the kernel's 512 entries."""
+    spec = inputs.workload_specs(inputs.LLAMA_MLP_BF16)[0]
+    rng = inputs.matrix_rng(inputs.LLAMA_MLP_BF16, 0, 0)
+    w = inputs.bf16_matrix(rng, 256, spec.cols)["bits"]
+    hb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, w)
+    L = lw.table_fields(hb.sections["table"])["code_len"][:16]
+    n = hb.stats.lut_entries
+    assert n == smallest_consistent_table(peek_codewords(L)) and 1 <= n <= 512
 
 
 def test_device_view_computes_the_hint_when_not_given():
