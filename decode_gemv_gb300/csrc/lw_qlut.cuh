@@ -282,19 +282,19 @@ struct LDec {
   uint32_t sh;     // 21 + s
 };
 
-// Decode the next two symbols of a stream: their table entries.  keep =
-// 0xFFFFFFE0 holds the stream where it is (the entries' lengths do not
-// count: a BF16 verbatim group has no symbols); the default all ones
-// folds away.
+// Decode the next two symbols of a stream: their table entries.  go = 0
+// holds the stream where it is (the entries' lengths do not count: a BF16
+// verbatim group has no symbols), go = 1 advances it -- a multiplier of the
+// multiply-add that advances the position anyway (FMA pipe, no extra op).
 __device__ __forceinline__ void l_decode2(LStream& st, const LDec& d, uint32_t& e0, uint32_t& e1,
-                                          uint32_t keep = 0xFFFFFFFFu) {
+                                          uint32_t go = 1u) {
   const uint32_t w = shf_l_wrap(st.nxt, st.cur, st.pos);
   const int i0 = __viaddmax_s32((int)(w >> 21), d.negC, (int)(w >> d.sh));
   e0 = lds_u32(imad((uint32_t)i0, 128u, d.lutl));
   const uint32_t w1 = shf_l_wrap(0u, w, e0);
   const int i1 = __viaddmax_s32((int)(w1 >> 21), d.negC, (int)(w1 >> d.sh));
   e1 = lds_u32(imad((uint32_t)i1, 128u, d.lutl));
-  const uint32_t p2 = imad(e1 & keep, 1u, imad(e0 & keep, 1u, st.pos));
+  const uint32_t p2 = imad(imad(e1, 1u, e0), go, st.pos);
   const uint32_t hb = p2 & 32u;   // 32 when the window moves on by a word
   st.pos = imad(hb, 0xFFFFFFFFu, p2);   // p2 - hb
   st.cur = shf_r_clamp(st.cur, st.nxt, hb);
@@ -879,13 +879,13 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
 #pragma unroll 1
         for (int k = 0; k < 16; ++k) {
           uint4 sm[2], ve[2];
-          uint32_t keep[2], vm[2];
+          uint32_t go[2], vm[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             sm[h] = nsm[h];
             ve[h] = nve[h];
             const bool v = (fw[h] >> (k >> 2)) & 1u;
-            keep[h] = v ? 0xFFFFFFE0u : 0xFFFFFFFFu;   // a verbatim group holds the stream
+            go[h] = v ? 0u : 1u;   // a verbatim group holds the stream
             vm[h] = v ? 0xFFFFFFFFu : 0u;
             if (k < 15) {
               const int g1 = (k + 1) >> 2;
@@ -902,13 +902,13 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint32_t e0, e1;
-              l_decode2(st[h], dec, e0, e1, keep[h]);
+              l_decode2(st[h], dec, e0, e1, go[h]);
               const uint32_t sw = l_word(sm[h], q >> 1), vw = l_word(ve[h], q >> 1);
               // exponent fields: the entry's, or the verbatim byte j (2 (q & 1) and
-              // 2 (q & 1) + 1 of word vw) moved to bits 23..30 by one shift
-              // (b16_value reads nothing else of it)
-              const uint32_t ve0 = (q & 1) ? vw << 7 : vw << 23;
-              const uint32_t ve1 = (q & 1) ? vw >> 1 : vw << 15;
+              // 2 (q & 1) + 1 of word vw) moved to bits 23..30 (b16_value reads
+              // nothing else of it) -- by a multiply where a left shift does
+              const uint32_t ve0 = (q & 1) ? imad(vw, 1u << 7, 0u) : imad(vw, 1u << 23, 0u);
+              const uint32_t ve1 = (q & 1) ? vw >> 1 : imad(vw, 1u << 15, 0u);
               const uint32_t E0 = (e0 & ~vm[h]) | (ve0 & vm[h]);
               const uint32_t E1 = (e1 & ~vm[h]) | (ve1 & vm[h]);
               f[h] = (q & 1) ? make_float2(b16_value<2>(sw, E0), b16_value<3>(sw, E1))
