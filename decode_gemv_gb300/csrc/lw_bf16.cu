@@ -60,20 +60,26 @@ dev::BArgs common_args(const lw_dev_bundle* b) {
   return a;
 }
 
-BKernel pick_b_tc(int ncmp) {
+BKernel pick_b_tc(int ncmp, bool lut) {
+  if (lut) return dev::b_tc_kernel<10, true>;
   switch (ncmp) {
-    case 4: return dev::b_tc_kernel<4>;
-    case 8: return dev::b_tc_kernel<8>;
-    default: return dev::b_tc_kernel<10>;
+    case 4: return dev::b_tc_kernel<4, false>;
+    case 8: return dev::b_tc_kernel<8, false>;
+    default: return dev::b_tc_kernel<10, false>;
   }
 }
+
+// entries of a replicated decode table the tensor-core kernel takes (128 B
+// each; larger tables decode by the comparator)
+constexpr int kTcLutCap = 256;
 
 }  // namespace
 
 // Tensor-core product for 16..64 activation rows (one launch).
 lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
                                  void* ws, int32_t* status, cudaStream_t st) {
-  BKernel k = pick_b_tc(ncmp_bucket_b(b->lmax - b->lmin));
+  const bool lut = b->lut_entries >= 1 && b->lut_entries <= kTcLutCap;
+  BKernel k = pick_b_tc(ncmp_bucket_b(b->lmax - b->lmin), lut);
   dev::BArgs a = common_args(b);
   a.x = x;
   a.y = y;
@@ -90,6 +96,11 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   a.xs_off = dev::kTcXsOff;
   a.wstage_off = a.xs_off + 2 * a.bpad * 256;
   size_t smem = (size_t)a.wstage_off + 8 * (size_t)a.stage_bytes;
+  if (lut) {   // the replicated decode table after the stages
+    a.lut_off = (int)((smem + 127) / 128 * 128);
+    a.lut_cap = b->lut_entries;
+    smem = (size_t)a.lut_off + (size_t)a.lut_cap * 128;
+  }
   const int per_sm = tc_resident_blocks((const void*)k, dev::kTcThreads, smem, a.tmem_cols);
   if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);

@@ -47,6 +47,7 @@ struct BArgs {
   int x_offset, mid_offset, xf_offset;   // byte offsets inside a stage
   // tensor-core product only
   int nsplit, bpad, tmem_cols, slab_off, xs_off, wstage_off;
+  int lut_off, lut_cap;   // table-driven decode: replicated table (bytes, entries)
 };
 
 // shared-memory map (bytes) for the CUDA-core BF16 kernels: the 4-/6-bit

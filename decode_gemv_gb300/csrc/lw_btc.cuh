@@ -35,6 +35,7 @@
 #pragma once
 
 #include "lw_bkern.cuh"
+#include "lw_lutdec.cuh"
 
 namespace lw {
 namespace dev {
@@ -183,7 +184,10 @@ constexpr int kTcThreads = 256;
 // tensor-memory columns: D0, D1 (bpad each), then the two operand rings
 __host__ __device__ constexpr int tc_tmem_need(int bpad) { return 2 * bpad + 2 * kSlots * kACols; }
 
-template <int NCMP>
+// LUT: exponents decoded through the compact table replicated per lane
+// (lw_lutdec.cuh; a.lut_off, a.lut_cap) instead of the comparator -- the
+// same operand values, so the same results.
+template <int NCMP, bool LUT>
 __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -253,6 +257,20 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   if (!failed) {
     cmp.load(tb, tb->lmax - tb->lmin);
     lmin = tb->lmin;
+  }
+  LDec ldec{0u, 0, 21u};
+  if (LUT && !failed) {
+    // every warp finds the table's shape and builds an eighth of its entries
+    const LutShape sh = lut_shape_warp(tb->lim_m1, tb->lmin, tb->lmax, lane);
+    if (sh.n > a.lut_cap) {
+      if (tid == 0) report(a.status, LW_DEV_BAD_TABLE);
+      failed = true;
+    } else {
+      lut_build(tb, sh, sbase + (uint32_t)a.lut_off, warp, kTcThreads / 32, lane);
+    }
+    ldec.lutl = sbase + (uint32_t)a.lut_off + 4u * (uint32_t)lane;
+    ldec.negC = -sh.C;
+    ldec.sh = 21u + (uint32_t)sh.s;
   }
   __syncthreads();
   pdl_wait();
@@ -325,11 +343,13 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       }
       const uint32_t wb = smem_addr(wstage);
       LaneBits lb;
+      LStream ls;
       uint32_t mid = 0;
       const bool dec = has && fit_cur && !to;
       if (dec) {
         mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
-        lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
+        if (LUT) ls.init(wb, lane, a.stage_rows, h ? mid : 0u);
+        else lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
       }
       if (has && !fit_cur && lead) report(a.status, LW_DEV_TILE_SIZE);
       if (to) *abort_flag = 1u;
@@ -371,14 +391,32 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
             if (nfw & 1u) n_ve = b_load_vexp(a, nvb, 0);
           }
 
+          if (LUT) {
+            // a verbatim group holds the stream (multiplier 0) and takes its
+            // raw exponent bytes, moved to bits 23..30 (b16_value reads no more)
+            const uint32_t go = v ? 0u : 1u, vm = v ? 0xFFFFFFFFu : 0u;
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            uint32_t E0, E1;
-            b_exponents<false, NP>(lb, cmp, lmin, s_off, s_tab, wb, h, lane, k, p, v, ve, E0, E1);
-            const uint32_t sw = u4w(sm, p >> 1);
-            const uint32_t f0 = __float_as_uint((p & 1) ? b_value<2>(sw, E0) : b_value<0>(sw, E0));
-            const uint32_t f1 = __float_as_uint((p & 1) ? b_value<3>(sw, E1) : b_value<1>(sw, E1));
-            W[p] = __byte_perm(f0, f1, 0x7632);   // (bf16 of f1) << 16 | bf16 of f0
+            for (int p = 0; p < 8; ++p) {
+              uint32_t e0, e1;
+              l_decode2<true>(ls, ldec, e0, e1, go);
+              const uint32_t sw = u4w(sm, p >> 1), vw = u4w(ve, p >> 1);
+              const uint32_t ve0 = (p & 1) ? imad(vw, 1u << 7, 0u) : imad(vw, 1u << 23, 0u);
+              const uint32_t ve1 = (p & 1) ? vw >> 1 : imad(vw, 1u << 15, 0u);
+              const uint32_t E0 = (e0 & ~vm) | (ve0 & vm), E1 = (e1 & ~vm) | (ve1 & vm);
+              const uint32_t f0 = __float_as_uint((p & 1) ? b16_value<2>(sw, E0) : b16_value<0>(sw, E0));
+              const uint32_t f1 = __float_as_uint((p & 1) ? b16_value<3>(sw, E1) : b16_value<1>(sw, E1));
+              W[p] = __byte_perm(f0, f1, 0x7632);   // (bf16 of f1) << 16 | bf16 of f0
+            }
+          } else {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              uint32_t E0, E1;
+              b_exponents<false, NP>(lb, cmp, lmin, s_off, s_tab, wb, h, lane, k, p, v, ve, E0, E1);
+              const uint32_t sw = u4w(sm, p >> 1);
+              const uint32_t f0 = __float_as_uint((p & 1) ? b_value<2>(sw, E0) : b_value<0>(sw, E0));
+              const uint32_t f1 = __float_as_uint((p & 1) ? b_value<3>(sw, E1) : b_value<1>(sw, E1));
+              W[p] = __byte_perm(f0, f1, 0x7632);   // (bf16 of f1) << 16 | bf16 of f0
+            }
           }
         } else {
 #pragma unroll
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       }
       if (dec) {
         const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
-        if (lb.consumed() != end) report(a.status, LW_DEV_LANE_LENGTH);
+        if ((LUT ? ls.consumed() : (uint32_t)lb.consumed()) != end) report(a.status, LW_DEV_LANE_LENGTH);
       }
       ++ts;
       fit_cur = fit_nxt;
