@@ -130,7 +130,7 @@ static bool q_use_tc(const lw_dev_bundle* b, int rows) {
 extern "C" size_t lw_workspace_bytes(const lw_dev_bundle* b, int32_t batch) {
   if (!b || batch < 1 || b->rows <= 0 || b->cols <= 0) return 0;
   size_t part = workspace_partials_bytes(b, 8);
-  const bool tc = b->fmt == LW_FMT_BF16_EXP ? !b->twin && batch >= 16 : q_use_tc(b, batch);
+  const bool tc = b->fmt == LW_FMT_BF16_EXP ? batch >= 16 : q_use_tc(b, batch);
   if (tc && workspace_tc_bytes(b) > part) part = workspace_tc_bytes(b);
   return workspace_counter_bytes(b) + part;
 }
@@ -151,7 +151,7 @@ static lw_status product(const lw_dev_bundle* b, const void* X, int32_t batch, f
     if ((reinterpret_cast<uintptr_t>(X) & 15u) != 0)
       return fail(LW_ERR_INVALID_ARG, "x must be 16-byte aligned");
     const uint16_t* xb = static_cast<const uint16_t*>(X);
-    if (!b->twin && batch >= 16) {
+    if (batch >= 16) {   // coded and direct-palette twin alike
       // tensor cores (tcgen05) for up to 64 activation rows per launch
       for (int b0 = 0; b0 < batch; b0 += 64) {
         const int nb = batch - b0 < 64 ? batch - b0 : 64;

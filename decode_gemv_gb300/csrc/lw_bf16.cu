@@ -60,12 +60,13 @@ dev::BArgs common_args(const lw_dev_bundle* b) {
   return a;
 }
 
-BKernel pick_b_tc(int ncmp, bool lut) {
-  if (lut) return dev::b_tc_kernel<10, true>;
+BKernel pick_b_tc(int ncmp, bool lut, bool twin) {
+  if (twin) return dev::b_tc_kernel<2, false, true>;
+  if (lut) return dev::b_tc_kernel<10, true, false>;
   switch (ncmp) {
-    case 4: return dev::b_tc_kernel<4, false>;
-    case 8: return dev::b_tc_kernel<8, false>;
-    default: return dev::b_tc_kernel<10, false>;
+    case 4: return dev::b_tc_kernel<4, false, false>;
+    case 8: return dev::b_tc_kernel<8, false, false>;
+    default: return dev::b_tc_kernel<10, false, false>;
   }
 }
 
@@ -75,11 +76,13 @@ constexpr int kTcLutCap = 256;
 
 }  // namespace
 
-// Tensor-core product for 16..64 activation rows (one launch).
+// Tensor-core product for 16..64 activation rows (one launch); coded
+// bundles and their direct-palette twins.
 lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
                                  void* ws, int32_t* status, cudaStream_t st) {
-  const bool lut = b->lut_entries >= 1 && b->lut_entries <= kTcLutCap;
-  BKernel k = pick_b_tc(ncmp_bucket_b(b->lmax - b->lmin), lut);
+  const bool twin = b->twin != 0;
+  const bool lut = !twin && b->lut_entries >= 1 && b->lut_entries <= kTcLutCap;
+  BKernel k = pick_b_tc(twin ? 0 : ncmp_bucket_b(b->lmax - b->lmin), lut, twin);
   dev::BArgs a = common_args(b);
   a.x = x;
   a.y = y;

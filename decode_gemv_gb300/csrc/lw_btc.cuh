@@ -186,8 +186,12 @@ __host__ __device__ constexpr int tc_tmem_need(int bpad) { return 2 * bpad + 2 *
 
 // LUT: exponents decoded through the compact table replicated per lane
 // (lw_lutdec.cuh; a.lut_off, a.lut_cap) instead of the comparator -- the
-// same operand values, so the same results.
-template <int NCMP, bool LUT>
+// same operand values, so the same results.  TWIN: the fixed-width twin
+// ("Unweight", "Four different execution pipelines": direct palette): each
+// weight's exponent is its 4-bit palette index looked up in the palette, a
+// verbatim group's raw byte as in the coded bundle -- again the same
+// operands, so twin and coded results are bitwise equal.
+template <int NCMP, bool LUT, bool TWIN>
 __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -241,10 +245,13 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   bool infl0 = false, infl1 = false;
   uint32_t wpar0 = 0u, wpar1 = 0u;
   const bool got = __syncthreads_and(mbar_wait(tbar, 0u));
-  if (!got || !__syncthreads_and(table_ok_warp(tb, LW_FMT_BF16_EXP, 16, NCMP, lane))) {
+  if (!got || !(TWIN || __syncthreads_and(table_ok_warp(tb, LW_FMT_BF16_EXP, 16, NCMP, lane)))) {
     if (tid == 0) report(a.status, got ? LW_DEV_BAD_TABLE : LW_DEV_TIMEOUT);
     if (!got) mbar_wait(tbar, 0u);
     failed = true;
+  } else if (TWIN) {
+    if (warp == 0 && lane < 16)   // exp << 23 per palette index
+      reinterpret_cast<uint32_t*>(smem + kBTabOff)[lane] = (uint32_t)tb->palette[lane] << 23;
   } else if (warp == 0 && lane < 16) {
     put_off<(NCMP + 1) / 2>(reinterpret_cast<uint32_t*>(smem + kOffOff), lane,
                             s_tab + (uint32_t)(4 * (lane < 12 ? tb->off[lane] : 0)));
@@ -253,8 +260,9 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   }
   constexpr int NP = (NCMP + 1) / 2;
   Cmp<NP> cmp;
+  Cmp<1> cmp1;   // (unused by the twin's lookup)
   int lmin = 1;
-  if (!failed) {
+  if (!TWIN && !failed) {
     cmp.load(tb, tb->lmax - tb->lmin);
     lmin = tb->lmin;
   }
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
     bool fit_cur = true, fit_nxt = true;
     if (has) {
       const int t = strip * a.TK + kt0;
-      fit_cur = b_issue<false, false>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1),
+      fit_cur = b_issue<false, TWIN>(a, t, __ldg(a.tile_off + t), __ldg(a.tile_off + t + 1),
                                       wst0 + (ts & 1) * a.stage_bytes, &wbar[ts & 1],
                                       lead ? 0 : 1);
       if (ts & 1) infl1 = true; else infl0 = true;
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       // next tile into the other stage (both of its readers finished the
       // previous tile before the barrier above)
       if (has && more) {
-        fit_nxt = b_issue<false, false>(a, t + 1, __ldg(a.tile_off + t + 1), __ldg(a.tile_off + t + 2),
+        fit_nxt = b_issue<false, TWIN>(a, t + 1, __ldg(a.tile_off + t + 1), __ldg(a.tile_off + t + 2),
                                         wst0 + (cur ^ 1u) * a.stage_bytes, &wbar[cur ^ 1u],
                                         lead ? 0 : 1);
         if (cur) infl0 = true; else infl1 = true;
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       LStream ls;
       uint32_t mid = 0;
       const bool dec = has && fit_cur && !to;
-      if (dec) {
+      if (dec && !TWIN) {
         mid = lds_u16(wb + (uint32_t)a.mid_offset + 2u * (uint32_t)lane);
         if (LUT) ls.init(wb, lane, a.stage_rows, h ? mid : 0u);
         else lb.init_at(wb, lane, a.stage_rows, h ? mid : 0u);
@@ -391,7 +399,17 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
             if (nfw & 1u) n_ve = b_load_vexp(a, nvb, 0);
           }
 
-          if (LUT) {
+          if (TWIN) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              uint32_t E0, E1;
+              b_exponents<true, 1>(lb, cmp1, 0, s_off, s_tab, wb, h, lane, k, p, v, ve, E0, E1);
+              const uint32_t sw = u4w(sm, p >> 1);
+              const uint32_t f0 = __float_as_uint((p & 1) ? b_value<2>(sw, E0) : b_value<0>(sw, E0));
+              const uint32_t f1 = __float_as_uint((p & 1) ? b_value<3>(sw, E1) : b_value<1>(sw, E1));
+              W[p] = __byte_perm(f0, f1, 0x7632);   // (bf16 of f1) << 16 | bf16 of f0
+            }
+          } else if (LUT) {
             // a verbatim group holds the stream (multiplier 0) and takes its
             // raw exponent bytes, moved to bits 23..30 (b16_value reads no more)
             const uint32_t go = v ? 0u : 1u, vm = v ? 0xFFFFFFFFu : 0u;
@@ -443,7 +461,7 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
         ++gchunk;
         if ((k & 7) == 7) ++xk;
       }
-      if (dec) {
+      if (dec && !TWIN) {
         const uint32_t end = h ? (uint32_t)__ldg(a.lane_bits + (size_t)t * 32 + lane) : mid;
         if ((LUT ? ls.consumed() : (uint32_t)lb.consumed()) != end) report(a.status, LW_DEV_LANE_LENGTH);
       }

@@ -374,8 +374,11 @@ lw_status lw_twin_gemv(const lw_dev_bundle* twin, const void* x, float* y,
                        void* ws, size_t ws_bytes, int32_t* d_status,
                        void* stream);
 
-/* Twin product for a batch of activation rows (same contract as
-   lw_decode_gemm). */
+/* Twin product for a batch of activation rows (same contract and passes
+   as lw_decode_gemm; a BF16 twin of 16..64 rows per pass takes the tensor
+   cores with the palette's exponents -- [UW] "Four different execution
+   pipelines", direct palette -- and gives bitwise what lw_decode_gemm gives
+   on the coded bundle). */
 lw_status lw_twin_gemm(const lw_dev_bundle* twin, const void* X, int32_t batch,
                        float* Y, void* ws, size_t ws_bytes, int32_t* d_status,
                        void* stream);

@@ -170,6 +170,27 @@ def test_bf16_tensor_core_batches(shape, batch):
     assert_close(Y, Yc, absprod)
     Y2, st = run_product(db, m["x"])           # twice in a row: counters reset
     assert st == 0 and np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+    # the direct-palette twin on the tensor cores: the same operands, so
+    # bitwise the coded product
+    _, dt = upload(m["bits"], twin=True)
+    Yt, st = run_product(dt, m["x"], twin=True)
+    assert st == 0 and np.array_equal(Y.view(np.uint32), Yt.view(np.uint32))
+
+
+def test_bf16_twin_tensor_core_all_verbatim_and_none():
+    """Direct-palette twin on the tensor cores with every 64-group verbatim,
+    and with none: against the oracle and bitwise against the coded product."""
+    for kind in ("all", "none"):
+        m = inputs.small_bf16(77, 256, 1024, batch=32, outlier_p=0.0)
+        if kind == "all":
+            m["bits"] = all_verbatim(m["bits"])
+        _, db = upload(m["bits"])
+        _, dt = upload(m["bits"], twin=True)
+        Y, st = run_product(db, m["x"])
+        Yt, stt = run_product(dt, m["x"], twin=True)
+        assert st == 0 and stt == 0
+        assert_close(Yt, oracle.reference_output(oracle.BF16, m), oracle.abs_row_products(oracle.BF16, m))
+        assert np.array_equal(Y.view(np.uint32), Yt.view(np.uint32))
 
 
 def test_bf16_tensor_core_full_size_down():

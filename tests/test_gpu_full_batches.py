@@ -96,6 +96,27 @@ def test_llama_mlp_bf16_tensor_core(index):
     check(spec, m, upload(spec, m), (16, 64), 131)
 
 
+def test_llama_mlp_bf16_twin_tensor_core():
+    """The direct-palette twin of the full-size gate on the tensor cores at
+    batches 16 and 64 (lw_twin_gemm), sampled rows against the oracle."""
+    spec = inputs.workload_specs(inputs.LLAMA_MLP_BF16)[0]
+    m = inputs.make_matrix(inputs.LLAMA_MLP_BF16, spec, 0, 0, batch=64)
+    hb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, m["bits"], twin=True)
+    dt = lw.DeviceBundle.upload(hb, DEV)
+    rows = sample_rows(spec.rows, 131)
+    for b in (16, 64):
+        x = m["x"][:b]
+        X = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(DEV)
+        Y = torch.full((b, spec.rows), float("nan"), dtype=torch.float32, device=DEV)
+        ws = torch.zeros(lw.lw_workspace_bytes(dt, b) // 4, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        lw.lw_twin_gemm(dt, X, b, Y, ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        ref, absprod = reference(spec, m, rows, x)
+        assert_close(Y.cpu().numpy()[:, rows], ref, absprod)
+
+
 def stack_bf16mlp_layer(layer):
     """(workload, index, spec) of one layer of the stack with a BF16 MLP: the
     stack's q, k, v, o and the BF16 MLP's gate, up, down."""
