@@ -474,7 +474,7 @@ def per_call_ms(torch, stream, calls_by_copy, reps=8):
     return out / reps
 
 
-KERNEL_SOURCES = ("lw_qlut.cuh", "lw_lut.h", "lw_qkern.cuh", "lw_dev.cuh", "lw_qlut.cu")
+KERNEL_SOURCES = ("lw_qlut.cuh", "lw_lutdec.cuh", "lw_lut.h", "lw_qkern.cuh", "lw_dev.cuh", "lw_qlut.cu")
 
 
 def kernel_source_digest():
