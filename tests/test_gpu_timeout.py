@@ -3,7 +3,8 @@ without a fault: lw_test_stall_next makes the next launch arm one stage for
 copies it never issues (nothing in flight) and limits its waits to 1 ms.
 The launch must report LW_DEV_TIMEOUT, return within the short limit, leave
 every workspace counter at zero, and the same workspace must then serve a
-normal call that is bitwise equal to one on a fresh workspace."""
+normal call that is bitwise equal to one on a fresh workspace -- for 4-bit
+coded and twin bundles and BF16 exponent bundles, at one and three rows."""
 import time
 
 import numpy as np
@@ -37,14 +38,20 @@ def call(db, X, Y, ws, st, batch, twin):
         lw.lw_decode_gemm(db, X, batch, Y, ws, st)
 
 
-@pytest.mark.parametrize("twin", [False, True])
+@pytest.mark.parametrize("fmt,twin", [(lw.LW_FMT_Q4_PAIR, False), (lw.LW_FMT_Q4_PAIR, True),
+                                      (lw.LW_FMT_BF16_EXP, False)])
 @pytest.mark.parametrize("batch", [1, 3])
-def test_stalled_stage_times_out_and_workspace_survives(twin, batch):
+def test_stalled_stage_times_out_and_workspace_survives(fmt, twin, batch):
     rows, cols = 2048, 4096    # 512 tiles: CTA 0 holds several
-    m = inputs.small_q4(907 + batch, rows, cols, batch=batch)
-    hb = lw.lw_encode_bundle(lw.LW_FMT_Q4_PAIR, m["codes"], m["scales"], m["mins"], twin=twin)
+    if fmt == lw.LW_FMT_BF16_EXP:
+        m = inputs.small_bf16(907 + batch, rows, cols, batch=batch)
+        hb = lw.lw_encode_bundle(fmt, m["bits"])
+        X = torch.from_numpy(m["x"].view(np.int16)).to(DEV)
+    else:
+        m = inputs.small_q4(907 + batch, rows, cols, batch=batch)
+        hb = lw.lw_encode_bundle(fmt, m["codes"], m["scales"], m["mins"], twin=twin)
+        X = torch.from_numpy(m["x"]).to(DEV)
     db = lw.DeviceBundle.upload(hb, DEV)
-    X = torch.from_numpy(m["x"]).to(DEV)
     nbytes = lw.lw_workspace_bytes(db, batch)
 
     def fresh():
