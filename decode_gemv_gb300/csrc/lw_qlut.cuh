@@ -295,6 +295,13 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
   // as this kernel's CTA there exits, and run their prologue (barriers,
   // decode table, first weight copies) while the other SMs still drain.
   pdl_trigger();
+  // the decoder table's copy goes out first (its barrier initialised just
+  // before it; the CTA barrier below publishes the initialisation)
+  if (!TWIN && threadIdx.x == 0) {
+    mbar_init(tbar, 1);
+    fence_barrier_init();
+    table_issue(smem + kLRawTab, a.table, tbar);
+  }
   // a producer's first loads (the row ranges of its first 32 tiles) go out
   // before anything else
   uint32_t cr0 = 0u, cr1 = 0u;
@@ -311,7 +318,6 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
   if (threadIdx.x == 0) {
     *reinterpret_cast<int*>(smem + kLHdrNext) = 0;
     *err = 0;
-    mbar_init(tbar, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 2 / R);   // every unit of the tile releases it
@@ -320,7 +326,6 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
     fence_barrier_init();
   }
   __syncthreads();
-  if (!TWIN && threadIdx.x == 0) table_issue(smem + kLRawTab, a.table, tbar);
 
   // ---- producers: fill the ring ----
   // kLProducers warps; producer p owns the stages s = p mod kLProducers and
@@ -339,9 +344,12 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
     int nt, cb = 0;
     rows_of(32 + lane, nr0, nr1, nt);
     int issued = -1;   // last local tile this warp issued
-    // The first pass over the ring (tiles i < S, chunk 0) needs no free stage
-    // and its weight copies read the bundle only: they go out before the
-    // wait for the previous kernel, their activation copies after it.
+    // A warp's first tile needs no free stage and its weight copies read the
+    // bundle only: they go out before the wait for the previous kernel, its
+    // activation copies after it.  Only one tile per warp: the CTA that
+    // enters last (after the previous kernel's last CTA left its SM, so the
+    // wait returns at once) must reach its activation copies quickly -- it
+    // is the one that finishes last -- while the others have slack.
     // an activation row of a tile: 256 fp32 (4-/6-bit) or bf16 (BF16)
     constexpr uint32_t XROW = FMT == kB16 ? 512u : 1024u;
     const uint32_t xbytes = (uint32_t)a.batch * XROW;
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__((kLMaxConsumersOf<FMT, R> + kLProducers) * 32,
     bool waited = false;
     for (int k = 0; pw + k * kLProducers < n_local; ++k) {
       const int i = pw + k * kLProducers;
-      if (!waited && i >= S) {
+      if (!waited && (i >= S || k >= 1)) {
         pdl_wait();
         waited = true;
         for (int kk = 0; kk < k; ++kk) copy_x(kk);
