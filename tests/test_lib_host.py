@@ -264,8 +264,8 @@ def test_host_calls_from_many_threads():
 def test_workspace_bytes_follow_the_documented_layout():
     """lw_workspace_bytes = per-strip counters (N/64 uint32, padded to 256
     bytes) + fp32 partial sums [K/256][8][N]; BF16 products of 16 or more
-    rows use the tensor-core K-split partials [min(max(K/512, 1), 32)][64][N]
-    when larger.  Host arithmetic only: the view's addresses are never used."""
+    rows (coded or direct-palette twin) use the tensor-core K-split partials
+    [min(max(K/512, 1), 32)][64][N] when larger.  Host arithmetic only: the view's addresses are never used."""
     lib = lw.load()
     for fmt in (lw.LW_FMT_Q4_PAIR, lw.LW_FMT_Q6, lw.LW_FMT_BF16_EXP):
         for n, k in ((64, 256), (192, 768), (4096, 4096), (14336, 4096), (4096, 14336)):
@@ -279,8 +279,9 @@ def test_workspace_bytes_follow_the_documented_layout():
                 splits = min(max(k // 512, 1), 32)
                 want = counters + max(part, splits * 64 * n * 4)
                 assert lib.lw_workspace_bytes(ctypes.byref(v), 16) == want
-                v.twin = 1                      # the twin stays on the CUDA cores
-                assert lib.lw_workspace_bytes(ctypes.byref(v), 16) == counters + part
+                v.twin = 1                      # the direct-palette twin takes the tensor cores too
+                assert lib.lw_workspace_bytes(ctypes.byref(v), 16) == want
+                assert lib.lw_workspace_bytes(ctypes.byref(v), 5) == counters + part
     v = lw.LwDevBundle()
     v.fmt, v.rows, v.cols = lw.LW_FMT_Q4_PAIR, 64, 256
     assert lib.lw_workspace_bytes(ctypes.byref(v), 0) == 0
