@@ -108,15 +108,71 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
   const int slots = per_sm * device_sm_count();
-  int nsplit = (slots + n_blocks - 1) / n_blocks;
-  if (nsplit > tc_max_split(b)) nsplit = tc_max_split(b);
-  if (nsplit > a.TK) nsplit = a.TK;
-  if (nsplit < 1) nsplit = 1;
-  a.nsplit = nsplit;
+  a.nsplit = tc_pick_split(n_blocks, a.TK, tc_max_split(b), slots, a.bpad);
+  const int nsplit = a.nsplit;
   int grid = n_blocks * nsplit;
   if (grid > slots) grid = slots;
   launch_pdl(k, grid, dev::kTcThreads, smem, st, a);
-  return check_launch("tensor-core product kernel");
+  lw_status s = check_launch("tensor-core product kernel");
+  if (s == LW_OK && nsplit > 1) s = launch_tc_sum(a.ws, y, (int)b->rows, batch, nsplit, st);
+  return s;
+}
+
+namespace dev {
+
+// The split-K sum of a tensor-core product whose K range was split over
+// CTAs: y[b][n] = partial 0 + partial 1 + ... in ascending split order
+// (partial q at ws[q][b][n]).  A kernel of its own, launched right behind the
+// product with programmatic dependent launch, so that every SM takes part in
+// the sum (a sum by one CTA per row block would be held to that SM's share
+// of the L2 bandwidth).  One thread
+// per 4 consecutive outputs (N is a multiple of 64), kSumDepth loads in
+// flight.
+struct TcSumArgs {
+  const float* ws;   // [nsplit][batch][N] fp32, 16-byte aligned
+  float* y;          // [batch][N] fp32, 8-byte aligned
+  int N, batch, nsplit;
+};
+constexpr int kSumThreads = 256;
+constexpr int kSumDepth = 8;
+
+__global__ void __launch_bounds__(kSumThreads) tc_sum_kernel(const TcSumArgs a) {
+  pdl_trigger();
+  pdl_wait();   // the product's partials are complete and visible
+  const size_t groups = (size_t)a.batch * a.N / 4;
+  const size_t g = (size_t)blockIdx.x * kSumThreads + threadIdx.x;
+  if (g >= groups) return;
+  const float4* p = reinterpret_cast<const float4*>(a.ws) + g;
+  const size_t step4 = groups;   // one split's partials, in float4
+  float4 acc = __ldcg(p);
+  for (int q0 = 1; q0 < a.nsplit; q0 += kSumDepth) {
+    float4 v[kSumDepth];
+#pragma unroll
+    for (int j = 0; j < kSumDepth; ++j)
+      if (q0 + j < a.nsplit) v[j] = __ldcg(p + (size_t)(q0 + j) * step4);
+#pragma unroll
+    for (int j = 0; j < kSumDepth; ++j) {
+      if (q0 + j < a.nsplit) {
+        acc.x += v[j].x;
+        acc.y += v[j].y;
+        acc.z += v[j].z;
+        acc.w += v[j].w;
+      }
+    }
+  }
+  float2* yp = reinterpret_cast<float2*>(a.y + 4 * g);
+  yp[0] = make_float2(acc.x, acc.y);
+  yp[1] = make_float2(acc.z, acc.w);
+}
+
+}  // namespace dev
+
+lw_status launch_tc_sum(const float* ws, float* y, int N, int batch, int nsplit, cudaStream_t st) {
+  dev::TcSumArgs a{ws, y, N, batch, nsplit};
+  const long long groups = (long long)batch * N / 4;
+  const int grid = (int)((groups + dev::kSumThreads - 1) / dev::kSumThreads);
+  launch_pdl(dev::tc_sum_kernel, grid, dev::kSumThreads, 0, st, a);
+  return check_launch("split-K sum kernel");
 }
 
 lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,

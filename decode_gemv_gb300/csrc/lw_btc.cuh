@@ -26,8 +26,9 @@
 //    next tile, the rows' verbatim flags and first sign+mantissa chunk are
 //    fetched while the current tile is decoded;
 //  * the accumulators are read back with tcgen05.ld by the warp that owns
-//    their lanes; split-K partials are added in ascending split order by the
-//    last CTA of each 256-row block;
+//    their lanes; with K split over CTAs each writes its partial sums and
+//    a sum kernel launched right behind (tc_sum_kernel, lw_bf16.cu) adds
+//    them in ascending split order;
 //  * the decoder table is bulk-copied into shared memory and checked
 //    lane-parallel.
 // Every wait is bounded; on a timeout the CTA reports LW_DEV_TIMEOUT, waits
@@ -204,7 +205,6 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   uint64_t* xbar = sbar + kSlots;                                             // [2] X^T buffers
   uint64_t* tbar = xbar + 2;                                                  // table copy
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kTcSlotOff);
-  volatile uint32_t* shared_word = tslot + 1;
   volatile uint32_t* abort_flag = tslot + 2;   // a wait ran out: stop at the next tile column
   uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + kTcSlotOff + 16);   // [kSlots]
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kTcRawTabOff);
@@ -495,24 +495,6 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
     }
     tc_fence_before();
     __syncthreads();   // accumulators read before the next unit overwrites them
-    if (a.nsplit > 1) {
-      // the last split of this row block to finish adds the splits in order
-      if (tid == 0) *shared_word = atom_inc_acq_rel(a.counters + rb, (unsigned)(a.nsplit - 1));
-      __syncthreads();
-      const bool last = *shared_word == (uint32_t)(a.nsplit - 1);
-      __syncthreads();
-      if (last) {
-        for (int i = tid; i < 256 * a.batch; i += kTcThreads) {
-          const int b = i >> 8;
-          const size_t row = (size_t)rb * 256 + (i & 255);
-          if (row >= (size_t)a.N) continue;
-          const float* p = a.ws + (size_t)b * a.N + row;
-          float acc = __ldcg(p);
-          for (int q = 1; q < a.nsplit; ++q) acc += __ldcg(p + (size_t)q * step);
-          a.y[(size_t)b * a.N + row] = acc;
-        }
-      }
-    }
   }
   if (timed_out) {
     if (tid == 0) report(a.status, LW_DEV_TIMEOUT);

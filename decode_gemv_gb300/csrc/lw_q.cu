@@ -82,15 +82,14 @@ lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch,
   if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
   const int slots = per_sm * device_sm_count();
-  int nsplit = (slots + n_blocks - 1) / n_blocks;
-  if (nsplit > tc_max_split(b)) nsplit = tc_max_split(b);
-  if (nsplit > a.TK) nsplit = a.TK;
-  if (nsplit < 1) nsplit = 1;
-  a.nsplit = nsplit;
+  a.nsplit = tc_pick_split(n_blocks, a.TK, tc_max_split(b), slots, a.bpad);
+  const int nsplit = a.nsplit;
   int grid = n_blocks * nsplit;
   if (grid > slots) grid = slots;
   launch_pdl(k, grid, dev::kQtThreads, smem, st, a);
-  return check_launch("tensor-core product kernel");
+  lw_status s = check_launch("tensor-core product kernel");
+  if (s == LW_OK && nsplit > 1) s = launch_tc_sum(a.ws, y, (int)b->rows, batch, nsplit, st);
+  return s;
 }
 
 // Fused products of n matrices of one format (one launch): matrix i reads

@@ -20,8 +20,9 @@
 // strip w % 4 and stores the split weights into tensor memory (lanes 32 s +
 // l of operand tile h; hi and lo rings of kQtSlots chunks); X^T (hi and lo
 // rows) is staged in 128-column halves one half ahead, loaded from global
-// memory two chunks before it is converted and stored; split-K partials are
-// added in ascending split order by the last CTA of each 256-row block.
+// memory two chunks before it is converted and stored; with K split over
+// CTAs each writes its partial sums and tc_sum_kernel (lw_bf16.cu) adds them
+// in ascending split order.
 // Every wait is bounded; on a timeout the CTA reports LW_DEV_TIMEOUT, waits
 // (bounded) for its own MMAs and copies, frees its tensor memory and returns.
 #pragma once
@@ -113,7 +114,6 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
   uint64_t* xbar = sbar + kQtSlots;                                          // [2] X^T buffers
   uint64_t* tbar = xbar + 2;                                                 // table copy
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(smem + kQtSlotOff);
-  volatile uint32_t* shared_word = tslot + 1;
   volatile uint32_t* abort_flag = tslot + 2;   // a wait ran out: stop at the next tile column
   uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + kQtSlotOff + 16);   // [kQtSlots]
   const lw_table* tb = reinterpret_cast<const lw_table*>(smem + kQtRawTabOff);
@@ -360,24 +360,6 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
     }
     tc_fence_before();
     __syncthreads();   // accumulators read before the next unit overwrites them
-    if (a.nsplit > 1) {
-      // the last split of this row block to finish adds the splits in order
-      if (tid == 0) *shared_word = atom_inc_acq_rel(a.counters + rb, (unsigned)(a.nsplit - 1));
-      __syncthreads();
-      const bool last = *shared_word == (uint32_t)(a.nsplit - 1);
-      __syncthreads();
-      if (last) {
-        for (int i = tid; i < 256 * a.batch; i += kQtThreads) {
-          const int b = i >> 8;
-          const size_t row = (size_t)rb * 256 + (i & 255);
-          if (row >= (size_t)a.N) continue;
-          const float* p = a.ws + (size_t)b * a.N + row;
-          float acc = __ldcg(p);
-          for (int q = 1; q < a.nsplit; ++q) acc += __ldcg(p + (size_t)q * step);
-          a.y[(size_t)b * a.N + row] = acc;
-        }
-      }
-    }
   }
   if (timed_out) {
     if (tid == 0) report(a.status, LW_DEV_TIMEOUT);

@@ -12,6 +12,8 @@ uploaded once; every call on the same device buffers):
   gate_q4_b32        lw_decode_gemm, batch 32
   gate_q4_decode     lw_decode (decode only) of the 4-bit gate
   llama_gate_bf16    lw_decode_gemv, Llama-3.1-8B MLP gate, BF16 exponent coding
+  llama_gate_bf16_b16      lw_decode_gemm of the same, batch 16 (tensor cores)
+  llama_gate_bf16_b64      lw_decode_gemm of the same, batch 64 (tensor cores)
   llama_gate_bf16_decode   lw_decode of the same
 
 Exits nonzero if a call reports a device status."""
@@ -23,7 +25,7 @@ import torch
 from decode_gemv_gb300 import inputs, lw
 
 TARGETS = ("gate_q4", "gate_q4_twin", "gate_q4_b16", "gate_q4_b32", "gate_q4_decode",
-           "llama_gate_bf16", "llama_gate_bf16_decode")
+           "llama_gate_bf16", "llama_gate_bf16_b16", "llama_gate_bf16_b64", "llama_gate_bf16_decode")
 
 
 def main(argv=None) -> int:
@@ -44,10 +46,10 @@ def main(argv=None) -> int:
         X = torch.from_numpy(m["x"]).to(dev)
     else:
         spec = inputs.workload_specs(inputs.LLAMA_MLP_BF16)[0]
-        batch = 1
-        m = inputs.make_matrix(inputs.LLAMA_MLP_BF16, spec, 0, 0)
+        batch = 16 if t.endswith("b16") else 64 if t.endswith("b64") else 1
+        m = inputs.make_matrix(inputs.LLAMA_MLP_BF16, spec, 0, 0, batch=batch)
         hb = lw.lw_encode_bundle(lw.LW_FMT_BF16_EXP, m["bits"], None, None)
-        X = torch.from_numpy(m["x"].view("int16")).to(dev)
+        X = torch.from_numpy(m["x"].view("int16")).to(dev).reshape(batch, -1)
     db = lw.DeviceBundle.upload(hb, dev)
     if t.endswith("decode"):
         if db.fmt == lw.LW_FMT_Q4_PAIR:
