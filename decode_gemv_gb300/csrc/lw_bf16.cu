@@ -107,52 +107,62 @@ lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int 
   const int per_sm = tc_resident_blocks((const void*)k, dev::kTcThreads, smem, a.tmem_cols);
   if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
-  const int slots = per_sm * device_sm_count();
-  a.nsplit = tc_pick_split(n_blocks, a.TK, tc_max_split(b), slots, a.bpad);
-  const int nsplit = a.nsplit;
-  int grid = n_blocks * nsplit;
-  if (grid > slots) grid = slots;
-  launch_pdl(k, grid, dev::kTcThreads, smem, st, a);
+  const TcGrid g = tc_pick_grid(n_blocks, a.TK, tc_max_split(b), per_sm * device_sm_count());
+  launch_pdl(k, g.G, dev::kTcThreads, smem, st, a);
   lw_status s = check_launch("tensor-core product kernel");
-  if (s == LW_OK && nsplit > 1) s = launch_tc_sum(a.ws, y, (int)b->rows, batch, nsplit, st);
+  if (s == LW_OK && g.owners > 1) s = launch_tc_sum(a.ws, y, (int)b->rows, batch, a.TK, g.G, st);
   return s;
 }
 
 namespace dev {
 
-// The split-K sum of a tensor-core product whose K range was split over
-// CTAs: y[b][n] = partial 0 + partial 1 + ... in ascending split order
-// (partial q at ws[q][b][n]).  A kernel of its own, launched right behind the
-// product with programmatic dependent launch, so that every SM takes part in
-// the sum (a sum by one CTA per row block would be held to that SM's share
-// of the L2 bandwidth).  One thread
-// per 4 consecutive outputs (N is a multiple of 64), kSumDepth loads in
-// flight.
+// The split-K sum of a tensor-core product whose row blocks were split over
+// CTAs (tc_owner): y[b][n] = partial 0 + partial 1 + ... of n's row block,
+// in ascending order (partial j at ws[j][b][n]).  A kernel of its own,
+// launched right behind the product with programmatic dependent launch, so
+// that every SM takes part in the sum (a sum by one CTA per row block would
+// be held to that SM's share of the L2 bandwidth).  One thread per 4
+// consecutive outputs (N is a multiple of 64), kSumDepth loads in flight.
 struct TcSumArgs {
-  const float* ws;   // [nsplit][batch][N] fp32, 16-byte aligned
+  const float* ws;   // [owners][batch][N] fp32, 16-byte aligned
   float* y;          // [batch][N] fp32, 8-byte aligned
-  int N, batch, nsplit;
+  int N, batch, TK, G;
 };
 constexpr int kSumThreads = 256;
 constexpr int kSumDepth = 8;
 
+// WIDE: T x (G + 1) does not fit 32 bits (the owners in 64-bit arithmetic)
+template <bool WIDE>
 __global__ void __launch_bounds__(kSumThreads) tc_sum_kernel(const TcSumArgs a) {
   pdl_trigger();
   pdl_wait();   // the product's partials are complete and visible
-  const size_t groups = (size_t)a.batch * a.N / 4;
+  const int n4 = a.N / 4;
+  const size_t groups = (size_t)a.batch * n4;
   const size_t g = (size_t)blockIdx.x * kSumThreads + threadIdx.x;
   if (g >= groups) return;
+  const int n = 4 * (int)(g % (size_t)n4);
+  const long long T = (long long)((a.N / 64 + 3) / 4) * a.TK;
+  const long long xb = (long long)(n >> 8) * a.TK;   // the row block's first tile column
+  int owners;   // tc_owner(xb + TK - 1) - tc_owner(xb) + 1
+  if (WIDE) {
+    owners = tc_owner(xb + a.TK - 1, T, a.G) - tc_owner(xb, T, a.G) + 1;
+  } else {
+    const uint32_t T32 = (uint32_t)T, G32 = (uint32_t)a.G, x32 = (uint32_t)xb;
+    owners = (int)(((x32 + (uint32_t)a.TK) * G32 + T32 - 1u) / T32 -
+                   ((x32 + 1u) * G32 + T32 - 1u) / T32) + 1;
+  }
+  if (owners == 1) return;   // written by the product
   const float4* p = reinterpret_cast<const float4*>(a.ws) + g;
-  const size_t step4 = groups;   // one split's partials, in float4
+  const size_t step4 = groups;   // one partial, in float4
   float4 acc = __ldcg(p);
-  for (int q0 = 1; q0 < a.nsplit; q0 += kSumDepth) {
+  for (int q0 = 1; q0 < owners; q0 += kSumDepth) {
     float4 v[kSumDepth];
 #pragma unroll
     for (int j = 0; j < kSumDepth; ++j)
-      if (q0 + j < a.nsplit) v[j] = __ldcg(p + (size_t)(q0 + j) * step4);
+      if (q0 + j < owners) v[j] = __ldcg(p + (size_t)(q0 + j) * step4);
 #pragma unroll
     for (int j = 0; j < kSumDepth; ++j) {
-      if (q0 + j < a.nsplit) {
+      if (q0 + j < owners) {
         acc.x += v[j].x;
         acc.y += v[j].y;
         acc.z += v[j].z;
@@ -167,12 +177,76 @@ __global__ void __launch_bounds__(kSumThreads) tc_sum_kernel(const TcSumArgs a) 
 
 }  // namespace dev
 
-lw_status launch_tc_sum(const float* ws, float* y, int N, int batch, int nsplit, cudaStream_t st) {
-  dev::TcSumArgs a{ws, y, N, batch, nsplit};
+lw_status launch_tc_sum(const float* ws, float* y, int N, int batch, int TK, int G, cudaStream_t st) {
+  dev::TcSumArgs a{ws, y, N, batch, TK, G};
   const long long groups = (long long)batch * N / 4;
   const int grid = (int)((groups + dev::kSumThreads - 1) / dev::kSumThreads);
-  launch_pdl(dev::tc_sum_kernel, grid, dev::kSumThreads, 0, st, a);
+  const unsigned long long T = (unsigned long long)((N / 64 + 3) / 4) * (unsigned long long)TK;
+  if (T * (unsigned long long)(G + 1) >= (1ull << 32))
+    launch_pdl(dev::tc_sum_kernel<true>, grid, dev::kSumThreads, 0, st, a);
+  else
+    launch_pdl(dev::tc_sum_kernel<false>, grid, dev::kSumThreads, 0, st, a);
   return check_launch("split-K sum kernel");
+}
+
+namespace {
+
+TcGrid pick_grid_uncached(int n_blocks, int TK, int max_split, int slots) {
+  const long long T = (long long)n_blocks * TK;
+  const int g0 = (int)(slots < T ? slots : T);
+  TcGrid best{1, 1};
+  double best_cost = 1e300;
+  auto consider = [&](long long Gl) {
+    if (Gl < 1 || Gl > g0) return;
+    const int G = (int)Gl;
+    int owners = 0;
+    for (int rb = 0; rb < n_blocks; ++rb) {
+      const long long xb = (long long)rb * TK;
+      const int k = dev::tc_owner(xb + TK - 1, T, G) - dev::tc_owner(xb, T, G) + 1;
+      if (k > owners) owners = k;
+    }
+    if (owners > max_split) return;
+    long long segs = 1;   // most row blocks one CTA's range touches
+    for (int c = 0; c < G; ++c) {
+      const long long x0 = T * c / G, x1 = T * (c + 1) / G;
+      const long long k = (x1 - 1) / TK - x0 / TK + 1;
+      if (k > segs) segs = k;
+    }
+    const double cost = (double)((T + G - 1) / G) + 0.5 * (double)segs;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = TcGrid{G, owners};
+    }
+  };
+  consider(g0);
+  for (int m = 1; m <= max_split && m <= TK; ++m) consider((long long)n_blocks * m);
+  for (int L = 1; L <= TK; ++L) consider(T / L);
+  consider(1);
+  return best;
+}
+
+}  // namespace
+
+TcGrid tc_pick_grid(int n_blocks, int TK, int max_split, int slots) {
+  // a few recent shapes per host thread (the pick is pure host arithmetic)
+  struct Entry {
+    int key[4];
+    TcGrid g;
+  };
+  thread_local Entry cache[8];
+  thread_local int used = 0, next = 0;
+  const int key[4] = {n_blocks, TK, max_split, slots};
+  for (int i = 0; i < used; ++i)
+    if (cache[i].key[0] == key[0] && cache[i].key[1] == key[1] && cache[i].key[2] == key[2] &&
+        cache[i].key[3] == key[3])
+      return cache[i].g;
+  const TcGrid g = pick_grid_uncached(n_blocks, TK, max_split, slots);
+  Entry& e = cache[next];
+  for (int i = 0; i < 4; ++i) e.key[i] = key[i];
+  e.g = g;
+  next = (next + 1) % 8;
+  if (used < 8) ++used;
+  return g;
 }
 
 lw_status launch_bf16_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,

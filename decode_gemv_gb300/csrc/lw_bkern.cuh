@@ -46,7 +46,7 @@ struct BArgs {
   int stage_rows, stage_bytes;
   int x_offset, mid_offset, xf_offset;   // byte offsets inside a stage
   // tensor-core product only
-  int nsplit, bpad, tmem_cols, slab_off, xs_off, wstage_off;
+  int bpad, tmem_cols, slab_off, xs_off, wstage_off;
   int lut_off, lut_cap;   // table-driven decode: replicated table (bytes, entries)
 };
 

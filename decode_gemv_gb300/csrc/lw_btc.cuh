@@ -185,6 +185,17 @@ constexpr int kTcThreads = 256;
 // tensor-memory columns: D0, D1 (bpad each), then the two operand rings
 __host__ __device__ constexpr int tc_tmem_need(int bpad) { return 2 * bpad + 2 * kSlots * kACols; }
 
+// Work of a tensor-core launch, split over its G CTAs in contiguous ranges
+// (a "stream-K" cut): the launch's T = row blocks x TK tile columns, row
+// block major, go to CTA c as [c T / G, (c + 1) T / G), so every CTA gets
+// within one tile column of the same work; a range may run on into the next
+// row block.  A row block's partial sums come from the CTAs owning its tile
+// columns, numbered from the first of them.  The CTA owning tile column x
+// (0 <= x < T, 1 <= G <= T): the largest c with floor(c T / G) <= x.
+__host__ __device__ inline int tc_owner(long long x, long long T, int G) {
+  return (int)(((x + 1) * G + T - 1) / T) - 1;
+}
+
 // LUT: exponents decoded through the compact table replicated per lane
 // (lw_lutdec.cuh; a.lut_off, a.lut_cap) instead of the comparator -- the
 // same operand values, so the same results.  TWIN: the fixed-width twin
@@ -285,20 +296,28 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
   const uint32_t idesc = idesc_bf16((uint32_t)a.bpad);
   const int n_strips = a.N / 64;
   const int n_blocks = (n_strips + 3) / 4;
-  const int units = n_blocks * a.nsplit;
+  const long long T = (long long)n_blocks * a.TK;   // tile columns of the launch
+  const int G = (int)gridDim.x;
+  long long x = T * blockIdx.x / G;                 // this CTA's range [x, xe)
+  const long long xe = T * (blockIdx.x + 1) / G;
   uint32_t gchunk = 0;   // ring commits issued by this CTA so far (uniform)
   uint32_t xk = 0;       // X^T halves consumed by this CTA so far (uniform): the
                          // current half sits in buffer xk & 1
   uint32_t ts = 0;       // tile columns this CTA has started (uniform)
 
-  for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
-    const int rb = u / a.nsplit, sp = u % a.nsplit;
-    const int kt0 = (int)((long long)a.TK * sp / a.nsplit);
-    const int kt1 = (int)((long long)a.TK * (sp + 1) / a.nsplit);
+  while (x < xe && !failed) {   // one segment: the range's part in one row block
+    const int rb = (int)(x / a.TK);
+    const long long xb = (long long)rb * a.TK;   // the row block's first tile column
+    const long long xs = xe < xb + a.TK ? xe : xb + a.TK;
+    const int kt0 = (int)(x - xb), kt1 = (int)(xs - xb);
+    const int owner0 = tc_owner(xb, T, G);
+    const int sp = (int)blockIdx.x - owner0;     // this CTA's partial of the row block
+    const bool alone = tc_owner(xb + a.TK - 1, T, G) == owner0;   // y directly
+    x = xs;
     const int strip = rb * 4 + sq;
     const bool has = strip < n_strips;
     const size_t r = (size_t)strip * 64 + 2 * lane + h;
-    // prologue: the unit's first tile, X^T and flags
+    // prologue: the segment's first tile, X^T and flags
     bool fit_cur = true, fit_nxt = true;
     if (has) {
       const int t = strip * a.TK + kt0;
@@ -471,8 +490,8 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
       vb = nvb;
     }
     if (failed || __syncthreads_or(*abort_flag != 0u)) { failed = timed_out = true; break; }
-    if (u + (int)gridDim.x >= units) pdl_trigger();   // last unit decoded
-    // all MMAs of this unit done -> read the accumulators (warp w: tile h,
+    if (x >= xe) pdl_trigger();   // last segment decoded
+    // all MMAs of this segment done -> read the accumulators (warp w: tile h,
     // lanes of strip sq)
     bool to3 = !mbar_wait(&sbar[(gchunk - 1) % kSlots], ((gchunk - 1) / kSlots) & 1u);
     if (__syncthreads_or(to3)) { failed = timed_out = true; break; }
@@ -487,14 +506,14 @@ __global__ void __launch_bounds__(kTcThreads, 3) b_tc_kernel(const BArgs a) {
         for (int i = 0; i < 16; ++i) {
           const int b = j + i;
           if (b < a.batch) {
-            if (a.nsplit == 1) a.y[(size_t)b * a.N + r] = __uint_as_float(rr[i]);
+            if (alone) a.y[(size_t)b * a.N + r] = __uint_as_float(rr[i]);
             else a.ws[(size_t)sp * step + (size_t)b * a.N + r] = __uint_as_float(rr[i]);
           }
         }
       }
     }
     tc_fence_before();
-    __syncthreads();   // accumulators read before the next unit overwrites them
+    __syncthreads();   // accumulators read before the next segment overwrites them
   }
   if (timed_out) {
     if (tid == 0) report(a.status, LW_DEV_TIMEOUT);

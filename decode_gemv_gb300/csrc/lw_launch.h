@@ -84,32 +84,23 @@ inline int tc_max_split(const lw_dev_bundle* b) {
   const int half_tk = (int)(b->cols / 512);
   return half_tk < 1 ? 1 : (half_tk > 32 ? 32 : half_tk);
 }
-// K splits of a tensor-core launch over n_blocks 256-row blocks of TK tile
-// columns on `slots` resident CTAs: the split count whose launch takes the
-// fewest tile columns on its busiest CTA -- waves of units times the longest
-// unit, plus about half a tile column per unit (prologue, accumulator
-// read-out) and the split-K sum's partial reads (split x batch) -- and the
-// fewest splits among equals.
-inline int tc_pick_split(int n_blocks, int TK, int max_split, int slots, int bpad) {
-  const int hi = max_split < TK ? max_split : TK;
-  int best = 1;
-  double best_cost = 1e300;
-  for (int ns = 1; ns <= hi; ++ns) {
-    const long long units = (long long)n_blocks * ns;
-    const long long waves = (units + slots - 1) / slots;
-    const int longest = (TK + ns - 1) / ns;
-    const double cost = (double)waves * (longest + 0.5) + (double)ns * bpad / 4096.0;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = ns;
-    }
-  }
-  return best;
-}
-// The split-K sum behind a tensor-core product of nsplit > 1 K splits:
-// y[b][n] = sum of ws[q][b][n] over q in ascending order (one launch,
-// programmatic dependent launch on `st`).
-lw_status launch_tc_sum(const float* ws, float* y, int N, int batch, int nsplit, cudaStream_t st);
+// Grid of a tensor-core launch over n_blocks 256-row blocks of TK tile
+// columns on `slots` resident CTAs, the tile columns cut into contiguous
+// per-CTA ranges (tc_owner, lw_btc.cuh): G CTAs, and the most CTAs any row
+// block's partial sums come from (<= max_split, which sizes the workspace).
+// Among the grids tried (every resident CTA; n_blocks x m; T / L) the one
+// with the fewest tile columns on its busiest CTA, counting about half a
+// tile column per row block a range touches (accumulator read-out).
+struct TcGrid {
+  int G;        // CTAs
+  int owners;   // most CTAs of one row block (1: no split-K sum)
+};
+TcGrid tc_pick_grid(int n_blocks, int TK, int max_split, int slots);
+// The split-K sum behind a tensor-core launch of grid G (owners > 1):
+// y[b][n] = sum of ws[j][b][n] over the owners j of n's row block in
+// ascending order; row blocks of one owner were written by the product and
+// are skipped (one launch, programmatic dependent launch on `st`).
+lw_status launch_tc_sum(const float* ws, float* y, int N, int batch, int TK, int G, cudaStream_t st);
 inline size_t workspace_counter_bytes(const lw_dev_bundle* b) {
   return ((size_t)(b->rows / 64) * sizeof(uint32_t) + 255) / 256 * 256;
 }

@@ -81,14 +81,10 @@ lw_status launch_q_tc_product(const lw_dev_bundle* b, const float* x, int batch,
   const size_t smem = a.nstage == 1 ? smem1 : smem2;
   if (per_sm < 1) return fail(LW_ERR_UNSUPPORTED, "tensor-core kernel does not fit (%zu B smem)", smem);
   const int n_blocks = (int)((b->rows / 64 + 3) / 4);
-  const int slots = per_sm * device_sm_count();
-  a.nsplit = tc_pick_split(n_blocks, a.TK, tc_max_split(b), slots, a.bpad);
-  const int nsplit = a.nsplit;
-  int grid = n_blocks * nsplit;
-  if (grid > slots) grid = slots;
-  launch_pdl(k, grid, dev::kQtThreads, smem, st, a);
+  const TcGrid g = tc_pick_grid(n_blocks, a.TK, tc_max_split(b), per_sm * device_sm_count());
+  launch_pdl(k, g.G, dev::kQtThreads, smem, st, a);
   lw_status s = check_launch("tensor-core product kernel");
-  if (s == LW_OK && nsplit > 1) s = launch_tc_sum(a.ws, y, (int)b->rows, batch, nsplit, st);
+  if (s == LW_OK && g.owners > 1) s = launch_tc_sum(a.ws, y, (int)b->rows, batch, a.TK, g.G, st);
   return s;
 }
 

@@ -185,16 +185,24 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
   const uint32_t idesc1 = idesc_bf16((uint32_t)a.bpad);         // lo x x_hi
   const int n_strips = a.N / 64;
   const int n_blocks = (n_strips + 3) / 4;
-  const int units = n_blocks * a.nsplit;
+  const long long T = (long long)n_blocks * a.TK;   // tile columns of the launch (tc_owner)
+  const int G = (int)gridDim.x;
+  long long x = T * blockIdx.x / G;                 // this CTA's range [x, xe)
+  const long long xe = T * (blockIdx.x + 1) / G;
   uint32_t gchunk = 0;   // ring commits issued by this CTA so far (uniform)
   uint32_t xk = 0;       // X^T halves consumed so far (uniform); current in buffer xk & 1
   uint32_t ts = 0;       // tile columns started (uniform)
   float4 xv[4];          // activations of the next X^T half, loaded ahead
 
-  for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
-    const int rb = u / a.nsplit, sp = u % a.nsplit;
-    const int kt0 = (int)((long long)a.TK * sp / a.nsplit);
-    const int kt1 = (int)((long long)a.TK * (sp + 1) / a.nsplit);
+  while (x < xe && !failed) {   // one segment: the range's part in one row block
+    const int rb = (int)(x / a.TK);
+    const long long xb = (long long)rb * a.TK;   // the row block's first tile column
+    const long long xs = xe < xb + a.TK ? xe : xb + a.TK;
+    const int kt0 = (int)(x - xb), kt1 = (int)(xs - xb);
+    const int owner0 = tc_owner(xb, T, G);
+    const int sp = (int)blockIdx.x - owner0;     // this CTA's partial of the row block
+    const bool alone = tc_owner(xb + a.TK - 1, T, G) == owner0;   // y directly
+    x = xs;
     const int strip = rb * 4 + sq;
     const bool has = strip < n_strips;
     const size_t r = (size_t)strip * 64 + 2 * lane + h;
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
                                    wst0 + (ts & 1) * a.stage_bytes, &wbar[ts & 1], lead, 0);
       if (ts & 1) infl1 = true; else infl0 = true;
     }
-    // the unit's first X^T half (its buffer's last reader, half xk - 2, done)
+    // the segment's first X^T half (its buffer's last reader, half xk - 2, done)
     if (xk >= 2 && !mbar_wait(&xbar[xk & 1], ((xk - 2) >> 1) & 1u)) timed_out = true;
     if (__syncthreads_or(timed_out)) { failed = true; break; }
     qt_x_load(a, kt0, 0, xv);
@@ -334,8 +342,8 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
       if (two) fit_cur = fit_nxt;
     }
     if (failed || __syncthreads_or(*abort_flag != 0u)) { failed = timed_out = true; break; }
-    if (u + (int)gridDim.x >= units) pdl_trigger();   // last unit decoded
-    // all MMAs of this unit done -> read the accumulators (warp w: tile h,
+    if (x >= xe) pdl_trigger();   // last segment decoded
+    // all MMAs of this segment done -> read the accumulators (warp w: tile h,
     // lanes of strip sq); y = hi-part columns + lo-part columns
     bool to3 = !mbar_wait(&sbar[(gchunk - 1) % kQtSlots], ((gchunk - 1) / kQtSlots) & 1u);
     if (__syncthreads_or(to3)) { failed = timed_out = true; break; }
@@ -352,14 +360,14 @@ __global__ void __launch_bounds__(kQtThreads, 3) q_tc_kernel(const QArgs a) {
           const int b = j + i;
           if (b < a.batch) {
             const float v = __uint_as_float(rh[i]) + __uint_as_float(rl[i]);
-            if (a.nsplit == 1) a.y[(size_t)b * a.N + r] = v;
+            if (alone) a.y[(size_t)b * a.N + r] = v;
             else a.ws[(size_t)sp * step + (size_t)b * a.N + r] = v;
           }
         }
       }
     }
     tc_fence_before();
-    __syncthreads();   // accumulators read before the next unit overwrites them
+    __syncthreads();   // accumulators read before the next segment overwrites them
   }
   if (timed_out) {
     if (tid == 0) report(a.status, LW_DEV_TIMEOUT);
