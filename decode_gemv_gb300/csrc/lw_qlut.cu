@@ -160,8 +160,15 @@ lw_status launch_q_lut(const lw_dev_bundle* const* bs, int n, const float* const
     g.stall_tile = 0;
   }
   const size_t smem = (size_t)g.lut_off + (size_t)lut_bytes;
-  // CTAs: one per SM, shared among the matrices in proportion to their tiles
-  const int G = device_sm_count();
+  // CTAs: one per SM but one, shared among the matrices in proportion to
+  // their tiles.  A CTA fills its SM's shared memory, so the next launch's
+  // CTAs can only enter SMs this launch leaves; with one SM always spare, the
+  // next launch's last CTA enters when this launch's second-to-last CTA
+  // exits, and every CTA has its prologue (decode table, first copies) done
+  // when the dependency wait returns.  With every SM in use, the CTA that
+  // enters last began its prologue only then, and it set the call's end.
+  const int sms = device_sm_count();
+  const int G = sms > 1 ? sms - 1 : 1;
   int left = G;
   int max_per_cta = 1;
   g.cfirst[0] = 0;
