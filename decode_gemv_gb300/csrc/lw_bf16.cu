@@ -142,15 +142,9 @@ __global__ void __launch_bounds__(kSumThreads) tc_sum_kernel(const TcSumArgs a) 
   if (g >= groups) return;
   const int n = 4 * (int)(g % (size_t)n4);
   const long long T = (long long)((a.N / 64 + 3) / 4) * a.TK;
-  const long long xb = (long long)(n >> 8) * a.TK;   // the row block's first tile column
-  int owners;   // tc_owner(xb + TK - 1) - tc_owner(xb) + 1
-  if (WIDE) {
-    owners = tc_owner(xb + a.TK - 1, T, a.G) - tc_owner(xb, T, a.G) + 1;
-  } else {
-    const uint32_t T32 = (uint32_t)T, G32 = (uint32_t)a.G, x32 = (uint32_t)xb;
-    owners = (int)(((x32 + (uint32_t)a.TK) * G32 + T32 - 1u) / T32 -
-                   ((x32 + 1u) * G32 + T32 - 1u) / T32) + 1;
-  }
+  const int rb = n >> 8;
+  const int owners = WIDE ? tc_owners_of(rb, a.TK, T, a.G)
+                          : tc_owners_of32(rb, a.TK, (uint32_t)T, (uint32_t)a.G);
   if (owners == 1) return;   // written by the product
   const float4* p = reinterpret_cast<const float4*>(a.ws) + g;
   const size_t step4 = groups;   // one partial, in float4
@@ -189,44 +183,6 @@ lw_status launch_tc_sum(const float* ws, float* y, int N, int batch, int TK, int
   return check_launch("split-K sum kernel");
 }
 
-namespace {
-
-TcGrid pick_grid_uncached(int n_blocks, int TK, int max_split, int slots) {
-  const long long T = (long long)n_blocks * TK;
-  const int g0 = (int)(slots < T ? slots : T);
-  TcGrid best{1, 1};
-  double best_cost = 1e300;
-  auto consider = [&](long long Gl) {
-    if (Gl < 1 || Gl > g0) return;
-    const int G = (int)Gl;
-    int owners = 0;
-    for (int rb = 0; rb < n_blocks; ++rb) {
-      const long long xb = (long long)rb * TK;
-      const int k = dev::tc_owner(xb + TK - 1, T, G) - dev::tc_owner(xb, T, G) + 1;
-      if (k > owners) owners = k;
-    }
-    if (owners > max_split) return;
-    long long segs = 1;   // most row blocks one CTA's range touches
-    for (int c = 0; c < G; ++c) {
-      const long long x0 = T * c / G, x1 = T * (c + 1) / G;
-      const long long k = (x1 - 1) / TK - x0 / TK + 1;
-      if (k > segs) segs = k;
-    }
-    const double cost = (double)((T + G - 1) / G) + 0.5 * (double)segs;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = TcGrid{G, owners};
-    }
-  };
-  consider(g0);
-  for (int m = 1; m <= max_split && m <= TK; ++m) consider((long long)n_blocks * m);
-  for (int L = 1; L <= TK; ++L) consider(T / L);
-  consider(1);
-  return best;
-}
-
-}  // namespace
-
 TcGrid tc_pick_grid(int n_blocks, int TK, int max_split, int slots) {
   // a few recent shapes per host thread (the pick is pure host arithmetic)
   struct Entry {
@@ -240,7 +196,7 @@ TcGrid tc_pick_grid(int n_blocks, int TK, int max_split, int slots) {
     if (cache[i].key[0] == key[0] && cache[i].key[1] == key[1] && cache[i].key[2] == key[2] &&
         cache[i].key[3] == key[3])
       return cache[i].g;
-  const TcGrid g = pick_grid_uncached(n_blocks, TK, max_split, slots);
+  const TcGrid g = tc_plan(n_blocks, TK, max_split, slots);
   Entry& e = cache[next];
   for (int i = 0; i < 4; ++i) e.key[i] = key[i];
   e.g = g;

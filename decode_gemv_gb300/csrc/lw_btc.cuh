@@ -37,6 +37,7 @@
 
 #include "lw_bkern.cuh"
 #include "lw_lutdec.cuh"
+#include "lw_tcplan.h"
 
 namespace lw {
 namespace dev {
@@ -185,16 +186,6 @@ constexpr int kTcThreads = 256;
 // tensor-memory columns: D0, D1 (bpad each), then the two operand rings
 __host__ __device__ constexpr int tc_tmem_need(int bpad) { return 2 * bpad + 2 * kSlots * kACols; }
 
-// Work of a tensor-core launch, split over its G CTAs in contiguous ranges
-// (a "stream-K" cut): the launch's T = row blocks x TK tile columns, row
-// block major, go to CTA c as [c T / G, (c + 1) T / G), so every CTA gets
-// within one tile column of the same work; a range may run on into the next
-// row block.  A row block's partial sums come from the CTAs owning its tile
-// columns, numbered from the first of them.  The CTA owning tile column x
-// (0 <= x < T, 1 <= G <= T): the largest c with floor(c T / G) <= x.
-__host__ __device__ inline int tc_owner(long long x, long long T, int G) {
-  return (int)(((x + 1) * G + T - 1) / T) - 1;
-}
 
 // LUT: exponents decoded through the compact table replicated per lane
 // (lw_lutdec.cuh; a.lut_off, a.lut_cap) instead of the comparator -- the

@@ -5,6 +5,7 @@
 
 #include "lw_internal.h"
 #include "lw_lut.h"
+#include "lw_tcplan.h"
 
 namespace lw {
 
@@ -85,16 +86,8 @@ inline int tc_max_split(const lw_dev_bundle* b) {
   return half_tk < 1 ? 1 : (half_tk > 32 ? 32 : half_tk);
 }
 // Grid of a tensor-core launch over n_blocks 256-row blocks of TK tile
-// columns on `slots` resident CTAs, the tile columns cut into contiguous
-// per-CTA ranges (tc_owner, lw_btc.cuh): G CTAs, and the most CTAs any row
-// block's partial sums come from (<= max_split, which sizes the workspace).
-// Among the grids tried (every resident CTA; n_blocks x m; T / L) the one
-// with the fewest tile columns on its busiest CTA, counting about half a
-// tile column per row block a range touches (accumulator read-out).
-struct TcGrid {
-  int G;        // CTAs
-  int owners;   // most CTAs of one row block (1: no split-K sum)
-};
+// columns on `slots` resident CTAs (tc_plan of lw_tcplan.h, remembered for a
+// few recent shapes per host thread).
 TcGrid tc_pick_grid(int n_blocks, int TK, int max_split, int slots);
 // The split-K sum behind a tensor-core launch of grid G (owners > 1):
 // y[b][n] = sum of ws[j][b][n] over the owners j of n's row block in
