@@ -1071,7 +1071,7 @@ def run_sweep(args):
                 (lambda d=m["db"][c], w=w: lw.lw_decode(d, w, st)),
                 (lambda w=w, x=x, y=y: torch.matmul(x, w.t(), out=y)))], steps)
         gbs = coded_step / (t_coded * 1e-3) / 1e9
-        rows_out.append({"batch": B, "launches": len(groups) if grouped else len(mats),
+        rows_out.append({"batch": B, "calls": len(groups) if grouped else len(mats),
                          "ms_per_step": t_coded, "coded_gbs": gbs,
                          "frac_of_hbm": gbs / peak, "b_eff_gbs": 2.0 * weights / (t_coded * 1e-3) / 1e9,
                          "twin_ms": t_twin, "twin_gbs": twin_step / (t_twin * 1e-3) / 1e9,
@@ -1086,8 +1086,11 @@ def run_sweep(args):
             "n_gpus": 1, "higher_is_better": True, "dtype": "f32" if mats[0]["fmt"] != lw.LW_FMT_BF16_EXP else "bf16",
             "data": "synthetic", "peak_gbs": peak, "peak_kind": peak_kind,
             "config": {"workload": label, "layers": layers, "matrices": len(mats), "weights": weights,
-                       "launches": "batch 1..5: one launch per group of a layer's independent 4-/6-bit "
-                                   "matrices (q+k+v, gate+up; coded and twin alike); else one per matrix",
+                       "calls": "library calls per step (rows[].calls): batch 1..5 one per group of a "
+                                "layer's independent 4-/6-bit matrices (q+k+v, gate+up; coded and twin "
+                                "alike), else one per matrix; a call on the CUDA cores is one kernel launch "
+                                "per pass, a tensor-core call the product and, when its K range is split "
+                                "over CTAs, the split-K sum",
                        "l2": (f"rotate {copies} device copies ({group} steps per CUDA graph)"
                               if copies > 1 else "working set > 4x L2"),
                        "dense_comparator": "torch.matmul on random bf16 weights of the same shapes (cuBLAS)",
