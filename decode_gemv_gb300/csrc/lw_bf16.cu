@@ -1,4 +1,6 @@
-// Launchers for the BF16 exponent-coded kernels (lw_bkern.cuh).
+// Launchers for the BF16 exponent-coded kernels (lw_bkern.cuh, lw_btc.cuh),
+// and the split-K sum and grid choice that both tensor-core products (BF16
+// and 4-/6-bit) share.
 #include "lw_btc.cuh"
 #include "lw_internal.h"
 #include "lw_launch.h"
@@ -76,8 +78,9 @@ constexpr int kTcLutCap = 256;
 
 }  // namespace
 
-// Tensor-core product for 16..64 activation rows (one launch); coded
-// bundles and their direct-palette twins.
+// Tensor-core product for 16..64 activation rows: the product kernel, and
+// the split-K sum behind it when a row block's K range is split over CTAs;
+// coded bundles and their direct-palette twins.
 lw_status launch_bf16_tc_product(const lw_dev_bundle* b, const uint16_t* x, int batch, float* y,
                                  void* ws, int32_t* status, cudaStream_t st) {
   const bool twin = b->twin != 0;

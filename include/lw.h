@@ -356,8 +356,10 @@ lw_status lw_decode_gemv(const lw_dev_bundle* b, const void* x, float* y,
  *    (tcgen05.mma, BF16 x BF16 -> FP32 in tensor memory), [UW] "How
  *    reconstructive matmul works".
  * Batches beyond one pass take as many passes as needed (the largest pass
- * first).  On the tensor cores the order within an MMA is the hardware's,
- * then K-splits are added in ascending order -- deterministic, but not
+ * first).  On the tensor cores the order within an MMA is the hardware's;
+ * a row block's K range may be cut among several CTAs (contiguous tile
+ * ranges; the cut follows the device's SM count), whose partial sums are
+ * added in ascending order -- deterministic on a given device, but not
  * bitwise equal to the CUDA-core path.  The workspace must hold
  * lw_workspace_bytes(b, batch) bytes.
  */
